@@ -1,0 +1,204 @@
+"""Seeded synthetic inputs for the S6 selective scan.
+
+This module only draws numbers. It holds no part of the scan's arithmetic
+(no softplus, no exponentials of delta*A, no recurrence). The oracle tests,
+the GPU parity tests and ``bench.py`` all take their inputs from here, so
+both sides of every comparison see the same values.
+
+Generator
+---------
+* SplitMix64 (Vigna's published mixer): ``state += 0x9E3779B97F4A7C15`` then
+  ``z = (z ^ z>>30) * 0xBF58476D1CE4E5B9``,
+  ``z = (z ^ z>>27) * 0x94D049BB133111EB``, ``z ^= z>>31``.
+  Output i of the stream seeded with s is the mix of ``s + (i+1)*golden``,
+  so any slice of a stream can be drawn on its own.
+* Uniforms: the top 53 bits of an output times 2**-53, in [0, 1).
+* Normals: Box-Muller on consecutive output pairs (u1, u2) with
+  r = sqrt(-2 ln(1 - u1)), theta = 2*pi*u2, giving r*cos(theta) and
+  r*sin(theta) in that order; computed in float64, scaled, then rounded
+  to float32.
+* Per-tensor seeds: the workload seed feeds one SplitMix64 stream whose
+  successive outputs seed x, z, Bm, Cm, dt, dy, h0, dh_last in that order
+  (the per-tensor SplitMix64-derived seeding the rustytorch commit log on
+  ``MambaBlock::new_seeded`` describes).
+* bf16 workloads round x, z, Bm, Cm and dy to bfloat16 (round to nearest
+  even) here, once; both sides then read the same rounded values.
+
+Workloads
+---------
+The five workload recipes follow the sizes and distributions of the
+selective-scan configurations this library is measured on: A[d, n] =
+-(n + 1) (the canonical A_log = ln(1..N) init), D = 1, gate on, h0 = 0,
+dh_last = 0, and dt_bias chosen so that softplus(dt_bias) equals a target
+delta (0.69 for the "active" tiny block, 0.01 for the canonical init).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+from typing import Dict, Optional
+
+import numpy as np
+
+_GOLDEN = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+_CHUNK = 1 << 22
+
+TENSOR_ORDER = ("x", "z", "Bm", "Cm", "dt", "dy", "h0", "dh_last")
+
+
+def splitmix64(seed: int, n: int, start: int = 0) -> np.ndarray:
+    """Outputs start .. start+n-1 of the SplitMix64 stream seeded with ``seed``."""
+    idx = np.arange(start + 1, start + n + 1, dtype=np.uint64)
+    with np.errstate(over="ignore"):
+        z = np.uint64(seed & 0xFFFFFFFFFFFFFFFF) + idx * _GOLDEN
+        z = (z ^ (z >> np.uint64(30))) * _M1
+        z = (z ^ (z >> np.uint64(27))) * _M2
+        z = z ^ (z >> np.uint64(31))
+    return z
+
+
+def uniform53(seed: int, n: int, start: int = 0) -> np.ndarray:
+    """float64 uniforms in [0, 1) from the top 53 bits of each output."""
+    return (splitmix64(seed, n, start) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+def normal_f32(seed: int, n: int, mean: float = 0.0, std: float = 1.0) -> np.ndarray:
+    """n float32 samples of N(mean, std^2) by Box-Muller, drawn in chunks."""
+    out = np.empty(n, dtype=np.float32)
+    pairs = (n + 1) // 2
+    done = 0
+    while done < pairs:
+        m = min(_CHUNK, pairs - done)
+        u = uniform53(seed, 2 * m, 2 * done)
+        r = np.sqrt(-2.0 * np.log1p(-u[0::2]))
+        th = (2.0 * math.pi) * u[1::2]
+        zz = np.empty(2 * m, dtype=np.float64)
+        zz[0::2] = r * np.cos(th)
+        zz[1::2] = r * np.sin(th)
+        lo = 2 * done
+        hi = min(n, lo + 2 * m)
+        out[lo:hi] = (mean + std * zz[: hi - lo]).astype(np.float32)
+        done += m
+    return out
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round float32 values to the nearest bfloat16 (ties to even); returns float32."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = a.view(np.uint32).astype(np.uint64)
+    bias = np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))
+    r = ((u + bias) & np.uint64(0xFFFF0000)).astype(np.uint32)
+    return r.view(np.float32)
+
+
+def tensor_seeds(seed: int) -> Dict[str, int]:
+    s = splitmix64(seed, len(TENSOR_ORDER))
+    return {name: int(v) for name, v in zip(TENSOR_ORDER, s)}
+
+
+def inverse_softplus(target: float) -> float:
+    """The dt_bias whose softplus is ``target``: ln(e^target - 1)."""
+    return math.log(math.expm1(target))
+
+
+@dataclass
+class Workload:
+    name: str
+    B: int
+    L: int
+    D: int
+    N: int
+    io: str            # "f32" or "bf16": dtype of x, z, Bm, Cm, y, dy, dx, dz
+    seed: int
+    dt_std: float
+    delta_target: float  # softplus(dt_bias) = delta_target
+    note: str = ""
+
+    @property
+    def tc(self) -> int:
+        return self.B * self.L * self.D
+
+
+WORKLOADS: Dict[str, Workload] = {
+    w.name: w
+    for w in (
+        Workload("s6-tiny-active-f32", 1, 64, 16, 16, "f32", 0, 0.1, 0.69,
+                 "active block: delta ~ 0.69"),
+        Workload("s6-small-f32", 2, 512, 256, 16, "f32", 1, 1.0, 0.01,
+                 "canonical dt_bias, dt ~ N(0,1): delta spread ~1e-3..1"),
+        Workload("mamba130m-bf16", 8, 2048, 1536, 16, "bf16", 2, 1.0, 0.01,
+                 "Mamba-130M-shaped: d_model 768, expand 2"),
+        Workload("mamba1.4b-bf16", 4, 4096, 4096, 16, "bf16", 3, 1.0, 0.01,
+                 "Mamba-1.4B-shaped: d_model 2048, expand 2"),
+        Workload("long65k-bf16", 1, 65536, 2048, 16, "bf16", 4, 1.0, 0.01,
+                 "long sequence, needs the multi-CTA carry along L"),
+    )
+}
+WORKLOAD_ORDER = list(WORKLOADS)
+
+
+@dataclass
+class Inputs:
+    """All inputs of one scan problem as float32 numpy arrays (bf16-rounded
+    where the workload's I/O dtype is bf16). Layouts: x, z, dt, dy [B,L,D];
+    Bm, Cm [B,L,N]; A [D,N]; Dskip, dt_bias [D]; h0, dh_last [B,D,N]."""
+    B: int
+    L: int
+    D: int
+    N: int
+    io: str
+    x: np.ndarray
+    dt: np.ndarray
+    z: Optional[np.ndarray]
+    Bm: np.ndarray
+    Cm: np.ndarray
+    A: np.ndarray
+    Dskip: Optional[np.ndarray]
+    dt_bias: Optional[np.ndarray]
+    h0: Optional[np.ndarray]
+    dy: np.ndarray
+    dh_last: Optional[np.ndarray]
+    delta_softplus: int = 1
+    meta: dict = field(default_factory=dict)
+
+
+def make_inputs(B: int, L: int, D: int, N: int, *, io: str = "f32", seed: int = 0,
+                dt_std: float = 1.0, delta_target: float = 0.01, gate: bool = True,
+                skip: bool = True, bias: bool = True, with_h0: bool = False,
+                with_dh_last: bool = False, delta_softplus: int = 1,
+                x_std: float = 1.0) -> Inputs:
+    """Draw one problem. ``with_h0`` / ``with_dh_last`` draw N(0, 1) initial
+    state and final-state gradient instead of zeros."""
+    s = tensor_seeds(seed)
+    tc = B * L * D
+    bl = B * L * N
+    rnd = round_bf16 if io == "bf16" else (lambda a: a)
+    x = rnd(normal_f32(s["x"], tc, 0.0, x_std)).reshape(B, L, D)
+    z = rnd(normal_f32(s["z"], tc)).reshape(B, L, D) if gate else None
+    Bm = rnd(normal_f32(s["Bm"], bl)).reshape(B, L, N)
+    Cm = rnd(normal_f32(s["Cm"], bl)).reshape(B, L, N)
+    dt = normal_f32(s["dt"], tc, 0.0, dt_std).reshape(B, L, D)
+    dy = rnd(normal_f32(s["dy"], tc)).reshape(B, L, D)
+    A = np.tile(-np.arange(1, N + 1, dtype=np.float32), (D, 1))
+    Dskip = np.ones(D, dtype=np.float32) if skip else None
+    dt_bias = np.full(D, inverse_softplus(delta_target), dtype=np.float32) if bias else None
+    h0 = normal_f32(s["h0"], B * D * N).reshape(B, D, N) if with_h0 else None
+    dh_last = normal_f32(s["dh_last"], B * D * N).reshape(B, D, N) if with_dh_last else None
+    return Inputs(B, L, D, N, io, x, dt, z, Bm, Cm, A, Dskip, dt_bias, h0, dy, dh_last,
+                  delta_softplus, {"seed": seed, "dt_std": dt_std, "delta_target": delta_target})
+
+
+def workload_inputs(name: str, **kw) -> Inputs:
+    w = WORKLOADS[name]
+    return make_inputs(w.B, w.L, w.D, w.N, io=w.io, seed=w.seed, dt_std=w.dt_std,
+                       delta_target=w.delta_target, **kw)
+
+
+def recipe_text() -> str:
+    lines = []
+    for w in WORKLOADS.values():
+        lines.append(f"{w.name}: B={w.B} L={w.L} D={w.D} N={w.N} io={w.io} seed={w.seed} "
+                     f"dt~N(0,{w.dt_std}^2) softplus(dt_bias)={w.delta_target} ({w.note})")
+    return "\n".join(lines)
