@@ -1,0 +1,182 @@
+/*
+ * ssm_scan.h -- C ABI of libssmscan.so, the Mamba S6 selective scan on one
+ * GB300 (sm_103a).
+ *
+ * The operation (rustytorch commit log, "MambaBlock" S6 forward commit:
+ * "delta=softplus(dt.dt_proj+dt_bias) -> A=-exp(A_log) -> sequential scan
+ * h=dA.h+dBu, y=sum C.h + D.u -> gate by SiLU(z)"):
+ *
+ *   Delta[b,t,d] = softplus(dt[b,t,d] + dt_bias[d])     (dt + dt_bias if delta_softplus == 0)
+ *   h[b,d,n]    <- exp(Delta*A[d,n]) * h[b,d,n] + Delta*x[b,t,d]*Bm[b,t,n]
+ *   y[b,t,d]     = (sum_n Cm[b,t,n]*h[b,d,n] + Dskip[d]*x[b,t,d]) * silu(z[b,t,d])
+ *
+ * with h starting from h0 (zeros when NULL). The caller folds A = -exp(A_log)
+ * itself; the gradient of A_log is dA * A (the analytic-VJP commit:
+ * "A_log (via A=-exp(A_log) => dA_log = dA.A)").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every pointer is DEVICE memory of the current CUDA device, owned
+ *   by the caller. The library allocates, frees and synchronises nothing on
+ *   these calls (ssm_poll_status excepted, which synchronises its stream).
+ * - Layout: dense row-major, channel-contiguous ("token-major"):
+ *     x, z, dt, y, dy, dx, dz, d_dt      [B, L, D]
+ *     Bm, Cm, dB, dC                      [B, L, N]   (per token, shared by all channels)
+ *     A, dA                               [D, N]
+ *     Dskip, dt_bias, dD, d_dt_bias       [D]
+ *     h0, h_last, dh_last, dh0, state     [B, D, N]
+ *     ckpt                                [B, ceil(L/16), D, N]  (state before tokens 0, 16, 32, ...)
+ * - Types: x, z, Bm, Cm, y, dy, dx, dz (and the step's x_t, z_t, Bm_t, Cm_t,
+ *   y_t) use the I/O dtype (SSM_F32 or SSM_BF16). Everything else is fp32.
+ *   All arithmetic and the recurrent state are fp32.
+ * - Shapes: N must be 16 (else SSM_ERR_UNSUPPORTED). D must be a multiple of
+ *   8 and every pointer 16-byte aligned (else SSM_ERR_ALIGNMENT). B, L or
+ *   D may be 0.
+ * - Streams: calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream). Inputs must stay valid until the work completes.
+ * - Errors: argument errors are found on the host before anything is
+ *   launched and return a negative code; nothing is written. A failed launch
+ *   returns SSM_ERR_CUDA. Non-finite outputs are latched on the device in the
+ *   workspace status word and reported by ssm_poll_status.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+enum {
+    SSM_OK = 0,
+    SSM_ERR_INVALID_ARG = -1, /* null required pointer, negative size, bad flag */
+    SSM_ERR_UNSUPPORTED = -2, /* N != 16, unknown dtype */
+    SSM_ERR_ALIGNMENT = -3,   /* D % 8 != 0 or a pointer not 16-byte aligned */
+    SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than ssm_scan_workspace_bytes */
+    SSM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+    SSM_ERR_NONFINITE = -7    /* (ssm_poll_status) a kernel produced Inf/NaN */
+};
+
+/* Forward over a whole sequence.
+ * Inputs: x, z (NULL = no gate: y = p), Bm, Cm [I/O dtype]; dt [fp32];
+ *   dt_bias, Dskip (NULL = 0), A [fp32]; h0 (NULL = zero state).
+ * Outputs: y [I/O dtype]; h_last (nullable) = state after token L-1;
+ *   ckpt (nullable) = the state before every 16th token, which
+ *   ssm_scan_bwd needs; size ssm_scan_ckpt_elems() floats.
+ * workspace: >= ssm_scan_workspace_bytes(B, L, D, N) bytes, 16-byte
+ *   aligned, holding the status word and the chunk carries along L.
+ * nsplit / groups: launch shape; 0 = automatic. nsplit in {1,2,4} lanes per
+ *   channel (each lane owns 16/nsplit states); groups = number of L-segments
+ *   scanned in parallel, joined by chunk carries. Results are the same up
+ *   to rounding for every choice; with groups == 1 the forward is bitwise
+ *   equal to stepping ssm_step through the sequence. */
+typedef struct {
+    int64_t B, L, D, N;
+    int32_t io_dtype;       /* ssm_dtype */
+    int32_t delta_softplus; /* 1: Delta = softplus(dt + dt_bias); 0: Delta = dt + dt_bias */
+    const void* x;
+    const void* z;
+    const void* Bm;
+    const void* Cm;
+    const float* dt;
+    const float* dt_bias;
+    const float* A;
+    const float* Dskip;
+    const float* h0;
+    void* y;
+    float* h_last;
+    float* ckpt;
+    void* workspace;
+    size_t workspace_bytes;
+    int32_t nsplit;
+    int32_t groups;
+} ssm_fwd_args;
+
+/* Reverse pass for loss = <dy, y> + <dh_last, h_last> (the analytic VJP:
+ * "reverse-time recurrence over the cached h trajectory", gradients summed
+ * over the batch).
+ * f: the forward arguments of the same call (x, z, Bm, Cm, dt, dt_bias, A,
+ *   Dskip, h0 are read; f.ckpt must hold what ssm_scan_fwd wrote; f.y and
+ *   f.h_last are not touched). f.nsplit / f.groups choose this pass's shape.
+ * dy [I/O dtype]; dh_last [fp32, nullable = 0].
+ * Outputs, written for every element:
+ *   dx, dz [I/O dtype] (dz required iff f.z != NULL); d_dt [fp32] = dLoss/d(dt);
+ *   dA [D,N], dD [D], d_dt_bias [D], dB, dC [B,L,N] fp32, OVERWRITTEN
+ *   (zeroed on the stream first; summed over batch and tokens / channels);
+ *   dh0 [B,D,N] fp32 (nullable).
+ * In place: dx may alias dy, dz may alias z, d_dt may alias dt. */
+typedef struct {
+    ssm_fwd_args f;
+    const void* dy;
+    const float* dh_last;
+    void* dx;
+    void* dz;
+    float* d_dt;
+    float* dA;
+    float* dD;
+    float* d_dt_bias;
+    float* dB;
+    float* dC;
+    float* dh0;
+} ssm_bwd_args;
+
+/* One token for every (b,d) channel ("MambaRecurrence ... step(state, x_t)
+ * -> (state', y_t)"): state [B,D,N] fp32 is updated in place and y_t [B,D]
+ * written. x_t, z_t (nullable), dt_t [B,D]; Bm_t, Cm_t [B,N]. Uses the very
+ * same per-token arithmetic as ssm_scan_fwd, so stepping from a state the
+ * forward passed through reproduces the forward's outputs bit for bit.
+ * workspace: nullable; when given (>= 256 bytes) non-finite outputs are
+ * latched in its status word. */
+typedef struct {
+    int64_t B, D, N;
+    int32_t io_dtype;
+    int32_t delta_softplus;
+    const void* x_t;
+    const void* z_t;
+    const void* Bm_t;
+    const void* Cm_t;
+    const float* dt_t;
+    const float* dt_bias;
+    const float* A;
+    const float* Dskip;
+    float* state;
+    void* y_t;
+    void* workspace;
+    int32_t nsplit;
+    int32_t pad_;
+} ssm_step_args;
+
+int ssm_scan_fwd(const ssm_fwd_args* args, void* stream);
+int ssm_scan_bwd(const ssm_bwd_args* args, void* stream);
+int ssm_step(const ssm_step_args* args, void* stream);
+
+/* Gradient of A_log for A = -exp(A_log) (the analytic-VJP commit: "A_log
+ * (via A=-exp(A_log) => dA_log = dA.A)"): dA_log[i] = dA[i] * A[i] for
+ * i < n, fp32 device arrays; dA_log may alias dA. Asynchronous on stream. */
+int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, void* stream);
+
+/* Bytes of workspace a fwd or bwd call of this shape needs (>= 256). */
+size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);
+/* fp32 elements of the checkpoint buffer: B * ceil(L/16) * D * N. */
+int64_t ssm_scan_ckpt_elems(int64_t B, int64_t L, int64_t D, int64_t N);
+/* Tokens between checkpoints (16). */
+int ssm_scan_ckpt_interval(void);
+/* Synchronises `stream`, reads and clears the workspace status word.
+ * Returns SSM_OK, SSM_ERR_NONFINITE, or SSM_ERR_CUDA. */
+int ssm_poll_status(void* workspace, void* stream);
+/* Zeroes the workspace status word on `stream` (asynchronous). */
+int ssm_clear_status(void* workspace, void* stream);
+/* Static English description of a status code. */
+const char* ssm_status_string(int code);
+/* Launches of the library's own kernels made by the most recent
+ * fwd / bwd / step / dA_log call on this host thread. */
+int ssm_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SSM_SCAN_H */

@@ -1,0 +1,353 @@
+"""GB300-native Mamba S6 selective scan.
+
+Python binding of ``libssmscan.so`` (C ABI in ``include/ssm_scan.h``). This
+module only marshals arguments: it checks dtypes, shapes, contiguity,
+devices and alignment, allocates outputs with PyTorch and passes raw device
+pointers and the current CUDA stream to the library. Every step of the scan
+runs in the library's CUDA kernels; there is no other implementation here,
+and calls fail loudly when the library is missing.
+
+The operation (rustytorch commit log, "MambaBlock" S6 forward commit):
+    Delta = softplus(dt + dt_bias);  h_t = exp(Delta*A) * h_{t-1} + Delta*B_t*x_t
+    y_t = (C_t . h_t + D*x_t) * silu(z_t)
+Layouts: x, z, dt, y [B, L, D]; Bm, Cm [B, L, 16]; A [D, 16]; Dskip,
+dt_bias [D]; states [B, D, 16]. x, z, Bm, Cm, y, dy, dx, dz are fp32 or bf16
+(one dtype per call); everything else is fp32.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Dict, Optional
+
+import torch
+
+__all__ = [
+    "SsmError", "build", "lib", "scan_fwd", "scan_bwd", "step", "dA_log_grad", "poll_status",
+    "clear_status", "workspace_bytes", "ckpt_elems", "CKPT_INTERVAL", "Workspace", "scan_fwd_bwd_host",
+    "last_launch_count",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libssmscan.so")
+CKPT_INTERVAL = 16
+_lock = threading.Lock()
+_lib = None
+
+SSM_F32, SSM_BF16 = 0, 1
+_IO = {torch.float32: SSM_F32, torch.bfloat16: SSM_BF16}
+
+
+class SsmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = lib().ssm_status_string(code).decode()
+        super().__init__(f"{where}: {msg} (code {code})")
+        self.code = code
+
+
+class FwdArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("L", ctypes.c_int64), ("D", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("io_dtype", ctypes.c_int32), ("delta_softplus", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in ("x", "z", "Bm", "Cm", "dt", "dt_bias", "A", "Dskip", "h0", "y",
+                                       "h_last", "ckpt", "workspace")] + [
+        ("workspace_bytes", ctypes.c_size_t), ("nsplit", ctypes.c_int32), ("groups", ctypes.c_int32)]
+
+
+class BwdArgs(ctypes.Structure):
+    _fields_ = [("f", FwdArgs)] + [
+        (n, ctypes.c_void_p) for n in ("dy", "dh_last", "dx", "dz", "d_dt", "dA", "dD", "d_dt_bias", "dB",
+                                       "dC", "dh0")]
+
+
+class StepArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("D", ctypes.c_int64), ("N", ctypes.c_int64),
+                ("io_dtype", ctypes.c_int32), ("delta_softplus", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in ("x_t", "z_t", "Bm_t", "Cm_t", "dt_t", "dt_bias", "A", "Dskip", "state",
+                                       "y_t", "workspace")] + [
+        ("nsplit", ctypes.c_int32), ("pad_", ctypes.c_int32)]
+
+
+EXPORTS = {
+    "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_step": ([ctypes.POINTER(StepArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_scan_workspace_bytes": ([ctypes.c_int64] * 4, ctypes.c_size_t),
+    "ssm_scan_ckpt_elems": ([ctypes.c_int64] * 4, ctypes.c_int64),
+    "ssm_scan_ckpt_interval": ([], ctypes.c_int),
+    "ssm_poll_status": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "ssm_clear_status": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
+    "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
+    "ssm_last_launch_count": ([], ctypes.c_int),
+    "ssm_dA_log_grad": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
+                        ctypes.c_int),
+}
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile libssmscan.so for sm_103a (no-op when up to date)."""
+    import importlib
+    return importlib.import_module(__name__ + "._builder").build(force=force, verbose=verbose)
+
+
+def lib():
+    """The loaded CUDA library. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: build it with selective_state_space_07_gb300.build()")
+            h = ctypes.CDLL(LIB_PATH)
+            for name, (argt, rest) in EXPORTS.items():
+                f = getattr(h, name)
+                f.argtypes = argt
+                f.restype = rest
+            _lib = h
+    return _lib
+
+
+def _p(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _need(t, name, shape, dtype, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (the library reads raw row-major memory)")
+    if t.numel() and t.data_ptr() % 16:
+        raise ValueError(f"{name} must be 16-byte aligned")
+
+
+def _opt(t, name, shape, dtype, device):
+    if t is not None:
+        _need(t, name, shape, dtype, device)
+    return t
+
+
+def _stream(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def workspace_bytes(B: int, L: int, D: int, N: int = 16) -> int:
+    return int(lib().ssm_scan_workspace_bytes(B, L, D, N))
+
+
+def ckpt_elems(B: int, L: int, D: int, N: int = 16) -> int:
+    return int(lib().ssm_scan_ckpt_elems(B, L, D, N))
+
+
+def last_launch_count() -> int:
+    """Kernels the library launched in the last fwd / bwd / step call of this thread."""
+    return int(lib().ssm_last_launch_count())
+
+
+class Workspace:
+    """Caller-owned scratch for fwd / bwd: status word + carries along L."""
+
+    def __init__(self, B: int, L: int, D: int, device, N: int = 16):
+        self.nbytes = workspace_bytes(B, L, D, N)
+        self.buf = torch.zeros(self.nbytes, dtype=torch.uint8, device=device)
+
+    def fits(self, B, L, D, N=16) -> bool:
+        return self.nbytes >= workspace_bytes(B, L, D, N)
+
+
+def _ws(ws, B, L, D, device):
+    if ws is None or not ws.fits(B, L, D):
+        ws = Workspace(B, L, D, device)
+    return ws
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise SsmError(rc, where)
+
+
+def _fwd_struct(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0, delta_softplus, y, h_last, ckpt, ws, nsplit, groups):
+    B, L, D = x.shape
+    N = A.shape[1]
+    return FwdArgs(B=B, L=L, D=D, N=N, io_dtype=_IO[x.dtype], delta_softplus=int(bool(delta_softplus)),
+                   x=_p(x), z=_p(z), Bm=_p(Bm), Cm=_p(Cm), dt=_p(dt), dt_bias=_p(dt_bias), A=_p(A),
+                   Dskip=_p(Dskip), h0=_p(h0), y=_p(y), h_last=_p(h_last), ckpt=_p(ckpt),
+                   workspace=ws.buf.data_ptr(), workspace_bytes=ws.nbytes, nsplit=nsplit, groups=groups)
+
+
+def _check_inputs(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0):
+    if x.dim() != 3:
+        raise ValueError("x must be [B, L, D]")
+    B, L, D = x.shape
+    dev, io = x.device, x.dtype
+    if dev.type != "cuda":
+        raise ValueError("the scan runs on a CUDA device; x is on " + str(dev))
+    if io not in _IO:
+        raise TypeError(f"x dtype must be float32 or bfloat16, got {io}")
+    if A.dim() != 2 or A.shape[0] != D:
+        raise ValueError("A must be [D, N]")
+    N = A.shape[1]
+    _need(x, "x", (B, L, D), io, dev)
+    _need(dt, "dt", (B, L, D), torch.float32, dev)
+    _need(A, "A", (D, N), torch.float32, dev)
+    _need(Bm, "Bm", (B, L, N), io, dev)
+    _need(Cm, "Cm", (B, L, N), io, dev)
+    _opt(z, "z", (B, L, D), io, dev)
+    _opt(Dskip, "Dskip", (D,), torch.float32, dev)
+    _opt(dt_bias, "dt_bias", (D,), torch.float32, dev)
+    _opt(h0, "h0", (B, D, N), torch.float32, dev)
+    return B, L, D, N, dev, io
+
+
+def scan_fwd(x, dt, A, Bm, Cm, z=None, Dskip=None, dt_bias=None, h0=None, delta_softplus=True, *,
+             return_last_state=False, save_ckpt=True, y=None, h_last=None, ckpt=None, workspace=None,
+             nsplit=0, groups=0, stream=None):
+    """Sequence forward. Returns (y, h_last or None, ckpt or None, workspace)."""
+    B, L, D, N, dev, io = _check_inputs(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0)
+    y = torch.empty_like(x) if y is None else y
+    _need(y, "y", (B, L, D), io, dev)
+    if return_last_state and h_last is None:
+        h_last = torch.empty(B, D, N, dtype=torch.float32, device=dev)
+    _opt(h_last, "h_last", (B, D, N), torch.float32, dev)
+    if save_ckpt and ckpt is None:
+        ckpt = torch.empty(max(1, ckpt_elems(B, L, D, N)), dtype=torch.float32, device=dev)
+    if ckpt is not None and ckpt.numel() < ckpt_elems(B, L, D, N):
+        raise ValueError("ckpt is smaller than ckpt_elems(B, L, D, N)")
+    ws = _ws(workspace, B, L, D, dev)
+    args = _fwd_struct(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0, delta_softplus, y, h_last, ckpt, ws, nsplit,
+                       groups)
+    _check(lib().ssm_scan_fwd(ctypes.byref(args), _stream(dev, stream)), "ssm_scan_fwd")
+    return y, h_last, ckpt, ws
+
+
+def scan_bwd(x, dt, A, Bm, Cm, dy, ckpt, z=None, Dskip=None, dt_bias=None, h0=None, dh_last=None,
+             delta_softplus=True, *, return_dh0=False, inplace=False, out: Optional[Dict] = None,
+             workspace=None, nsplit=0, groups=0, stream=None) -> Dict[str, torch.Tensor]:
+    """Reverse pass for loss = <dy, y> + <dh_last, h_last>. Returns a dict with dx, dz (if z), d_dt,
+    dA, dD, d_dt_bias, dB, dC and dh0 (if asked). ``inplace`` writes dx into dy, dz into z and d_dt
+    into dt."""
+    B, L, D, N, dev, io = _check_inputs(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0)
+    _need(dy, "dy", (B, L, D), io, dev)
+    _opt(dh_last, "dh_last", (B, D, N), torch.float32, dev)
+    if ckpt is None or ckpt.numel() < ckpt_elems(B, L, D, N) or ckpt.dtype != torch.float32:
+        raise ValueError("ckpt must be the fp32 checkpoint buffer scan_fwd filled")
+    o = dict(out or {})
+    if inplace:
+        o.setdefault("dx", dy)
+        o.setdefault("d_dt", dt)
+        if z is not None:
+            o.setdefault("dz", z)
+    f32 = dict(dtype=torch.float32, device=dev)
+    o.setdefault("dx", torch.empty_like(x))
+    if z is not None:
+        o.setdefault("dz", torch.empty_like(x))
+    o.setdefault("d_dt", torch.empty(B, L, D, **f32))
+    o.setdefault("dA", torch.empty(D, N, **f32))
+    o.setdefault("dD", torch.empty(D, **f32))
+    o.setdefault("d_dt_bias", torch.empty(D, **f32))
+    o.setdefault("dB", torch.empty(B, L, N, **f32))
+    o.setdefault("dC", torch.empty(B, L, N, **f32))
+    if return_dh0:
+        o.setdefault("dh0", torch.empty(B, D, N, **f32))
+    for k, shp, dt_ in (("dx", (B, L, D), io), ("dz", (B, L, D), io), ("d_dt", (B, L, D), torch.float32),
+                        ("dA", (D, N), torch.float32), ("dD", (D,), torch.float32),
+                        ("d_dt_bias", (D,), torch.float32), ("dB", (B, L, N), torch.float32),
+                        ("dC", (B, L, N), torch.float32), ("dh0", (B, D, N), torch.float32)):
+        _opt(o.get(k), k, shp, dt_, dev)
+    ws = _ws(workspace, B, L, D, dev)
+    fa = _fwd_struct(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0, delta_softplus, None, None, ckpt, ws, nsplit,
+                     groups)
+    args = BwdArgs(f=fa, dy=_p(dy), dh_last=_p(dh_last), dx=_p(o["dx"]), dz=_p(o.get("dz")),
+                   d_dt=_p(o["d_dt"]), dA=_p(o["dA"]), dD=_p(o["dD"]), d_dt_bias=_p(o["d_dt_bias"]),
+                   dB=_p(o["dB"]), dC=_p(o["dC"]), dh0=_p(o.get("dh0")))
+    _check(lib().ssm_scan_bwd(ctypes.byref(args), _stream(dev, stream)), "ssm_scan_bwd")
+    o["workspace"] = ws
+    return o
+
+
+def step(state, x_t, dt_t, A, Bm_t, Cm_t, z_t=None, Dskip=None, dt_bias=None, delta_softplus=True, *,
+         y_t=None, workspace=None, nsplit=0, stream=None):
+    """One token for every channel; ``state`` [B, D, 16] fp32 is updated in place. Returns y_t [B, D]."""
+    if x_t.dim() != 2:
+        raise ValueError("x_t must be [B, D]")
+    B, D = x_t.shape
+    dev, io = x_t.device, x_t.dtype
+    if dev.type != "cuda":
+        raise ValueError("the step runs on a CUDA device; x_t is on " + str(dev))
+    if io not in _IO:
+        raise TypeError(f"x_t dtype must be float32 or bfloat16, got {io}")
+    N = A.shape[1]
+    _need(state, "state", (B, D, N), torch.float32, dev)
+    _need(x_t, "x_t", (B, D), io, dev)
+    _need(dt_t, "dt_t", (B, D), torch.float32, dev)
+    _need(A, "A", (D, N), torch.float32, dev)
+    _need(Bm_t, "Bm_t", (B, N), io, dev)
+    _need(Cm_t, "Cm_t", (B, N), io, dev)
+    _opt(z_t, "z_t", (B, D), io, dev)
+    _opt(Dskip, "Dskip", (D,), torch.float32, dev)
+    _opt(dt_bias, "dt_bias", (D,), torch.float32, dev)
+    y_t = torch.empty_like(x_t) if y_t is None else y_t
+    _need(y_t, "y_t", (B, D), io, dev)
+    args = StepArgs(B=B, D=D, N=N, io_dtype=_IO[io], delta_softplus=int(bool(delta_softplus)), x_t=_p(x_t),
+                    z_t=_p(z_t), Bm_t=_p(Bm_t), Cm_t=_p(Cm_t), dt_t=_p(dt_t), dt_bias=_p(dt_bias), A=_p(A),
+                    Dskip=_p(Dskip), state=_p(state), y_t=_p(y_t),
+                    workspace=None if workspace is None else workspace.buf.data_ptr(), nsplit=nsplit)
+    _check(lib().ssm_step(ctypes.byref(args), _stream(dev, stream)), "ssm_step")
+    return y_t
+
+
+def dA_log_grad(dA, A, out=None, stream=None):
+    """Gradient of A_log for A = -exp(A_log): dA_log = dA * A (elementwise, on the GPU)."""
+    _need(A, "A", tuple(A.shape), torch.float32, A.device)
+    _need(dA, "dA", tuple(A.shape), torch.float32, A.device)
+    out = torch.empty_like(A) if out is None else out
+    _need(out, "out", tuple(A.shape), torch.float32, A.device)
+    _check(lib().ssm_dA_log_grad(_p(dA), _p(A), _p(out), A.numel(), _stream(A.device, stream)),
+           "ssm_dA_log_grad")
+    return out
+
+
+def poll_status(workspace, stream=None) -> int:
+    """Synchronise, read and clear the status word. 0 = ok, -7 = non-finite output seen."""
+    dev = workspace.buf.device
+    return int(lib().ssm_poll_status(workspace.buf.data_ptr(), _stream(dev, stream)))
+
+
+def clear_status(workspace, stream=None) -> None:
+    dev = workspace.buf.device
+    _check(lib().ssm_clear_status(workspace.buf.data_ptr(), _stream(dev, stream)), "ssm_clear_status")
+
+
+def scan_fwd_bwd_host(host: Dict[str, torch.Tensor], device, *, dev_buffers: Optional[Dict] = None,
+                      results: Optional[Dict] = None, stream=None, delta_softplus=True):
+    """End-to-end call for host callers: copies the inputs from (pinned) host memory to the device,
+    runs ssm_scan_fwd then ssm_scan_bwd, and copies y and every gradient back to host memory.
+    ``host`` holds x, dt, A, Bm, Cm, z, Dskip, dt_bias, dy as CPU tensors. Device buffers and
+    pinned result buffers are reused when passed in. Returns (results, dev_buffers)."""
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    dv = dev_buffers if dev_buffers is not None else {
+        k: torch.empty(v.shape, dtype=v.dtype, device=device) for k, v in host.items() if v is not None}
+    with torch.cuda.stream(s):
+        for k, v in host.items():
+            if v is not None:
+                dv[k].copy_(v, non_blocking=True)
+        y, _, ckpt, ws = scan_fwd(dv["x"], dv["dt"], dv["A"], dv["Bm"], dv["Cm"], dv.get("z"), dv.get("Dskip"),
+                                  dv.get("dt_bias"), None, delta_softplus, y=dv.get("y"), ckpt=dv.get("ckpt"),
+                                  workspace=dv.get("ws"), stream=s)
+        dv["y"], dv["ckpt"], dv["ws"] = y, ckpt, ws
+        g = scan_bwd(dv["x"], dv["dt"], dv["A"], dv["Bm"], dv["Cm"], dv["dy"], ckpt, dv.get("z"),
+                     dv.get("Dskip"), dv.get("dt_bias"), None, None, delta_softplus, out=dv.get("grads"),
+                     workspace=ws, stream=s)
+        g.pop("workspace", None)
+        dv["grads"] = g
+        outs = {"y": y, **g}
+        if results is None:
+            results = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in outs.items()}
+        for k, v in outs.items():
+            results[k].copy_(v, non_blocking=True)
+    return results, dv

@@ -1,0 +1,290 @@
+// C entry points of libssmscan.so: argument validation (nothing is launched
+// when an argument is wrong), launch-shape choice, and the sequence of
+// kernels each call runs on the caller's stream. See include/ssm_scan.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "../../include/ssm_scan.h"
+#include "ssm_internal.h"
+
+namespace {
+
+using ssm::BwdParams;
+using ssm::FwdParams;
+using ssm::StepParams;
+
+constexpr int64_t kCK = 16;
+constexpr int64_t kGroupBudget = 131072;  // cap on B*D*groups held in the carry buffers
+constexpr size_t kStatusBytes = 256;
+
+thread_local int g_launches = 0;
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int64_t max_groups(int64_t B, int64_t L, int64_t D) {
+    const int64_t nck = std::max<int64_t>(1, ceil_div(L, kCK));
+    const int64_t ch = std::max<int64_t>(1, B * D);
+    return std::max<int64_t>(1, std::min<int64_t>(nck, std::max<int64_t>(1, kGroupBudget / ch)));
+}
+
+struct WsLayout {
+    size_t aggV, aggS, carry, total;
+};
+
+WsLayout ws_layout(int64_t B, int64_t L, int64_t D) {
+    const int64_t gm = max_groups(B, L, D);
+    const size_t nv = (size_t)B * gm * D * 16 * sizeof(float);
+    const size_t ns = (size_t)B * gm * D * sizeof(float);
+    WsLayout w;
+    w.aggV = kStatusBytes;
+    w.aggS = w.aggV + nv;
+    w.carry = w.aggS + ((ns + 255) / 256) * 256;
+    w.total = w.carry + nv;
+    return w;
+}
+
+bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+// Lanes per channel: enough warps to fill 152 SMs.
+int auto_nsplit(int64_t channels) {
+    if (channels >= 65536) return 1;
+    if (channels >= 32768) return 2;
+    return 4;
+}
+
+int auto_groups(int64_t channels, int nsplit, int64_t L, int64_t gmax) {
+    const int64_t warps = std::max<int64_t>(1, channels * nsplit / 32);
+    if (warps >= 1024) return 1;
+    const int64_t want = ceil_div(2048, warps);
+    return (int)std::max<int64_t>(1, std::min<int64_t>({want, ceil_div(L, kCK), gmax}));
+}
+
+// Common checks of the forward-shaped arguments. Returns SSM_OK or an error.
+int check_fwd(const ssm_fwd_args* a, bool need_y) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->B < 0 || a->L < 0 || a->D < 0 || a->N < 0) return SSM_ERR_INVALID_ARG;
+    if (a->N != 16) return SSM_ERR_UNSUPPORTED;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->nsplit != 0 && a->nsplit != 1 && a->nsplit != 2 && a->nsplit != 4) return SSM_ERR_INVALID_ARG;
+    if (a->groups < 0) return SSM_ERR_INVALID_ARG;
+    if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
+    if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 40))
+        return SSM_ERR_INVALID_ARG;
+    const bool work = a->B > 0 && a->L > 0 && a->D > 0;
+    if (work && (!a->x || !a->dt || !a->Bm || !a->Cm || !a->A || (need_y && !a->y))) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->x, a->z, a->Bm, a->Cm, a->dt, a->dt_bias, a->A, a->Dskip, a->h0, a->y, a->h_last,
+                          a->ckpt, a->workspace};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return SSM_ERR_ALIGNMENT;
+    if (!a->workspace || a->workspace_bytes < ssm_scan_workspace_bytes(a->B, a->L, a->D, a->N))
+        return SSM_ERR_WORKSPACE;
+    return SSM_OK;
+}
+
+__global__ void dA_log_kernel(const float* dA, const float* __restrict__ A, float* dA_log, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        dA_log[i] = dA[i] * A[i];
+}
+
+int tally(int r) {
+    if (r < 0) return SSM_ERR_CUDA;
+    g_launches += r;
+    return SSM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
+    (void)N;
+    if (B < 0 || L < 0 || D < 0) return kStatusBytes;
+    return ws_layout(B, L, D).total;
+}
+
+int64_t ssm_scan_ckpt_elems(int64_t B, int64_t L, int64_t D, int64_t N) {
+    if (B < 0 || L < 0 || D < 0 || N < 0) return 0;
+    return B * ceil_div(L, kCK) * D * N;
+}
+
+int ssm_scan_ckpt_interval(void) { return (int)kCK; }
+
+int ssm_last_launch_count(void) { return g_launches; }
+
+const char* ssm_status_string(int code) {
+    switch (code) {
+        case SSM_OK: return "ok";
+        case SSM_ERR_INVALID_ARG: return "invalid argument (null required pointer, negative size or bad flag)";
+        case SSM_ERR_UNSUPPORTED: return "unsupported (d_state must be 16; dtype must be fp32 or bf16)";
+        case SSM_ERR_ALIGNMENT: return "alignment (D must be a multiple of 8 and pointers 16-byte aligned)";
+        case SSM_ERR_WORKSPACE: return "workspace missing or smaller than ssm_scan_workspace_bytes()";
+        case SSM_ERR_CUDA: return "a CUDA call or kernel launch failed";
+        case SSM_ERR_NONFINITE: return "a kernel produced a non-finite value";
+        default: return "unknown status";
+    }
+}
+
+int ssm_clear_status(void* workspace, void* stream) {
+    if (!workspace) return SSM_ERR_INVALID_ARG;
+    return cudaMemsetAsync(workspace, 0, sizeof(unsigned), (cudaStream_t)stream) == cudaSuccess ? SSM_OK
+                                                                                                : SSM_ERR_CUDA;
+}
+
+int ssm_poll_status(void* workspace, void* stream) {
+    if (!workspace) return SSM_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    unsigned v = 0;
+    if (cudaMemcpyAsync(&v, workspace, sizeof(unsigned), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_CUDA;
+    return (v & ssm::kStatusNonFinite) ? SSM_ERR_NONFINITE : SSM_OK;
+}
+
+int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
+    g_launches = 0;
+    int rc = check_fwd(a, true);
+    if (rc != SSM_OK) return rc;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int64_t B = a->B, L = a->L, D = a->D;
+    if (B == 0 || D == 0) return SSM_OK;
+    if (L == 0) {
+        if (a->h_last) {
+            const size_t bytes = (size_t)B * D * 16 * sizeof(float);
+            cudaError_t e = a->h0 ? cudaMemcpyAsync(a->h_last, a->h0, bytes, cudaMemcpyDeviceToDevice, s)
+                                  : cudaMemsetAsync(a->h_last, 0, bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
+    const int nsplit = a->nsplit ? a->nsplit : auto_nsplit(ch);
+    int G = a->groups ? (int)std::min<int64_t>({(int64_t)a->groups, nck, gmax}) : auto_groups(ch, nsplit, L, gmax);
+    const int64_t Lg = ceil_div(nck, G) * kCK;
+    G = (int)ceil_div(L, Lg);
+    const WsLayout w = ws_layout(B, L, D);
+    char* ws = (char*)a->workspace;
+
+    FwdParams p{};
+    p.B = B; p.L = L; p.D = D; p.G = G; p.Lg = Lg;
+    p.has_z = a->z != nullptr; p.sp = a->delta_softplus;
+    p.x = a->x; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm;
+    p.dt = a->dt; p.dt_bias = a->dt_bias; p.A = a->A; p.Dskip = a->Dskip;
+    p.hstart = a->h0; p.y = a->y; p.h_last = a->h_last; p.ckpt = a->ckpt;
+    p.aggH = (float*)(ws + w.aggV); p.aggS = (float*)(ws + w.aggS);
+    p.status = (unsigned*)ws;
+    if (G > 1) {
+        if ((rc = tally(ssm::launch_fwd_agg(a->io_dtype, nsplit, p, s))) != SSM_OK) return rc;
+        if ((rc = tally(ssm::launch_carry(B, D, G, false, a->A, a->h0, p.aggH, p.aggS, (float*)(ws + w.carry), s))) !=
+            SSM_OK)
+            return rc;
+        p.hstart = (const float*)(ws + w.carry);
+    }
+    return tally(ssm::launch_fwd(a->io_dtype, nsplit, p, s));
+}
+
+int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
+    g_launches = 0;
+    if (!a) return SSM_ERR_INVALID_ARG;
+    int rc = check_fwd(&a->f, false);
+    if (rc != SSM_OK) return rc;
+    const ssm_fwd_args& f = a->f;
+    const int64_t B = f.B, L = f.L, D = f.D;
+    const bool work = B > 0 && L > 0 && D > 0;
+    if (work && (!a->dy || !a->dx || !a->d_dt || !f.ckpt || (f.z && !a->dz))) return SSM_ERR_INVALID_ARG;
+    if (D > 0 && (!a->dA || !a->dD || !a->d_dt_bias)) return SSM_ERR_INVALID_ARG;
+    if (B > 0 && L > 0 && (!a->dB || !a->dC)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->dy, a->dh_last, a->dx, a->dz, a->d_dt, a->dA, a->dD, a->d_dt_bias, a->dB, a->dC, a->dh0};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return SSM_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    // The reductions are overwritten: zero them on the stream first.
+    if (D > 0) {
+        if (cudaMemsetAsync(a->dA, 0, (size_t)D * 16 * sizeof(float), s) != cudaSuccess ||
+            cudaMemsetAsync(a->dD, 0, (size_t)D * sizeof(float), s) != cudaSuccess ||
+            cudaMemsetAsync(a->d_dt_bias, 0, (size_t)D * sizeof(float), s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (B > 0 && L > 0) {
+        const size_t bl = (size_t)B * L * 16 * sizeof(float);
+        if (cudaMemsetAsync(a->dB, 0, bl, s) != cudaSuccess || cudaMemsetAsync(a->dC, 0, bl, s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (!work) {
+        if (a->dh0 && B > 0 && D > 0) {
+            const size_t bytes = (size_t)B * D * 16 * sizeof(float);
+            cudaError_t e = a->dh_last ? cudaMemcpyAsync(a->dh0, a->dh_last, bytes, cudaMemcpyDeviceToDevice, s)
+                                       : cudaMemsetAsync(a->dh0, 0, bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
+    const int nsplit = f.nsplit ? f.nsplit : auto_nsplit(ch);
+    int G = f.groups ? (int)std::min<int64_t>({(int64_t)f.groups, nck, gmax}) : auto_groups(ch, nsplit, L, gmax);
+    const int64_t Lg = ceil_div(nck, G) * kCK;
+    G = (int)ceil_div(L, Lg);
+    const WsLayout w = ws_layout(B, L, D);
+    char* ws = (char*)f.workspace;
+
+    BwdParams p{};
+    p.B = B; p.L = L; p.D = D; p.G = G; p.Lg = Lg;
+    p.has_z = f.z != nullptr; p.sp = f.delta_softplus;
+    p.x = f.x; p.z = f.z; p.Bm = f.Bm; p.Cm = f.Cm; p.dy = a->dy;
+    p.dt = f.dt; p.dt_bias = f.dt_bias; p.A = f.A; p.Dskip = f.Dskip;
+    p.ckpt = f.ckpt; p.gstart = a->dh_last;
+    p.dx = a->dx; p.dz = a->dz; p.ddt = a->d_dt; p.dA = a->dA; p.dD = a->dD; p.ddt_bias = a->d_dt_bias;
+    p.dB = a->dB; p.dC = a->dC; p.dh0 = a->dh0;
+    p.aggQ = (float*)(ws + w.aggV); p.aggS = (float*)(ws + w.aggS);
+    p.status = (unsigned*)ws;
+    if (G > 1) {
+        if ((rc = tally(ssm::launch_bwd_agg(f.io_dtype, nsplit, p, s))) != SSM_OK) return rc;
+        if ((rc = tally(ssm::launch_carry(B, D, G, true, f.A, a->dh_last, p.aggQ, p.aggS, (float*)(ws + w.carry), s))) !=
+            SSM_OK)
+            return rc;
+        p.gstart = (const float*)(ws + w.carry);
+    }
+    return tally(ssm::launch_bwd(f.io_dtype, nsplit, p, s));
+}
+
+int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, void* stream) {
+    g_launches = 0;
+    if (n < 0) return SSM_ERR_INVALID_ARG;
+    if (n == 0) return SSM_OK;
+    if (!dA || !A || !dA_log) return SSM_ERR_INVALID_ARG;
+    const int64_t blocks = std::min<int64_t>(ceil_div(n, 256), 4096);
+    dA_log_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(dA, A, dA_log, n);
+    return tally(cudaGetLastError() == cudaSuccess ? 1 : -1);
+}
+
+int ssm_step(const ssm_step_args* a, void* stream) {
+    g_launches = 0;
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->B < 0 || a->D < 0 || a->N < 0) return SSM_ERR_INVALID_ARG;
+    if (a->N != 16) return SSM_ERR_UNSUPPORTED;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->nsplit != 0 && a->nsplit != 1 && a->nsplit != 2 && a->nsplit != 4) return SSM_ERR_INVALID_ARG;
+    if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
+    const bool work = a->B > 0 && a->D > 0;
+    if (work && (!a->x_t || !a->dt_t || !a->Bm_t || !a->Cm_t || !a->A || !a->state || !a->y_t))
+        return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->x_t, a->z_t, a->Bm_t, a->Cm_t, a->dt_t, a->dt_bias, a->A, a->Dskip, a->state, a->y_t,
+                          a->workspace};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return SSM_ERR_ALIGNMENT;
+    if (!work) return SSM_OK;
+    StepParams p{};
+    p.B = a->B; p.D = a->D;
+    p.has_z = a->z_t != nullptr; p.sp = a->delta_softplus;
+    p.x = a->x_t; p.z = a->z_t; p.Bm = a->Bm_t; p.Cm = a->Cm_t;
+    p.dt = a->dt_t; p.dt_bias = a->dt_bias; p.A = a->A; p.Dskip = a->Dskip;
+    p.state = a->state; p.y = a->y_t; p.status = (unsigned*)a->workspace;
+    const int nsplit = a->nsplit ? a->nsplit : auto_nsplit(a->B * a->D);
+    return tally(ssm::launch_step(a->io_dtype, nsplit, p, (cudaStream_t)stream));
+}
+
+}  // extern "C"

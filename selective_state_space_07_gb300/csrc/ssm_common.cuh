@@ -1,0 +1,224 @@
+// Device-side building blocks shared by the forward, backward and step
+// kernels of the S6 selective scan (sm_103a).
+//
+// Scan definition (rustytorch commit log, "MambaBlock" S6 forward commit):
+//   Delta = softplus(dt + dt_bias); a = exp(Delta*A[d,n]);
+//   h = a*h + (Delta*x)*Bm[t,n];  y = (sum_n Cm[t,n]*h + D*x) * silu(z).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ssm_internal.h"
+
+namespace ssm {
+
+constexpr int kN = 16;         // d_state supported by the kernels
+constexpr int kCK = 16;        // tokens per checkpoint = tokens per staged tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// ------------------------------------------------------------ MUFU wrappers
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------------------ I/O types
+template <typename IO> struct IOT;
+template <> struct IOT<float> {
+    // fp32 I/O: per-token helpers call CUDA's full-precision expf/log1pf and
+    // use IEEE division.
+    static constexpr bool kFast = false;
+    __device__ static float to_f(float v) { return v; }
+    __device__ static float from_f(float v) { return v; }
+};
+template <> struct IOT<__nv_bfloat16> {
+    // bf16 I/O: outputs carry 8 significant bits, so the per-token helpers
+    // use the MUFU forms (relative error ~1e-6 or better where it matters).
+    static constexpr bool kFast = true;
+    __device__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ static __nv_bfloat16 from_f(float v) { return __float2bfloat16_rn(v); }
+};
+
+// ------------------------------------------------------------ per-token math
+// softplus(v) = max(v,0) + log1p(exp(-|v|)) ("numerically-stable softplus").
+// Also returns sigmoid(v), which the backward needs for d(dt). Every
+// rounding step is explicit so that each kernel that inlines these helpers
+// gets the same bits (the compiler may not contract them differently).
+template <bool FAST>
+__device__ __forceinline__ float softplus_sig(float v, float* sig) {
+    if (FAST) {
+        const float e = ex2(__fmul_rn(-fabsf(v), kLog2e));  // exp(-|v|) in (0, 1]
+        const float w = __fadd_rn(1.0f, e);
+        if (sig) {
+            const float r = rcp(w);
+            *sig = v >= 0.0f ? r : __fmul_rn(e, r);
+        }
+        return __fmaf_rn(kLn2, lg2(w), fmaxf(v, 0.0f));
+    } else {
+        const float e = expf(-fabsf(v));
+        const float w = __fadd_rn(1.0f, e);
+        if (sig) *sig = v >= 0.0f ? __fdiv_rn(1.0f, w) : __fdiv_rn(e, w);
+        return __fadd_rn(fmaxf(v, 0.0f), log1pf(e));
+    }
+}
+template <bool FAST> __device__ __forceinline__ float softplus(float v) {
+    return softplus_sig<FAST>(v, nullptr);
+}
+// Logistic sigmoid; exp(-z) may overflow to +inf for very negative z,
+// which gives 1/inf = 0 as required.
+template <bool FAST> __device__ __forceinline__ float sigmoid(float z) {
+    if (FAST) return rcp(__fadd_rn(1.0f, ex2(__fmul_rn(-z, kLog2e))));
+    return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z)));
+}
+// Delta of one token.
+template <bool FAST>
+__device__ __forceinline__ float token_delta(float dtv, float bias, bool sp) {
+    const float v = __fadd_rn(dtv, bias);
+    return sp ? softplus<FAST>(v) : v;
+}
+
+// ------------------------------------------------------------ cp.async staging
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+    unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    int n = valid ? 16 : 0;  // 0 source bytes => the 16 destination bytes are zero-filled
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(s), "l"(gmem), "r"(n)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+// Stage a [rows x chunks*16 bytes] block whose rows are `gstride` bytes
+// apart in global memory into shared memory rows `sstride` bytes apart.
+// Rows >= valid_rows and chunks >= valid_chunks are zero-filled (their
+// global address is never formed).
+template <int NT>
+__device__ __forceinline__ void stage_block(char* sdst, int sstride, const char* gsrc, int64_t gstride,
+                                            int rows, int chunks, int valid_rows, int valid_chunks) {
+    for (int idx = threadIdx.x; idx < rows * chunks; idx += NT) {
+        const int r = idx / chunks, ch = idx - r * chunks;
+        const bool v = r < valid_rows && ch < valid_chunks;
+        const char* src = v ? gsrc + (int64_t)r * gstride + ch * 16 : gsrc;
+        cp_async16(sdst + r * sstride + ch * 16, src, v);
+    }
+}
+
+__device__ __forceinline__ void red_add_v4(float* gptr, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"l"(gptr), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+// ------------------------------------------------------------ state update
+// One token for the NS consecutive states this lane owns:
+//   h_n <- exp2(Delta*A2_n) * h_n + u*B_n,   (A2 = A*log2(e), u = Delta*x)
+template <int NS>
+__device__ __forceinline__ void token_update(float2 (&h)[NS / 2], const float2 (&A2)[NS / 2], float delta,
+                                             float u, const float* Bt) {
+    const float2 d2 = make_float2(delta, delta), u2 = make_float2(u, u);
+#pragma unroll
+    for (int q = 0; q < NS / 4; ++q) {
+        const float4 b4 = *reinterpret_cast<const float4*>(Bt + 4 * q);
+        const float2 arg0 = __fmul2_rn(d2, A2[2 * q]);
+        const float2 arg1 = __fmul2_rn(d2, A2[2 * q + 1]);
+        const float2 a0 = make_float2(ex2(arg0.x), ex2(arg0.y));
+        const float2 a1 = make_float2(ex2(arg1.x), ex2(arg1.y));
+        h[2 * q] = __ffma2_rn(a0, h[2 * q], __fmul2_rn(u2, make_float2(b4.x, b4.y)));
+        h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], __fmul2_rn(u2, make_float2(b4.z, b4.w)));
+    }
+}
+
+// The lane's partial readout sum_n C_n h_n in the CANONICAL order: states
+// are grouped in blocks of four, a block sums as (C0 h0 + C2 h2) +
+// (C1 h1 + C3 h3) with the second product of each pair fused (fma), and
+// blocks combine as a balanced tree ((blk0 + blk1) + (blk2 + blk3)). A lane
+// owning 4 / 8 / 16 states forms one / two / all four blocks; lanes then
+// combine in the same tree, so the readout is bitwise the same for every
+// lane split, in the sequence forward and in the step form.
+template <int NS>
+__device__ __forceinline__ float token_readout(const float2 (&h)[NS / 2], const float* Ct) {
+    float blk[NS / 4];
+#pragma unroll
+    for (int q = 0; q < NS / 4; ++q) {
+        const float4 c4 = *reinterpret_cast<const float4*>(Ct + 4 * q);
+        float2 acc = __fmul2_rn(make_float2(c4.x, c4.y), h[2 * q]);
+        acc = __ffma2_rn(make_float2(c4.z, c4.w), h[2 * q + 1], acc);
+        blk[q] = __fadd_rn(acc.x, acc.y);
+    }
+    if constexpr (NS == 4) return blk[0];
+    else if constexpr (NS == 8) return __fadd_rn(blk[0], blk[1]);
+    else return __fadd_rn(__fadd_rn(blk[0], blk[1]), __fadd_rn(blk[2], blk[3]));
+}
+
+template <int NS>
+__device__ __forceinline__ float token_states(float2 (&h)[NS / 2], const float2 (&A2)[NS / 2],
+                                              float delta, float u, const float* Bt, const float* Ct) {
+    static_assert(NS == 4 || NS == 8 || NS == 16, "lane owns 4, 8 or 16 states");
+    token_update<NS>(h, A2, delta, u, Bt);
+    return token_readout<NS>(h, Ct);
+}
+
+// y for one token from the channel's full readout p (lanes combined).
+template <bool FAST>
+__device__ __forceinline__ float gate_out(float p, float Dd, float xv, float zv, bool has_z) {
+    const float pp = __fmaf_rn(Dd, xv, p);
+    if (!has_z) return pp;
+    return __fmul_rn(pp, __fmul_rn(zv, sigmoid<FAST>(zv)));
+}
+
+// Combine the per-lane partial readouts of NSPLIT lanes sharing a channel
+// into the full readout of token `k` (reduce-scatter), in the canonical tree
+// ((lane0 + lane1) + (lane2 + lane3)); P[j] holds this lane's partial for
+// token j of the group.
+template <int NSPLIT>
+__device__ __forceinline__ float readout_scatter(const float (&P)[NSPLIT], int k) {
+    if constexpr (NSPLIT == 1) {
+        return P[0];
+    } else if constexpr (NSPLIT == 2) {
+        const float send = k ? P[0] : P[1];
+        const float keep = k ? P[1] : P[0];
+        return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+    } else {
+        const int k0 = k & 1, k1 = k >> 1;
+        float Q[2];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const float keep = k0 ? P[2 * m + 1] : P[2 * m];
+            const float send = k0 ? P[2 * m] : P[2 * m + 1];
+            Q[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
+        }
+        const float keep = k1 ? Q[1] : Q[0];
+        const float send = k1 ? Q[0] : Q[1];
+        return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
+    }
+}
+// Same combination, every lane receiving the full readout of one token.
+template <int NSPLIT> __device__ __forceinline__ float readout_allreduce(float P) {
+    if constexpr (NSPLIT >= 2) P = __fadd_rn(P, __shfl_xor_sync(0xffffffffu, P, 1));
+    if constexpr (NSPLIT >= 4) P = __fadd_rn(P, __shfl_xor_sync(0xffffffffu, P, 2));
+    return P;
+}
+
+__device__ __forceinline__ void flag_nonfinite(unsigned* status, float acc) {
+    // acc accumulates y*0 over the outputs: 0 unless one of them was Inf/NaN.
+    const bool bad = !(acc == 0.0f);
+    if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0 && status) atomicOr(status, kStatusNonFinite);
+}
+
+}  // namespace ssm

@@ -1,0 +1,77 @@
+// Internal declarations shared by the translation units of libssmscan.so:
+// kernel parameter blocks and the launchers ssm_api.cu calls.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ssm {
+
+constexpr unsigned kStatusNonFinite = 1u;  // workspace status bit: an output was Inf/NaN
+constexpr int kFwdThreads = 128;
+constexpr int kBwdThreads = 128;
+
+struct FwdParams {
+    int64_t B, L, D;
+    int G;          // number of L-segments ("groups") scanned in parallel
+    int64_t Lg;     // tokens per group, a multiple of 16
+    int has_z, sp;  // gate present; Delta = softplus(dt + dt_bias)
+    const void *x, *z, *Bm, *Cm;
+    const float *dt, *dt_bias, *A, *Dskip;
+    const float* hstart;  // G == 1: h0 [B,D,16] (nullable); G > 1: carries [B,G,D,16]
+    void* y;
+    float *h_last, *ckpt;
+    float *aggH, *aggS;   // chunk aggregates [B,G,D,16] and [B,G,D]
+    unsigned* status;
+};
+
+struct BwdParams {
+    int64_t B, L, D;
+    int G;
+    int64_t Lg;
+    int has_z, sp;
+    const void *x, *z, *Bm, *Cm, *dy;
+    const float *dt, *dt_bias, *A, *Dskip;
+    const float* ckpt;    // [B, ceil(L/16), D, 16]
+    const float* gstart;  // G == 1: dh_last [B,D,16] (nullable); G > 1: carries [B,G,D,16]
+    void *dx, *dz;
+    float *ddt, *dA, *dD, *ddt_bias, *dB, *dC, *dh0;
+    float *aggQ, *aggS;
+    unsigned* status;
+};
+
+struct StepParams {
+    int64_t B, D;
+    int has_z, sp;
+    const void *x, *z, *Bm, *Cm;
+    const float *dt, *dt_bias, *A, *Dskip;
+    float* state;
+    void* y;
+    unsigned* status;
+};
+
+// Raise a kernel's dynamic shared-memory limit once per device (the
+// attribute is per device; `mask` is one bit per device ordinal).
+template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long long& mask) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (mask & bit) return true;
+    if (bytes > 48 * 1024 &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    mask |= bit;
+    return true;
+}
+
+// io: 0 = fp32, 1 = bf16. Each launcher returns the number of kernels it
+// launched (>= 0) or -1 if a launch failed.
+int launch_fwd(int io, int nsplit, const FwdParams& p, cudaStream_t s);
+int launch_fwd_agg(int io, int nsplit, const FwdParams& p, cudaStream_t s);
+int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start,
+                 const float* aggV, const float* aggS, float* out, cudaStream_t s);
+int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s);
+int launch_bwd(int io, int nsplit, const BwdParams& p, cudaStream_t s);
+int launch_bwd_agg(int io, int nsplit, const BwdParams& p, cudaStream_t s);
+
+}  // namespace ssm
