@@ -1,0 +1,144 @@
+"""The C ABI boundary without a GPU: the library builds for sm_103a, exports
+every entry point include/ssm_scan.h declares, and rejects bad arguments on
+the host with the documented codes before anything is launched."""
+import ctypes
+import importlib
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, NONFINITE = 0, -1, -2, -3, -4, -5, -7
+
+
+@pytest.fixture(scope="module")
+def ssm():
+    import selective_state_space_07_gb300 as m
+    m.build()
+    return m
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(ssm_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("ssm_scan_fwd", "ssm_scan_bwd", "ssm_step", "ssm_scan_workspace_bytes", "ssm_scan_ckpt_elems",
+              "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(ssm):
+    lib = ctypes.CDLL(ssm.LIB_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    assert set(ssm.EXPORTS) == declared_functions()
+
+
+def test_library_is_built_for_sm_103a(ssm):
+    b = importlib.import_module("selective_state_space_07_gb300._builder")
+    assert "arch=compute_103a,code=sm_103a" in b.ARCH
+    assert open(ssm.LIB_PATH, "rb").read().find(b"sm_103a") >= 0
+
+
+def test_sizes(ssm):
+    assert ssm.ckpt_elems(4, 4096, 4096) == 4 * 256 * 4096 * 16
+    assert ssm.ckpt_elems(1, 17, 8) == 2 * 8 * 16
+    assert ssm.ckpt_elems(2, 0, 8) == 0
+    assert ssm.lib().ssm_scan_ckpt_interval() == 16
+    assert ssm.workspace_bytes(1, 1, 8) >= 256
+    # carries are bounded: B*D*groups <= 131072, fp32 [.., 16] x2 + sums
+    assert ssm.workspace_bytes(4, 4096, 4096) <= 256 + 131072 * 33 * 4 + 512
+    assert ssm.workspace_bytes(1, 65536, 2048) <= 256 + 131072 * 33 * 4 + 512
+
+
+def test_status_strings(ssm):
+    for code in (OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, NONFINITE, 12345):
+        assert isinstance(ssm.lib().ssm_status_string(code), bytes)
+
+
+FAKE = 1 << 20  # a 16-byte aligned address; never dereferenced: every case fails validation first
+
+
+def fwd_args(ssm, **over):
+    a = dict(B=2, L=32, D=16, N=16, io_dtype=1, delta_softplus=1, x=FAKE, z=FAKE, Bm=FAKE, Cm=FAKE, dt=FAKE,
+             dt_bias=FAKE, A=FAKE, Dskip=FAKE, h0=None, y=FAKE, h_last=None, ckpt=FAKE, workspace=FAKE,
+             workspace_bytes=1 << 30, nsplit=0, groups=0)
+    a.update(over)
+    return ssm.FwdArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(N=8), UNSUPPORTED), (dict(io_dtype=7), UNSUPPORTED), (dict(D=12), ALIGNMENT),
+    (dict(x=None), INVALID), (dict(y=None), INVALID), (dict(B=-1), INVALID), (dict(delta_softplus=2), INVALID),
+    (dict(nsplit=3), INVALID), (dict(groups=-2), INVALID), (dict(x=FAKE + 4), ALIGNMENT),
+    (dict(h0=FAKE + 8), ALIGNMENT), (dict(workspace=None), WORKSPACE), (dict(workspace_bytes=16), WORKSPACE),
+])
+def test_fwd_rejects_bad_arguments(ssm, over, code):
+    args = fwd_args(ssm, **over)
+    assert ssm.lib().ssm_scan_fwd(ctypes.byref(args), None) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dy=None), INVALID), (dict(dx=None), INVALID), (dict(dz=None), INVALID), (dict(dA=None), INVALID),
+    (dict(dB=None), INVALID), (dict(dC=FAKE + 2), ALIGNMENT), (dict(d_dt=None), INVALID),
+])
+def test_bwd_rejects_bad_arguments(ssm, over, code):
+    g = dict(dy=FAKE, dh_last=None, dx=FAKE, dz=FAKE, d_dt=FAKE, dA=FAKE, dD=FAKE, d_dt_bias=FAKE, dB=FAKE,
+             dC=FAKE, dh0=None)
+    g.update(over)
+    args = ssm.BwdArgs(f=fwd_args(ssm), **g)
+    assert ssm.lib().ssm_scan_bwd(ctypes.byref(args), None) == code
+
+
+def test_bwd_needs_the_checkpoints(ssm):
+    args = ssm.BwdArgs(f=fwd_args(ssm, ckpt=None), dy=FAKE, dx=FAKE, dz=FAKE, d_dt=FAKE, dA=FAKE, dD=FAKE,
+                       d_dt_bias=FAKE, dB=FAKE, dC=FAKE)
+    assert ssm.lib().ssm_scan_bwd(ctypes.byref(args), None) == INVALID
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(N=4), UNSUPPORTED), (dict(D=20), ALIGNMENT), (dict(state=None), INVALID), (dict(y_t=FAKE + 1), ALIGNMENT),
+    (dict(io_dtype=-1), UNSUPPORTED), (dict(nsplit=8), INVALID),
+])
+def test_step_rejects_bad_arguments(ssm, over, code):
+    a = dict(B=2, D=16, N=16, io_dtype=0, delta_softplus=1, x_t=FAKE, z_t=None, Bm_t=FAKE, Cm_t=FAKE, dt_t=FAKE,
+             dt_bias=None, A=FAKE, Dskip=None, state=FAKE, y_t=FAKE, workspace=None, nsplit=0)
+    a.update(over)
+    args = ssm.StepArgs(**a)
+    assert ssm.lib().ssm_step(ctypes.byref(args), None) == code
+
+
+def test_null_args_struct(ssm):
+    assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
+    assert ssm.lib().ssm_scan_bwd(None, None) == INVALID
+    assert ssm.lib().ssm_step(None, None) == INVALID
+
+
+def test_dA_log_rejects_bad_arguments(ssm):
+    assert ssm.lib().ssm_dA_log_grad(None, FAKE, FAKE, 4, None) == INVALID
+    assert ssm.lib().ssm_dA_log_grad(FAKE, FAKE, FAKE, -1, None) == INVALID
+    assert ssm.lib().ssm_dA_log_grad(None, None, None, 0, None) == OK
+
+
+def test_binding_refuses_cpu_tensors(ssm):
+    torch = pytest.importorskip("torch")
+    x = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError, match="CUDA"):
+        ssm.scan_fwd(x, x, torch.zeros(8, 16), torch.zeros(1, 4, 16), torch.zeros(1, 4, 16))
+
+
+def test_binding_fails_loudly_without_the_library(ssm, monkeypatch, tmp_path):
+    monkeypatch.setattr(ssm, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(ssm, "_lib", None)
+    with pytest.raises(ImportError):
+        ssm.lib()
