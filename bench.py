@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Throughput of the S6 selective scan (forward + backward) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one forward (ssm_scan_fwd) and one backward (ssm_scan_bwd) over one
+batch of the workload, inputs resident in HBM. Metric: G(token*channel)/s =
+B*L*D / (t_fwd + t_bwd) / 1e9, summed over ranks. Each pass is timed with
+CUDA events on the launching stream; L2 (129 MB) is flushed before every
+pass, outside the timed segments, and the inputs are larger than L2 anyway.
+
+Multi-GPU: one process per GPU (torchrun). Every rank runs the same workload
+as an independent replica (the scan needs no exchange between replicas);
+the job's time is the max over ranks.
+
+--impl reference times the oracle (plain sequential C++, fp32, all host
+cores) on bounded samples of the same workload, on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+from dataclasses import replace
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gen  # noqa: E402
+
+METRIC = "selective-scan fwd+bwd G(token·channel)/s on 1 GB300; % of HBM roofline"
+UNIT = "G(token·channel)/s"
+DEFAULT_WORKLOAD = "mamba1.4b-bf16"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ bytes
+def algorithmic_bytes(w, pass_):
+    """Bytes a pass must move at least once (no checkpoints, no workspace, no
+    re-reads): e = I/O element size; per token-channel, per token, fixed."""
+    e = 2 if w.io == "bf16" else 4
+    tc, bl = w.B * w.L * w.D, w.B * w.L
+    if pass_ == "fwd":   # read x, z (e), dt (4); write y (e); read Bm, Cm; A, Dskip, dt_bias
+        return tc * (3 * e + 4) + bl * 2 * w.N * e + w.D * w.N * 4 + 2 * w.D * 4
+    # bwd: read x, z, dy (e), dt (4); write dx, dz (e), d_dt (4); read Bm, Cm (e), write dB, dC (4);
+    # read A, Dskip, dt_bias; write dA, dD, d_dt_bias
+    return tc * (5 * e + 8) + bl * 2 * w.N * (e + 4) + w.D * w.N * 8 + 4 * w.D * 4
+
+
+def mufu_ops(w, pass_):
+    """Special-function-unit operations per pass (bf16 path): one exp2 per
+    (token, channel, state) plus the per-token softplus / sigmoid work."""
+    tc = w.B * w.L * w.D
+    return tc * w.N + tc * (4 if pass_ == "fwd" else 9)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback", {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "selective_state_space_07_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        ent = d.get(kernel, {}).get(workload)
+        if ent and ent.get("source_hash") == kernel_source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self):
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except Exception as ex:  # nvidia-smi missing: report no clocks
+            log("clock sampling unavailable:", ex)
+            self.proc = None
+
+    def stop(self, gpus):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(5)
+        except Exception:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    idx = int(parts[0])
+                except ValueError:
+                    continue
+                if idx in gpus:
+                    rows.append(parts)
+        os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        reasons = set()
+        for r in rows:
+            for name, val in zip(self.NAMES, r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_median": statistics.median(pw) if pw else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ dist
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def init_dist(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def visible_gpu_ids(world):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [int(v) for v in vis.split(",") if v.strip().isdigit()][:world]
+    return ids or list(range(world))
+
+
+# ------------------------------------------------------------------ cpu work
+def _row(w):
+    """Batch row 0 of the workload (the generator is indexed by position, so
+    a one-row draw equals the first row of the full draw)."""
+    return gen.make_inputs(1, w.L, w.D, w.N, io=w.io, seed=w.seed, dt_std=w.dt_std, delta_target=w.delta_target)
+
+
+def _sample(row, ds):
+    return replace(row, D=ds, x=row.x[:, :, :ds], dt=row.dt[:, :, :ds], z=row.z[:, :, :ds],
+                   dy=row.dy[:, :, :ds], A=row.A[:ds], Dskip=row.Dskip[:ds], dt_bias=row.dt_bias[:ds])
+
+
+def _oracle_step(s, cores):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.fwd(s, "f32", cores)
+    oracle.bwd(s, "f32", cores)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s=12.0):
+    """The oracle as it stands (fp32 instantiation: the plain sequential loop
+    per channel, threads over channels) timed on a bounded sample of the
+    workload: batch row 0, all tokens, the first D_s channels (D_s sized for
+    about budget_s of forward + backward), repeated up to the budget."""
+    import oracle
+    cores = oracle.hardware_threads()
+    row = _row(w)
+    ds = min(w.D, max(8, cores * 2))
+    t = _oracle_step(_sample(row, ds), cores)
+    ds = int(min(w.D, max(ds, ds * budget_s / max(t, 1e-3))) // 8 * 8)
+    s = _sample(row, ds)
+    ts = []
+    while sum(ts) < budget_s and len(ts) < 50:
+        ts.append(_oracle_step(s, cores))
+    tc = w.L * ds * len(ts)
+    return {"value": tc / sum(ts) / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"batch row 0, first {ds} of {w.D} channels, all {w.L} tokens, fp32 oracle fwd+bwd, "
+                      f"{len(ts)} repetitions, {sum(ts):.1f} s"}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    cores = oracle.hardware_threads()
+    row = _row(w)
+    # size each step so that warmup + steps fit in about 150 s
+    per_step = 150.0 / max(1, args.steps + args.warmup)
+    t = _oracle_step(_sample(row, 8), cores)
+    ds = int(min(w.D, max(8, 8 * per_step / max(t, 1e-4))) // 8 * 8)
+    s = _sample(row, ds)
+    for _ in range(args.warmup):
+        _oracle_step(s, cores)
+    ts = [_oracle_step(s, cores) for _ in range(args.steps)]
+    tc = w.L * ds
+    total = sum(ts)
+    val = tc * len(ts) / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * total / len(ts), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "D": w.D, "N": w.N, "io_dtype": w.io,
+                   "sample_per_step": f"batch row 0, first {ds} channels, all {w.L} tokens"},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: {tc} token-channels (batch row 0, first {ds} of {w.D} "
+                                   f"channels), fp32 oracle fwd+bwd on {cores} threads"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ ours
+def run_ours(args, w):
+    import torch
+    import selective_state_space_07_gb300 as ssm
+
+    rank, world, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm.build()
+
+    t0 = time.time()
+    inp = gen.workload_inputs(w.name)
+    log(f"[rank {rank}] inputs generated in {time.time() - t0:.1f}s")
+    io = torch.bfloat16 if w.io == "bf16" else torch.float32
+
+    def up(a, dtype):
+        return None if a is None else torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev, dtype)
+
+    dv = {"x": up(inp.x, io), "z": up(inp.z, io), "Bm": up(inp.Bm, io), "Cm": up(inp.Cm, io),
+          "dy": up(inp.dy, io), "dt": up(inp.dt, torch.float32), "A": up(inp.A, torch.float32),
+          "Dskip": up(inp.Dskip, torch.float32), "dt_bias": up(inp.dt_bias, torch.float32)}
+    del inp
+    ws = ssm.Workspace(w.B, w.L, w.D, dev)
+    y = torch.empty_like(dv["x"])
+    ckpt = torch.empty(ssm.ckpt_elems(w.B, w.L, w.D), dtype=torch.float32, device=dev)
+    grads = None
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    kw = dict(nsplit=args.nsplit, groups=args.groups)
+
+    def fwd():
+        ssm.scan_fwd(dv["x"], dv["dt"], dv["A"], dv["Bm"], dv["Cm"], dv["z"], dv["Dskip"], dv["dt_bias"],
+                     y=y, ckpt=ckpt, workspace=ws, **kw)
+        return ssm.last_launch_count()
+
+    def bwd():
+        nonlocal grads
+        grads = ssm.scan_bwd(dv["x"], dv["dt"], dv["A"], dv["Bm"], dv["Cm"], dv["dy"], ckpt, dv["z"],
+                             dv["Dskip"], dv["dt_bias"], out=grads, workspace=ws, **kw)
+        grads.pop("workspace", None)
+        return ssm.last_launch_count()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        flush.zero_()
+        bwd()
+    torch.cuda.synchronize()
+    if ssm.poll_status(ws) != 0:
+        raise RuntimeError("non-finite outputs during warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        e = ev[k]
+        flush.zero_()
+        e[0].record(stream)
+        launches += fwd()
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        launches += bwd()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop(set(visible_gpu_ids(world))) if rank == 0 else None
+    tf = [e[0].elapsed_time(e[1]) for e in ev]
+    tb = [e[2].elapsed_time(e[3]) for e in ev]
+    ms_f, ms_b = sum(tf) / len(tf), sum(tb) / len(tb)
+    ms_step = ms_f + ms_b
+    if dist:
+        t = torch.tensor([ms_f, ms_b, ms_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_f, ms_b, ms_step = [float(v) for v in t]
+    status = ssm.poll_status(ws)
+    tc = w.B * w.L * w.D
+    value = world * tc / (ms_step * 1e-3) / 1e9
+
+    # ---- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {k: v.detach().cpu().pin_memory() for k, v in dv.items() if v is not None}
+        e2e_steps = max(3, min(args.steps, 10))
+        res, dbuf = ssm.scan_fwd_bwd_host(host, dev)
+        torch.cuda.synchronize()
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        es.record(stream)
+        for _ in range(e2e_steps):
+            res, dbuf = ssm.scan_fwd_bwd_host(host, dev, dev_buffers=dbuf, results=res)
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = es.elapsed_time(ee) / e2e_steps
+        if dist:
+            t = torch.tensor([e2e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": round(world * tc / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in res.values()),
+               "ms_per_step": round(e2e_ms, 4)}
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind, _ = measured_peaks()
+    rf = {}
+    for name, ms in (("fwd", ms_f), ("bwd", ms_b)):
+        ab = algorithmic_bytes(w, name)
+        ach = ab / (ms * 1e-3) / 1e9
+        kern = "ssm_bwd_kernel" if name == "bwd" else "ssm_fwd_kernel"
+        rf[name] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(ach / peak, 4), "peak_kind": peak_kind, "kernel": kern,
+                    "algorithmic_bytes_per_launch": ab, "ms_per_launch": round(ms, 5),
+                    "traffic": profiled_traffic(kern, w.name),
+                    "mufu_ops_per_s": round(mufu_ops(w, name) / (ms * 1e-3), 1)}
+    dom = "bwd" if ms_b >= ms_f else "fwd"
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        try:
+            cpu = cpu_baseline(w)
+        except Exception as ex:
+            log("cpu baseline failed:", ex)
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "L": w.L, "D": w.D, "N": w.N, "io_dtype": w.io,
+                   "seed": w.seed, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (129 MB) and a 512 MiB write flushes L2 before every pass",
+                   "ms_fwd": round(ms_f, 5), "ms_bwd": round(ms_b, 5),
+                   "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
+        "roofline": rf[dom],
+        "roofline_other": rf["fwd" if dom == "bwd" else "bwd"],
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "status": status,
+        "wall_s_timed_loop": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=gen.WORKLOAD_ORDER)
+    ap.add_argument("--nsplit", type=int, default=0, help="lanes per channel (0 = library's choice)")
+    ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
