@@ -58,7 +58,8 @@ enum {
     SSM_ERR_ALIGNMENT = -3,   /* D % 8 != 0 or a pointer not 16-byte aligned */
     SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
-    SSM_ERR_NONFINITE = -7    /* (ssm_poll_status) a kernel produced Inf/NaN */
+    SSM_ERR_NONFINITE = -7,   /* (ssm_poll_status) a kernel produced Inf/NaN */
+    SSM_ERR_SCRATCH_LIMIT = -8 /* (ssm_scan_fwd_noalloc) carries exceed the built-in 8 MiB array */
 };
 
 /* Forward over a whole sequence.
@@ -153,6 +154,22 @@ typedef struct {
 int ssm_scan_fwd(const ssm_fwd_args* args, void* stream);
 int ssm_scan_bwd(const ssm_bwd_args* args, void* stream);
 int ssm_step(const ssm_step_args* args, void* stream);
+
+/* The paper has no counterpart to this entry point. It is ssm_scan_fwd for
+ * callers that cannot allocate device memory (code running inside an
+ * allocator or memory-pool callback, a process whose device memory another
+ * component plans in full, a plug-in handed only its input and output
+ * tensors): the chunk carries along L, which ssm_scan_fwd keeps in the
+ * caller's workspace, live in an 8 MiB array compiled into the library,
+ * reserved on every GPU that loads it until the process exits. Nothing is
+ * allocated. Arguments and results are those of ssm_scan_fwd, except:
+ * workspace is optional and, when given (>= 256 bytes), only receives the
+ * status word; groups == 0 picks at most the L-groups whose carries fit the
+ * array; an explicit groups that does not fit returns SSM_ERR_SCRATCH_LIMIT
+ * before anything runs. The first call on a device looks up the array's
+ * address; make it before any stream capture. All calls share the array:
+ * calls that overlap on the GPU race and must be serialised. */
+int ssm_scan_fwd_noalloc(const ssm_fwd_args* args, void* stream);
 
 /* Gradient of A_log for A = -exp(A_log) (the analytic-VJP commit: "A_log
  * (via A=-exp(A_log) => dA_log = dA.A)"): dA_log[i] = dA[i] * A[i] for

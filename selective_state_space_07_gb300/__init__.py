@@ -71,6 +71,7 @@ class StepArgs(ctypes.Structure):
 EXPORTS = {
     "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_scan_fwd_noalloc": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_step": ([ctypes.POINTER(StepArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_workspace_bytes": ([ctypes.c_int64] * 4, ctypes.c_size_t),
     "ssm_scan_ckpt_elems": ([ctypes.c_int64] * 4, ctypes.c_int64),

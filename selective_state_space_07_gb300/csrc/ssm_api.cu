@@ -123,6 +123,8 @@ const char* ssm_status_string(int code) {
         case SSM_ERR_WORKSPACE: return "workspace missing or smaller than ssm_scan_workspace_bytes()";
         case SSM_ERR_CUDA: return "a CUDA call or kernel launch failed";
         case SSM_ERR_NONFINITE: return "a kernel produced a non-finite value";
+        case SSM_ERR_SCRATCH_LIMIT:
+            return "the requested L-groups need more scratch than the library's built-in 8 MiB array holds";
         default: return "unknown status";
     }
 }
