@@ -225,7 +225,9 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
         return SSM_OK;
     }
     const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
-    const int nsplit = f.nsplit ? f.nsplit : auto_nsplit(ch);
+    // the reverse pass keeps 16-token trajectories per state in registers:
+    // two lanes per channel balance its register file against parallelism
+    const int nsplit = f.nsplit ? f.nsplit : (ch >= 65536 ? 1 : 2);
     int G = f.groups ? (int)std::min<int64_t>({(int64_t)f.groups, nck, gmax}) : auto_groups(ch, nsplit, L, gmax);
     const int64_t Lg = ceil_div(nck, G) * kCK;
     G = (int)ceil_div(L, Lg);

@@ -34,6 +34,11 @@ template <typename IO, int NSPLIT> struct BwdLayout {
     static constexpr int CH = NT / NSPLIT;
     static constexpr int NS = kN / NSPLIT;
     static constexpr int ES = sizeof(IO);
+    // tokens per recompute pass: the whole 16-token sub-chunk, or (with 4
+    // lanes per channel, where registers are capped at 128) two halves
+    static constexpr int HALF = NSPLIT >= 4 ? kCK / 2 : kCK;
+    static constexpr int NH = kCK / HALF;                      // passes per sub-chunk
+    static constexpr int SPR = kCK / HALF;                     // states per transpose reduction
     static constexpr int XROW = CH * ES + 16;
     static constexpr int DTROW = CH * 4 + 16;
     static constexpr int BCROW = kN * ES;
@@ -45,39 +50,43 @@ template <typename IO, int NSPLIT> struct BwdLayout {
     static constexpr int OFF_C = OFF_B + kCK * BCROW;
     static constexpr int OFF_H = OFF_C + kCK * BCROW;         // checkpoint tile [CH][16] fp32
     static constexpr int STAGE = OFF_H + CH * kN * 4;
-    static constexpr int OFF_BT = 2 * STAGE;                   // fp32 B^T [16 states][16 tokens]
-    static constexpr int OFF_CT = OFF_BT + kN * kCK * 4;       // fp32 C^T
+    static constexpr int OFF_T = 2 * STAGE;                    // per-token [5][16 tokens][CH] fp32
+    static constexpr int NTOK = 5;                             // Delta, u, dp, sigmoid(v), dy*silu'(z)
+    static constexpr int SMEM = OFF_T + NTOK * kCK * CH * 4;   // dynamic shared memory
     static constexpr int WROW = 36;                            // floats per lane row of the transpose buffer
-    static constexpr int OFF_W = OFF_CT + kN * kCK * 4;        // [NW][32][WROW]
-    static constexpr int OFF_O = OFF_W + NW * 32 * WROW * 4;   // [NW][2][16 states][16 tokens]
-    static constexpr int SMEM = OFF_O + NW * 2 * kN * kCK * 4;
+    static constexpr int WFLOATS = NW * 32 * WROW;
+    static constexpr int SFLOATS = 3 * HALF * CH * NSPLIT;     // lane partial state sums [3][8][CH][NSPLIT]
+    static constexpr int UFLOATS = WFLOATS > SFLOATS ? WFLOATS : SFLOATS;
+    static constexpr int MINB = NSPLIT == 4 ? 4 : (NSPLIT == 2 ? 2 : 1);
 };
 
-template <int NSPLIT> __device__ __forceinline__ float pick(const float (&a)[kCK], int m, int k) {
-    // a[NSPLIT*m + k] with m static and k the lane's part index
-    if constexpr (NSPLIT == 1) return a[m];
-    else if constexpr (NSPLIT == 2) return k ? a[2 * m + 1] : a[2 * m];
-    else {
-        const float lo = (k & 1) ? a[4 * m + 1] : a[4 * m];
-        const float hi = (k & 1) ? a[4 * m + 3] : a[4 * m + 2];
-        return (k & 2) ? hi : lo;
-    }
-}
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// One CTA: CH channels of one batch row over one L-group; lane k of a
+// channel owns states k, k+NSPLIT, ... Each 16-token sub-chunk (walked from
+// last to first) is processed in NH passes of HALF tokens, last pass first:
+//   A  per (token, channel): Delta, u, dp, sigmoid(v), dy*silu'(z); B/C^T
+//   P1 (two passes only) per lane: each state's forward over the first half
+//      from the checkpoint, giving the state at the middle of the sub-chunk
+//   C  per pass, per state: forward over the pass (a, h in registers), then
+//      the reverse E_t = a_{t+1} E_{t+1} + dp_t C_t; dB/dC contributions go
+//      through a per-warp transpose every SPR states; per-token state sums
+//      accumulate in registers and leave through shared memory
+//   E  per (token, channel) of the pass: dx, dz, d(dt) in place, dD and
+//      d_dt_bias partials; dB/dC of the pass leave as vector atomics
 template <typename IO, int NSPLIT>
-__global__ void __launch_bounds__(kBwdThreads) ssm_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, BwdLayout<IO, NSPLIT>::MINB) ssm_bwd_kernel(const BwdParams p) {
     using Ly = BwdLayout<IO, NSPLIT>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, NS = Ly::NS, ES = Ly::ES;
-    constexpr int MI = kCK / NSPLIT;  // tokens whose per-token work this lane does
+    constexpr int NT = Ly::NT, CH = Ly::CH, NS = Ly::NS, ES = Ly::ES, HALF = Ly::HALF, NH = Ly::NH, SPR = Ly::SPR;
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(16) char smem[];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = tid / NSPLIT, k = tid % NSPLIT;
-    const int base = lane & ~(NSPLIT - 1);
+    const int c = tid / NSPLIT, k = tid % NSPLIT;   // scan role: channel c, states k, k+NSPLIT, ...
+    const int ce = tid % CH;                         // per-token role: channel ce
     const int64_t D = p.D, L = p.L;
-    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c;
-    const bool dv = d < D;
+    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c, de = d0 + ce;
+    const bool dv = d < D, dve = de < D;
     const int g = blockIdx.y;
     const int64_t b = blockIdx.z;
     const int64_t tb0 = (int64_t)g * p.Lg;
@@ -86,20 +95,19 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_kernel(const BwdParams p)
     const int64_t nck = (L + kCK - 1) / kCK;
     const bool has_z = p.has_z != 0, sp = p.sp != 0;
 
-    float An[NS], A2n[NS], Gc[NS], dAacc[NS];
+    float Gc[NS], dAacc[NS];
+    const float* Arow = p.A + (dv ? d : 0) * kN;
 #pragma unroll
     for (int j = 0; j < NS; ++j) {
-        const int n = k * NS + j;
-        An[j] = dv ? p.A[d * kN + n] : 0.f;
-        A2n[j] = __fmul_rn(An[j], kLog2e);
+        const int n = k + NSPLIT * j;
         float gi = 0.f;
         if (dv && p.gstart)
             gi = p.G == 1 ? p.gstart[(b * D + d) * kN + n] : p.gstart[((b * p.G + g) * D + d) * kN + n];
         Gc[j] = gi;
         dAacc[j] = 0.f;
     }
-    const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
-    const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
+    const float Dde = (dve && p.Dskip) ? p.Dskip[de] : 0.f;
+    const float biase = (dve && p.dt_bias) ? p.dt_bias[de] : 0.f;
     float dDacc = 0.f, dbacc = 0.f, nf = 0.f;
 
     const int vchx = (int)(min64(CH, D - d0) * ES / 16);
@@ -127,10 +135,18 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_kernel(const BwdParams p)
         cp_async_commit();
     };
 
-    float* BT = reinterpret_cast<float*>(smem + Ly::OFF_BT);
-    float* CT = reinterpret_cast<float*>(smem + Ly::OFF_CT);
-    float* wb = reinterpret_cast<float*>(smem + Ly::OFF_W) + warp * 32 * Ly::WROW;
-    float* wo = reinterpret_cast<float*>(smem + Ly::OFF_O);
+    // B^T / C^T tiles, the transpose buffer (reused for the lane partial
+    // state sums), and the per-warp reduced outputs are separate shared
+    // objects so the compiler can reorder loads from one across stores to
+    // another.
+    __shared__ __align__(16) float BT[kN * kCK];                // [16 states][16 tokens]
+    __shared__ __align__(16) float CT[kN * kCK];
+    __shared__ __align__(16) float WU[Ly::UFLOATS];
+    __shared__ __align__(16) float wo[Ly::NW * 2 * kN * HALF];  // [NW][2][16 states][8 tokens]
+    float* TL = reinterpret_cast<float*>(smem + Ly::OFF_T);   // [5][16][CH]
+    float* wb = WU + warp * 32 * Ly::WROW;
+    float* SS = WU;                                            // [3][8][CH][NSPLIT]
+    constexpr int TS = kCK * CH;                              // stride between the per-token arrays
 
     if (nsub > 0) issue(nsub - 1, smem);
     for (int it = 0; it < nsub; ++it) {
@@ -143,186 +159,257 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_kernel(const BwdParams p)
             cp_async_wait<0>();
         }
         __syncthreads();
+        const int64_t t0 = tb0 + (int64_t)s * kCK;
+        const int rows = (int)min64(kCK, tb1 - t0);
+
+        // ---- A: B/C to fp32 (transposed), per-token quantities once per (token, channel)
         {
             const IO* Braw = reinterpret_cast<const IO*>(st + Ly::OFF_B);
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
             for (int i = tid; i < kCK * kN; i += NT) {
-                const int tok = i / kN, n = i % kN;  // raw is [token][state]; store [state][token]
-                BT[n * kCK + tok] = IOT<IO>::to_f(Braw[i]);
-                CT[n * kCK + tok] = IOT<IO>::to_f(Craw[i]);
-            }
-        }
-        __syncthreads();
-
-        const int64_t t0 = tb0 + (int64_t)s * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
-
-        // ---- per-token quantities: this lane prepares tokens k, k+NSPLIT, ...
-        float Dl[kCK], Ul[kCK], Pl[kCK];
-        {
-            float md[MI], mu[MI], mp[MI];
-#pragma unroll
-            for (int m = 0; m < MI; ++m) {
-                const int i = NSPLIT * m + k;
-                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + i * Ly::XROW)[c]);
-                const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + i * Ly::XROW)[c]);
-                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + i * Ly::DTROW)[c];
-                float delta = token_delta<FAST>(dtv, bias, sp);
-                float dpv = dyv;
-                if (has_z) {
-                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + i * Ly::XROW)[c]);
-                    dpv = __fmul_rn(dyv, __fmul_rn(zv, sigmoid<FAST>(zv)));
-                }
-                const bool live = i < rows;  // tokens past the end act as identity
-                md[m] = live ? delta : 0.f;
-                mu[m] = live ? __fmul_rn(delta, xv) : 0.f;
-                mp[m] = live ? dpv : 0.f;
+                const int n = i / kCK, tok = i % kCK;
+                BT[i] = IOT<IO>::to_f(Braw[tok * kN + n]);
+                CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
             }
 #pragma unroll
-            for (int i = 0; i < kCK; ++i) {
-                const int m = i / NSPLIT, src = base + i % NSPLIT;
-                Dl[i] = NSPLIT == 1 ? md[m] : __shfl_sync(0xffffffffu, md[m], src);
-                Ul[i] = NSPLIT == 1 ? mu[m] : __shfl_sync(0xffffffffu, mu[m], src);
-                Pl[i] = NSPLIT == 1 ? mp[m] : __shfl_sync(0xffffffffu, mp[m], src);
-            }
-        }
-
-        float S1[kCK], S2[kCK], S3[kCK];
-#pragma unroll
-        for (int i = 0; i < kCK; ++i) S1[i] = S2[i] = S3[i] = 0.f;
-        const float* hck = reinterpret_cast<const float*>(st + Ly::OFF_H) + c * kN;
-
-#pragma unroll
-        for (int j = 0; j < NS; ++j) {
-            const int n = k * NS + j;
-            const float* Bn = BT + n * kCK;
-            const float* Cn = CT + n * kCK;
-            const float hstart = hck[n];
-            float a[kCK], hh[kCK];
-            float hp = hstart;
-#pragma unroll
-            for (int q = 0; q < kCK / 4; ++q) {
-                const float4 b4 = *reinterpret_cast<const float4*>(Bn + 4 * q);
-                const float4 c4 = *reinterpret_cast<const float4*>(Cn + 4 * q);
-                const float bq[4] = {b4.x, b4.y, b4.z, b4.w}, cq[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int i = 4 * q + r;
-                    a[i] = ex2(__fmul_rn(Dl[i], A2n[j]));
-                    hh[i] = __fmaf_rn(a[i], hp, __fmul_rn(Ul[i], bq[r]));
-                    hp = hh[i];
-                    S3[i] = __fmaf_rn(cq[r], hh[i], S3[i]);
-                }
-            }
-            float G = Gc[j];
-#pragma unroll
-            for (int q = kCK / 4 - 1; q >= 0; --q) {
-                const float4 b4 = *reinterpret_cast<const float4*>(Bn + 4 * q);
-                const float4 c4 = *reinterpret_cast<const float4*>(Cn + 4 * q);
-                const float bq[4] = {b4.x, b4.y, b4.z, b4.w}, cq[4] = {c4.x, c4.y, c4.z, c4.w};
-                float vb[4], vc[4];
-#pragma unroll
-                for (int r = 3; r >= 0; --r) {
-                    const int i = 4 * q + r;
-                    const float Gn = __fmaf_rn(Pl[i], cq[r], G);
-                    vb[r] = __fmul_rn(Gn, Ul[i]);
-                    vc[r] = __fmul_rn(Pl[i], hh[i]);
-                    S1[i] = __fmaf_rn(Gn, bq[r], S1[i]);
-                    const float hprev = i > 0 ? hh[i - 1] : hstart;
-                    const float w = __fmul_rn(Gn, __fmul_rn(a[i], hprev));
-                    dAacc[j] = __fmaf_rn(Dl[i], w, dAacc[j]);
-                    S2[i] = __fmaf_rn(An[j], w, S2[i]);
-                    G = __fmul_rn(Gn, a[i]);
-                }
-                *reinterpret_cast<float4*>(wb + lane * Ly::WROW + 4 * q) = make_float4(vb[0], vb[1], vb[2], vb[3]);
-                *reinterpret_cast<float4*>(wb + lane * Ly::WROW + kCK + 4 * q) =
-                    make_float4(vc[0], vc[1], vc[2], vc[3]);
-            }
-            Gc[j] = G;
-            __syncwarp();
-            {
-                // Sum the transpose buffer over the channel lanes that share
-                // this state: lane = (quad qd of the 32 values, part kk, row
-                // block hpb); rows (hpb*8 + r)*NSPLIT + kk, r = 0..7.
-                const int qd = lane & 7, rest = lane >> 3, kk = rest % NSPLIT, hpb = rest / NSPLIT;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                    const int row = (hpb * 8 + r) * NSPLIT + kk;
-                    const float4 v = *reinterpret_cast<const float4*>(wb + row * Ly::WROW + 4 * qd);
-                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-                }
-#pragma unroll
-                for (int off = 8 * NSPLIT; off < 32; off <<= 1) {
-                    acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
-                    acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
-                    acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
-                    acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
-                }
-                if (hpb == 0) {
-                    const int nk = kk * NS + j, type = qd >> 2, i0 = (qd & 3) * 4;
-                    *reinterpret_cast<float4*>(wo + ((warp * 2 + type) * kN + nk) * kCK + i0) = acc;
-                }
-            }
-            __syncwarp();
-        }
-
-        // ---- per-token sums over the lane's states -> over all 16 states
-#pragma unroll
-        for (int i = 0; i < kCK; ++i) {
-            if constexpr (NSPLIT >= 2) {
-                S1[i] += __shfl_xor_sync(0xffffffffu, S1[i], 1);
-                S2[i] += __shfl_xor_sync(0xffffffffu, S2[i], 1);
-                S3[i] += __shfl_xor_sync(0xffffffffu, S3[i], 1);
-            }
-            if constexpr (NSPLIT >= 4) {
-                S1[i] += __shfl_xor_sync(0xffffffffu, S1[i], 2);
-                S2[i] += __shfl_xor_sync(0xffffffffu, S2[i], 2);
-                S3[i] += __shfl_xor_sync(0xffffffffu, S3[i], 2);
-            }
-        }
-
-        // ---- per-token outputs of this lane's tokens, written in place
-#pragma unroll
-        for (int m = 0; m < MI; ++m) {
-            const int i = NSPLIT * m + k;
-            if (i < rows) {
-                IO* xs = reinterpret_cast<IO*>(st + Ly::OFF_X + i * Ly::XROW);
-                IO* zs = reinterpret_cast<IO*>(st + Ly::OFF_Z + i * Ly::XROW);
-                IO* dys = reinterpret_cast<IO*>(st + Ly::OFF_DY + i * Ly::XROW);
-                float* dts = reinterpret_cast<float*>(st + Ly::OFF_DT + i * Ly::DTROW);
-                const float xv = IOT<IO>::to_f(xs[c]);
-                const float dyv = IOT<IO>::to_f(dys[c]);
-                float sg = 1.f;
-                const float v = __fadd_rn(dts[c], bias);
-                float delta = v;
+            for (int r = 0; r < kCK * CH / NT; ++r) {
+                const int t = tid / CH + (NT / CH) * r;
+                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[ce]);
+                const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + t * Ly::XROW)[ce]);
+                const float v = __fadd_rn(reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[ce], biase);
+                float sg = 1.f, delta = v;
                 if (sp) delta = softplus_sig<FAST>(v, &sg);
-                const float s1 = pick<NSPLIT>(S1, m, k), s2 = pick<NSPLIT>(S2, m, k), s3 = pick<NSPLIT>(S3, m, k);
-                const float pr = __fmaf_rn(Dd, xv, s3);
-                float dpv = dyv;
+                float dpv = dyv, dyds = 0.f;
                 if (has_z) {
-                    const float zv = IOT<IO>::to_f(zs[c]);
+                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[ce]);
                     const float sz = sigmoid<FAST>(zv);
                     dpv = __fmul_rn(dyv, __fmul_rn(zv, sz));
-                    const float dsilu = sz * (1.0f + zv * (1.0f - sz));
-                    const float dzv = dyv * pr * dsilu;
-                    nf = __fmaf_rn(dzv, 0.0f, nf);
-                    zs[c] = IOT<IO>::from_f(dzv);
+                    dyds = dyv * (sz * (1.0f + zv * (1.0f - sz)));
                 }
-                const float dxv = __fmaf_rn(dpv, Dd, delta * s1);
-                const float ddelta = __fmaf_rn(xv, s1, s2);
-                const float ddtv = sp ? ddelta * sg : ddelta;
-                dDacc = __fmaf_rn(dpv, xv, dDacc);
-                dbacc += ddtv;
-                nf = __fmaf_rn(dxv, 0.0f, nf);
-                nf = __fmaf_rn(ddtv, 0.0f, nf);
-                dys[c] = IOT<IO>::from_f(dxv);
-                dts[c] = ddtv;
+                const bool live = t < rows;  // tokens past the end act as identity (a = 1, no input)
+                TL[0 * TS + t * CH + ce] = live ? delta : 0.f;
+                TL[1 * TS + t * CH + ce] = live ? __fmul_rn(delta, xv) : 0.f;
+                TL[2 * TS + t * CH + ce] = live ? dpv : 0.f;
+                TL[3 * TS + t * CH + ce] = sg;
+                TL[4 * TS + t * CH + ce] = dyds;
             }
         }
         __syncthreads();
+        const float* hck = reinterpret_cast<const float*>(st + Ly::OFF_H) + c * kN;
 
-        // ---- copy dx, dz, d_dt out; dB / dC: sum the warps, one atomic per 4
+        // ---- P1: the state at the middle of the sub-chunk, per lane state
+        float hmid[NS];
+        if constexpr (NH == 2) {
+            float2 Dl[HALF / 2], Ul[HALF / 2];
+#pragma unroll
+            for (int m = 0; m < HALF / 2; ++m) {
+                Dl[m] = f2(TL[0 * TS + (2 * m) * CH + c], TL[0 * TS + (2 * m + 1) * CH + c]);
+                Ul[m] = f2(TL[1 * TS + (2 * m) * CH + c], TL[1 * TS + (2 * m + 1) * CH + c]);
+            }
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                const int n = k + NSPLIT * j;
+                const float A2 = __fmul_rn(dv ? __ldg(Arow + n) : 0.f, kLog2e);
+                const float2 A2p = f2(A2, A2);
+                float hp = hck[n];
+#pragma unroll
+                for (int q = 0; q < HALF / 4; ++q) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(BT + n * kCK + 4 * q);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int m = 2 * q + h2;
+                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
+                        const float2 arg = __fmul2_rn(Dl[m], A2p);
+                        const float2 ub = __fmul2_rn(Ul[m], bb);
+                        hp = __fmaf_rn(ex2(arg.x), hp, ub.x);
+                        hp = __fmaf_rn(ex2(arg.y), hp, ub.y);
+                    }
+                }
+                hmid[j] = hp;
+            }
+        }
+
+#pragma unroll
+        for (int half = NH - 1; half >= 0; --half) {
+            const int i0 = HALF * half;
+            float2 Dl[HALF / 2], Ul[HALF / 2], Pl[HALF / 2];
+#pragma unroll
+            for (int m = 0; m < HALF / 2; ++m) {
+                const int ta = i0 + 2 * m;
+                Dl[m] = f2(TL[0 * TS + ta * CH + c], TL[0 * TS + (ta + 1) * CH + c]);
+                Ul[m] = f2(TL[1 * TS + ta * CH + c], TL[1 * TS + (ta + 1) * CH + c]);
+                Pl[m] = f2(TL[2 * TS + ta * CH + c], TL[2 * TS + (ta + 1) * CH + c]);
+            }
+            float2 S1[HALF / 2], S2[HALF / 2], S3[HALF / 2];
+#pragma unroll
+            for (int m = 0; m < HALF / 2; ++m) S1[m] = S2[m] = S3[m] = f2(0.f, 0.f);
+
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                const int n = k + NSPLIT * j;
+                const float* Bn = BT + n * kCK + i0;
+                const float* Cn = CT + n * kCK + i0;
+                const float An = dv ? __ldg(Arow + n) : 0.f;
+                const float A2 = __fmul_rn(An, kLog2e);
+                const float2 A2p = f2(A2, A2), Ap = f2(An, An);
+                float2 a[HALF / 2], hh[HALF / 2];
+                float hp = (NH == 2 && half == 1) ? hmid[j] : hck[n];
+#pragma unroll
+                for (int q = 0; q < HALF / 4; ++q) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(Bn + 4 * q);
+                    const float4 c4 = *reinterpret_cast<const float4*>(Cn + 4 * q);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int m = 2 * q + h2;
+                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
+                        const float2 cc = h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
+                        const float2 arg = __fmul2_rn(Dl[m], A2p);
+                        a[m] = f2(ex2(arg.x), ex2(arg.y));
+                        const float2 ub = __fmul2_rn(Ul[m], bb);
+                        const float h0v = __fmaf_rn(a[m].x, hp, ub.x);
+                        const float h1v = __fmaf_rn(a[m].y, h0v, ub.y);
+                        hp = h1v;
+                        hh[m] = f2(h0v, h1v);
+                        S3[m] = __ffma2_rn(cc, hh[m], S3[m]);
+                    }
+                }
+                // adjoint E_t = a_{t+1} E_{t+1} + dp_t C_t; the carry Gc holds a_{t+1} E_{t+1}
+                float E = Gc[j];
+                float anext = 1.f;
+                float dAj = 0.f;
+                const int jj = j % SPR;
+#pragma unroll
+                for (int q = HALF / 4 - 1; q >= 0; --q) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(Bn + 4 * q);
+                    const float4 c4 = *reinterpret_cast<const float4*>(Cn + 4 * q);
+                    float2 vb[2], vc[2];
+#pragma unroll
+                    for (int h2 = 1; h2 >= 0; --h2) {
+                        const int m = 2 * q + h2;
+                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
+                        const float2 rr = __fmul2_rn(Pl[m], h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y));
+                        const float e1 = __fmaf_rn(anext, E, rr.y);
+                        const float e0 = __fmaf_rn(a[m].y, e1, rr.x);
+                        E = e0;
+                        anext = a[m].x;
+                        const float2 E2 = f2(e0, e1);
+                        vb[h2] = __fmul2_rn(E2, Ul[m]);
+                        vc[h2] = __fmul2_rn(Pl[m], hh[m]);
+                        S1[m] = __ffma2_rn(E2, bb, S1[m]);
+                        // a_t h_{t-1} = h_t - u_t B_t
+                        const float2 qv = __ffma2_rn(f2(-Ul[m].x, -Ul[m].y), bb, hh[m]);
+                        const float2 w = __fmul2_rn(E2, qv);
+                        const float2 dw = __fmul2_rn(Dl[m], w);
+                        dAj = __fadd_rn(dAj, __fadd_rn(dw.x, dw.y));
+                        S2[m] = __ffma2_rn(Ap, w, S2[m]);
+                    }
+                    // row layout per reduction group: [state jj][vb 0..HALF-1 | vc 0..HALF-1]
+                    *reinterpret_cast<float4*>(wb + lane * Ly::WROW + jj * 2 * HALF + 4 * q) =
+                        make_float4(vb[0].x, vb[0].y, vb[1].x, vb[1].y);
+                    *reinterpret_cast<float4*>(wb + lane * Ly::WROW + jj * 2 * HALF + HALF + 4 * q) =
+                        make_float4(vc[0].x, vc[0].y, vc[1].x, vc[1].y);
+                }
+                Gc[j] = __fmul_rn(anext, E);  // carried to the previous half: a_{t_first} E_{t_first}
+                dAacc[j] += dAj;
+                if (jj == SPR - 1 || j == NS - 1) {
+                    __syncwarp();
+                    // Sum the transpose buffer over the channel lanes that hold
+                    // these states: lane = (quad qd of the 32 values, part kk,
+                    // row block hpb); rows (hpb*8 + r)*NSPLIT + kk, r = 0..7.
+                    const int qd = lane & 7, rest = lane >> 3, kk = rest % NSPLIT, hpb = rest / NSPLIT;
+                    float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int row = (hpb * 8 + r) * NSPLIT + kk;
+                        const float4 v = *reinterpret_cast<const float4*>(wb + row * Ly::WROW + 4 * qd);
+                        acc0 = __fadd2_rn(acc0, f2(v.x, v.y));
+                        acc1 = __fadd2_rn(acc1, f2(v.z, v.w));
+                    }
+#pragma unroll
+                    for (int off = 8 * NSPLIT; off < 32; off <<= 1) {
+                        acc0.x += __shfl_xor_sync(0xffffffffu, acc0.x, off);
+                        acc0.y += __shfl_xor_sync(0xffffffffu, acc0.y, off);
+                        acc1.x += __shfl_xor_sync(0xffffffffu, acc1.x, off);
+                        acc1.y += __shfl_xor_sync(0xffffffffu, acc1.y, off);
+                    }
+                    const int sj = qd / (HALF / 2), type = (qd / (HALF / 4)) & 1, iq = (qd % (HALF / 4)) * 4;
+                    const int jbase = j - jj;
+                    if (hpb == 0 && jbase + sj < NS) {
+                        const int nk = kk + NSPLIT * (jbase + sj);
+                        *reinterpret_cast<float4*>(wo + ((warp * 2 + type) * kN + nk) * HALF + iq) =
+                            make_float4(acc0.x, acc0.y, acc1.x, acc1.y);
+                    }
+                    __syncwarp();
+                }
+            }
+            __syncthreads();  // every warp is done with its transpose buffer
+            // lane partial per-token state sums -> shared memory [3][8][CH][NSPLIT]
+#pragma unroll
+            for (int m = 0; m < HALF / 2; ++m) {
+                SS[((0 * HALF + 2 * m) * CH + c) * NSPLIT + k] = S1[m].x;
+                SS[((0 * HALF + 2 * m + 1) * CH + c) * NSPLIT + k] = S1[m].y;
+                SS[((1 * HALF + 2 * m) * CH + c) * NSPLIT + k] = S2[m].x;
+                SS[((1 * HALF + 2 * m + 1) * CH + c) * NSPLIT + k] = S2[m].y;
+                SS[((2 * HALF + 2 * m) * CH + c) * NSPLIT + k] = S3[m].x;
+                SS[((2 * HALF + 2 * m + 1) * CH + c) * NSPLIT + k] = S3[m].y;
+            }
+            __syncthreads();
+
+            // ---- E: per-token outputs of the half, written in place into the staged tiles
+#pragma unroll
+            for (int r = 0; r < HALF * CH / NT; ++r) {
+                const int ti = tid / CH + (NT / CH) * r;  // 0..7 within the half
+                const int t = i0 + ti;
+                if (t < rows) {
+                    IO* xs = reinterpret_cast<IO*>(st + Ly::OFF_X + t * Ly::XROW);
+                    IO* zs = reinterpret_cast<IO*>(st + Ly::OFF_Z + t * Ly::XROW);
+                    IO* dys = reinterpret_cast<IO*>(st + Ly::OFF_DY + t * Ly::XROW);
+                    float* dts = reinterpret_cast<float*>(st + Ly::OFF_DT + t * Ly::DTROW);
+                    const float xv = IOT<IO>::to_f(xs[ce]);
+                    const float delta = TL[0 * TS + t * CH + ce], dpv = TL[2 * TS + t * CH + ce];
+                    const float sg = TL[3 * TS + t * CH + ce], dyds = TL[4 * TS + t * CH + ce];
+                    float s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+                    for (int kk = 0; kk < NSPLIT; ++kk) {
+                        s1 += SS[((0 * HALF + ti) * CH + ce) * NSPLIT + kk];
+                        s2 += SS[((1 * HALF + ti) * CH + ce) * NSPLIT + kk];
+                        s3 += SS[((2 * HALF + ti) * CH + ce) * NSPLIT + kk];
+                    }
+                    if (has_z) {
+                        const float dzv = __fmaf_rn(Dde, xv, s3) * dyds;
+                        nf = __fmaf_rn(dzv, 0.0f, nf);
+                        zs[ce] = IOT<IO>::from_f(dzv);
+                    }
+                    const float dxv = __fmaf_rn(dpv, Dde, delta * s1);
+                    const float ddelta = __fmaf_rn(xv, s1, s2);
+                    const float ddtv = sp ? ddelta * sg : ddelta;
+                    dDacc = __fmaf_rn(dpv, xv, dDacc);
+                    dbacc += ddtv;
+                    nf = __fmaf_rn(dxv, 0.0f, nf);
+                    nf = __fmaf_rn(ddtv, 0.0f, nf);
+                    dys[ce] = IOT<IO>::from_f(dxv);
+                    dts[ce] = ddtv;
+                }
+            }
+            // dB / dC of the half: sum the warps, one vector atomic per 4 outputs
+            for (int o = tid; o < 2 * HALF * (kN / 4); o += NT) {
+                const int type = o / (HALF * kN / 4), rem = o % (HALF * kN / 4);
+                const int n0 = (rem / HALF) * 4, ti = rem % HALF;
+                if (i0 + ti < rows) {
+                    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int w = 0; w < Ly::NW; ++w) {
+                        const float* src = wo + ((w * 2 + type) * kN + n0) * HALF + ti;
+                        s4.x += src[0]; s4.y += src[HALF]; s4.z += src[2 * HALF]; s4.w += src[3 * HALF];
+                    }
+                    float* dst = (type == 0 ? p.dB : p.dC) + (b * L + t0 + i0 + ti) * kN + n0;
+                    red_add_v4(dst, s4);
+                }
+            }
+            __syncthreads();
+        }
+
+        // ---- copy dx, dz, d_dt out
         {
             constexpr int CHX = CH * ES / 16, CHD = CH * 4 / 16;
             for (int i = tid; i < rows * CHX; i += NT) {
@@ -342,21 +429,6 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_kernel(const BwdParams p)
                     *reinterpret_cast<int4*>((char*)p.ddt + ((b * L + t0 + r) * D + d0) * 4 + ch * 16) =
                         *reinterpret_cast<const int4*>(st + Ly::OFF_DT + r * Ly::DTROW + ch * 16);
             }
-            // 2 types x 16 tokens x 4 state-quads = 128 float4 outputs
-            for (int o = tid; o < 2 * kCK * (kN / 4); o += NT) {
-                const int type = o / (kCK * kN / 4), rem = o % (kCK * kN / 4);
-                const int i = rem / (kN / 4), n0 = (rem % (kN / 4)) * 4;
-                if (i < rows) {
-                    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int w = 0; w < Ly::NW; ++w) {
-                        const float* src = wo + ((w * 2 + type) * kN + n0) * kCK + i;
-                        s4.x += src[0]; s4.y += src[kCK]; s4.z += src[2 * kCK]; s4.w += src[3 * kCK];
-                    }
-                    float* dst = (type == 0 ? p.dB : p.dC) + (b * L + t0 + i) * kN + n0;
-                    red_add_v4(dst, s4);
-                }
-            }
         }
         __syncthreads();
     }
@@ -364,23 +436,15 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_kernel(const BwdParams p)
     // ---- reductions over the group
     if (dv) {
 #pragma unroll
-        for (int j = 0; j < NS; ++j) atomicAdd(p.dA + d * kN + k * NS + j, dAacc[j]);
+        for (int j = 0; j < NS; ++j) atomicAdd(p.dA + d * kN + k + NSPLIT * j, dAacc[j]);
         if (g == 0 && p.dh0) {
 #pragma unroll
-            for (int j = 0; j < NS; ++j) p.dh0[(b * D + d) * kN + k * NS + j] = Gc[j];
+            for (int j = 0; j < NS; ++j) p.dh0[(b * D + d) * kN + k + NSPLIT * j] = Gc[j];
         }
     }
-    if constexpr (NSPLIT >= 2) {
-        dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 1);
-        dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 1);
-    }
-    if constexpr (NSPLIT >= 4) {
-        dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 2);
-        dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 2);
-    }
-    if (dv && k == 0) {
-        atomicAdd(p.dD + d, dDacc);
-        atomicAdd(p.ddt_bias + d, dbacc);
+    if (dve) {
+        atomicAdd(p.dD + de, dDacc);
+        atomicAdd(p.ddt_bias + de, dbacc);
     }
     flag_nonfinite(p.status, nf);
 }

@@ -37,12 +37,32 @@ template <typename IO, int NSPLIT> struct FwdLayout {
     static constexpr int OFF_B = OFF_DT + kCK * DTROW;
     static constexpr int OFF_C = OFF_B + kCK * BCROW;
     static constexpr int STAGE = OFF_C + kCK * BCROW;
-    static constexpr int OFF_BF = 2 * STAGE;                    // fp32 B tile [16][16]
-    static constexpr int OFF_CF = OFF_BF + kCK * kN * 4;        // fp32 C tile [16][16]
-    static constexpr int OFF_Y = OFF_CF + kCK * kN * 4;         // y tile [16][XROW]
-    static constexpr int SMEM = OFF_Y + kCK * XROW;
+    // cp.async pipeline depth: enough tiles in flight to cover DRAM latency
+    static constexpr int NSTAGE = STAGE <= 12 * 1024 ? 4 : 2;
+    static constexpr int SMEM = NSTAGE * STAGE;                 // staged tiles (dynamic shared memory)
 };
 
+
+// Full readout of one (token, channel) from its NSPLIT lane partials, in the
+// canonical tree ((lane0 + lane1) + (lane2 + lane3)) -- the association
+// readout_allreduce uses in the step form.
+template <int NSPLIT> __device__ __forceinline__ float combine_partials(const float* P) {
+    if constexpr (NSPLIT == 1) return P[0];
+    else if constexpr (NSPLIT == 2) {
+        const float2 v = *reinterpret_cast<const float2*>(P);
+        return __fadd_rn(v.x, v.y);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(P);
+        return __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w));
+    }
+}
+
+// One CTA: CH channels of one batch row over one L-group, 16 tokens per
+// staged tile. Per tile: (A) every thread prepares (Delta, u) and the gate
+// factor for (token, channel) pairs; (B) each lane advances its NS states
+// through the tile's tokens and leaves its partial readouts in shared
+// memory; (E) every thread combines the partials of (token, channel)
+// pairs, applies skip and gate and stages y.
 template <typename IO, int NSPLIT, bool AGG>
 __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p) {
     using Ly = FwdLayout<IO, NSPLIT>;
@@ -50,12 +70,12 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(16) char smem[];
 
-    const int tid = threadIdx.x, lane = tid & 31;
-    const int c = tid / NSPLIT, k = tid % NSPLIT;
-    const int base = lane & ~(NSPLIT - 1);
+    const int tid = threadIdx.x;
+    const int c = tid / NSPLIT, k = tid % NSPLIT;  // lane role: channel c, states [k*NS, k*NS+NS)
+    const int ce = tid % CH;                        // per-token role: channel ce
     const int64_t D = p.D, L = p.L;
-    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c;
-    const bool dv = d < D;
+    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c, de = d0 + ce;
+    const bool dv = d < D, dve = de < D;
     const int g = blockIdx.y;
     const int64_t b = blockIdx.z;
     const int64_t tb0 = (int64_t)g * p.Lg;
@@ -65,7 +85,6 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
     const bool has_z = !AGG && p.has_z;
     const bool sp = p.sp != 0;
 
-    // per-lane constants and the starting state
     float2 A2[NS / 2], h[NS / 2];
 #pragma unroll
     for (int j = 0; j < NS / 2; ++j) {
@@ -79,8 +98,8 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
         }
         h[j] = hv;
     }
-    const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
-    const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
+    const float Dde = (dve && p.Dskip) ? p.Dskip[de] : 0.f;
+    const float biase = (dve && p.dt_bias) ? p.dt_bias[de] : 0.f;
 
     const int vchx = (int)(min64(CH, D - d0) * ES / 16);  // valid 16-byte chunks per x row
     const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
@@ -103,22 +122,36 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
         cp_async_commit();
     };
 
-    float* Bf = reinterpret_cast<float*>(smem + Ly::OFF_BF);
-    float* Cf = reinterpret_cast<float*>(smem + Ly::OFF_CF);
-    char* ys = smem + Ly::OFF_Y;
+    // per-tile working arrays: each its own shared object, so the compiler
+    // knows loads from one never alias stores to another
+    __shared__ __align__(16) float Bf[kCK * kN];
+    __shared__ __align__(16) float Cf[kCK * kN];
+    __shared__ __align__(16) float2 DU[kCK * CH];
+    __shared__ __align__(16) float GZ[AGG ? 1 : kCK * CH];
+    __shared__ __align__(16) float PB[AGG ? 1 : kCK * CH * NSPLIT];
+    __shared__ __align__(16) char ys[AGG ? 16 : kCK * Ly::XROW];
     float nf = 0.f;     // Inf/NaN detector
     float ssum = 0.f;   // AGG: sum of Delta over the group
 
-    if (ntile > 0) issue(0, smem);
+    // prologue: tiles 0 .. NSTAGE-2 in flight (one commit group per tile,
+    // empty groups past the end keep the group count uniform)
+#pragma unroll
+    for (int q = 0; q < Ly::NSTAGE - 1; ++q) {
+        if (q < ntile) issue(q, smem + q * Ly::STAGE);
+        else cp_async_commit();
+    }
     for (int j = 0; j < ntile; ++j) {
-        char* st = smem + (j & 1) * Ly::STAGE;
-        if (j + 1 < ntile) {
-            issue(j + 1, smem + ((j + 1) & 1) * Ly::STAGE);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        char* st = smem + (j % Ly::NSTAGE) * Ly::STAGE;
+        {
+            const int jn = j + Ly::NSTAGE - 1;  // refill the slot tile j-1 used
+            if (jn < ntile) issue(jn, smem + (jn % Ly::NSTAGE) * Ly::STAGE);
+            else cp_async_commit();
         }
+        cp_async_wait<Ly::NSTAGE - 1>();
         __syncthreads();
+        const int64_t t0 = tb0 + (int64_t)j * kCK;
+        const int rows = (int)min64(kCK, tb1 - t0);
+        // ---- (A) per (token, channel): Delta, u, gate factor; B/C to fp32
         {
             const IO* Braw = reinterpret_cast<const IO*>(st + Ly::OFF_B);
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
@@ -126,11 +159,20 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
                 Bf[i] = IOT<IO>::to_f(Braw[i]);
                 if (!AGG) Cf[i] = IOT<IO>::to_f(Craw[i]);
             }
+#pragma unroll
+            for (int r = 0; r < kCK * CH / NT; ++r) {
+                const int t = tid / CH + (NT / CH) * r;
+                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[ce]);
+                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[ce];
+                const float delta = token_delta<FAST>(dtv, biase, sp);
+                DU[t * CH + ce] = make_float2(delta, __fmul_rn(delta, xv));
+                if (has_z) {
+                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[ce]);
+                    GZ[t * CH + ce] = __fmul_rn(zv, sigmoid<FAST>(zv));
+                }
+            }
         }
         __syncthreads();
-
-        const int64_t t0 = tb0 + (int64_t)j * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
         if (!AGG && p.ckpt && dv) {
             // state before token t0 (t0 is a multiple of 16)
             float* cp = p.ckpt + ((b * nck + t0 / kCK) * D + d) * kN + k * NS;
@@ -138,43 +180,43 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
             for (int q = 0; q < NS / 4; ++q)
                 reinterpret_cast<float4*>(cp)[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
         }
+        // ---- (B) the lane's states through the tile's tokens; partial
+        // readouts stay in registers until the tile is done
+        float Pt[kCK];
 #pragma unroll
-        for (int tb = 0; tb < kCK; tb += NSPLIT) {
-            if (tb >= rows) break;
-            const int tm = tb + k;  // the token this lane prepares
-            const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + tm * Ly::XROW)[c]);
-            const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + tm * Ly::DTROW)[c];
-            const float delta = token_delta<FAST>(dtv, bias, sp);
-            const float u = __fmul_rn(delta, xv);
-            float P[NSPLIT];
-#pragma unroll
-            for (int jj = 0; jj < NSPLIT; ++jj) {
-                const float dj = NSPLIT == 1 ? delta : __shfl_sync(0xffffffffu, delta, base + jj);
-                const float uj = NSPLIT == 1 ? u : __shfl_sync(0xffffffffu, u, base + jj);
-                P[jj] = 0.f;
-                if (tb + jj < rows) {
-                    const float* Bt = Bf + (tb + jj) * kN + k * NS;
-                    if (AGG) {
-                        token_update<NS>(h, A2, dj, uj, Bt);
-                        ssum = __fadd_rn(ssum, dj);
-                    } else {
-                        P[jj] = token_states<NS>(h, A2, dj, uj, Bt, Cf + (tb + jj) * kN + k * NS);
-                    }
-                }
-            }
-            if (!AGG) {
-                const float pr = readout_scatter<NSPLIT>(P, k);
-                if (tm < rows) {
-                    const float zv =
-                        has_z ? IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + tm * Ly::XROW)[c]) : 0.f;
-                    const float yv = gate_out<FAST>(pr, Dd, xv, zv, has_z);
-                    nf = __fmaf_rn(yv, 0.0f, nf);
-                    reinterpret_cast<IO*>(ys + tm * Ly::XROW)[c] = IOT<IO>::from_f(yv);
+        for (int t = 0; t < kCK; ++t) {
+            Pt[t] = 0.f;
+            if (t < rows) {
+                const float2 du = DU[t * CH + c];
+                const float* Bt = Bf + t * kN + k * NS;
+                if (AGG) {
+                    token_update<NS>(h, A2, du.x, du.y, Bt);
+                    ssum = __fadd_rn(ssum, du.x);
+                } else {
+                    Pt[t] = token_states<NS>(h, A2, du.x, du.y, Bt, Cf + t * kN + k * NS);
                 }
             }
         }
-        __syncthreads();
         if (!AGG) {
+#pragma unroll
+            for (int t = 0; t < kCK; ++t) PB[(t * CH + c) * NSPLIT + k] = Pt[t];
+        }
+        if (!AGG) {
+            __syncthreads();
+            // ---- (E) per (token, channel): combine partials, skip term, gate
+#pragma unroll
+            for (int r = 0; r < kCK * CH / NT; ++r) {
+                const int t = tid / CH + (NT / CH) * r;
+                if (t < rows) {
+                    const float pr = combine_partials<NSPLIT>(PB + (t * CH + ce) * NSPLIT);
+                    const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[ce]);
+                    const float pp = __fmaf_rn(Dde, xv, pr);
+                    const float yv = has_z ? __fmul_rn(pp, GZ[t * CH + ce]) : pp;
+                    nf = __fmaf_rn(yv, 0.0f, nf);
+                    reinterpret_cast<IO*>(ys + t * Ly::XROW)[ce] = IOT<IO>::from_f(yv);
+                }
+            }
+            __syncthreads();
             constexpr int CHX = CH * ES / 16;
             for (int i = tid; i < rows * CHX; i += NT) {
                 const int r = i / CHX, ch = i - r * CHX;
@@ -183,6 +225,7 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
                         *reinterpret_cast<const int4*>(ys + r * Ly::XROW + ch * 16);
             }
         }
+        __syncthreads();
     }
 
     if (AGG) {

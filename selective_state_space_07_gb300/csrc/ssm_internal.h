@@ -50,15 +50,16 @@ struct StepParams {
     unsigned* status;
 };
 
-// Raise a kernel's dynamic shared-memory limit once per device (the
-// attribute is per device; `mask` is one bit per device ordinal).
+// Set a kernel's dynamic shared-memory limit once per device (the attribute
+// is per device; `mask` is one bit per device ordinal). It is set whatever
+// the size, because static plus dynamic shared memory above 48 KB needs it
+// even when the dynamic part alone is smaller.
 template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long long& mask) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
     const unsigned long long bit = 1ull << (dev & 63);
     if (mask & bit) return true;
-    if (bytes > 48 * 1024 &&
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return false;
     mask |= bit;
     return true;
