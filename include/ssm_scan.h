@@ -25,7 +25,8 @@
  *     A, dA                               [D, N]
  *     Dskip, dt_bias, dD, d_dt_bias       [D]
  *     h0, h_last, dh_last, dh0, state     [B, D, N]
- *     ckpt                                [B, ceil(L/16), D, N]  (state before tokens 0, 16, 32, ...)
+ *     ckpt                                [B, ceil(L/8), N, D]  (state before tokens 0, 8, 16, ...;
+ *                                          state-major: one row of D channels per state)
  * - Types: x, z, Bm, Cm, y, dy, dx, dz (and the step's x_t, z_t, Bm_t, Cm_t,
  *   y_t) use the I/O dtype (SSM_F32 or SSM_BF16). Everything else is fp32.
  *   All arithmetic and the recurrent state are fp32.
@@ -66,7 +67,7 @@ enum {
  * Inputs: x, z (NULL = no gate: y = p), Bm, Cm [I/O dtype]; dt [fp32];
  *   dt_bias, Dskip (NULL = 0), A [fp32]; h0 (NULL = zero state).
  * Outputs: y [I/O dtype]; h_last (nullable) = state after token L-1;
- *   ckpt (nullable) = the state before every 16th token, which
+ *   ckpt (nullable) = the state before every 8th token, which
  *   ssm_scan_bwd needs; size ssm_scan_ckpt_elems() floats.
  * workspace: >= ssm_scan_workspace_bytes(B, L, D, N) bytes, 16-byte
  *   aligned, holding the status word and the chunk carries along L.
@@ -102,7 +103,10 @@ typedef struct {
  * over the batch).
  * f: the forward arguments of the same call (x, z, Bm, Cm, dt, dt_bias, A,
  *   Dskip, h0 are read; f.ckpt must hold what ssm_scan_fwd wrote; f.y and
- *   f.h_last are not touched). f.nsplit / f.groups choose this pass's shape.
+ *   f.h_last are not touched). f.groups sets this pass's L-groups; the
+ *   backward kernel has one lane layout (two lanes share a pair of channels,
+ *   each taking 8 of the 16 states), so f.nsplit only shapes the pass that
+ *   aggregates the reverse carries between L-groups.
  * dy [I/O dtype]; dh_last [fp32, nullable = 0].
  * Outputs, written for every element:
  *   dx, dz [I/O dtype] (dz required iff f.z != NULL); d_dt [fp32] = dLoss/d(dt);
@@ -178,9 +182,9 @@ int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, v
 
 /* Bytes of workspace a fwd or bwd call of this shape needs (>= 256). */
 size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);
-/* fp32 elements of the checkpoint buffer: B * ceil(L/16) * D * N. */
+/* fp32 elements of the checkpoint buffer: B * ceil(L/8) * N * D. */
 int64_t ssm_scan_ckpt_elems(int64_t B, int64_t L, int64_t D, int64_t N);
-/* Tokens between checkpoints (16). */
+/* Tokens between checkpoints (8). */
 int ssm_scan_ckpt_interval(void);
 /* Synchronises `stream`, reads and clears the workspace status word.
  * Returns SSM_OK, SSM_ERR_NONFINITE, or SSM_ERR_CUDA. */

@@ -31,7 +31,7 @@ __all__ = [
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libssmscan.so")
-CKPT_INTERVAL = 16
+CKPT_INTERVAL = 8
 _lock = threading.Lock()
 _lib = None
 

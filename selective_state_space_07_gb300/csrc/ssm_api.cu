@@ -15,7 +15,8 @@ using ssm::BwdParams;
 using ssm::FwdParams;
 using ssm::StepParams;
 
-constexpr int64_t kCK = 16;
+constexpr int64_t kCK = 16;   // L-groups are whole forward tiles
+constexpr int64_t kCkpt = 8;  // tokens between saved forward states
 constexpr int64_t kGroupBudget = 131072;  // cap on B*D*groups held in the carry buffers
 constexpr size_t kStatusBytes = 256;
 
@@ -58,6 +59,29 @@ int auto_groups(int64_t channels, int nsplit, int64_t L, int64_t gmax) {
     const int64_t warps = std::max<int64_t>(1, channels * nsplit / 32);
     if (warps >= 1024) return 1;
     const int64_t want = ceil_div(2048, warps);
+    return (int)std::max<int64_t>(1, std::min<int64_t>({want, ceil_div(L, kCK), gmax}));
+}
+
+// Multiprocessors of the current device (cached per device ordinal).
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    int& c = cache[dev & 63];
+    if (c == 0) {
+        int v = 0;
+        c = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 152;
+    }
+    return c;
+}
+
+// Backward L-groups: the backward kernel runs 128 channels per CTA and two
+// CTAs per SM; split L until the grid fills the SMs once (a group costs one
+// extra reverse-aggregate pass over its tokens, which is cheap next to the
+// backward itself).
+int auto_groups_bwd(int64_t B, int64_t D, int64_t L, int64_t gmax) {
+    const int64_t ctas = std::max<int64_t>(1, B * ceil_div(D, 128));
+    const int64_t want = std::max<int64_t>(1, 2 * (int64_t)sm_count() / ctas);
     return (int)std::max<int64_t>(1, std::min<int64_t>({want, ceil_div(L, kCK), gmax}));
 }
 
@@ -107,10 +131,10 @@ size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
 
 int64_t ssm_scan_ckpt_elems(int64_t B, int64_t L, int64_t D, int64_t N) {
     if (B < 0 || L < 0 || D < 0 || N < 0) return 0;
-    return B * ceil_div(L, kCK) * D * N;
+    return B * ceil_div(L, kCkpt) * D * N;
 }
 
-int ssm_scan_ckpt_interval(void) { return (int)kCK; }
+int ssm_scan_ckpt_interval(void) { return (int)kCkpt; }
 
 int ssm_last_launch_count(void) { return g_launches; }
 
@@ -225,10 +249,10 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
         return SSM_OK;
     }
     const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
-    // the reverse pass keeps 16-token trajectories per state in registers:
-    // two lanes per channel balance its register file against parallelism
-    const int nsplit = f.nsplit ? f.nsplit : (ch >= 65536 ? 1 : 2);
-    int G = f.groups ? (int)std::min<int64_t>({(int64_t)f.groups, nck, gmax}) : auto_groups(ch, nsplit, L, gmax);
+    // f.nsplit shapes only the reverse-aggregate pass here: the backward
+    // kernel has one lane layout (a lane pair per two channels)
+    const int nsplit = f.nsplit ? f.nsplit : auto_nsplit(ch);
+    int G = f.groups ? (int)std::min<int64_t>({(int64_t)f.groups, nck, gmax}) : auto_groups_bwd(B, D, L, gmax);
     const int64_t Lg = ceil_div(nck, G) * kCK;
     G = (int)ceil_div(L, Lg);
     const WsLayout w = ws_layout(B, L, D);
@@ -251,7 +275,7 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
             return rc;
         p.gstart = (const float*)(ws + w.carry);
     }
-    return tally(ssm::launch_bwd(f.io_dtype, nsplit, p, s));
+    return tally(ssm::launch_bwd(f.io_dtype, p, s));
 }
 
 int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, void* stream) {

@@ -11,16 +11,22 @@
 //   dA  += Delta_t G a_t h_{t-1}   (over b, t)      dD += dp_t x_t
 //   dB[b,t,n] += G u_t,  dC[b,t,n] += dp_t h_t      (over d)
 //
-// Work split: a CTA owns CH channels x one L-group and walks the group's
-// 16-token sub-chunks from last to first. For each sub-chunk it restarts
-// the forward from the checkpoint the forward pass saved, one state at a
-// time: the 16 values of a_t and h_t of that state live in registers, the
-// reverse recurrence runs over them at once, and the per-token sums over
-// states (sum G B, sum A G a h, sum C h) accumulate in registers. dB / dC
-// contributions go through a per-warp shared-memory transpose (channel
-// reduction), then a per-CTA sum over warps, then one vector atomic per
-// 4 outputs. dA, dD, d_dt_bias accumulate in registers over the whole
-// group and leave with one atomic each.
+// Work split. A CTA owns 128 channels x one L-group and walks the group's
+// 8-token chunks (one per saved forward state) from last to first. Lanes l
+// and l^16 of a warp share the channel pair {l, l^16}: each works on both
+// channels for half of the 16 states (8*(l>>4) ...), so its dB/dC
+// contributions are summed over two channels in registers before they leave
+// the lane. Per chunk:
+//   A  each lane computes Delta, u, dp (and sigmoid(v), dy*silu'(z)) for its
+//      own channel and swaps Delta, u, dp with its partner (shuffle);
+//   S  per state: forward from the checkpoint over the 8 tokens (a_t, h_t in
+//      registers) and the reverse recurrence over them, for both channels;
+//      per-token state sums stay in registers; dB/dC contributions go
+//      through a per-warp shared-memory transpose every 4 states, then a
+//      per-CTA sum over warps and one vector atomic per 4 outputs;
+//   E  the partners add their per-token state sums (shuffle) and each lane
+//      writes dx, dz, d(dt) of its own channel.
+// dA, dD, d_dt_bias accumulate in registers over the whole group.
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
 
@@ -28,423 +34,341 @@ namespace ssm {
 
 namespace {
 
-template <typename IO, int NSPLIT> struct BwdLayout {
+template <typename IO> struct BwdLayout {
     static constexpr int NT = kBwdThreads;
     static constexpr int NW = NT / 32;
-    static constexpr int CH = NT / NSPLIT;
-    static constexpr int NS = kN / NSPLIT;
+    static constexpr int CH = NT;                  // channels per CTA (one own channel per lane)
     static constexpr int ES = sizeof(IO);
-    // tokens per recompute pass: the whole 16-token sub-chunk, or (with 4
-    // lanes per channel, where registers are capped at 128) two halves
-    static constexpr int HALF = NSPLIT >= 4 ? kCK / 2 : kCK;
-    static constexpr int NH = kCK / HALF;                      // passes per sub-chunk
-    static constexpr int SPR = kCK / HALF;                     // states per transpose reduction
-    static constexpr int XROW = CH * ES + 16;
-    static constexpr int DTROW = CH * 4 + 16;
+    static constexpr int T = kCkpt;                // tokens per chunk
+    static constexpr int XROW = CH * ES;           // staged row of x / z / dy (bytes)
+    static constexpr int DTROW = CH * 4;
     static constexpr int BCROW = kN * ES;
+    static constexpr int HROW = CH * 4;            // one state of the checkpoint tile
     static constexpr int OFF_X = 0;
-    static constexpr int OFF_Z = OFF_X + kCK * XROW;
-    static constexpr int OFF_DY = OFF_Z + kCK * XROW;
-    static constexpr int OFF_DT = OFF_DY + kCK * XROW;
-    static constexpr int OFF_B = OFF_DT + kCK * DTROW;
-    static constexpr int OFF_C = OFF_B + kCK * BCROW;
-    static constexpr int OFF_H = OFF_C + kCK * BCROW;         // checkpoint tile [CH][16] fp32
-    static constexpr int STAGE = OFF_H + CH * kN * 4;
-    static constexpr int OFF_T = 2 * STAGE;                    // per-token [5][16 tokens][CH] fp32
-    static constexpr int NTOK = 5;                             // Delta, u, dp, sigmoid(v), dy*silu'(z)
-    static constexpr int SMEM = OFF_T + NTOK * kCK * CH * 4;   // dynamic shared memory
-    static constexpr int WROW = 36;                            // floats per lane row of the transpose buffer
-    static constexpr int WFLOATS = NW * 32 * WROW;
-    static constexpr int SFLOATS = 3 * HALF * CH * NSPLIT;     // lane partial state sums [3][8][CH][NSPLIT]
-    static constexpr int UFLOATS = WFLOATS > SFLOATS ? WFLOATS : SFLOATS;
-    static constexpr int MINB = NSPLIT == 4 ? 4 : (NSPLIT == 2 ? 2 : 1);
+    static constexpr int OFF_Z = OFF_X + T * XROW;
+    static constexpr int OFF_DY = OFF_Z + T * XROW;
+    static constexpr int OFF_DT = OFF_DY + T * XROW;
+    static constexpr int OFF_B = OFF_DT + T * DTROW;
+    static constexpr int OFF_C = OFF_B + T * BCROW;
+    static constexpr int OFF_H = OFF_C + T * BCROW;
+    static constexpr int STAGE = OFF_H + kN * HROW;
+    static constexpr int NSTAGE = 2;
+    // transpose buffer: per lane a row [4 states][dB | dC][T tokens] plus 4
+    // floats of padding (row stride 68 floats: conflict-free 16-byte stores
+    // down a column and 16-byte loads along a row)
+    static constexpr int SPB = 4;                  // states per transpose
+    static constexpr int TBROW = SPB * 2 * T + 4;
+    static constexpr int OFF_TB = NSTAGE * STAGE;
+    static constexpr int SMEM = OFF_TB + NW * 32 * TBROW * 4;
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
-// One CTA: CH channels of one batch row over one L-group; lane k of a
-// channel owns states k, k+NSPLIT, ... Each 16-token sub-chunk (walked from
-// last to first) is processed in NH passes of HALF tokens, last pass first:
-//   A  per (token, channel): Delta, u, dp, sigmoid(v), dy*silu'(z); B/C^T
-//   P1 (two passes only) per lane: each state's forward over the first half
-//      from the checkpoint, giving the state at the middle of the sub-chunk
-//   C  per pass, per state: forward over the pass (a, h in registers), then
-//      the reverse E_t = a_{t+1} E_{t+1} + dp_t C_t; dB/dC contributions go
-//      through a per-warp transpose every SPR states; per-token state sums
-//      accumulate in registers and leave through shared memory
-//   E  per (token, channel) of the pass: dx, dz, d(dt) in place, dD and
-//      d_dt_bias partials; dB/dC of the pass leave as vector atomics
-template <typename IO, int NSPLIT>
-__global__ void __launch_bounds__(kBwdThreads, BwdLayout<IO, NSPLIT>::MINB) ssm_bwd_kernel(const BwdParams p) {
-    using Ly = BwdLayout<IO, NSPLIT>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, NS = Ly::NS, ES = Ly::ES, HALF = Ly::HALF, NH = Ly::NH, SPR = Ly::SPR;
+template <typename IO>
+__global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams p) {
+    using Ly = BwdLayout<IO>;
+    constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = Ly::T, SPB = Ly::SPB;
+    constexpr int NS = kN / 2;  // states per lane
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(16) char smem[];
+    __shared__ __align__(16) float AT[kN * CH];               // A^T of the CTA's channels
+    __shared__ __align__(16) float BT[kN * T];                // B^T, C^T of the chunk (fp32)
+    __shared__ __align__(16) float CT[kN * T];
+    __shared__ __align__(16) float OB[Ly::NW * 2 * T * kN];  // per-warp dB/dC [warp][dB|dC][token][state]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int c = tid / NSPLIT, k = tid % NSPLIT;   // scan role: channel c, states k, k+NSPLIT, ...
-    const int ce = tid % CH;                         // per-token role: channel ce
+    const int hk = lane >> 4;                   // states 8*hk .. 8*hk+7
+    const int cO = tid;                         // own channel (slot 0)
+    const int cP = (warp << 5) + (lane ^ 16);   // partner's channel (slot 1)
     const int64_t D = p.D, L = p.L;
-    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c, de = d0 + ce;
-    const bool dv = d < D, dve = de < D;
+    const int64_t d0 = (int64_t)blockIdx.x * CH;
+    const int64_t dO = d0 + cO, dP = d0 + cP;
+    const bool vO = dO < D, vP = dP < D;
     const int g = blockIdx.y;
     const int64_t b = blockIdx.z;
     const int64_t tb0 = (int64_t)g * p.Lg;
     const int64_t tb1 = min64(L, tb0 + p.Lg);
-    const int nsub = (int)((tb1 - tb0 + kCK - 1) / kCK);
-    const int64_t nck = (L + kCK - 1) / kCK;
+    const int nsub = (int)((tb1 - tb0 + T - 1) / T);
+    const int64_t nck = (L + T - 1) / T;
     const bool has_z = p.has_z != 0, sp = p.sp != 0;
+    float* TB = reinterpret_cast<float*>(smem + Ly::OFF_TB) + warp * 32 * Ly::TBROW;
 
-    float Gc[NS], dAacc[NS];
-    const float* Arow = p.A + (dv ? d : 0) * kN;
-#pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        const int n = k + NSPLIT * j;
-        float gi = 0.f;
-        if (dv && p.gstart)
-            gi = p.G == 1 ? p.gstart[(b * D + d) * kN + n] : p.gstart[((b * p.G + g) * D + d) * kN + n];
-        Gc[j] = gi;
-        dAacc[j] = 0.f;
+    for (int i = tid; i < kN * CH; i += NT) {
+        const int n = i / CH, c = i - n * CH;
+        AT[i] = d0 + c < D ? p.A[(d0 + c) * kN + n] : 0.f;
     }
-    const float Dde = (dve && p.Dskip) ? p.Dskip[de] : 0.f;
-    const float biase = (dve && p.dt_bias) ? p.dt_bias[de] : 0.f;
+    float Gc[2][NS], dA[2][NS];
+#pragma unroll
+    for (int s = 0; s < NS; ++s) {
+        const int n = NS * hk + s;
+        float g0 = 0.f, g1 = 0.f;
+        if (p.gstart) {
+            const int64_t base = p.G == 1 ? b * D : (b * p.G + g) * D;
+            if (vO) g0 = p.gstart[(base + dO) * kN + n];
+            if (vP) g1 = p.gstart[(base + dP) * kN + n];
+        }
+        Gc[0][s] = g0;
+        Gc[1][s] = g1;
+        dA[0][s] = dA[1][s] = 0.f;
+    }
+    const float Dd = (vO && p.Dskip) ? p.Dskip[dO] : 0.f;
+    const float bias = (vO && p.dt_bias) ? p.dt_bias[dO] : 0.f;
     float dDacc = 0.f, dbacc = 0.f, nf = 0.f;
 
     const int vchx = (int)(min64(CH, D - d0) * ES / 16);
     const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
-    const int vchh = (int)(min64(CH, D - d0) * kN * 4 / 16);
     auto issue = [&](int s, char* st) {
-        const int64_t t0 = tb0 + (int64_t)s * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
+        const int64_t t0 = tb0 + (int64_t)s * T;
+        const int rows = (int)min64(T, tb1 - t0);
         const int64_t row0 = b * L + t0;
-        stage_block<NT>(st + Ly::OFF_X, Ly::XROW, (const char*)p.x + (row0 * D + d0) * ES, D * ES, kCK,
-                        CH * ES / 16, rows, vchx);
+        stage_block<NT>(st + Ly::OFF_X, Ly::XROW, (const char*)p.x + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
+                        rows, vchx);
         if (has_z)
-            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, kCK,
+            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, T,
                             CH * ES / 16, rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DY, Ly::XROW, (const char*)p.dy + (row0 * D + d0) * ES, D * ES, kCK,
-                        CH * ES / 16, rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, kCK,
-                        CH * 4 / 16, rows, vchd);
-        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * kN * ES, kN * ES, kCK,
-                        Ly::BCROW / 16, rows, Ly::BCROW / 16);
-        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, kCK,
-                        Ly::BCROW / 16, rows, Ly::BCROW / 16);
-        stage_block<NT>(st + Ly::OFF_H, CH * kN * 4, (const char*)(p.ckpt + ((b * nck + t0 / kCK) * D + d0) * kN),
-                        CH * kN * 4, 1, CH * kN * 4 / 16, 1, vchh);
+        stage_block<NT>(st + Ly::OFF_DY, Ly::XROW, (const char*)p.dy + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
+                        rows, vchx);
+        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
+                        rows, vchd);
+        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+                        rows, Ly::BCROW / 16);
+        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+                        rows, Ly::BCROW / 16);
+        // checkpoint tile: the 16 state rows [n][d0 .. d0+CH) of chunk t0/T
+        stage_block<NT>(st + Ly::OFF_H, Ly::HROW, (const char*)(p.ckpt + ((b * nck + t0 / T) * kN) * D + d0),
+                        D * 4, kN, CH * 4 / 16, kN, vchd);
         cp_async_commit();
     };
 
-    // B^T / C^T tiles, the transpose buffer (reused for the lane partial
-    // state sums), and the per-warp reduced outputs are separate shared
-    // objects so the compiler can reorder loads from one across stores to
-    // another.
-    __shared__ __align__(16) float BT[kN * kCK];                // [16 states][16 tokens]
-    __shared__ __align__(16) float CT[kN * kCK];
-    __shared__ __align__(16) float WU[Ly::UFLOATS];
-    __shared__ __align__(16) float wo[Ly::NW * 2 * kN * HALF];  // [NW][2][16 states][8 tokens]
-    float* TL = reinterpret_cast<float*>(smem + Ly::OFF_T);   // [5][16][CH]
-    float* wb = WU + warp * 32 * Ly::WROW;
-    float* SS = WU;                                            // [3][8][CH][NSPLIT]
-    constexpr int TS = kCK * CH;                              // stride between the per-token arrays
-
     if (nsub > 0) issue(nsub - 1, smem);
     for (int it = 0; it < nsub; ++it) {
-        const int s = nsub - 1 - it;
+        const int s_ = nsub - 1 - it;
         char* st = smem + (it & 1) * Ly::STAGE;
-        if (s > 0) {
-            issue(s - 1, smem + ((it + 1) & 1) * Ly::STAGE);
+        if (s_ > 0) {
+            issue(s_ - 1, smem + ((it + 1) & 1) * Ly::STAGE);
             cp_async_wait<1>();
         } else {
             cp_async_wait<0>();
         }
         __syncthreads();
-        const int64_t t0 = tb0 + (int64_t)s * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
-
-        // ---- A: B/C to fp32 (transposed), per-token quantities once per (token, channel)
+        const int64_t t0 = tb0 + (int64_t)s_ * T;
+        const int rows = (int)min64(T, tb1 - t0);
         {
             const IO* Braw = reinterpret_cast<const IO*>(st + Ly::OFF_B);
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
-            for (int i = tid; i < kCK * kN; i += NT) {
-                const int n = i / kCK, tok = i % kCK;
+            for (int i = tid; i < kN * T; i += NT) {
+                const int n = i / T, tok = i - n * T;
                 BT[i] = IOT<IO>::to_f(Braw[tok * kN + n]);
                 CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
             }
-#pragma unroll
-            for (int r = 0; r < kCK * CH / NT; ++r) {
-                const int t = tid / CH + (NT / CH) * r;
-                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[ce]);
-                const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + t * Ly::XROW)[ce]);
-                const float v = __fadd_rn(reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[ce], biase);
-                float sg = 1.f, delta = v;
-                if (sp) delta = softplus_sig<FAST>(v, &sg);
-                float dpv = dyv, dyds = 0.f;
-                if (has_z) {
-                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[ce]);
-                    const float sz = sigmoid<FAST>(zv);
-                    dpv = __fmul_rn(dyv, __fmul_rn(zv, sz));
-                    dyds = dyv * (sz * (1.0f + zv * (1.0f - sz)));
-                }
-                const bool live = t < rows;  // tokens past the end act as identity (a = 1, no input)
-                TL[0 * TS + t * CH + ce] = live ? delta : 0.f;
-                TL[1 * TS + t * CH + ce] = live ? __fmul_rn(delta, xv) : 0.f;
-                TL[2 * TS + t * CH + ce] = live ? dpv : 0.f;
-                TL[3 * TS + t * CH + ce] = sg;
-                TL[4 * TS + t * CH + ce] = dyds;
-            }
-        }
-        __syncthreads();
-        const float* hck = reinterpret_cast<const float*>(st + Ly::OFF_H) + c * kN;
-
-        // ---- P1: the state at the middle of the sub-chunk, per lane state
-        float hmid[NS];
-        if constexpr (NH == 2) {
-            float2 Dl[HALF / 2], Ul[HALF / 2];
-#pragma unroll
-            for (int m = 0; m < HALF / 2; ++m) {
-                Dl[m] = f2(TL[0 * TS + (2 * m) * CH + c], TL[0 * TS + (2 * m + 1) * CH + c]);
-                Ul[m] = f2(TL[1 * TS + (2 * m) * CH + c], TL[1 * TS + (2 * m + 1) * CH + c]);
-            }
-#pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                const int n = k + NSPLIT * j;
-                const float A2 = __fmul_rn(dv ? __ldg(Arow + n) : 0.f, kLog2e);
-                const float2 A2p = f2(A2, A2);
-                float hp = hck[n];
-#pragma unroll
-                for (int q = 0; q < HALF / 4; ++q) {
-                    const float4 b4 = *reinterpret_cast<const float4*>(BT + n * kCK + 4 * q);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int m = 2 * q + h2;
-                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
-                        const float2 arg = __fmul2_rn(Dl[m], A2p);
-                        const float2 ub = __fmul2_rn(Ul[m], bb);
-                        hp = __fmaf_rn(ex2(arg.x), hp, ub.x);
-                        hp = __fmaf_rn(ex2(arg.y), hp, ub.y);
-                    }
-                }
-                hmid[j] = hp;
-            }
         }
 
+        // ---- A: per-token quantities of the own channel; tokens past the
+        // end act as identity (a = 1, no input, no adjoint input)
+        float2 Dl[2][T / 2], Ul[2][T / 2], Pl[2][T / 2];
+        float sg[T], dd[T];
 #pragma unroll
-        for (int half = NH - 1; half >= 0; --half) {
-            const int i0 = HALF * half;
-            float2 Dl[HALF / 2], Ul[HALF / 2], Pl[HALF / 2];
-#pragma unroll
-            for (int m = 0; m < HALF / 2; ++m) {
-                const int ta = i0 + 2 * m;
-                Dl[m] = f2(TL[0 * TS + ta * CH + c], TL[0 * TS + (ta + 1) * CH + c]);
-                Ul[m] = f2(TL[1 * TS + ta * CH + c], TL[1 * TS + (ta + 1) * CH + c]);
-                Pl[m] = f2(TL[2 * TS + ta * CH + c], TL[2 * TS + (ta + 1) * CH + c]);
+        for (int t = 0; t < T; ++t) {
+            const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[cO]);
+            const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + t * Ly::XROW)[cO]);
+            const float v = __fadd_rn(reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[cO], bias);
+            float sgv = 1.f, delta = v;
+            if (sp) delta = softplus_sig<FAST>(v, &sgv);
+            float dpv = dyv, dyds = 0.f;
+            if (has_z) {
+                const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[cO]);
+                const float sz = sigmoid<FAST>(zv);
+                dpv = __fmul_rn(dyv, __fmul_rn(zv, sz));
+                dyds = dyv * (sz * (1.0f + zv * (1.0f - sz)));
             }
-            float2 S1[HALF / 2], S2[HALF / 2], S3[HALF / 2];
+            const bool live = t < rows;
+            const float dl = live ? delta : 0.f, ul = live ? __fmul_rn(delta, xv) : 0.f, pl = live ? dpv : 0.f;
+            if (t & 1) {
+                Dl[0][t / 2].y = dl; Ul[0][t / 2].y = ul; Pl[0][t / 2].y = pl;
+            } else {
+                Dl[0][t / 2].x = dl; Ul[0][t / 2].x = ul; Pl[0][t / 2].x = pl;
+            }
+            sg[t] = sgv;
+            dd[t] = dyds;
+        }
 #pragma unroll
-            for (int m = 0; m < HALF / 2; ++m) S1[m] = S2[m] = S3[m] = f2(0.f, 0.f);
+        for (int m = 0; m < T / 2; ++m) {
+            Dl[1][m] = f2(__shfl_xor_sync(0xffffffffu, Dl[0][m].x, 16), __shfl_xor_sync(0xffffffffu, Dl[0][m].y, 16));
+            Ul[1][m] = f2(__shfl_xor_sync(0xffffffffu, Ul[0][m].x, 16), __shfl_xor_sync(0xffffffffu, Ul[0][m].y, 16));
+            Pl[1][m] = f2(__shfl_xor_sync(0xffffffffu, Pl[0][m].x, 16), __shfl_xor_sync(0xffffffffu, Pl[0][m].y, 16));
+        }
+        __syncthreads();  // B^T / C^T ready
+
+        // ---- S: per state, both channels; per-token state sums in registers
+        float2 S1[2][T / 2], S2[2][T / 2], S3[2][T / 2];
+#pragma unroll
+        for (int sl = 0; sl < 2; ++sl)
+#pragma unroll
+            for (int m = 0; m < T / 2; ++m) S1[sl][m] = S2[sl][m] = S3[sl][m] = f2(0.f, 0.f);
+        const float* hck = reinterpret_cast<const float*>(st + Ly::OFF_H);
 
 #pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                const int n = k + NSPLIT * j;
-                const float* Bn = BT + n * kCK + i0;
-                const float* Cn = CT + n * kCK + i0;
-                const float An = dv ? __ldg(Arow + n) : 0.f;
+        for (int s = 0; s < NS; ++s) {
+            const int n = NS * hk + s;
+            const float4 b4a = *reinterpret_cast<const float4*>(BT + n * T);
+            const float4 b4b = *reinterpret_cast<const float4*>(BT + n * T + 4);
+            const float4 c4a = *reinterpret_cast<const float4*>(CT + n * T);
+            const float4 c4b = *reinterpret_cast<const float4*>(CT + n * T + 4);
+            const float2 bb[4] = {f2(b4a.x, b4a.y), f2(b4a.z, b4a.w), f2(b4b.x, b4b.y), f2(b4b.z, b4b.w)};
+            const float2 cc[4] = {f2(c4a.x, c4a.y), f2(c4a.z, c4a.w), f2(c4b.x, c4b.y), f2(c4b.z, c4b.w)};
+            float2 vb[T / 2], vc[T / 2];
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
+                const int c = sl ? cP : cO;
+                const float An = AT[n * CH + c];
                 const float A2 = __fmul_rn(An, kLog2e);
                 const float2 A2p = f2(A2, A2), Ap = f2(An, An);
-                float2 a[HALF / 2], hh[HALF / 2];
-                float hp = (NH == 2 && half == 1) ? hmid[j] : hck[n];
+                // forward from the checkpoint over the chunk
+                float2 a[T / 2], hh[T / 2];
+                float hp = hck[n * CH + c];
 #pragma unroll
-                for (int q = 0; q < HALF / 4; ++q) {
-                    const float4 b4 = *reinterpret_cast<const float4*>(Bn + 4 * q);
-                    const float4 c4 = *reinterpret_cast<const float4*>(Cn + 4 * q);
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int m = 2 * q + h2;
-                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
-                        const float2 cc = h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
-                        const float2 arg = __fmul2_rn(Dl[m], A2p);
-                        a[m] = f2(ex2(arg.x), ex2(arg.y));
-                        const float2 ub = __fmul2_rn(Ul[m], bb);
-                        const float h0v = __fmaf_rn(a[m].x, hp, ub.x);
-                        const float h1v = __fmaf_rn(a[m].y, h0v, ub.y);
-                        hp = h1v;
-                        hh[m] = f2(h0v, h1v);
-                        S3[m] = __ffma2_rn(cc, hh[m], S3[m]);
-                    }
+                for (int m = 0; m < T / 2; ++m) {
+                    const float2 arg = __fmul2_rn(Dl[sl][m], A2p);
+                    a[m] = f2(ex2(arg.x), ex2(arg.y));
+                    const float2 ub = __fmul2_rn(Ul[sl][m], bb[m]);
+                    const float h0v = __fmaf_rn(a[m].x, hp, ub.x);
+                    const float h1v = __fmaf_rn(a[m].y, h0v, ub.y);
+                    hp = h1v;
+                    hh[m] = f2(h0v, h1v);
                 }
-                // adjoint E_t = a_{t+1} E_{t+1} + dp_t C_t; the carry Gc holds a_{t+1} E_{t+1}
-                float E = Gc[j];
-                float anext = 1.f;
-                float dAj = 0.f;
-                const int jj = j % SPR;
+                // reverse: E_t = a_{t+1} E_{t+1} + dp_t C_t, carry Gc = a_{t+1} E_{t+1}
+                float E = Gc[sl][s], anext = 1.f;
+                float2 dAp = f2(0.f, 0.f);
 #pragma unroll
-                for (int q = HALF / 4 - 1; q >= 0; --q) {
-                    const float4 b4 = *reinterpret_cast<const float4*>(Bn + 4 * q);
-                    const float4 c4 = *reinterpret_cast<const float4*>(Cn + 4 * q);
-                    float2 vb[2], vc[2];
-#pragma unroll
-                    for (int h2 = 1; h2 >= 0; --h2) {
-                        const int m = 2 * q + h2;
-                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
-                        const float2 rr = __fmul2_rn(Pl[m], h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y));
-                        const float e1 = __fmaf_rn(anext, E, rr.y);
-                        const float e0 = __fmaf_rn(a[m].y, e1, rr.x);
-                        E = e0;
-                        anext = a[m].x;
-                        const float2 E2 = f2(e0, e1);
-                        vb[h2] = __fmul2_rn(E2, Ul[m]);
-                        vc[h2] = __fmul2_rn(Pl[m], hh[m]);
-                        S1[m] = __ffma2_rn(E2, bb, S1[m]);
-                        // a_t h_{t-1} = h_t - u_t B_t
-                        const float2 qv = __ffma2_rn(f2(-Ul[m].x, -Ul[m].y), bb, hh[m]);
-                        const float2 w = __fmul2_rn(E2, qv);
-                        const float2 dw = __fmul2_rn(Dl[m], w);
-                        dAj = __fadd_rn(dAj, __fadd_rn(dw.x, dw.y));
-                        S2[m] = __ffma2_rn(Ap, w, S2[m]);
+                for (int m = T / 2 - 1; m >= 0; --m) {
+                    const float2 rr = __fmul2_rn(Pl[sl][m], cc[m]);
+                    const float e1 = __fmaf_rn(anext, E, rr.y);
+                    const float e0 = __fmaf_rn(a[m].y, e1, rr.x);
+                    E = e0;
+                    anext = a[m].x;
+                    const float2 E2 = f2(e0, e1);
+                    if (sl == 0) {
+                        vb[m] = __fmul2_rn(E2, Ul[0][m]);
+                        vc[m] = __fmul2_rn(Pl[0][m], hh[m]);
+                    } else {
+                        vb[m] = __ffma2_rn(E2, Ul[1][m], vb[m]);
+                        vc[m] = __ffma2_rn(Pl[1][m], hh[m], vc[m]);
                     }
-                    // row layout per reduction group: [state jj][vb 0..HALF-1 | vc 0..HALF-1]
-                    *reinterpret_cast<float4*>(wb + lane * Ly::WROW + jj * 2 * HALF + 4 * q) =
-                        make_float4(vb[0].x, vb[0].y, vb[1].x, vb[1].y);
-                    *reinterpret_cast<float4*>(wb + lane * Ly::WROW + jj * 2 * HALF + HALF + 4 * q) =
-                        make_float4(vc[0].x, vc[0].y, vc[1].x, vc[1].y);
+                    S1[sl][m] = __ffma2_rn(E2, bb[m], S1[sl][m]);
+                    // a_t h_{t-1} = h_t - u_t B_t
+                    const float2 q = __ffma2_rn(f2(-Ul[sl][m].x, -Ul[sl][m].y), bb[m], hh[m]);
+                    const float2 w = __fmul2_rn(E2, q);
+                    dAp = __ffma2_rn(Dl[sl][m], w, dAp);
+                    S2[sl][m] = __ffma2_rn(Ap, w, S2[sl][m]);
+                    S3[sl][m] = __ffma2_rn(cc[m], hh[m], S3[sl][m]);
                 }
-                Gc[j] = __fmul_rn(anext, E);  // carried to the previous half: a_{t_first} E_{t_first}
-                dAacc[j] += dAj;
-                if (jj == SPR - 1 || j == NS - 1) {
-                    __syncwarp();
-                    // Sum the transpose buffer over the channel lanes that hold
-                    // these states: lane = (quad qd of the 32 values, part kk,
-                    // row block hpb); rows (hpb*8 + r)*NSPLIT + kk, r = 0..7.
-                    const int qd = lane & 7, rest = lane >> 3, kk = rest % NSPLIT, hpb = rest / NSPLIT;
-                    float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const int row = (hpb * 8 + r) * NSPLIT + kk;
-                        const float4 v = *reinterpret_cast<const float4*>(wb + row * Ly::WROW + 4 * qd);
-                        acc0 = __fadd2_rn(acc0, f2(v.x, v.y));
-                        acc1 = __fadd2_rn(acc1, f2(v.z, v.w));
-                    }
-#pragma unroll
-                    for (int off = 8 * NSPLIT; off < 32; off <<= 1) {
-                        acc0.x += __shfl_xor_sync(0xffffffffu, acc0.x, off);
-                        acc0.y += __shfl_xor_sync(0xffffffffu, acc0.y, off);
-                        acc1.x += __shfl_xor_sync(0xffffffffu, acc1.x, off);
-                        acc1.y += __shfl_xor_sync(0xffffffffu, acc1.y, off);
-                    }
-                    const int sj = qd / (HALF / 2), type = (qd / (HALF / 4)) & 1, iq = (qd % (HALF / 4)) * 4;
-                    const int jbase = j - jj;
-                    if (hpb == 0 && jbase + sj < NS) {
-                        const int nk = kk + NSPLIT * (jbase + sj);
-                        *reinterpret_cast<float4*>(wo + ((warp * 2 + type) * kN + nk) * HALF + iq) =
-                            make_float4(acc0.x, acc0.y, acc1.x, acc1.y);
-                    }
-                    __syncwarp();
-                }
+                Gc[sl][s] = __fmul_rn(anext, E);
+                dA[sl][s] += __fadd_rn(dAp.x, dAp.y);
             }
-            __syncthreads();  // every warp is done with its transpose buffer
-            // lane partial per-token state sums -> shared memory [3][8][CH][NSPLIT]
+            // dB/dC contributions of this state, summed over the two channels
+            const int sb = s % SPB;
+            float* row = TB + lane * Ly::TBROW + sb * 2 * T;
+            *reinterpret_cast<float4*>(row + 0) = make_float4(vb[0].x, vb[0].y, vb[1].x, vb[1].y);
+            *reinterpret_cast<float4*>(row + 4) = make_float4(vb[2].x, vb[2].y, vb[3].x, vb[3].y);
+            *reinterpret_cast<float4*>(row + T) = make_float4(vc[0].x, vc[0].y, vc[1].x, vc[1].y);
+            *reinterpret_cast<float4*>(row + T + 4) = make_float4(vc[2].x, vc[2].y, vc[3].x, vc[3].y);
+            if (sb == SPB - 1) {
+                __syncwarp();
+                // lane (hk, o) sums its half-warp's 16 rows at column quad o:
+                // state s-3 + o/4, dB or dC by (o/2)&1, tokens 4*(o&1) .. +3
+                const int o = lane & 15;
+                const float* col = TB + (16 * hk) * Ly::TBROW + 4 * o;
+                float4 acc = *reinterpret_cast<const float4*>(col);
 #pragma unroll
-            for (int m = 0; m < HALF / 2; ++m) {
-                SS[((0 * HALF + 2 * m) * CH + c) * NSPLIT + k] = S1[m].x;
-                SS[((0 * HALF + 2 * m + 1) * CH + c) * NSPLIT + k] = S1[m].y;
-                SS[((1 * HALF + 2 * m) * CH + c) * NSPLIT + k] = S2[m].x;
-                SS[((1 * HALF + 2 * m + 1) * CH + c) * NSPLIT + k] = S2[m].y;
-                SS[((2 * HALF + 2 * m) * CH + c) * NSPLIT + k] = S3[m].x;
-                SS[((2 * HALF + 2 * m + 1) * CH + c) * NSPLIT + k] = S3[m].y;
+                for (int r = 1; r < 16; ++r) {
+                    const float4 v = *reinterpret_cast<const float4*>(col + r * Ly::TBROW);
+                    const float2 lo = __fadd2_rn(f2(acc.x, acc.y), f2(v.x, v.y));
+                    const float2 hi = __fadd2_rn(f2(acc.z, acc.w), f2(v.z, v.w));
+                    acc = make_float4(lo.x, lo.y, hi.x, hi.y);
+                }
+                const int nn = NS * hk + s - (SPB - 1) + (o >> 2), type = (o >> 1) & 1, tk = (o & 1) * 4;
+                float* ob = OB + ((warp * 2 + type) * T + tk) * kN + nn;
+                ob[0] = acc.x;
+                ob[kN] = acc.y;
+                ob[2 * kN] = acc.z;
+                ob[3 * kN] = acc.w;
+                __syncwarp();
             }
-            __syncthreads();
+        }
 
-            // ---- E: per-token outputs of the half, written in place into the staged tiles
+        // ---- E: the partners add their per-token state sums; each lane
+        // finishes its own channel
 #pragma unroll
-            for (int r = 0; r < HALF * CH / NT; ++r) {
-                const int ti = tid / CH + (NT / CH) * r;  // 0..7 within the half
-                const int t = i0 + ti;
+        for (int m = 0; m < T / 2; ++m) {
+            S1[0][m] = __fadd2_rn(S1[0][m], f2(__shfl_xor_sync(0xffffffffu, S1[1][m].x, 16),
+                                               __shfl_xor_sync(0xffffffffu, S1[1][m].y, 16)));
+            S2[0][m] = __fadd2_rn(S2[0][m], f2(__shfl_xor_sync(0xffffffffu, S2[1][m].x, 16),
+                                               __shfl_xor_sync(0xffffffffu, S2[1][m].y, 16)));
+            S3[0][m] = __fadd2_rn(S3[0][m], f2(__shfl_xor_sync(0xffffffffu, S3[1][m].x, 16),
+                                               __shfl_xor_sync(0xffffffffu, S3[1][m].y, 16)));
+        }
+        if (vO) {
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
                 if (t < rows) {
-                    IO* xs = reinterpret_cast<IO*>(st + Ly::OFF_X + t * Ly::XROW);
-                    IO* zs = reinterpret_cast<IO*>(st + Ly::OFF_Z + t * Ly::XROW);
-                    IO* dys = reinterpret_cast<IO*>(st + Ly::OFF_DY + t * Ly::XROW);
-                    float* dts = reinterpret_cast<float*>(st + Ly::OFF_DT + t * Ly::DTROW);
-                    const float xv = IOT<IO>::to_f(xs[ce]);
-                    const float delta = TL[0 * TS + t * CH + ce], dpv = TL[2 * TS + t * CH + ce];
-                    const float sg = TL[3 * TS + t * CH + ce], dyds = TL[4 * TS + t * CH + ce];
-                    float s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-                    for (int kk = 0; kk < NSPLIT; ++kk) {
-                        s1 += SS[((0 * HALF + ti) * CH + ce) * NSPLIT + kk];
-                        s2 += SS[((1 * HALF + ti) * CH + ce) * NSPLIT + kk];
-                        s3 += SS[((2 * HALF + ti) * CH + ce) * NSPLIT + kk];
-                    }
+                    const int m = t / 2;
+                    const bool odd = t & 1;
+                    const float s1 = odd ? S1[0][m].y : S1[0][m].x;
+                    const float s2 = odd ? S2[0][m].y : S2[0][m].x;
+                    const float s3 = odd ? S3[0][m].y : S3[0][m].x;
+                    const float delta = odd ? Dl[0][m].y : Dl[0][m].x;
+                    const float dpv = odd ? Pl[0][m].y : Pl[0][m].x;
+                    const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[cO]);
+                    const int64_t off = (b * L + t0 + t) * D + dO;
                     if (has_z) {
-                        const float dzv = __fmaf_rn(Dde, xv, s3) * dyds;
+                        const float dzv = __fmaf_rn(Dd, xv, s3) * dd[t];
                         nf = __fmaf_rn(dzv, 0.0f, nf);
-                        zs[ce] = IOT<IO>::from_f(dzv);
+                        reinterpret_cast<IO*>(p.dz)[off] = IOT<IO>::from_f(dzv);
                     }
-                    const float dxv = __fmaf_rn(dpv, Dde, delta * s1);
+                    const float dxv = __fmaf_rn(dpv, Dd, delta * s1);
                     const float ddelta = __fmaf_rn(xv, s1, s2);
-                    const float ddtv = sp ? ddelta * sg : ddelta;
+                    const float ddtv = sp ? ddelta * sg[t] : ddelta;
                     dDacc = __fmaf_rn(dpv, xv, dDacc);
                     dbacc += ddtv;
                     nf = __fmaf_rn(dxv, 0.0f, nf);
                     nf = __fmaf_rn(ddtv, 0.0f, nf);
-                    dys[ce] = IOT<IO>::from_f(dxv);
-                    dts[ce] = ddtv;
+                    reinterpret_cast<IO*>(p.dx)[off] = IOT<IO>::from_f(dxv);
+                    p.ddt[off] = ddtv;
                 }
             }
-            // dB / dC of the half: sum the warps, one vector atomic per 4 outputs
-            for (int o = tid; o < 2 * HALF * (kN / 4); o += NT) {
-                const int type = o / (HALF * kN / 4), rem = o % (HALF * kN / 4);
-                const int n0 = (rem / HALF) * 4, ti = rem % HALF;
-                if (i0 + ti < rows) {
-                    float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int w = 0; w < Ly::NW; ++w) {
-                        const float* src = wo + ((w * 2 + type) * kN + n0) * HALF + ti;
-                        s4.x += src[0]; s4.y += src[HALF]; s4.z += src[2 * HALF]; s4.w += src[3 * HALF];
-                    }
-                    float* dst = (type == 0 ? p.dB : p.dC) + (b * L + t0 + i0 + ti) * kN + n0;
-                    red_add_v4(dst, s4);
-                }
-            }
-            __syncthreads();
         }
-
-        // ---- copy dx, dz, d_dt out
-        {
-            constexpr int CHX = CH * ES / 16, CHD = CH * 4 / 16;
-            for (int i = tid; i < rows * CHX; i += NT) {
-                const int r = i / CHX, ch = i - r * CHX;
-                if (ch < vchx) {
-                    const int64_t off = ((b * L + t0 + r) * D + d0) * ES + ch * 16;
-                    *reinterpret_cast<int4*>((char*)p.dx + off) =
-                        *reinterpret_cast<const int4*>(st + Ly::OFF_DY + r * Ly::XROW + ch * 16);
-                    if (has_z)
-                        *reinterpret_cast<int4*>((char*)p.dz + off) =
-                            *reinterpret_cast<const int4*>(st + Ly::OFF_Z + r * Ly::XROW + ch * 16);
+        __syncthreads();  // every warp's dB/dC rows are in OB
+        // dB / dC of the chunk: sum the warps, one vector atomic per 4 outputs
+        if (tid < 2 * T * (kN / 4)) {
+            const int type = tid / (T * kN / 4), rem = tid % (T * kN / 4);
+            const int tk = rem / (kN / 4), n0 = (rem % (kN / 4)) * 4;
+            if (tk < rows) {
+                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int w = 0; w < Ly::NW; ++w) {
+                    const float4 v = *reinterpret_cast<const float4*>(OB + ((w * 2 + type) * T + tk) * kN + n0);
+                    s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
                 }
-            }
-            for (int i = tid; i < rows * CHD; i += NT) {
-                const int r = i / CHD, ch = i - r * CHD;
-                if (ch < vchd)
-                    *reinterpret_cast<int4*>((char*)p.ddt + ((b * L + t0 + r) * D + d0) * 4 + ch * 16) =
-                        *reinterpret_cast<const int4*>(st + Ly::OFF_DT + r * Ly::DTROW + ch * 16);
+                red_add_v4((type == 0 ? p.dB : p.dC) + (b * L + t0 + tk) * kN + n0, s4);
             }
         }
         __syncthreads();
     }
 
     // ---- reductions over the group
-    if (dv) {
 #pragma unroll
-        for (int j = 0; j < NS; ++j) atomicAdd(p.dA + d * kN + k + NSPLIT * j, dAacc[j]);
+    for (int s = 0; s < NS; ++s) {
+        const int n = NS * hk + s;
+        if (vO) atomicAdd(p.dA + dO * kN + n, dA[0][s]);
+        if (vP) atomicAdd(p.dA + dP * kN + n, dA[1][s]);
         if (g == 0 && p.dh0) {
-#pragma unroll
-            for (int j = 0; j < NS; ++j) p.dh0[(b * D + d) * kN + k + NSPLIT * j] = Gc[j];
+            if (vO) p.dh0[(b * D + dO) * kN + n] = Gc[0][s];
+            if (vP) p.dh0[(b * D + dP) * kN + n] = Gc[1][s];
         }
     }
-    if (dve) {
-        atomicAdd(p.dD + de, dDacc);
-        atomicAdd(p.ddt_bias + de, dbacc);
+    if (vO) {
+        atomicAdd(p.dD + dO, dDacc);
+        atomicAdd(p.ddt_bias + dO, dbacc);
     }
     flag_nonfinite(p.status, nf);
 }
@@ -564,9 +488,9 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
     }
 }
 
-template <typename IO, int NSPLIT> int launch_bwd_t(const BwdParams& p, cudaStream_t s) {
-    using Ly = BwdLayout<IO, NSPLIT>;
-    auto kern = ssm_bwd_kernel<IO, NSPLIT>;
+template <typename IO> int launch_bwd_t(const BwdParams& p, cudaStream_t s) {
+    using Ly = BwdLayout<IO>;
+    auto kern = ssm_bwd_kernel<IO>;
     static unsigned long long mask = 0;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
     if (p.B == 0 || p.D == 0 || p.G == 0) return 0;
@@ -589,15 +513,8 @@ template <typename IO, int NSPLIT> int launch_bwd_agg_t(const BwdParams& p, cuda
 
 }  // namespace
 
-int launch_bwd(int io, int nsplit, const BwdParams& p, cudaStream_t s) {
-    if (io == 0) {
-        if (nsplit == 1) return launch_bwd_t<float, 1>(p, s);
-        if (nsplit == 2) return launch_bwd_t<float, 2>(p, s);
-        return launch_bwd_t<float, 4>(p, s);
-    }
-    if (nsplit == 1) return launch_bwd_t<__nv_bfloat16, 1>(p, s);
-    if (nsplit == 2) return launch_bwd_t<__nv_bfloat16, 2>(p, s);
-    return launch_bwd_t<__nv_bfloat16, 4>(p, s);
+int launch_bwd(int io, const BwdParams& p, cudaStream_t s) {
+    return io == 0 ? launch_bwd_t<float>(p, s) : launch_bwd_t<__nv_bfloat16>(p, s);
 }
 
 int launch_bwd_agg(int io, int nsplit, const BwdParams& p, cudaStream_t s) {

@@ -14,7 +14,8 @@
 namespace ssm {
 
 constexpr int kN = 16;         // d_state supported by the kernels
-constexpr int kCK = 16;        // tokens per checkpoint = tokens per staged tile
+constexpr int kCK = 16;        // tokens per staged forward tile
+constexpr int kCkpt = 8;       // tokens between saved forward states (backward chunk)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.69314718055994531f;
 

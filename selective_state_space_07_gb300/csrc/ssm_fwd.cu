@@ -71,7 +71,12 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
     extern __shared__ __align__(16) char smem[];
 
     const int tid = threadIdx.x;
-    const int c = tid / NSPLIT, k = tid % NSPLIT;  // lane role: channel c, states [k*NS, k*NS+NS)
+    // lane role: channel c, states [k*NS, k*NS+NS). Lanes sharing k sit in
+    // the same quarter / half of the warp, so the per-token B/C loads of a
+    // quarter-warp hit one address (a broadcast takes half the wavefronts of
+    // four interleaved addresses).
+    constexpr int CPW = 32 / NSPLIT;  // channels per warp
+    const int c = (tid >> 5) * CPW + (tid & (CPW - 1)), k = (tid & 31) / CPW;
     const int ce = tid % CH;                        // per-token role: channel ce
     const int64_t D = p.D, L = p.L;
     const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c, de = d0 + ce;
@@ -81,7 +86,7 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
     const int64_t tb0 = (int64_t)g * p.Lg;
     const int64_t tb1 = min64(L, tb0 + p.Lg);
     const int ntile = (int)((tb1 - tb0 + kCK - 1) / kCK);
-    const int64_t nck = (L + kCK - 1) / kCK;
+    const int64_t nck = (L + kCkpt - 1) / kCkpt;  // saved states per sequence
     const bool has_z = !AGG && p.has_z;
     const bool sp = p.sp != 0;
 
@@ -173,19 +178,21 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
             }
         }
         __syncthreads();
-        if (!AGG && p.ckpt && dv) {
-            // state before token t0 (t0 is a multiple of 16)
-            float* cp = p.ckpt + ((b * nck + t0 / kCK) * D + d) * kN + k * NS;
-#pragma unroll
-            for (int q = 0; q < NS / 4; ++q)
-                reinterpret_cast<float4*>(cp)[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
-        }
         // ---- (B) the lane's states through the tile's tokens; partial
         // readouts stay in registers until the tile is done
         float Pt[kCK];
 #pragma unroll
         for (int t = 0; t < kCK; ++t) {
             Pt[t] = 0.f;
+            if (!AGG && t % kCkpt == 0 && t < rows && p.ckpt && dv) {
+                // state before token t0+t: ckpt[b][(t0+t)/8][n][d]
+                float* cp = p.ckpt + ((b * nck + (t0 + t) / kCkpt) * kN + k * NS) * D + d;
+#pragma unroll
+                for (int q = 0; q < NS / 2; ++q) {
+                    cp[(2 * q) * D] = h[q].x;
+                    cp[(2 * q + 1) * D] = h[q].y;
+                }
+            }
             if (t < rows) {
                 const float2 du = DU[t * CH + c];
                 const float* Bt = Bf + t * kN + k * NS;

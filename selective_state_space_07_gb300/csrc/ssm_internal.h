@@ -32,7 +32,7 @@ struct BwdParams {
     int has_z, sp;
     const void *x, *z, *Bm, *Cm, *dy;
     const float *dt, *dt_bias, *A, *Dskip;
-    const float* ckpt;    // [B, ceil(L/16), D, 16]
+    const float* ckpt;    // [B, ceil(L/8), 16, D]: state before every 8th token, state-major
     const float* gstart;  // G == 1: dh_last [B,D,16] (nullable); G > 1: carries [B,G,D,16]
     void *dx, *dz;
     float *ddt, *dA, *dD, *ddt_bias, *dB, *dC, *dh0;
@@ -72,7 +72,7 @@ int launch_fwd_agg(int io, int nsplit, const FwdParams& p, cudaStream_t s);
 int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start,
                  const float* aggV, const float* aggS, float* out, cudaStream_t s);
 int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s);
-int launch_bwd(int io, int nsplit, const BwdParams& p, cudaStream_t s);
+int launch_bwd(int io, const BwdParams& p, cudaStream_t s);
 int launch_bwd_agg(int io, int nsplit, const BwdParams& p, cudaStream_t s);
 
 }  // namespace ssm

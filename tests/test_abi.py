@@ -51,10 +51,10 @@ def test_library_is_built_for_sm_103a(ssm):
 
 
 def test_sizes(ssm):
-    assert ssm.ckpt_elems(4, 4096, 4096) == 4 * 256 * 4096 * 16
-    assert ssm.ckpt_elems(1, 17, 8) == 2 * 8 * 16
+    assert ssm.ckpt_elems(4, 4096, 4096) == 4 * 512 * 16 * 4096
+    assert ssm.ckpt_elems(1, 17, 8) == 3 * 16 * 8
     assert ssm.ckpt_elems(2, 0, 8) == 0
-    assert ssm.lib().ssm_scan_ckpt_interval() == 16
+    assert ssm.lib().ssm_scan_ckpt_interval() == ssm.CKPT_INTERVAL == 8
     assert ssm.workspace_bytes(1, 1, 8) >= 256
     # carries are bounded: B*D*groups <= 131072, fp32 [.., 16] x2 + sums
     assert ssm.workspace_bytes(4, 4096, 4096) <= 256 + 131072 * 33 * 4 + 512

@@ -47,21 +47,24 @@ def test_step_from_zero_is_bitwise_the_forward(ssm, fwd_split, step_split, io):
 
 
 def test_step_from_every_checkpoint_is_bitwise_the_forward(ssm):
-    # A forward split into 3 L-groups of 2 chunks: stepping from any saved
-    # checkpoint reproduces that chunk's outputs exactly, and the state it
-    # reaches equals the next checkpoint exactly inside a group. A group's
-    # first checkpoint comes from the carry scan over groups, which
-    # re-associates the products, so there it agrees to rounding only.
+    # A forward split into 3 L-groups of 32 tokens: stepping from any saved
+    # checkpoint (one every 8 tokens, stored state-major [B, L/8, N, D])
+    # reproduces those tokens' outputs exactly, and the state it reaches
+    # equals the next checkpoint exactly inside a group. A group's first
+    # checkpoint comes from the carry scan over groups, which re-associates
+    # the products, so there it agrees to rounding only.
+    K = ssm.CKPT_INTERVAL
     inp = gen.make_inputs(2, 96, 64, 16, io="bf16", seed=17, with_h0=True)
     dv = to_dev(inp)
     y, h_last, ckpt, _ = run_fwd(ssm, dv, inp, nsplit=2, groups=3)
-    ck = ckpt[: ssm.ckpt_elems(2, 96, 64)].view(2, 6, 64, 16)
-    group_starts = {0, 2, 4}
-    for c in range(6):
+    nck = 96 // K
+    ck = ckpt[: ssm.ckpt_elems(2, 96, 64)].view(2, nck, 16, 64).transpose(2, 3)  # -> [B, nck, D, N]
+    group_starts = {0, 32 // K, 64 // K}
+    for c in range(nck):
         state = ck[:, c].contiguous().clone()
-        ys = step_through(ssm, dv, state, 16 * c, 16 * c + 16, 4)
-        assert torch.equal(ys, y[:, 16 * c:16 * c + 16])
-        nxt = ck[:, c + 1] if c < 5 else h_last
+        ys = step_through(ssm, dv, state, K * c, K * c + K, 4)
+        assert torch.equal(ys, y[:, K * c:K * c + K])
+        nxt = ck[:, c + 1] if c < nck - 1 else h_last
         if c + 1 in group_starts:
             assert rel_err(to_np(state), to_np(nxt)) < 1e-5
         else:
