@@ -55,13 +55,6 @@ int auto_nsplit(int64_t channels) {
     return 4;
 }
 
-int auto_groups(int64_t channels, int nsplit, int64_t L, int64_t gmax) {
-    const int64_t warps = std::max<int64_t>(1, channels * nsplit / 32);
-    if (warps >= 1024) return 1;
-    const int64_t want = ceil_div(2048, warps);
-    return (int)std::max<int64_t>(1, std::min<int64_t>({want, ceil_div(L, kCK), gmax}));
-}
-
 // Multiprocessors of the current device (cached per device ordinal).
 int sm_count() {
     static int cache[64] = {0};
@@ -187,8 +180,7 @@ int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
         return SSM_OK;
     }
     const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
-    const int nsplit = a->nsplit ? a->nsplit : auto_nsplit(ch);
-    int G = a->groups ? (int)std::min<int64_t>({(int64_t)a->groups, nck, gmax}) : auto_groups(ch, nsplit, L, gmax);
+    int G = (int)std::min<int64_t>({a->groups ? (int64_t)a->groups : ssm::fwd_auto_groups(ch, nck), nck, gmax});
     const int64_t Lg = ceil_div(nck, G) * kCK;
     G = (int)ceil_div(L, Lg);
     const WsLayout w = ws_layout(B, L, D);
@@ -203,13 +195,13 @@ int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
     p.aggH = (float*)(ws + w.aggV); p.aggS = (float*)(ws + w.aggS);
     p.status = (unsigned*)ws;
     if (G > 1) {
-        if ((rc = tally(ssm::launch_fwd_agg(a->io_dtype, nsplit, p, s))) != SSM_OK) return rc;
+        if ((rc = tally(ssm::launch_fwd_agg(a->io_dtype, p, s))) != SSM_OK) return rc;
         if ((rc = tally(ssm::launch_carry(B, D, G, false, a->A, a->h0, p.aggH, p.aggS, (float*)(ws + w.carry), s))) !=
             SSM_OK)
             return rc;
         p.hstart = (const float*)(ws + w.carry);
     }
-    return tally(ssm::launch_fwd(a->io_dtype, nsplit, p, s));
+    return tally(ssm::launch_fwd(a->io_dtype, p, s));
 }
 
 int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
@@ -311,7 +303,9 @@ int ssm_step(const ssm_step_args* a, void* stream) {
     p.x = a->x_t; p.z = a->z_t; p.Bm = a->Bm_t; p.Cm = a->Cm_t;
     p.dt = a->dt_t; p.dt_bias = a->dt_bias; p.A = a->A; p.Dskip = a->Dskip;
     p.state = a->state; p.y = a->y_t; p.status = (unsigned*)a->workspace;
-    const int nsplit = a->nsplit ? a->nsplit : auto_nsplit(a->B * a->D);
+    // one lane per channel when the channels alone fill the GPU, else two
+    // (the readout has two halves; nsplit = 4 runs as 2)
+    const int nsplit = a->nsplit ? std::min(a->nsplit, 2) : (a->B * a->D >= 65536 ? 1 : 2);
     return tally(ssm::launch_step(a->io_dtype, nsplit, p, (cudaStream_t)stream));
 }
 

@@ -126,94 +126,12 @@ __device__ __forceinline__ void red_add_v4(float* gptr, float4 v) {
                  : "memory");
 }
 
-// ------------------------------------------------------------ state update
-// One token for the NS consecutive states this lane owns:
-//   h_n <- exp2(Delta*A2_n) * h_n + u*B_n,   (A2 = A*log2(e), u = Delta*x)
-template <int NS>
-__device__ __forceinline__ void token_update(float2 (&h)[NS / 2], const float2 (&A2)[NS / 2], float delta,
-                                             float u, const float* Bt) {
-    const float2 d2 = make_float2(delta, delta), u2 = make_float2(u, u);
-#pragma unroll
-    for (int q = 0; q < NS / 4; ++q) {
-        const float4 b4 = *reinterpret_cast<const float4*>(Bt + 4 * q);
-        const float2 arg0 = __fmul2_rn(d2, A2[2 * q]);
-        const float2 arg1 = __fmul2_rn(d2, A2[2 * q + 1]);
-        const float2 a0 = make_float2(ex2(arg0.x), ex2(arg0.y));
-        const float2 a1 = make_float2(ex2(arg1.x), ex2(arg1.y));
-        h[2 * q] = __ffma2_rn(a0, h[2 * q], __fmul2_rn(u2, make_float2(b4.x, b4.y)));
-        h[2 * q + 1] = __ffma2_rn(a1, h[2 * q + 1], __fmul2_rn(u2, make_float2(b4.z, b4.w)));
-    }
-}
-
-// The lane's partial readout sum_n C_n h_n in the CANONICAL order: states
-// are grouped in blocks of four, a block sums as (C0 h0 + C2 h2) +
-// (C1 h1 + C3 h3) with the second product of each pair fused (fma), and
-// blocks combine as a balanced tree ((blk0 + blk1) + (blk2 + blk3)). A lane
-// owning 4 / 8 / 16 states forms one / two / all four blocks; lanes then
-// combine in the same tree, so the readout is bitwise the same for every
-// lane split, in the sequence forward and in the step form.
-template <int NS>
-__device__ __forceinline__ float token_readout(const float2 (&h)[NS / 2], const float* Ct) {
-    float blk[NS / 4];
-#pragma unroll
-    for (int q = 0; q < NS / 4; ++q) {
-        const float4 c4 = *reinterpret_cast<const float4*>(Ct + 4 * q);
-        float2 acc = __fmul2_rn(make_float2(c4.x, c4.y), h[2 * q]);
-        acc = __ffma2_rn(make_float2(c4.z, c4.w), h[2 * q + 1], acc);
-        blk[q] = __fadd_rn(acc.x, acc.y);
-    }
-    if constexpr (NS == 4) return blk[0];
-    else if constexpr (NS == 8) return __fadd_rn(blk[0], blk[1]);
-    else return __fadd_rn(__fadd_rn(blk[0], blk[1]), __fadd_rn(blk[2], blk[3]));
-}
-
-template <int NS>
-__device__ __forceinline__ float token_states(float2 (&h)[NS / 2], const float2 (&A2)[NS / 2],
-                                              float delta, float u, const float* Bt, const float* Ct) {
-    static_assert(NS == 4 || NS == 8 || NS == 16, "lane owns 4, 8 or 16 states");
-    token_update<NS>(h, A2, delta, u, Bt);
-    return token_readout<NS>(h, Ct);
-}
-
 // y for one token from the channel's full readout p (lanes combined).
 template <bool FAST>
 __device__ __forceinline__ float gate_out(float p, float Dd, float xv, float zv, bool has_z) {
     const float pp = __fmaf_rn(Dd, xv, p);
     if (!has_z) return pp;
     return __fmul_rn(pp, __fmul_rn(zv, sigmoid<FAST>(zv)));
-}
-
-// Combine the per-lane partial readouts of NSPLIT lanes sharing a channel
-// into the full readout of token `k` (reduce-scatter), in the canonical tree
-// ((lane0 + lane1) + (lane2 + lane3)); P[j] holds this lane's partial for
-// token j of the group.
-template <int NSPLIT>
-__device__ __forceinline__ float readout_scatter(const float (&P)[NSPLIT], int k) {
-    if constexpr (NSPLIT == 1) {
-        return P[0];
-    } else if constexpr (NSPLIT == 2) {
-        const float send = k ? P[0] : P[1];
-        const float keep = k ? P[1] : P[0];
-        return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
-    } else {
-        const int k0 = k & 1, k1 = k >> 1;
-        float Q[2];
-#pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const float keep = k0 ? P[2 * m + 1] : P[2 * m];
-            const float send = k0 ? P[2 * m] : P[2 * m + 1];
-            Q[m] = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 1));
-        }
-        const float keep = k1 ? Q[1] : Q[0];
-        const float send = k1 ? Q[0] : Q[1];
-        return __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, send, 2));
-    }
-}
-// Same combination, every lane receiving the full readout of one token.
-template <int NSPLIT> __device__ __forceinline__ float readout_allreduce(float P) {
-    if constexpr (NSPLIT >= 2) P = __fadd_rn(P, __shfl_xor_sync(0xffffffffu, P, 1));
-    if constexpr (NSPLIT >= 4) P = __fadd_rn(P, __shfl_xor_sync(0xffffffffu, P, 2));
-    return P;
 }
 
 __device__ __forceinline__ void flag_nonfinite(unsigned* status, float acc) {

@@ -4,12 +4,24 @@
 // Recurrence (rustytorch commit log, "MambaBlock" S6 forward commit:
 // "sequential scan h=dA.h+dBu, y=sum C.h + D.u -> gate by SiLU(z)"):
 // per (b, d) channel the 16 states are an independent first-order linear
-// recurrence in t. Each channel is owned by NSPLIT adjacent lanes of a warp
-// (lane k holds states [k*16/NSPLIT, (k+1)*16/NSPLIT)) and walks its tokens
-// sequentially with the state in registers. Tiles of 16 tokens x CH
-// channels of x, z, dt and the 16-wide B_t / C_t rows are staged into shared
-// memory with cp.async (double-buffered), B/C are widened to fp32 once per
-// tile, and y leaves through a shared-memory tile as 16-byte stores.
+// recurrence in t. Lanes l and l^16 of a warp share one channel: lane l
+// holds states 8*(l>>4) .. 8*(l>>4)+7 in registers and walks the tokens in
+// order. Tiles of 16 tokens x 64 channels of x, z, dt and the 16-wide B_t /
+// C_t rows are staged into shared memory with cp.async (four tiles in
+// flight); B/C are widened to fp32 and transposed (state-major) once per
+// tile, so a half-warp reads one state's row of 4 tokens with one broadcast
+// 16-byte load. The arithmetic is packed over token pairs (f32x2).
+//
+// Per tile: (A) each lane prepares Delta, u and the gate factor for its 8
+// tokens (one lane of the pair per token) and shares Delta/u with its
+// partner through shared memory; (S) per state, the 16-token recurrence and
+// the readout chain; (E) the two half-readouts of each token are added and
+// each lane gates and writes y for its 8 tokens.
+//
+// Canonical readout order (the step kernel evaluates the same operations):
+// each half of the states is a sequential fused multiply-add chain
+// C_0 h_0 -> fma(C_1, h_1, .) -> ... -> fma(C_7, h_7, .), and the two halves
+// are added; p + D x is fused, then multiplied by z * sigmoid(z).
 //
 // Parallelism along L: the sequence splits into G groups. A first pass
 // (AGG) runs every group but the last from a zero state and publishes its
@@ -23,13 +35,12 @@ namespace ssm {
 
 namespace {
 
-template <typename IO, int NSPLIT> struct FwdLayout {
+template <typename IO> struct FwdLayout {
     static constexpr int NT = kFwdThreads;
-    static constexpr int CH = NT / NSPLIT;        // channels per CTA
-    static constexpr int NS = kN / NSPLIT;        // states per lane
+    static constexpr int CH = NT / 2;             // channels per CTA (a lane pair per channel)
     static constexpr int ES = sizeof(IO);
-    static constexpr int XROW = CH * ES + 16;     // padded shared row (bytes) of x / z / y
-    static constexpr int DTROW = CH * 4 + 16;     // padded shared row of dt
+    static constexpr int XROW = CH * ES;          // staged row of x / z (bytes)
+    static constexpr int DTROW = CH * 4;          // staged row of dt
     static constexpr int BCROW = kN * ES;         // one token of B or C
     static constexpr int OFF_X = 0;
     static constexpr int OFF_Z = OFF_X + kCK * XROW;
@@ -37,106 +48,77 @@ template <typename IO, int NSPLIT> struct FwdLayout {
     static constexpr int OFF_B = OFF_DT + kCK * DTROW;
     static constexpr int OFF_C = OFF_B + kCK * BCROW;
     static constexpr int STAGE = OFF_C + kCK * BCROW;
-    // cp.async pipeline depth: enough tiles in flight to cover DRAM latency
-    static constexpr int NSTAGE = STAGE <= 12 * 1024 ? 4 : 2;
-    static constexpr int SMEM = NSTAGE * STAGE;                 // staged tiles (dynamic shared memory)
+    static constexpr int NSTAGE = 4;              // tiles in flight
+    static constexpr int SMEM = NSTAGE * STAGE;   // dynamic shared memory
+    static constexpr int ROW = 2 * kCK + 4;       // per-channel row of DU / PB (floats, padded)
 };
 
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
-// Full readout of one (token, channel) from its NSPLIT lane partials, in the
-// canonical tree ((lane0 + lane1) + (lane2 + lane3)) -- the association
-// readout_allreduce uses in the step form.
-template <int NSPLIT> __device__ __forceinline__ float combine_partials(const float* P) {
-    if constexpr (NSPLIT == 1) return P[0];
-    else if constexpr (NSPLIT == 2) {
-        const float2 v = *reinterpret_cast<const float2*>(P);
-        return __fadd_rn(v.x, v.y);
-    } else {
-        const float4 v = *reinterpret_cast<const float4*>(P);
-        return __fadd_rn(__fadd_rn(v.x, v.y), __fadd_rn(v.z, v.w));
-    }
-}
-
-// One CTA: CH channels of one batch row over one L-group, 16 tokens per
-// staged tile. Per tile: (A) every thread prepares (Delta, u) and the gate
-// factor for (token, channel) pairs; (B) each lane advances its NS states
-// through the tile's tokens and leaves its partial readouts in shared
-// memory; (E) every thread combines the partials of (token, channel)
-// pairs, applies skip and gate and stages y.
-template <typename IO, int NSPLIT, bool AGG>
+template <typename IO, bool AGG>
 __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p) {
-    using Ly = FwdLayout<IO, NSPLIT>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, NS = Ly::NS, ES = Ly::ES;
+    using Ly = FwdLayout<IO>;
+    constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(16) char smem[];
+    __shared__ __align__(16) float BT[kN * T];                 // B^T of the tile [state][token]
+    __shared__ __align__(16) float CT[AGG ? 4 : kN * T];
+    __shared__ __align__(16) float DU[CH * Ly::ROW];           // per channel [Delta 0..15 | u 0..15]
+    __shared__ __align__(16) float PB[AGG ? 4 : CH * Ly::ROW]; // per channel [half-0 readouts | half-1]
 
-    const int tid = threadIdx.x;
-    // lane role: channel c, states [k*NS, k*NS+NS). Lanes sharing k sit in
-    // the same quarter / half of the warp, so the per-token B/C loads of a
-    // quarter-warp hit one address (a broadcast takes half the wavefronts of
-    // four interleaved addresses).
-    constexpr int CPW = 32 / NSPLIT;  // channels per warp
-    const int c = (tid >> 5) * CPW + (tid & (CPW - 1)), k = (tid & 31) / CPW;
-    const int ce = tid % CH;                        // per-token role: channel ce
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hk = lane >> 4;                 // states 8*hk .. 8*hk+7; tokens 8*hk .. 8*hk+7 of the tile
+    const int c = warp * 16 + (lane & 15);    // channel within the CTA
     const int64_t D = p.D, L = p.L;
-    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c, de = d0 + ce;
-    const bool dv = d < D, dve = de < D;
+    const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c;
+    const bool dv = d < D;
     const int g = blockIdx.y;
     const int64_t b = blockIdx.z;
     const int64_t tb0 = (int64_t)g * p.Lg;
     const int64_t tb1 = min64(L, tb0 + p.Lg);
-    const int ntile = (int)((tb1 - tb0 + kCK - 1) / kCK);
+    const int ntile = (int)((tb1 - tb0 + T - 1) / T);
     const int64_t nck = (L + kCkpt - 1) / kCkpt;  // saved states per sequence
     const bool has_z = !AGG && p.has_z;
     const bool sp = p.sp != 0;
 
-    float2 A2[NS / 2], h[NS / 2];
+    float A2[NS], h[NS];
 #pragma unroll
-    for (int j = 0; j < NS / 2; ++j) {
-        const int n = k * NS + 2 * j;
-        A2[j] = dv ? make_float2(__fmul_rn(p.A[d * kN + n], kLog2e), __fmul_rn(p.A[d * kN + n + 1], kLog2e))
-                   : make_float2(0.f, 0.f);
-        float2 hv = make_float2(0.f, 0.f);
-        if (!AGG && dv && p.hstart) {
-            const float* hs = p.G == 1 ? p.hstart + (b * D + d) * kN : p.hstart + ((b * p.G + g) * D + d) * kN;
-            hv = make_float2(hs[n], hs[n + 1]);
-        }
-        h[j] = hv;
+    for (int s = 0; s < NS; ++s) {
+        const int n = NS * hk + s;
+        A2[s] = dv ? __fmul_rn(p.A[d * kN + n], kLog2e) : 0.f;
+        float hv = 0.f;
+        if (!AGG && dv && p.hstart)
+            hv = p.G == 1 ? p.hstart[(b * D + d) * kN + n] : p.hstart[((b * p.G + g) * D + d) * kN + n];
+        h[s] = hv;
     }
-    const float Dde = (dve && p.Dskip) ? p.Dskip[de] : 0.f;
-    const float biase = (dve && p.dt_bias) ? p.dt_bias[de] : 0.f;
+    const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
+    const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
 
     const int vchx = (int)(min64(CH, D - d0) * ES / 16);  // valid 16-byte chunks per x row
     const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
     auto issue = [&](int j, char* st) {
-        const int64_t t0 = tb0 + (int64_t)j * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
+        const int64_t t0 = tb0 + (int64_t)j * T;
+        const int rows = (int)min64(T, tb1 - t0);
         const int64_t row0 = b * L + t0;
-        stage_block<NT>(st + Ly::OFF_X, Ly::XROW, (const char*)p.x + (row0 * D + d0) * ES, D * ES, kCK,
-                        CH * ES / 16, rows, vchx);
+        stage_block<NT>(st + Ly::OFF_X, Ly::XROW, (const char*)p.x + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
+                        rows, vchx);
         if (has_z)
-            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, kCK,
+            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, T,
                             CH * ES / 16, rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, kCK,
-                        CH * 4 / 16, rows, vchd);
-        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * kN * ES, kN * ES, kCK,
-                        Ly::BCROW / 16, rows, Ly::BCROW / 16);
+        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
+                        rows, vchd);
+        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+                        rows, Ly::BCROW / 16);
         if (!AGG)
-            stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, kCK,
+            stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, T,
                             Ly::BCROW / 16, rows, Ly::BCROW / 16);
         cp_async_commit();
     };
 
-    // per-tile working arrays: each its own shared object, so the compiler
-    // knows loads from one never alias stores to another
-    __shared__ __align__(16) float Bf[kCK * kN];
-    __shared__ __align__(16) float Cf[kCK * kN];
-    __shared__ __align__(16) float2 DU[kCK * CH];
-    __shared__ __align__(16) float GZ[AGG ? 1 : kCK * CH];
-    __shared__ __align__(16) float PB[AGG ? 1 : kCK * CH * NSPLIT];
-    __shared__ __align__(16) char ys[AGG ? 16 : kCK * Ly::XROW];
+    float* du = DU + c * Ly::ROW;
+    float* pb = PB + c * Ly::ROW;
     float nf = 0.f;     // Inf/NaN detector
-    float ssum = 0.f;   // AGG: sum of Delta over the group
+    float ssum = 0.f;   // AGG: this lane's part of the sum of Delta over the group
 
     // prologue: tiles 0 .. NSTAGE-2 in flight (one commit group per tile,
     // empty groups past the end keep the group count uniform)
@@ -154,101 +136,134 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
         }
         cp_async_wait<Ly::NSTAGE - 1>();
         __syncthreads();
-        const int64_t t0 = tb0 + (int64_t)j * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
-        // ---- (A) per (token, channel): Delta, u, gate factor; B/C to fp32
+        const int64_t t0 = tb0 + (int64_t)j * T;
+        const int rows = (int)min64(T, tb1 - t0);
+
+        // ---- B/C to fp32, state-major
         {
             const IO* Braw = reinterpret_cast<const IO*>(st + Ly::OFF_B);
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
-            for (int i = tid; i < kCK * kN; i += NT) {
-                Bf[i] = IOT<IO>::to_f(Braw[i]);
-                if (!AGG) Cf[i] = IOT<IO>::to_f(Craw[i]);
+            for (int i = tid; i < kN * T; i += NT) {
+                const int n = i / T, tok = i - n * T;
+                BT[i] = IOT<IO>::to_f(Braw[tok * kN + n]);
+                if (!AGG) CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
             }
+        }
+        // ---- A: Delta, u and the gate factor of this lane's 8 tokens;
+        // tokens past the end act as identity (Delta = u = 0)
+        float xo[NS], gz[NS];
+        {
+            float dl[NS], ul[NS];
 #pragma unroll
-            for (int r = 0; r < kCK * CH / NT; ++r) {
-                const int t = tid / CH + (NT / CH) * r;
-                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[ce]);
-                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[ce];
-                const float delta = token_delta<FAST>(dtv, biase, sp);
-                DU[t * CH + ce] = make_float2(delta, __fmul_rn(delta, xv));
+            for (int i = 0; i < NS; ++i) {
+                const int t = NS * hk + i;
+                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[c]);
+                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[c];
+                const float delta = token_delta<FAST>(dtv, bias, sp);
+                const bool live = t < rows;
+                dl[i] = live ? delta : 0.f;
+                ul[i] = live ? __fmul_rn(delta, xv) : 0.f;
+                xo[i] = xv;
+                if (AGG) ssum = __fadd_rn(ssum, dl[i]);
                 if (has_z) {
-                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[ce]);
-                    GZ[t * CH + ce] = __fmul_rn(zv, sigmoid<FAST>(zv));
+                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[c]);
+                    gz[i] = __fmul_rn(zv, sigmoid<FAST>(zv));
                 }
             }
+            *reinterpret_cast<float4*>(du + NS * hk) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            *reinterpret_cast<float4*>(du + NS * hk + 4) = make_float4(dl[4], dl[5], dl[6], dl[7]);
+            *reinterpret_cast<float4*>(du + T + NS * hk) = make_float4(ul[0], ul[1], ul[2], ul[3]);
+            *reinterpret_cast<float4*>(du + T + NS * hk + 4) = make_float4(ul[4], ul[5], ul[6], ul[7]);
         }
         __syncthreads();
-        // ---- (B) the lane's states through the tile's tokens; partial
-        // readouts stay in registers until the tile is done
-        float Pt[kCK];
+        float2 Dl[T / 2], Ul[T / 2];
 #pragma unroll
-        for (int t = 0; t < kCK; ++t) {
-            Pt[t] = 0.f;
-            if (!AGG && t % kCkpt == 0 && t < rows && p.ckpt && dv) {
-                // state before token t0+t: ckpt[b][(t0+t)/8][n][d]
-                float* cp = p.ckpt + ((b * nck + (t0 + t) / kCkpt) * kN + k * NS) * D + d;
+        for (int q = 0; q < T / 4; ++q) {
+            const float4 dq = *reinterpret_cast<const float4*>(du + 4 * q);
+            const float4 uq = *reinterpret_cast<const float4*>(du + T + 4 * q);
+            Dl[2 * q] = f2(dq.x, dq.y);
+            Dl[2 * q + 1] = f2(dq.z, dq.w);
+            Ul[2 * q] = f2(uq.x, uq.y);
+            Ul[2 * q + 1] = f2(uq.z, uq.w);
+        }
+
+        // ---- S: per state, the tile's 16 tokens; the readout chain runs
+        // over this lane's 8 states
+        const bool ck = !AGG && p.ckpt && dv;
+        float* ckp = ck ? p.ckpt + ((b * nck + t0 / kCkpt) * kN + NS * hk) * D + d : nullptr;
+        float2 acc[T / 2];
 #pragma unroll
-                for (int q = 0; q < NS / 2; ++q) {
-                    cp[(2 * q) * D] = h[q].x;
-                    cp[(2 * q + 1) * D] = h[q].y;
+        for (int s = 0; s < NS; ++s) {
+            const int n = NS * hk + s;
+            const float2 A2p = f2(A2[s], A2[s]);
+            float hp = h[s];
+            if (ck) ckp[s * D] = hp;  // state before token t0
+#pragma unroll
+            for (int q = 0; q < T / 4; ++q) {
+                const float4 b4 = *reinterpret_cast<const float4*>(BT + n * T + 4 * q);
+                float4 c4;
+                if (!AGG) c4 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int m = 2 * q + h2;
+                    const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
+                    const float2 arg = __fmul2_rn(Dl[m], A2p);
+                    const float a0 = ex2(arg.x), a1 = ex2(arg.y);
+                    const float2 ub = __fmul2_rn(Ul[m], bb);
+                    const float h0v = __fmaf_rn(a0, hp, ub.x);
+                    const float h1v = __fmaf_rn(a1, h0v, ub.y);
+                    hp = h1v;
+                    if (!AGG) {
+                        const float2 cc = h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
+                        acc[m] = s == 0 ? __fmul2_rn(cc, f2(h0v, h1v)) : __ffma2_rn(cc, f2(h0v, h1v), acc[m]);
+                    }
                 }
+                if (q == 1 && ck && rows > kCkpt) ckp[s * D + kN * D] = hp;  // state before token t0+8
             }
-            if (t < rows) {
-                const float2 du = DU[t * CH + c];
-                const float* Bt = Bf + t * kN + k * NS;
-                if (AGG) {
-                    token_update<NS>(h, A2, du.x, du.y, Bt);
-                    ssum = __fadd_rn(ssum, du.x);
-                } else {
-                    Pt[t] = token_states<NS>(h, A2, du.x, du.y, Bt, Cf + t * kN + k * NS);
-                }
-            }
+            h[s] = hp;
         }
         if (!AGG) {
+            // ---- E: half readouts -> full readout of this lane's 8 tokens
+            *reinterpret_cast<float4*>(pb + T * hk) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+            *reinterpret_cast<float4*>(pb + T * hk + 4) = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+            *reinterpret_cast<float4*>(pb + T * hk + 8) = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
+            *reinterpret_cast<float4*>(pb + T * hk + 12) = make_float4(acc[6].x, acc[6].y, acc[7].x, acc[7].y);
+            __syncwarp();
+            const float4 p0a = *reinterpret_cast<const float4*>(pb + NS * hk);
+            const float4 p0b = *reinterpret_cast<const float4*>(pb + NS * hk + 4);
+            const float4 p1a = *reinterpret_cast<const float4*>(pb + T + NS * hk);
+            const float4 p1b = *reinterpret_cast<const float4*>(pb + T + NS * hk + 4);
+            const float P0[NS] = {p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, p0b.y, p0b.z, p0b.w};
+            const float P1[NS] = {p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, p1b.y, p1b.z, p1b.w};
+            IO* yrow = reinterpret_cast<IO*>(p.y) + (b * L + t0) * D + d;
 #pragma unroll
-            for (int t = 0; t < kCK; ++t) PB[(t * CH + c) * NSPLIT + k] = Pt[t];
-        }
-        if (!AGG) {
-            __syncthreads();
-            // ---- (E) per (token, channel): combine partials, skip term, gate
-#pragma unroll
-            for (int r = 0; r < kCK * CH / NT; ++r) {
-                const int t = tid / CH + (NT / CH) * r;
-                if (t < rows) {
-                    const float pr = combine_partials<NSPLIT>(PB + (t * CH + ce) * NSPLIT);
-                    const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[ce]);
-                    const float pp = __fmaf_rn(Dde, xv, pr);
-                    const float yv = has_z ? __fmul_rn(pp, GZ[t * CH + ce]) : pp;
+            for (int i = 0; i < NS; ++i) {
+                const int t = NS * hk + i;
+                const float pr = __fadd_rn(P0[i], P1[i]);
+                const float pp = __fmaf_rn(Dd, xo[i], pr);
+                const float yv = has_z ? __fmul_rn(pp, gz[i]) : pp;
+                if (dv && t < rows) {
                     nf = __fmaf_rn(yv, 0.0f, nf);
-                    reinterpret_cast<IO*>(ys + t * Ly::XROW)[ce] = IOT<IO>::from_f(yv);
+                    yrow[(int64_t)t * D] = IOT<IO>::from_f(yv);
                 }
-            }
-            __syncthreads();
-            constexpr int CHX = CH * ES / 16;
-            for (int i = tid; i < rows * CHX; i += NT) {
-                const int r = i / CHX, ch = i - r * CHX;
-                if (ch < vchx)
-                    *reinterpret_cast<int4*>((char*)p.y + (((b * L + t0 + r) * D + d0) * ES + ch * 16)) =
-                        *reinterpret_cast<const int4*>(ys + r * Ly::XROW + ch * 16);
             }
         }
         __syncthreads();
     }
 
     if (AGG) {
+        ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, 16));
         if (dv) {
-            float* H = p.aggH + ((b * p.G + g) * D + d) * kN + k * NS;
+            float* H = p.aggH + ((b * p.G + g) * D + d) * kN + NS * hk;
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q)
-                reinterpret_cast<float4*>(H)[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
-            if (k == 0) p.aggS[(b * p.G + g) * D + d] = ssum;
+            for (int s = 0; s < NS; ++s) H[s] = h[s];
+            if (hk == 0) p.aggS[(b * p.G + g) * D + d] = ssum;
         }
     } else {
         if (g == p.G - 1 && p.h_last && dv) {
-            float* hl = p.h_last + (b * D + d) * kN + k * NS;
+            float* hl = p.h_last + (b * D + d) * kN + NS * hk;
 #pragma unroll
-            for (int q = 0; q < NS / 4; ++q)
-                reinterpret_cast<float4*>(hl)[q] = make_float4(h[2 * q].x, h[2 * q].y, h[2 * q + 1].x, h[2 * q + 1].y);
+            for (int s = 0; s < NS; ++s) hl[s] = h[s];
         }
         flag_nonfinite(p.status, nf);
     }
@@ -304,11 +319,12 @@ __global__ void ssm_carry_kernel(int64_t B, int64_t D, int G, int reverse, const
     }
 }
 
-// One token for every (b, d): the same per-token arithmetic as the forward
-// (token_delta, token_states, readout tree, gate_out).
+// One token for every (b, d) channel with the forward's arithmetic and
+// canonical readout order: NSPLIT = 1 (a lane per channel, both half chains)
+// or 2 (adjacent lanes take the two halves).
 template <typename IO, int NSPLIT>
 __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams p) {
-    constexpr int CH = kFwdThreads / NSPLIT, NS = kN / NSPLIT;
+    constexpr int CH = kFwdThreads / NSPLIT;
     constexpr bool FAST = IOT<IO>::kFast;
     __shared__ __align__(16) float Bs[kN], Cs[kN];
     const int tid = threadIdx.x, c = tid / NSPLIT, k = tid % NSPLIT;
@@ -319,15 +335,6 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
         Cs[tid] = IOT<IO>::to_f(reinterpret_cast<const IO*>(p.Cm)[b * kN + tid]);
     }
     __syncthreads();
-    float2 A2[NS / 2], h[NS / 2];
-    float* st = p.state + (b * D + (dv ? d : 0)) * kN + k * NS;
-#pragma unroll
-    for (int j = 0; j < NS / 2; ++j) {
-        const int n = k * NS + 2 * j;
-        A2[j] = dv ? make_float2(__fmul_rn(p.A[d * kN + n], kLog2e), __fmul_rn(p.A[d * kN + n + 1], kLog2e))
-                   : make_float2(0.f, 0.f);
-        h[j] = dv ? make_float2(st[2 * j], st[2 * j + 1]) : make_float2(0.f, 0.f);
-    }
     const int64_t i = b * D + (dv ? d : 0);
     const float xv = dv ? IOT<IO>::to_f(reinterpret_cast<const IO*>(p.x)[i]) : 0.f;
     const float dtv = dv ? p.dt[i] : 0.f;
@@ -335,26 +342,42 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
     const float delta = token_delta<FAST>(dtv, bias, p.sp != 0);
     const float u = __fmul_rn(delta, xv);
-    const float P = token_states<NS>(h, A2, delta, u, Bs + k * NS, Cs + k * NS);
-    const float pr = readout_allreduce<NSPLIT>(P);
+    float* st = p.state + (b * D + (dv ? d : 0)) * kN;
+    float half[2] = {0.f, 0.f};
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        if (NSPLIT == 2 && hf != k) continue;
+        float acc = 0.f;
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+            const int n = 8 * hf + s;
+            const float A2 = dv ? __fmul_rn(p.A[d * kN + n], kLog2e) : 0.f;
+            const float a = ex2(__fmul_rn(delta, A2));
+            const float ub = __fmul_rn(u, Bs[n]);
+            const float hv = __fmaf_rn(a, dv ? st[n] : 0.f, ub);
+            if (dv) st[n] = hv;
+            acc = s == 0 ? __fmul_rn(Cs[n], hv) : __fmaf_rn(Cs[n], hv, acc);
+        }
+        half[hf] = acc;
+    }
+    float pr;
+    if (NSPLIT == 1) {
+        pr = __fadd_rn(half[0], half[1]);
+    } else {
+        const float mine = half[k];
+        pr = __fadd_rn(mine, __shfl_xor_sync(0xffffffffu, mine, 1));  // addition commutes: same bits in both lanes
+    }
     const bool has_z = p.has_z != 0;
     const float zv = (has_z && dv) ? IOT<IO>::to_f(reinterpret_cast<const IO*>(p.z)[i]) : 0.f;
     const float yv = gate_out<FAST>(pr, Dd, xv, zv, has_z);
-    if (dv) {
-#pragma unroll
-        for (int j = 0; j < NS / 2; ++j) {
-            st[2 * j] = h[j].x;
-            st[2 * j + 1] = h[j].y;
-        }
-        if (k == 0) reinterpret_cast<IO*>(p.y)[i] = IOT<IO>::from_f(yv);
-    }
+    if (dv && k == 0) reinterpret_cast<IO*>(p.y)[i] = IOT<IO>::from_f(yv);
     flag_nonfinite(p.status, __fmaf_rn(yv, 0.0f, 0.0f));
 }
 
-template <typename IO, int NSPLIT, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream_t s) {
-    using Ly = FwdLayout<IO, NSPLIT>;
+template <typename IO, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream_t s) {
+    using Ly = FwdLayout<IO>;
     static unsigned long long mask = 0;
-    auto kern = ssm_fwd_kernel<IO, NSPLIT, AGG>;
+    auto kern = ssm_fwd_kernel<IO, AGG>;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
     const int gy = AGG ? p.G - 1 : p.G;
     if (gy <= 0 || p.B == 0 || p.D == 0) return 0;
@@ -371,21 +394,14 @@ template <typename IO, int NSPLIT> int launch_step_t(const StepParams& p, cudaSt
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
-template <bool AGG> int dispatch_fwd(int io, int nsplit, const FwdParams& p, cudaStream_t s) {
-    if (io == 0) {
-        if (nsplit == 1) return launch_fwd_t<float, 1, AGG>(p, s);
-        if (nsplit == 2) return launch_fwd_t<float, 2, AGG>(p, s);
-        return launch_fwd_t<float, 4, AGG>(p, s);
-    }
-    if (nsplit == 1) return launch_fwd_t<__nv_bfloat16, 1, AGG>(p, s);
-    if (nsplit == 2) return launch_fwd_t<__nv_bfloat16, 2, AGG>(p, s);
-    return launch_fwd_t<__nv_bfloat16, 4, AGG>(p, s);
-}
-
 }  // namespace
 
-int launch_fwd(int io, int nsplit, const FwdParams& p, cudaStream_t s) { return dispatch_fwd<false>(io, nsplit, p, s); }
-int launch_fwd_agg(int io, int nsplit, const FwdParams& p, cudaStream_t s) { return dispatch_fwd<true>(io, nsplit, p, s); }
+int launch_fwd(int io, const FwdParams& p, cudaStream_t s) {
+    return io == 0 ? launch_fwd_t<float, false>(p, s) : launch_fwd_t<__nv_bfloat16, false>(p, s);
+}
+int launch_fwd_agg(int io, const FwdParams& p, cudaStream_t s) {
+    return io == 0 ? launch_fwd_t<float, true>(p, s) : launch_fwd_t<__nv_bfloat16, true>(p, s);
+}
 
 int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start, const float* aggV,
                  const float* aggS, float* out, cudaStream_t s) {
@@ -398,14 +414,8 @@ int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, cons
 }
 
 int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s) {
-    if (io == 0) {
-        if (nsplit == 1) return launch_step_t<float, 1>(p, s);
-        if (nsplit == 2) return launch_step_t<float, 2>(p, s);
-        return launch_step_t<float, 4>(p, s);
-    }
-    if (nsplit == 1) return launch_step_t<__nv_bfloat16, 1>(p, s);
-    if (nsplit == 2) return launch_step_t<__nv_bfloat16, 2>(p, s);
-    return launch_step_t<__nv_bfloat16, 4>(p, s);
+    if (io == 0) return nsplit == 1 ? launch_step_t<float, 1>(p, s) : launch_step_t<float, 2>(p, s);
+    return nsplit == 1 ? launch_step_t<__nv_bfloat16, 1>(p, s) : launch_step_t<__nv_bfloat16, 2>(p, s);
 }
 
 }  // namespace ssm

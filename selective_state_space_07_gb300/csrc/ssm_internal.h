@@ -65,10 +65,21 @@ template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long l
     return true;
 }
 
+// Forward L-groups when the caller leaves the choice. The forward kernel
+// runs a lane pair per channel (16 channels per warp); with fewer than 512
+// warps the sequence is split so that about 1024 warps run, at the price of
+// the aggregate pass over all groups but the last.
+inline int64_t fwd_auto_groups(int64_t channels, int64_t nchunks) {
+    const int64_t warps = channels / 16 > 0 ? channels / 16 : 1;
+    if (warps >= 512) return 1;
+    const int64_t want = (1024 + warps - 1) / warps;
+    return want < nchunks ? want : (nchunks > 0 ? nchunks : 1);
+}
+
 // io: 0 = fp32, 1 = bf16. Each launcher returns the number of kernels it
 // launched (>= 0) or -1 if a launch failed.
-int launch_fwd(int io, int nsplit, const FwdParams& p, cudaStream_t s);
-int launch_fwd_agg(int io, int nsplit, const FwdParams& p, cudaStream_t s);
+int launch_fwd(int io, const FwdParams& p, cudaStream_t s);
+int launch_fwd_agg(int io, const FwdParams& p, cudaStream_t s);
 int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start,
                  const float* aggV, const float* aggS, float* out, cudaStream_t s);
 int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s);

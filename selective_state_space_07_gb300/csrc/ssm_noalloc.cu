@@ -100,7 +100,6 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
 
     // launch shape: as ssm_scan_fwd chooses it, within the array
     const int64_t ch = B * D, nck = std::max<int64_t>(1, cdiv(L, kChunk));
-    const int nsplit = a->nsplit ? a->nsplit : (ch >= 65536 ? 1 : ch >= 32768 ? 2 : 4);
     int G = 1;
     if (work) {
         if (a->groups) {
@@ -108,9 +107,7 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
             G = (int)cdiv(L, cdiv(nck, G) * kChunk);
             if (scratch_need(B, D, G) > kNoAllocScratchBytes) return SSM_ERR_SCRATCH_LIMIT;
         } else {
-            const int64_t warps = std::max<int64_t>(1, ch * nsplit / 32);
-            int64_t want = warps >= 1024 ? 1 : cdiv(2048, warps);
-            want = std::max<int64_t>(1, std::min<int64_t>(want, nck));
+            int64_t want = ssm::fwd_auto_groups(ch, nck);
             while (want > 1 && scratch_need(B, D, (int)want) > kNoAllocScratchBytes) --want;
             G = (int)cdiv(L, cdiv(nck, want) * kChunk);
         }
@@ -148,9 +145,9 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
     p.status = status;
     if (G > 1) {
         float* carry = (float*)(scratch + kStatus + nv + ns);
-        if (ssm::launch_fwd_agg(a->io_dtype, nsplit, p, s) < 0) return SSM_ERR_CUDA;
+        if (ssm::launch_fwd_agg(a->io_dtype, p, s) < 0) return SSM_ERR_CUDA;
         if (ssm::launch_carry(B, D, G, false, a->A, a->h0, p.aggH, p.aggS, carry, s) < 0) return SSM_ERR_CUDA;
         p.hstart = carry;
     }
-    return ssm::launch_fwd(a->io_dtype, nsplit, p, s) < 0 ? SSM_ERR_CUDA : SSM_OK;
+    return ssm::launch_fwd(a->io_dtype, p, s) < 0 ? SSM_ERR_CUDA : SSM_OK;
 }
