@@ -40,6 +40,15 @@ METRIC = "selective-scan fwd+bwd G(token·channel)/s on 1 GB300; % of HBM roofli
 UNIT = "G(token·channel)/s"
 DEFAULT_WORKLOAD = "mamba1.4b-bf16"
 FALLBACK_HBM_GBS = 6800.0
+# Special-function unit: ex2.approx issues 32 results per clock per SM on
+# GB300 (measured with a throughput probe); the SFU roofline is that rate at
+# the SM count and the maximum SM clock.
+SFU_EX2_PER_CLK_PER_SM = 32
+# A "pass" is one C-ABI call; its kernels (the main one plus, when the
+# sequence is split into L-groups, the aggregate pass and the carry scan)
+# are timed together between CUDA events.
+PASS_KERNELS = {"fwd": "ssm_scan_fwd (ssm_fwd_kernel; + ssm_fwd_kernel<AGG> and ssm_carry_kernel when L-groups > 1)",
+                "bwd": "ssm_scan_bwd (ssm_bwd_agg_kernel + ssm_carry_kernel when L-groups > 1, then ssm_bwd_kernel)"}
 
 
 def log(*a):
@@ -60,10 +69,12 @@ def algorithmic_bytes(w, pass_):
 
 
 def mufu_ops(w, pass_):
-    """Special-function-unit operations per pass (bf16 path): one exp2 per
-    (token, channel, state) plus the per-token softplus / sigmoid work."""
+    """Special-function-unit results a pass needs (bf16 path): one exp2 per
+    (token, channel, state) for the decay, plus per (token, channel) the
+    softplus (exp2, log2), the gate's sigmoid (exp2, reciprocal) and, in the
+    backward, the reciprocal behind sigmoid(dt + dt_bias)."""
     tc = w.B * w.L * w.D
-    return tc * w.N + tc * (4 if pass_ == "fwd" else 9)
+    return tc * w.N + tc * (4 if pass_ == "fwd" else 5)
 
 
 def measured_peaks():
@@ -85,9 +96,18 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def sfu_peak_per_s(peaks):
+    """ex2 results per second at the maximum SM clock (MEASURED_PEAKS.json
+    sm_max_mhz, else 2070 MHz) on the current device's SMs."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = float(peaks.get("sm_max_mhz", 2070.0)) if peaks else 2070.0
+    return SFU_EX2_PER_CLK_PER_SM * sms * mhz * 1e6
+
+
 def profiled_traffic(kernel, workload):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; otherwise None."""
+    """DRAM bytes per call (summed over the pass's kernels) from the committed
+    ncu summary, if it was taken on the current kernel sources; else None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
@@ -370,17 +390,21 @@ def run_ours(args, w):
             dist.destroy_process_group()
         return 0
 
-    peak, peak_kind, _ = measured_peaks()
-    rf = {}
+    peak, peak_kind, peaks = measured_peaks()
+    sfu_peak = sfu_peak_per_s(peaks)
+    rf, sfu = {}, {}
     for name, ms in (("fwd", ms_f), ("bwd", ms_b)):
         ab = algorithmic_bytes(w, name)
         ach = ab / (ms * 1e-3) / 1e9
-        kern = "ssm_bwd_kernel" if name == "bwd" else "ssm_fwd_kernel"
+        call = "ssm_scan_" + name
         rf[name] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(ach / peak, 4), "peak_kind": peak_kind, "kernel": kern,
+                    "frac": round(ach / peak, 4), "peak_kind": peak_kind, "kernel": PASS_KERNELS[name],
                     "algorithmic_bytes_per_launch": ab, "ms_per_launch": round(ms, 5),
-                    "traffic": profiled_traffic(kern, w.name),
-                    "mufu_ops_per_s": round(mufu_ops(w, name) / (ms * 1e-3), 1)}
+                    "traffic": profiled_traffic(call, w.name)}
+        ops = mufu_ops(w, name) / (ms * 1e-3)
+        sfu[name] = {"bound": "sfu", "achieved": round(ops / 1e12, 3), "peak": round(sfu_peak / 1e12, 3),
+                     "unit": "Tex2/s", "frac": round(ops / sfu_peak, 4),
+                     "peak_kind": "derived: 32 ex2/clk/SM x SMs x max SM clock"}
     dom = "bwd" if ms_b >= ms_f else "fwd"
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
@@ -399,6 +423,7 @@ def run_ours(args, w):
                    "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
         "roofline": rf[dom],
         "roofline_other": rf["fwd" if dom == "bwd" else "bwd"],
+        "sfu_roofline": sfu,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

@@ -55,27 +55,19 @@ int auto_nsplit(int64_t channels) {
     return 4;
 }
 
-// Multiprocessors of the current device (cached per device ordinal).
-int sm_count() {
-    static int cache[64] = {0};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-    int& c = cache[dev & 63];
-    if (c == 0) {
-        int v = 0;
-        c = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 152;
-    }
-    return c;
-}
+// Price of the aggregate pass relative to the main pass, per direction: the
+// forward's aggregate runs the whole recurrence, the backward's only the
+// adjoint chain.
+constexpr double kFwdAggCost = 0.8;
+constexpr double kBwdAggCost = 0.15;
 
-// Backward L-groups: the backward kernel runs 128 channels per CTA and two
-// CTAs per SM; split L until the grid fills the SMs once (a group costs one
-// extra reverse-aggregate pass over its tokens, which is cheap next to the
-// backward itself).
-int auto_groups_bwd(int64_t B, int64_t D, int64_t L, int64_t gmax) {
-    const int64_t ctas = std::max<int64_t>(1, B * ceil_div(D, 128));
-    const int64_t want = std::max<int64_t>(1, 2 * (int64_t)sm_count() / ctas);
-    return (int)std::max<int64_t>(1, std::min<int64_t>({want, ceil_div(L, kCK), gmax}));
+int auto_groups_fwd(int io, int64_t B, int64_t D, int64_t gmax) {
+    const int64_t ctas = B * ceil_div(D, ssm::fwd_channels_per_cta());
+    return ssm::choose_groups(ctas, (int64_t)ssm::fwd_blocks_per_sm(io) * ssm::sm_count(), kFwdAggCost, gmax);
+}
+int auto_groups_bwd(int io, int64_t B, int64_t D, int64_t gmax) {
+    const int64_t ctas = B * ceil_div(D, ssm::bwd_channels_per_cta());
+    return ssm::choose_groups(ctas, (int64_t)ssm::bwd_blocks_per_sm(io) * ssm::sm_count(), kBwdAggCost, gmax);
 }
 
 // Common checks of the forward-shaped arguments. Returns SSM_OK or an error.
@@ -179,8 +171,9 @@ int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
         }
         return SSM_OK;
     }
-    const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
-    int G = (int)std::min<int64_t>({a->groups ? (int64_t)a->groups : ssm::fwd_auto_groups(ch, nck), nck, gmax});
+    const int64_t nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
+    const int64_t gcap = std::min<int64_t>(nck, gmax);
+    int G = a->groups ? (int)std::min<int64_t>(a->groups, gcap) : auto_groups_fwd(a->io_dtype, B, D, gcap);
     const int64_t Lg = ceil_div(nck, G) * kCK;
     G = (int)ceil_div(L, Lg);
     const WsLayout w = ws_layout(B, L, D);
@@ -244,7 +237,8 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
     // f.nsplit shapes only the reverse-aggregate pass here: the backward
     // kernel has one lane layout (a lane pair per two channels)
     const int nsplit = f.nsplit ? f.nsplit : auto_nsplit(ch);
-    int G = f.groups ? (int)std::min<int64_t>({(int64_t)f.groups, nck, gmax}) : auto_groups_bwd(B, D, L, gmax);
+    const int64_t gcap = std::min<int64_t>(nck, gmax);
+    int G = f.groups ? (int)std::min<int64_t>(f.groups, gcap) : auto_groups_bwd(f.io_dtype, B, D, gcap);
     const int64_t Lg = ceil_div(nck, G) * kCK;
     G = (int)ceil_div(L, Lg);
     const WsLayout w = ws_layout(B, L, D);

@@ -513,6 +513,33 @@ template <typename IO, int NSPLIT> int launch_bwd_agg_t(const BwdParams& p, cuda
 
 }  // namespace
 
+int bwd_blocks_per_sm(int io) {
+    static int cache[2][64] = {{0}};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    int& c = cache[io ? 1 : 0][dev & 63];
+    if (c == 0) {
+        int v = 0;
+        cudaError_t e;
+        if (io == 0) {
+            auto kern = ssm_bwd_kernel<float>;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdLayout<float>::SMEM);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kBwdThreads, BwdLayout<float>::SMEM);
+        } else {
+            auto kern = ssm_bwd_kernel<__nv_bfloat16>;
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     BwdLayout<__nv_bfloat16>::SMEM);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, kBwdThreads,
+                                                                  BwdLayout<__nv_bfloat16>::SMEM);
+        }
+        c = (e == cudaSuccess && v > 0) ? v : 1;
+    }
+    return c;
+}
+int bwd_channels_per_cta() { return BwdLayout<float>::CH; }
+
 int launch_bwd(int io, const BwdParams& p, cudaStream_t s) {
     return io == 0 ? launch_bwd_t<float>(p, s) : launch_bwd_t<__nv_bfloat16>(p, s);
 }

@@ -396,6 +396,42 @@ template <typename IO, int NSPLIT> int launch_step_t(const StepParams& p, cudaSt
 
 }  // namespace
 
+namespace {
+template <typename K> int blocks_per_sm(K kern, int threads, int smem, int* cache) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    int& c = cache[dev & 63];
+    if (c == 0) {
+        int v = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, kern, threads, smem) != cudaSuccess || v < 1)
+            v = 1;
+        c = v;
+    }
+    return c;
+}
+}  // namespace
+
+int fwd_blocks_per_sm(int io) {
+    static int cache_f[64] = {0}, cache_b[64] = {0};
+    return io == 0 ? blocks_per_sm(ssm_fwd_kernel<float, false>, kFwdThreads, FwdLayout<float>::SMEM, cache_f)
+                   : blocks_per_sm(ssm_fwd_kernel<__nv_bfloat16, false>, kFwdThreads,
+                                   FwdLayout<__nv_bfloat16>::SMEM, cache_b);
+}
+int fwd_channels_per_cta() { return FwdLayout<float>::CH; }
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    int& c = cache[dev & 63];
+    if (c == 0) {
+        int v = 0;
+        c = (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && v > 0) ? v : 152;
+    }
+    return c;
+}
+
 int launch_fwd(int io, const FwdParams& p, cudaStream_t s) {
     return io == 0 ? launch_fwd_t<float, false>(p, s) : launch_fwd_t<__nv_bfloat16, false>(p, s);
 }

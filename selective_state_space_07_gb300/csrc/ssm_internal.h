@@ -65,16 +65,37 @@ template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long l
     return true;
 }
 
-// Forward L-groups when the caller leaves the choice. The forward kernel
-// runs a lane pair per channel (16 channels per warp); with fewer than 512
-// warps the sequence is split so that about 1024 warps run, at the price of
-// the aggregate pass over all groups but the last.
-inline int64_t fwd_auto_groups(int64_t channels, int64_t nchunks) {
-    const int64_t warps = channels / 16 > 0 ? channels / 16 : 1;
-    if (warps >= 512) return 1;
-    const int64_t want = (1024 + warps - 1) / warps;
-    return want < nchunks ? want : (nchunks > 0 ? nchunks : 1);
+// L-groups when the caller leaves the choice. A pass over G groups runs
+// G * ctas_per_group CTAs in waves of `capacity` (resident CTAs on the
+// device); a wave that is partly empty wastes its share, and every group but
+// the last costs an aggregate pass of relative price `alpha`. Returns the G
+// in [1, gmax] that minimises 1/fill(G) + alpha*(G-1)/G, fill = waves /
+// ceil(waves).
+inline int choose_groups(int64_t ctas_per_group, int64_t capacity, double alpha, int64_t gmax) {
+    if (ctas_per_group < 1) ctas_per_group = 1;
+    if (capacity < 1) capacity = 1;
+    int best = 1;
+    double best_cost = 1e30;
+    const int64_t top = gmax < 64 ? gmax : 64;
+    for (int64_t G = 1; G <= top; ++G) {
+        const double waves = (double)(G * ctas_per_group) / (double)capacity;
+        const double full = (double)((G * ctas_per_group + capacity - 1) / capacity);
+        const double cost = full / waves + alpha * (double)(G - 1) / (double)G;
+        if (cost < best_cost - 1e-9) {
+            best_cost = cost;
+            best = (int)G;
+        }
+    }
+    return best;
 }
+
+// Resident CTAs per SM of the forward / backward main kernels (occupancy
+// query, cached per device), channels per CTA, and the SM count.
+int fwd_blocks_per_sm(int io);
+int bwd_blocks_per_sm(int io);
+int fwd_channels_per_cta();
+int bwd_channels_per_cta();
+int sm_count();
 
 // io: 0 = fp32, 1 = bf16. Each launcher returns the number of kernels it
 // launched (>= 0) or -1 if a launch failed.

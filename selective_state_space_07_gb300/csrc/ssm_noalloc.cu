@@ -99,7 +99,7 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
     if (a->workspace && a->workspace_bytes < kStatus) return SSM_ERR_WORKSPACE;
 
     // launch shape: as ssm_scan_fwd chooses it, within the array
-    const int64_t ch = B * D, nck = std::max<int64_t>(1, cdiv(L, kChunk));
+    const int64_t nck = std::max<int64_t>(1, cdiv(L, kChunk));
     int G = 1;
     if (work) {
         if (a->groups) {
@@ -107,7 +107,9 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
             G = (int)cdiv(L, cdiv(nck, G) * kChunk);
             if (scratch_need(B, D, G) > kNoAllocScratchBytes) return SSM_ERR_SCRATCH_LIMIT;
         } else {
-            int64_t want = ssm::fwd_auto_groups(ch, nck);
+            int64_t want = ssm::choose_groups(B * cdiv(D, ssm::fwd_channels_per_cta()),
+                                              (int64_t)ssm::fwd_blocks_per_sm(a->io_dtype) * ssm::sm_count(), 0.8,
+                                              nck);
             while (want > 1 && scratch_need(B, D, (int)want) > kNoAllocScratchBytes) --want;
             G = (int)cdiv(L, cdiv(nck, want) * kChunk);
         }
