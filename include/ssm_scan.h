@@ -71,11 +71,13 @@ enum {
  *   ssm_scan_bwd needs; size ssm_scan_ckpt_elems() floats.
  * workspace: >= ssm_scan_workspace_bytes(B, L, D, N) bytes, 16-byte
  *   aligned, holding the status word and the chunk carries along L.
- * nsplit / groups: launch shape; 0 = automatic. nsplit in {1,2,4} lanes per
- *   channel (each lane owns 16/nsplit states); groups = number of L-segments
- *   scanned in parallel, joined by chunk carries. Results are the same up
- *   to rounding for every choice; with groups == 1 the forward is bitwise
- *   equal to stepping ssm_step through the sequence. */
+ * nsplit / groups: launch shape; 0 = automatic. groups = number of
+ *   L-segments scanned in parallel, joined by chunk carries (0: chosen from
+ *   the device's occupancy). The forward kernel has one lane layout (two
+ *   lanes per channel, 8 states each): nsplit must be 0, 1, 2 or 4 and is
+ *   otherwise ignored here. Results are the same up to rounding for every
+ *   choice; with groups == 1 the forward is bitwise equal to stepping
+ *   ssm_step through the sequence. */
 typedef struct {
     int64_t B, L, D, N;
     int32_t io_dtype;       /* ssm_dtype */
@@ -135,7 +137,9 @@ typedef struct {
  * same per-token arithmetic as ssm_scan_fwd, so stepping from a state the
  * forward passed through reproduces the forward's outputs bit for bit.
  * workspace: nullable; when given (>= 256 bytes) non-finite outputs are
- * latched in its status word. */
+ * latched in its status word.
+ * nsplit: lanes per channel, 1 or 2 (each lane takes one or both halves of
+ * the readout); 4 runs as 2; 0 = automatic. */
 typedef struct {
     int64_t B, D, N;
     int32_t io_dtype;
