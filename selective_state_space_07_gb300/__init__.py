@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "SsmError", "build", "lib", "scan_fwd", "scan_bwd", "step", "dA_log_grad", "poll_status",
     "clear_status", "workspace_bytes", "ckpt_elems", "CKPT_INTERVAL", "Workspace", "scan_fwd_bwd_host",
-    "last_launch_count",
+    "last_launch_count", "HostPipeline",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -244,17 +244,17 @@ def scan_bwd(x, dt, A, Bm, Cm, dy, ckpt, z=None, Dskip=None, dt_bias=None, h0=No
         if z is not None:
             o.setdefault("dz", z)
     f32 = dict(dtype=torch.float32, device=dev)
-    o.setdefault("dx", torch.empty_like(x))
+    want = {"dx": lambda: torch.empty_like(x), "d_dt": lambda: torch.empty(B, L, D, **f32),
+            "dA": lambda: torch.empty(D, N, **f32), "dD": lambda: torch.empty(D, **f32),
+            "d_dt_bias": lambda: torch.empty(D, **f32), "dB": lambda: torch.empty(B, L, N, **f32),
+            "dC": lambda: torch.empty(B, L, N, **f32)}
     if z is not None:
-        o.setdefault("dz", torch.empty_like(x))
-    o.setdefault("d_dt", torch.empty(B, L, D, **f32))
-    o.setdefault("dA", torch.empty(D, N, **f32))
-    o.setdefault("dD", torch.empty(D, **f32))
-    o.setdefault("d_dt_bias", torch.empty(D, **f32))
-    o.setdefault("dB", torch.empty(B, L, N, **f32))
-    o.setdefault("dC", torch.empty(B, L, N, **f32))
+        want["dz"] = lambda: torch.empty_like(x)
     if return_dh0:
-        o.setdefault("dh0", torch.empty(B, D, N, **f32))
+        want["dh0"] = lambda: torch.empty(B, D, N, **f32)
+    for k, make in want.items():
+        if k not in o:
+            o[k] = make()
     for k, shp, dt_ in (("dx", (B, L, D), io), ("dz", (B, L, D), io), ("d_dt", (B, L, D), torch.float32),
                         ("dA", (D, N), torch.float32), ("dD", (D,), torch.float32),
                         ("d_dt_bias", (D,), torch.float32), ("dB", (B, L, N), torch.float32),
@@ -322,6 +322,81 @@ def poll_status(workspace, stream=None) -> int:
 def clear_status(workspace, stream=None) -> None:
     dev = workspace.buf.device
     _check(lib().ssm_clear_status(workspace.buf.data_ptr(), _stream(dev, stream)), "ssm_clear_status")
+
+
+class HostPipeline:
+    """Back-to-back end-to-end calls for host callers, overlapped.
+
+    Each ``step`` copies one batch of inputs from pinned host memory to the
+    device, runs ssm_scan_fwd and ssm_scan_bwd, and copies y and every
+    gradient back into the pinned ``results`` buffers; it returns without
+    waiting. Copies in, compute and copies out run on three streams over two
+    sets of device buffers, so step k's inputs travel while step k-1
+    computes and step k-2's results travel back (the host link carries both
+    directions at once). Within a step the forward starts once its own
+    inputs are in (dy follows), and y leaves while the backward runs.
+    ``synchronize`` waits for every enqueued step; results of a step are
+    valid after it."""
+
+    _FWD_INPUTS = ("x", "dt", "A", "Bm", "Cm", "z", "Dskip", "dt_bias")
+
+    def __init__(self, host: Dict[str, torch.Tensor], device, delta_softplus=True, depth=2):
+        self.dev = torch.device(device)
+        self.sp = delta_softplus
+        self.depth = depth
+        self.s_in, self.s_comp, self.s_out = (torch.cuda.Stream(self.dev) for _ in range(3))
+        self.sets = []
+        for _ in range(depth):
+            # one plain call per set allocates (and zero-fills) every device
+            # buffer up front, so no allocation happens on the pipeline's streams
+            res, d = scan_fwd_bwd_host(host, self.dev, delta_softplus=delta_softplus)
+            ev = {n: torch.cuda.Event() for n in ("in_fwd", "in_bwd", "fwd", "bwd", "out")}
+            self.sets.append({"dev": d, "ev": ev, "used": False})
+        torch.cuda.synchronize(self.dev)
+        self.k = 0
+
+    def step(self, host: Dict[str, torch.Tensor], results: Optional[Dict] = None) -> Dict[str, torch.Tensor]:
+        st = self.sets[self.k % self.depth]
+        self.k += 1
+        d, ev = st["dev"], st["ev"]
+        if st["used"]:
+            self.s_in.wait_event(ev["bwd"])     # the set's inputs are no longer read
+        with torch.cuda.stream(self.s_in):
+            for k in self._FWD_INPUTS:
+                if host.get(k) is not None:
+                    d[k].copy_(host[k], non_blocking=True)
+            ev["in_fwd"].record(self.s_in)
+            d["dy"].copy_(host["dy"], non_blocking=True)
+            ev["in_bwd"].record(self.s_in)
+        self.s_comp.wait_event(ev["in_fwd"])
+        if st["used"]:
+            self.s_comp.wait_event(ev["out"])   # the set's outputs have left
+        y, _, ck, ws = scan_fwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d.get("z"), d.get("Dskip"),
+                                d.get("dt_bias"), None, self.sp, y=d.get("y"), ckpt=d.get("ckpt"),
+                                workspace=d.get("ws"), stream=self.s_comp)
+        d["y"], d["ckpt"], d["ws"] = y, ck, ws
+        ev["fwd"].record(self.s_comp)
+        self.s_comp.wait_event(ev["in_bwd"])
+        g = scan_bwd(d["x"], d["dt"], d["A"], d["Bm"], d["Cm"], d["dy"], ck, d.get("z"), d.get("Dskip"),
+                     d.get("dt_bias"), None, None, self.sp, out=d.get("grads"), workspace=ws, stream=self.s_comp)
+        g.pop("workspace", None)
+        d["grads"] = g
+        ev["bwd"].record(self.s_comp)
+        if results is None:
+            results = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in {"y": y, **g}.items()}
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(ev["fwd"])
+            results["y"].copy_(y, non_blocking=True)
+            self.s_out.wait_event(ev["bwd"])
+            for k, v in g.items():
+                results[k].copy_(v, non_blocking=True)
+            ev["out"].record(self.s_out)
+        st["used"] = True
+        return results
+
+    def synchronize(self):
+        for s_ in (self.s_in, self.s_comp, self.s_out):
+            s_.synchronize()
 
 
 def scan_fwd_bwd_host(host: Dict[str, torch.Tensor], device, *, dev_buffers: Optional[Dict] = None,
