@@ -55,15 +55,13 @@ int auto_nsplit(int64_t channels) {
     return 4;
 }
 
-// Price of the aggregate pass relative to the main pass, per direction: the
-// forward's aggregate runs the whole recurrence, the backward's only the
-// adjoint chain.
-constexpr double kFwdAggCost = 0.8;
+// Price of the backward's aggregate pass (only the adjoint chain) relative to
+// the backward main pass.
 constexpr double kBwdAggCost = 0.15;
 
 int auto_groups_fwd(int io, int64_t B, int64_t D, int64_t gmax) {
     const int64_t ctas = B * ceil_div(D, ssm::fwd_channels_per_cta());
-    return ssm::choose_groups(ctas, (int64_t)ssm::fwd_blocks_per_sm(io) * ssm::sm_count(), kFwdAggCost, gmax);
+    return ssm::choose_groups_fwd(ctas, ssm::sm_count(), ssm::fwd_blocks_per_sm(io), gmax);
 }
 int auto_groups_bwd(int io, int64_t B, int64_t D, int64_t gmax) {
     const int64_t ctas = B * ceil_div(D, ssm::bwd_channels_per_cta());

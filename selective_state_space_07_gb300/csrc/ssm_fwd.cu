@@ -192,35 +192,53 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
         const bool ck = !AGG && p.ckpt && dv;
         float* ckp = ck ? p.ckpt + ((b * nck + t0 / kCkpt) * kN + NS * hk) * D + d : nullptr;
         float2 acc[T / 2];
+        // two states advance together through the tokens (independent
+        // chains for the scheduler); the readout chain still takes the
+        // states in order
 #pragma unroll
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NS; s += 2) {
             const int n = NS * hk + s;
-            const float2 A2p = f2(A2[s], A2[s]);
-            float hp = h[s];
-            if (ck) ckp[s * D] = hp;  // state before token t0
+            const float2 A2p0 = f2(A2[s], A2[s]), A2p1 = f2(A2[s + 1], A2[s + 1]);
+            float hp0 = h[s], hp1 = h[s + 1];
+            if (ck) {  // states before token t0
+                ckp[s * D] = hp0;
+                ckp[(s + 1) * D] = hp1;
+            }
 #pragma unroll
             for (int q = 0; q < T / 4; ++q) {
-                const float4 b4 = *reinterpret_cast<const float4*>(BT + n * T + 4 * q);
-                float4 c4;
-                if (!AGG) c4 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
+                const float4 b40 = *reinterpret_cast<const float4*>(BT + n * T + 4 * q);
+                const float4 b41 = *reinterpret_cast<const float4*>(BT + (n + 1) * T + 4 * q);
+                float4 c40, c41;
+                if (!AGG) {
+                    c40 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
+                    c41 = *reinterpret_cast<const float4*>(CT + (n + 1) * T + 4 * q);
+                }
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int m = 2 * q + h2;
-                    const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
-                    const float2 arg = __fmul2_rn(Dl[m], A2p);
-                    const float a0 = ex2(arg.x), a1 = ex2(arg.y);
-                    const float2 ub = __fmul2_rn(Ul[m], bb);
-                    const float h0v = __fmaf_rn(a0, hp, ub.x);
-                    const float h1v = __fmaf_rn(a1, h0v, ub.y);
-                    hp = h1v;
+                    const float2 bb0 = h2 ? f2(b40.z, b40.w) : f2(b40.x, b40.y);
+                    const float2 bb1 = h2 ? f2(b41.z, b41.w) : f2(b41.x, b41.y);
+                    const float2 arg0 = __fmul2_rn(Dl[m], A2p0), arg1 = __fmul2_rn(Dl[m], A2p1);
+                    const float a00 = ex2(arg0.x), a01 = ex2(arg0.y), a10 = ex2(arg1.x), a11 = ex2(arg1.y);
+                    const float2 ub0 = __fmul2_rn(Ul[m], bb0), ub1 = __fmul2_rn(Ul[m], bb1);
+                    const float h00 = __fmaf_rn(a00, hp0, ub0.x), h10 = __fmaf_rn(a10, hp1, ub1.x);
+                    const float h01 = __fmaf_rn(a01, h00, ub0.y), h11 = __fmaf_rn(a11, h10, ub1.y);
+                    hp0 = h01;
+                    hp1 = h11;
                     if (!AGG) {
-                        const float2 cc = h2 ? f2(c4.z, c4.w) : f2(c4.x, c4.y);
-                        acc[m] = s == 0 ? __fmul2_rn(cc, f2(h0v, h1v)) : __ffma2_rn(cc, f2(h0v, h1v), acc[m]);
+                        const float2 cc0 = h2 ? f2(c40.z, c40.w) : f2(c40.x, c40.y);
+                        const float2 cc1 = h2 ? f2(c41.z, c41.w) : f2(c41.x, c41.y);
+                        float2 r = s == 0 ? __fmul2_rn(cc0, f2(h00, h01)) : __ffma2_rn(cc0, f2(h00, h01), acc[m]);
+                        acc[m] = __ffma2_rn(cc1, f2(h10, h11), r);
                     }
                 }
-                if (q == 1 && ck && rows > kCkpt) ckp[s * D + kN * D] = hp;  // state before token t0+8
+                if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
+                    ckp[s * D + kN * D] = hp0;
+                    ckp[(s + 1) * D + kN * D] = hp1;
+                }
             }
-            h[s] = hp;
+            h[s] = hp0;
+            h[s + 1] = hp1;
         }
         if (!AGG) {
             // ---- E: half readouts -> full readout of this lane's 8 tokens
@@ -269,53 +287,57 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
     }
 }
 
-// Carries along L. One warp per (b, d, n); lanes take the groups in windows
-// of 32 and run an inclusive warp-shuffle scan of the affine maps
-// f_g(h) = a_g*h + v_g (a_g = exp(A*sum Delta_g)), composed as
-// (a2, v2) o (a1, v1) = (a2*a1, a2*v1 + v2). Forward: map g takes the
-// state at the start of group g to its end; out[g] = state entering group g.
+// Carries along L. A segment of W lanes (W = the power of two >= G, at most
+// 32) serves one (b, d, n); a warp holds 32/W segments. Lanes take the groups
+// in windows of W and run an inclusive segmented warp-shuffle scan of the
+// affine maps f_g(h) = a_g*h + v_g (a_g = exp(A*sum Delta_g)), composed as
+// (a2, v2) o (a1, v1) = (a2*a1, a2*v1 + v2). Forward: map g takes the state
+// at the start of group g to its end; out[g] = state entering group g.
 // Reverse (backward pass): map m takes the adjoint carry at the end of group
 // G-1-m to the end of group G-2-m; out[g] = carry entering group g from
 // the right.
+template <int W>
 __global__ void ssm_carry_kernel(int64_t B, int64_t D, int G, int reverse, const float* __restrict__ A,
                                  const float* __restrict__ start, const float* __restrict__ aggV,
                                  const float* __restrict__ aggS, float* __restrict__ out) {
-    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (wid >= B * D * kN) return;  // whole warp leaves together
-    const int n = (int)(wid % kN);
-    const int64_t bd = wid / kN, d = bd % D, b = bd / D;
-    const float An = A[d * kN + n];
-    float carry = start ? start[(b * D + d) * kN + n] : 0.f;
+    const int lane = threadIdx.x & 31, sl = lane & (W - 1);
+    const int64_t item = (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * (32 / W) + lane / W;
+    const bool valid = item < B * D * kN;  // invalid segments still shuffle (full-warp masks)
+    const int n = (int)(item % kN);
+    const int64_t bd = valid ? item / kN : 0, d = bd % D, b = bd / D;
+    const float An = valid ? A[d * kN + n] : 0.f;
+    float carry = (valid && start) ? start[(b * D + d) * kN + n] : 0.f;
     const int nmaps = G - 1;
-    for (int w0 = 0; w0 < G; w0 += 32) {
-        const int m = w0 + lane;
+    for (int w0 = 0; w0 < G; w0 += W) {
+        const int m = w0 + sl;
         float a = 1.f, v = 0.f;
-        if (m < nmaps) {
+        if (valid && m < nmaps) {
             const int gsrc = reverse ? G - 1 - m : m;
             a = expf(An * aggS[(b * G + gsrc) * D + d]);
             v = aggV[((b * G + gsrc) * D + d) * kN + n];
         }
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const float ap = __shfl_up_sync(0xffffffffu, a, off);
-            const float vp = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) {
+        for (int off = 1; off < W; off <<= 1) {
+            const float ap = __shfl_up_sync(0xffffffffu, a, off, W);
+            const float vp = __shfl_up_sync(0xffffffffu, v, off, W);
+            if (sl >= off) {
                 v = fmaf(a, vp, v);
                 a = a * ap;
             }
         }
         const float after = fmaf(a, carry, v);  // value after map m
-        // value entering position w0 is `carry`; after map m it enters position m+1
-        if (lane == 0) {
-            const int gdst = reverse ? G - 1 - w0 : w0;
-            out[((b * G + gdst) * D + d) * kN + n] = carry;
+        if (valid) {
+            // value entering position w0 is `carry`; after map m it enters position m+1
+            if (sl == 0) {
+                const int gdst = reverse ? G - 1 - w0 : w0;
+                out[((b * G + gdst) * D + d) * kN + n] = carry;
+            }
+            if (sl < W - 1 && m + 1 < G) {
+                const int gdst = reverse ? G - 2 - m : m + 1;
+                out[((b * G + gdst) * D + d) * kN + n] = after;
+            }
         }
-        if (lane < 31 && m + 1 < G) {
-            const int gdst = reverse ? G - 2 - m : m + 1;
-            out[((b * G + gdst) * D + d) * kN + n] = after;
-        }
-        carry = __shfl_sync(0xffffffffu, after, 31);
+        carry = __shfl_sync(0xffffffffu, after, W - 1, W);
     }
 }
 
@@ -439,14 +461,24 @@ int launch_fwd_agg(int io, const FwdParams& p, cudaStream_t s) {
     return io == 0 ? launch_fwd_t<float, true>(p, s) : launch_fwd_t<__nv_bfloat16, true>(p, s);
 }
 
-int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start, const float* aggV,
-                 const float* aggS, float* out, cudaStream_t s) {
-    const int64_t warps = B * D * kN;
-    if (warps == 0) return 0;
+template <int W>
+int launch_carry_w(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start,
+                   const float* aggV, const float* aggS, float* out, cudaStream_t s) {
+    const int64_t warps = (B * D * kN + 32 / W - 1) / (32 / W);
     const int threads = 256;
     const int64_t blocks = (warps * 32 + threads - 1) / threads;
-    ssm_carry_kernel<<<(unsigned)blocks, threads, 0, s>>>(B, D, G, reverse ? 1 : 0, A, start, aggV, aggS, out);
+    ssm_carry_kernel<W><<<(unsigned)blocks, threads, 0, s>>>(B, D, G, reverse ? 1 : 0, A, start, aggV, aggS, out);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start, const float* aggV,
+                 const float* aggS, float* out, cudaStream_t s) {
+    if (B * D == 0) return 0;
+    if (G <= 2) return launch_carry_w<2>(B, D, G, reverse, A, start, aggV, aggS, out, s);
+    if (G <= 4) return launch_carry_w<4>(B, D, G, reverse, A, start, aggV, aggS, out, s);
+    if (G <= 8) return launch_carry_w<8>(B, D, G, reverse, A, start, aggV, aggS, out, s);
+    if (G <= 16) return launch_carry_w<16>(B, D, G, reverse, A, start, aggV, aggS, out, s);
+    return launch_carry_w<32>(B, D, G, reverse, A, start, aggV, aggS, out, s);
 }
 
 int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s) {

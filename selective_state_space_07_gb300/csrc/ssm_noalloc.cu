@@ -107,9 +107,8 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
             G = (int)cdiv(L, cdiv(nck, G) * kChunk);
             if (scratch_need(B, D, G) > kNoAllocScratchBytes) return SSM_ERR_SCRATCH_LIMIT;
         } else {
-            int64_t want = ssm::choose_groups(B * cdiv(D, ssm::fwd_channels_per_cta()),
-                                              (int64_t)ssm::fwd_blocks_per_sm(a->io_dtype) * ssm::sm_count(), 0.8,
-                                              nck);
+            int64_t want = ssm::choose_groups_fwd(B * cdiv(D, ssm::fwd_channels_per_cta()), ssm::sm_count(),
+                                                  ssm::fwd_blocks_per_sm(a->io_dtype), nck);
             while (want > 1 && scratch_need(B, D, (int)want) > kNoAllocScratchBytes) --want;
             G = (int)cdiv(L, cdiv(nck, want) * kChunk);
         }
