@@ -217,53 +217,66 @@ __global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams
             const float2 bb[4] = {f2(b4a.x, b4a.y), f2(b4a.z, b4a.w), f2(b4b.x, b4b.y), f2(b4b.z, b4b.w)};
             const float2 cc[4] = {f2(c4a.x, c4a.y), f2(c4a.z, c4a.w), f2(c4b.x, c4b.y), f2(c4b.z, c4b.w)};
             float2 vb[T / 2], vc[T / 2];
+            // both channels advance together (independent chains for the scheduler)
+            float An[2], hp[2];
+            float2 A2p[2], Ap[2];
 #pragma unroll
             for (int sl = 0; sl < 2; ++sl) {
                 const int c = sl ? cP : cO;
-                const float An = AT[n * CH + c];
-                const float A2 = __fmul_rn(An, kLog2e);
-                const float2 A2p = f2(A2, A2), Ap = f2(An, An);
-                // forward from the checkpoint over the chunk
-                float2 a[T / 2], hh[T / 2];
-                float hp = hck[n * CH + c];
+                An[sl] = AT[n * CH + c];
+                const float A2 = __fmul_rn(An[sl], kLog2e);
+                A2p[sl] = f2(A2, A2);
+                Ap[sl] = f2(An[sl], An[sl]);
+                hp[sl] = hck[n * CH + c];
+            }
+            // forward from the checkpoint over the chunk
+            float2 a[2][T / 2], hh[2][T / 2];
 #pragma unroll
-                for (int m = 0; m < T / 2; ++m) {
-                    const float2 arg = __fmul2_rn(Dl[sl][m], A2p);
-                    a[m] = f2(ex2(arg.x), ex2(arg.y));
+            for (int m = 0; m < T / 2; ++m) {
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
+                    const float2 arg = __fmul2_rn(Dl[sl][m], A2p[sl]);
+                    a[sl][m] = f2(ex2(arg.x), ex2(arg.y));
                     const float2 ub = __fmul2_rn(Ul[sl][m], bb[m]);
-                    const float h0v = __fmaf_rn(a[m].x, hp, ub.x);
-                    const float h1v = __fmaf_rn(a[m].y, h0v, ub.y);
-                    hp = h1v;
-                    hh[m] = f2(h0v, h1v);
+                    const float h0v = __fmaf_rn(a[sl][m].x, hp[sl], ub.x);
+                    const float h1v = __fmaf_rn(a[sl][m].y, h0v, ub.y);
+                    hp[sl] = h1v;
+                    hh[sl][m] = f2(h0v, h1v);
                 }
-                // reverse: E_t = a_{t+1} E_{t+1} + dp_t C_t, carry Gc = a_{t+1} E_{t+1}
-                float E = Gc[sl][s], anext = 1.f;
-                float2 dAp = f2(0.f, 0.f);
+            }
+            // reverse: E_t = a_{t+1} E_{t+1} + dp_t C_t, carry Gc = a_{t+1} E_{t+1}
+            float E[2] = {Gc[0][s], Gc[1][s]}, anext[2] = {1.f, 1.f};
+            float2 dAp[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
-                for (int m = T / 2 - 1; m >= 0; --m) {
+            for (int m = T / 2 - 1; m >= 0; --m) {
+#pragma unroll
+                for (int sl = 0; sl < 2; ++sl) {
                     const float2 rr = __fmul2_rn(Pl[sl][m], cc[m]);
-                    const float e1 = __fmaf_rn(anext, E, rr.y);
-                    const float e0 = __fmaf_rn(a[m].y, e1, rr.x);
-                    E = e0;
-                    anext = a[m].x;
+                    const float e1 = __fmaf_rn(anext[sl], E[sl], rr.y);
+                    const float e0 = __fmaf_rn(a[sl][m].y, e1, rr.x);
+                    E[sl] = e0;
+                    anext[sl] = a[sl][m].x;
                     const float2 E2 = f2(e0, e1);
                     if (sl == 0) {
                         vb[m] = __fmul2_rn(E2, Ul[0][m]);
-                        vc[m] = __fmul2_rn(Pl[0][m], hh[m]);
+                        vc[m] = __fmul2_rn(Pl[0][m], hh[0][m]);
                     } else {
                         vb[m] = __ffma2_rn(E2, Ul[1][m], vb[m]);
-                        vc[m] = __ffma2_rn(Pl[1][m], hh[m], vc[m]);
+                        vc[m] = __ffma2_rn(Pl[1][m], hh[1][m], vc[m]);
                     }
                     S1[sl][m] = __ffma2_rn(E2, bb[m], S1[sl][m]);
                     // a_t h_{t-1} = h_t - u_t B_t
-                    const float2 q = __ffma2_rn(f2(-Ul[sl][m].x, -Ul[sl][m].y), bb[m], hh[m]);
+                    const float2 q = __ffma2_rn(f2(-Ul[sl][m].x, -Ul[sl][m].y), bb[m], hh[sl][m]);
                     const float2 w = __fmul2_rn(E2, q);
-                    dAp = __ffma2_rn(Dl[sl][m], w, dAp);
-                    S2[sl][m] = __ffma2_rn(Ap, w, S2[sl][m]);
-                    S3[sl][m] = __ffma2_rn(cc[m], hh[m], S3[sl][m]);
+                    dAp[sl] = __ffma2_rn(Dl[sl][m], w, dAp[sl]);
+                    S2[sl][m] = __ffma2_rn(Ap[sl], w, S2[sl][m]);
+                    S3[sl][m] = __ffma2_rn(cc[m], hh[sl][m], S3[sl][m]);
                 }
-                Gc[sl][s] = __fmul_rn(anext, E);
-                dA[sl][s] += __fadd_rn(dAp.x, dAp.y);
+            }
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
+                Gc[sl][s] = __fmul_rn(anext[sl], E[sl]);
+                dA[sl][s] += __fadd_rn(dAp[sl].x, dAp[sl].y);
             }
             // dB/dC contributions of this state, summed over the two channels
             const int sb = s % SPB;
