@@ -105,10 +105,10 @@ typedef struct {
  * over the batch).
  * f: the forward arguments of the same call (x, z, Bm, Cm, dt, dt_bias, A,
  *   Dskip, h0 are read; f.ckpt must hold what ssm_scan_fwd wrote; f.y and
- *   f.h_last are not touched). f.groups sets this pass's L-groups; the
- *   backward kernel has one lane layout (two lanes share a pair of channels,
- *   each taking 8 of the 16 states), so f.nsplit only shapes the pass that
- *   aggregates the reverse carries between L-groups.
+ *   f.h_last are not touched). f.groups sets this pass's L-groups (0:
+ *   chosen from the device's occupancy); the backward kernels have one lane
+ *   layout (two lanes share a pair of channels, each taking 8 of the 16
+ *   states), so f.nsplit is validated and otherwise ignored here.
  * dy [I/O dtype]; dh_last [fp32, nullable = 0].
  * Outputs, written for every element:
  *   dx, dz [I/O dtype] (dz required iff f.z != NULL); d_dt [fp32] = dLoss/d(dt);

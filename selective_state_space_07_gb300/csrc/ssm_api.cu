@@ -48,13 +48,6 @@ WsLayout ws_layout(int64_t B, int64_t L, int64_t D) {
 
 bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-// Lanes per channel: enough warps to fill 152 SMs.
-int auto_nsplit(int64_t channels) {
-    if (channels >= 65536) return 1;
-    if (channels >= 32768) return 2;
-    return 4;
-}
-
 // Price of the backward's aggregate pass (only the adjoint chain) relative to
 // the backward main pass.
 constexpr double kBwdAggCost = 0.15;
@@ -231,10 +224,7 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
         }
         return SSM_OK;
     }
-    const int64_t ch = B * D, nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
-    // f.nsplit shapes only the reverse-aggregate pass here: the backward
-    // kernel has one lane layout (a lane pair per two channels)
-    const int nsplit = f.nsplit ? f.nsplit : auto_nsplit(ch);
+    const int64_t nck = ceil_div(L, kCK), gmax = max_groups(B, L, D);
     const int64_t gcap = std::min<int64_t>(nck, gmax);
     int G = f.groups ? (int)std::min<int64_t>(f.groups, gcap) : auto_groups_bwd(f.io_dtype, B, D, gcap);
     const int64_t Lg = ceil_div(nck, G) * kCK;
@@ -253,7 +243,7 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
     p.aggQ = (float*)(ws + w.aggV); p.aggS = (float*)(ws + w.aggS);
     p.status = (unsigned*)ws;
     if (G > 1) {
-        if ((rc = tally(ssm::launch_bwd_agg(f.io_dtype, nsplit, p, s))) != SSM_OK) return rc;
+        if ((rc = tally(ssm::launch_bwd_agg(f.io_dtype, p, s))) != SSM_OK) return rc;
         if ((rc = tally(ssm::launch_carry(B, D, G, true, f.A, a->dh_last, p.aggQ, p.aggS, (float*)(ws + w.carry), s))) !=
             SSM_OK)
             return rc;

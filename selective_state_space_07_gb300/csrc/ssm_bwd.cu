@@ -387,117 +387,166 @@ __global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams
 }
 
 // Chunk aggregate of the reverse recurrence for groups 1..G-1: with the
-// adjoint carry set to zero at the group's end, run G <- (G + dp*C)*a back to
-// the group's start; publish that value (Q) and the group's sum of Delta.
-// The carry entering group g-1 from the right is then
-// exp(A*sum Delta_g) * carry_g + Q_g.
-template <typename IO, int NSPLIT> constexpr int bwd_agg_smem() {
-    constexpr int CH = kBwdThreads / NSPLIT, ES = sizeof(IO);
-    constexpr int XROW = CH * ES + 16, DTROW = CH * 4 + 16, BCROW = kN * ES;
-    return 2 * (2 * kCK * XROW + kCK * DTROW + kCK * BCROW) + kCK * kN * 4;
-}
+// adjoint carry set to zero at the group's end, run E_t = a_{t+1} E_{t+1} +
+// dp_t C_t back to the group's start and publish Q = a_{t0} E_{t0} (the carry
+// the group passes to its left neighbour) and the group's sum of Delta. The
+// carry entering group g-1 from the right is then exp(A*sum Delta_g) *
+// carry_g + Q_g. Layout as in the forward: a lane pair per channel, each lane
+// 8 states and 8 of a tile's 16 tokens for the per-token work; C staged
+// state-major (broadcast loads); two states advance together.
+template <typename IO> struct BwdAggLayout {
+    static constexpr int NT = kBwdThreads;
+    static constexpr int CH = NT / 2;
+    static constexpr int ES = sizeof(IO);
+    static constexpr int XROW = CH * ES, DTROW = CH * 4, BCROW = kN * ES;
+    static constexpr int OFF_Z = 0, OFF_DY = kCK * XROW, OFF_DT = 2 * kCK * XROW, OFF_C = OFF_DT + kCK * DTROW;
+    static constexpr int STAGE = OFF_C + kCK * BCROW;
+    static constexpr int NSTAGE = 3;
+    static constexpr int SMEM = NSTAGE * STAGE;
+    static constexpr int ROW = 2 * kCK + 4;  // per-channel row [Delta 0..15 | dp 0..15], padded
+};
 
-template <typename IO, int NSPLIT>
+template <typename IO>
 __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParams p) {
-    constexpr int NT = kBwdThreads, CH = NT / NSPLIT, NS = kN / NSPLIT, ES = sizeof(IO);
+    using Ly = BwdAggLayout<IO>;
+    constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
     constexpr bool FAST = IOT<IO>::kFast;
-    constexpr int XROW = CH * ES + 16, DTROW = CH * 4 + 16, BCROW = kN * ES;
-    constexpr int OFF_Z = 0, OFF_DY = kCK * XROW, OFF_DT = 2 * kCK * XROW, OFF_C = OFF_DT + kCK * DTROW;
-    constexpr int STAGE = OFF_C + kCK * BCROW;
     extern __shared__ __align__(16) char smem[];
-    float* Cf = reinterpret_cast<float*>(smem + 2 * STAGE);
+    __shared__ __align__(16) float CT[kN * T];
+    __shared__ __align__(16) float DP[CH * Ly::ROW];
 
-    const int tid = threadIdx.x, lane = tid & 31, c = tid / NSPLIT, k = tid % NSPLIT;
-    const int base = lane & ~(NSPLIT - 1);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int hk = lane >> 4;
+    const int c = warp * 16 + (lane & 15);
     const int64_t D = p.D, L = p.L;
     const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c;
     const bool dv = d < D;
     const int g = blockIdx.y + 1;  // groups 1..G-1
     const int64_t b = blockIdx.z;
     const int64_t tb0 = (int64_t)g * p.Lg, tb1 = min64(L, tb0 + p.Lg);
-    const int ntile = (int)((tb1 - tb0 + kCK - 1) / kCK);
+    const int ntile = (int)((tb1 - tb0 + T - 1) / T);
     const bool has_z = p.has_z != 0, sp = p.sp != 0;
 
-    float2 A2[NS / 2], Gv[NS / 2];
+    float A2[NS], E[NS], an[NS];
 #pragma unroll
-    for (int j = 0; j < NS / 2; ++j) {
-        const int n = k * NS + 2 * j;
-        A2[j] = dv ? make_float2(__fmul_rn(p.A[d * kN + n], kLog2e), __fmul_rn(p.A[d * kN + n + 1], kLog2e))
-                   : make_float2(0.f, 0.f);
-        Gv[j] = make_float2(0.f, 0.f);
+    for (int s = 0; s < NS; ++s) {
+        A2[s] = dv ? __fmul_rn(p.A[d * kN + NS * hk + s], kLog2e) : 0.f;
+        E[s] = 0.f;
+        an[s] = 1.f;
     }
     const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
     const int vchx = (int)(min64(CH, D - d0) * ES / 16);
     const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
-    auto issue = [&](int j, char* st) {
-        const int64_t t0 = tb0 + (int64_t)j * kCK;
-        const int rows = (int)min64(kCK, tb1 - t0);
+    auto issue = [&](int j, char* st) {  // tile j counted from the group's end
+        const int64_t t0 = tb0 + (int64_t)(ntile - 1 - j) * T;
+        const int rows = (int)min64(T, tb1 - t0);
         const int64_t row0 = b * L + t0;
         if (has_z)
-            stage_block<NT>(st + OFF_Z, XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, kCK, CH * ES / 16, rows,
-                            vchx);
-        stage_block<NT>(st + OFF_DY, XROW, (const char*)p.dy + (row0 * D + d0) * ES, D * ES, kCK, CH * ES / 16, rows,
-                        vchx);
-        stage_block<NT>(st + OFF_DT, DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, kCK, CH * 4 / 16, rows,
-                        vchd);
-        stage_block<NT>(st + OFF_C, BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, kCK, BCROW / 16, rows,
-                        BCROW / 16);
+            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, T,
+                            CH * ES / 16, rows, vchx);
+        stage_block<NT>(st + Ly::OFF_DY, Ly::XROW, (const char*)p.dy + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
+                        rows, vchx);
+        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
+                        rows, vchd);
+        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+                        rows, Ly::BCROW / 16);
         cp_async_commit();
     };
+    float* dp = DP + c * Ly::ROW;
     float ssum = 0.f;
-    if (ntile > 0) issue(ntile - 1, smem);
-    for (int it = 0; it < ntile; ++it) {
-        const int j = ntile - 1 - it;
-        char* st = smem + (it & 1) * STAGE;
-        if (j > 0) {
-            issue(j - 1, smem + ((it + 1) & 1) * STAGE);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+#pragma unroll
+    for (int q = 0; q < Ly::NSTAGE - 1; ++q) {
+        if (q < ntile) issue(q, smem + q * Ly::STAGE);
+        else cp_async_commit();
+    }
+    for (int j = 0; j < ntile; ++j) {
+        char* st = smem + (j % Ly::NSTAGE) * Ly::STAGE;
+        {
+            const int jn = j + Ly::NSTAGE - 1;
+            if (jn < ntile) issue(jn, smem + (jn % Ly::NSTAGE) * Ly::STAGE);
+            else cp_async_commit();
+        }
+        cp_async_wait<Ly::NSTAGE - 1>();
+        __syncthreads();
+        const int64_t t0 = tb0 + (int64_t)(ntile - 1 - j) * T;
+        const int rows = (int)min64(T, tb1 - t0);
+        {
+            const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
+            for (int i = tid; i < kN * T; i += NT) {
+                const int n = i / T, tok = i - n * T;
+                CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
+            }
+        }
+        {
+            float dl[NS], pl[NS];
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                const int t = NS * hk + i;
+                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[c];
+                const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + t * Ly::XROW)[c]);
+                const float delta = token_delta<FAST>(dtv, bias, sp);
+                float dpv = dyv;
+                if (has_z) {
+                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[c]);
+                    dpv = __fmul_rn(dyv, __fmul_rn(zv, sigmoid<FAST>(zv)));
+                }
+                const bool live = t < rows;  // tokens past the end: a = 1, no adjoint input
+                dl[i] = live ? delta : 0.f;
+                pl[i] = live ? dpv : 0.f;
+                ssum = __fadd_rn(ssum, dl[i]);
+            }
+            *reinterpret_cast<float4*>(dp + NS * hk) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            *reinterpret_cast<float4*>(dp + NS * hk + 4) = make_float4(dl[4], dl[5], dl[6], dl[7]);
+            *reinterpret_cast<float4*>(dp + T + NS * hk) = make_float4(pl[0], pl[1], pl[2], pl[3]);
+            *reinterpret_cast<float4*>(dp + T + NS * hk + 4) = make_float4(pl[4], pl[5], pl[6], pl[7]);
         }
         __syncthreads();
-        for (int i = tid; i < kCK * kN; i += NT) Cf[i] = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + OFF_C)[i]);
-        __syncthreads();
-        const int rows = (int)min64(kCK, tb1 - (tb0 + (int64_t)j * kCK));
+        float2 Dl[T / 2], Pl[T / 2];
 #pragma unroll
-        for (int tb = kCK - NSPLIT; tb >= 0; tb -= NSPLIT) {
-            const int tm = tb + k;
-            const float dtv = reinterpret_cast<const float*>(st + OFF_DT + tm * DTROW)[c];
-            const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + OFF_DY + tm * XROW)[c]);
-            const float delta = token_delta<FAST>(dtv, bias, sp);
-            float dpv = dyv;
-            if (has_z) {
-                const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + OFF_Z + tm * XROW)[c]);
-                dpv = __fmul_rn(dyv, __fmul_rn(zv, sigmoid<FAST>(zv)));
-            }
+        for (int q = 0; q < T / 4; ++q) {
+            const float4 dq = *reinterpret_cast<const float4*>(dp + 4 * q);
+            const float4 pq = *reinterpret_cast<const float4*>(dp + T + 4 * q);
+            Dl[2 * q] = make_float2(dq.x, dq.y);
+            Dl[2 * q + 1] = make_float2(dq.z, dq.w);
+            Pl[2 * q] = make_float2(pq.x, pq.y);
+            Pl[2 * q + 1] = make_float2(pq.z, pq.w);
+        }
 #pragma unroll
-            for (int jj = NSPLIT - 1; jj >= 0; --jj) {
-                const float dj = NSPLIT == 1 ? delta : __shfl_sync(0xffffffffu, delta, base + jj);
-                const float pj = NSPLIT == 1 ? dpv : __shfl_sync(0xffffffffu, dpv, base + jj);
-                if (tb + jj < rows) {
-                    ssum = __fadd_rn(ssum, dj);
-                    const float2 d2 = make_float2(dj, dj), p2 = make_float2(pj, pj);
-                    const float* Ct = Cf + (tb + jj) * kN + k * NS;
+        for (int s = 0; s < NS; s += 2) {
+            const int n = NS * hk + s;
+            const float2 A2p0 = make_float2(A2[s], A2[s]), A2p1 = make_float2(A2[s + 1], A2[s + 1]);
+            float E0 = E[s], E1 = E[s + 1], n0 = an[s], n1 = an[s + 1];
 #pragma unroll
-                    for (int q = 0; q < NS / 2; ++q) {
-                        const float2 arg = __fmul2_rn(d2, A2[q]);
-                        const float2 a = make_float2(ex2(arg.x), ex2(arg.y));
-                        const float2 cc = *reinterpret_cast<const float2*>(Ct + 2 * q);
-                        Gv[q] = __fmul2_rn(__ffma2_rn(p2, cc, Gv[q]), a);
-                    }
+            for (int q = T / 4 - 1; q >= 0; --q) {
+                const float4 c40 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
+                const float4 c41 = *reinterpret_cast<const float4*>(CT + (n + 1) * T + 4 * q);
+#pragma unroll
+                for (int h2 = 1; h2 >= 0; --h2) {
+                    const int m = 2 * q + h2;
+                    const float2 cc0 = h2 ? make_float2(c40.z, c40.w) : make_float2(c40.x, c40.y);
+                    const float2 cc1 = h2 ? make_float2(c41.z, c41.w) : make_float2(c41.x, c41.y);
+                    const float2 arg0 = __fmul2_rn(Dl[m], A2p0), arg1 = __fmul2_rn(Dl[m], A2p1);
+                    const float2 r0 = __fmul2_rn(Pl[m], cc0), r1 = __fmul2_rn(Pl[m], cc1);
+                    const float a01 = ex2(arg0.y), a11 = ex2(arg1.y);
+                    E0 = __fmaf_rn(n0, E0, r0.y);
+                    E1 = __fmaf_rn(n1, E1, r1.y);
+                    const float a00 = ex2(arg0.x), a10 = ex2(arg1.x);
+                    E0 = __fmaf_rn(a01, E0, r0.x);
+                    E1 = __fmaf_rn(a11, E1, r1.x);
+                    n0 = a00;
+                    n1 = a10;
                 }
             }
+            E[s] = E0; E[s + 1] = E1; an[s] = n0; an[s + 1] = n1;
         }
         __syncthreads();
     }
+    ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, 16));
     if (dv) {
-        float* Q = p.aggQ + ((b * p.G + g) * D + d) * kN + k * NS;
+        float* Q = p.aggQ + ((b * p.G + g) * D + d) * kN + NS * hk;
 #pragma unroll
-        for (int q = 0; q < NS / 2; ++q) {
-            Q[2 * q] = Gv[q].x;
-            Q[2 * q + 1] = Gv[q].y;
-        }
-        if (k == 0) p.aggS[(b * p.G + g) * D + d] = ssum;
+        for (int s = 0; s < NS; ++s) Q[s] = __fmul_rn(an[s], E[s]);
+        if (hk == 0) p.aggS[(b * p.G + g) * D + d] = ssum;
     }
 }
 
@@ -512,15 +561,14 @@ template <typename IO> int launch_bwd_t(const BwdParams& p, cudaStream_t s) {
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
-template <typename IO, int NSPLIT> int launch_bwd_agg_t(const BwdParams& p, cudaStream_t s) {
-    constexpr int CH = kBwdThreads / NSPLIT;
-    constexpr int SMEM = bwd_agg_smem<IO, NSPLIT>();
-    auto kern = ssm_bwd_agg_kernel<IO, NSPLIT>;
+template <typename IO> int launch_bwd_agg_t(const BwdParams& p, cudaStream_t s) {
+    using Ly = BwdAggLayout<IO>;
+    auto kern = ssm_bwd_agg_kernel<IO>;
     static unsigned long long mask = 0;
-    if (!ensure_smem(kern, SMEM, mask)) return -1;
+    if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
     if (p.B == 0 || p.D == 0 || p.G <= 1) return 0;
-    dim3 grid((unsigned)((p.D + CH - 1) / CH), (unsigned)(p.G - 1), (unsigned)p.B);
-    kern<<<grid, kBwdThreads, SMEM, s>>>(p);
+    dim3 grid((unsigned)((p.D + Ly::CH - 1) / Ly::CH), (unsigned)(p.G - 1), (unsigned)p.B);
+    kern<<<grid, kBwdThreads, Ly::SMEM, s>>>(p);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -557,15 +605,8 @@ int launch_bwd(int io, const BwdParams& p, cudaStream_t s) {
     return io == 0 ? launch_bwd_t<float>(p, s) : launch_bwd_t<__nv_bfloat16>(p, s);
 }
 
-int launch_bwd_agg(int io, int nsplit, const BwdParams& p, cudaStream_t s) {
-    if (io == 0) {
-        if (nsplit == 1) return launch_bwd_agg_t<float, 1>(p, s);
-        if (nsplit == 2) return launch_bwd_agg_t<float, 2>(p, s);
-        return launch_bwd_agg_t<float, 4>(p, s);
-    }
-    if (nsplit == 1) return launch_bwd_agg_t<__nv_bfloat16, 1>(p, s);
-    if (nsplit == 2) return launch_bwd_agg_t<__nv_bfloat16, 2>(p, s);
-    return launch_bwd_agg_t<__nv_bfloat16, 4>(p, s);
+int launch_bwd_agg(int io, const BwdParams& p, cudaStream_t s) {
+    return io == 0 ? launch_bwd_agg_t<float>(p, s) : launch_bwd_agg_t<__nv_bfloat16>(p, s);
 }
 
 }  // namespace ssm

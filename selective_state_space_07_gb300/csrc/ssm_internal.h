@@ -118,6 +118,6 @@ int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, cons
                  const float* aggV, const float* aggS, float* out, cudaStream_t s);
 int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s);
 int launch_bwd(int io, const BwdParams& p, cudaStream_t s);
-int launch_bwd_agg(int io, int nsplit, const BwdParams& p, cudaStream_t s);
+int launch_bwd_agg(int io, const BwdParams& p, cudaStream_t s);
 
 }  // namespace ssm
