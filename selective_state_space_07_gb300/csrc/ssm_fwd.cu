@@ -55,8 +55,12 @@ template <typename IO> struct FwdLayout {
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
-template <typename IO, bool AGG>
-__global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p) {
+// MINB: resident CTAs per SM the register budget is cut for (3 when the grid
+// can use a third CTA per SM; 1 -- no cut -- when one L-group's grid fits in
+// two CTAs per SM, which leaves the scheduler registers for the interleaved
+// state chains).
+template <typename IO, bool AGG, int MINB>
+__global__ void __launch_bounds__(kFwdThreads, MINB) ssm_fwd_kernel(const FwdParams p) {
     using Ly = FwdLayout<IO>;
     constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
     constexpr bool FAST = IOT<IO>::kFast;
@@ -192,53 +196,59 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_fwd_kernel(const FwdParams p)
         const bool ck = !AGG && p.ckpt && dv;
         float* ckp = ck ? p.ckpt + ((b * nck + t0 / kCkpt) * kN + NS * hk) * D + d : nullptr;
         float2 acc[T / 2];
-        // two states advance together through the tokens (independent
-        // chains for the scheduler); the readout chain still takes the
-        // states in order
+        // SI states advance together through the tokens (independent chains
+        // for the scheduler); the readout chain still takes the states in order
+        constexpr int SI = 8;
 #pragma unroll
-        for (int s = 0; s < NS; s += 2) {
+        for (int s = 0; s < NS; s += SI) {
             const int n = NS * hk + s;
-            const float2 A2p0 = f2(A2[s], A2[s]), A2p1 = f2(A2[s + 1], A2[s + 1]);
-            float hp0 = h[s], hp1 = h[s + 1];
-            if (ck) {  // states before token t0
-                ckp[s * D] = hp0;
-                ckp[(s + 1) * D] = hp1;
+            float2 A2p[SI];
+            float hp[SI];
+#pragma unroll
+            for (int i = 0; i < SI; ++i) {
+                A2p[i] = f2(A2[s + i], A2[s + i]);
+                hp[i] = h[s + i];
+                if (ck) ckp[(s + i) * D] = hp[i];  // states before token t0
             }
 #pragma unroll
             for (int q = 0; q < T / 4; ++q) {
-                const float4 b40 = *reinterpret_cast<const float4*>(BT + n * T + 4 * q);
-                const float4 b41 = *reinterpret_cast<const float4*>(BT + (n + 1) * T + 4 * q);
-                float4 c40, c41;
-                if (!AGG) {
-                    c40 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
-                    c41 = *reinterpret_cast<const float4*>(CT + (n + 1) * T + 4 * q);
+                float4 b4[SI], c4[SI];
+#pragma unroll
+                for (int i = 0; i < SI; ++i) {
+                    b4[i] = *reinterpret_cast<const float4*>(BT + (n + i) * T + 4 * q);
+                    if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CT + (n + i) * T + 4 * q);
                 }
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
                     const int m = 2 * q + h2;
-                    const float2 bb0 = h2 ? f2(b40.z, b40.w) : f2(b40.x, b40.y);
-                    const float2 bb1 = h2 ? f2(b41.z, b41.w) : f2(b41.x, b41.y);
-                    const float2 arg0 = __fmul2_rn(Dl[m], A2p0), arg1 = __fmul2_rn(Dl[m], A2p1);
-                    const float a00 = ex2(arg0.x), a01 = ex2(arg0.y), a10 = ex2(arg1.x), a11 = ex2(arg1.y);
-                    const float2 ub0 = __fmul2_rn(Ul[m], bb0), ub1 = __fmul2_rn(Ul[m], bb1);
-                    const float h00 = __fmaf_rn(a00, hp0, ub0.x), h10 = __fmaf_rn(a10, hp1, ub1.x);
-                    const float h01 = __fmaf_rn(a01, h00, ub0.y), h11 = __fmaf_rn(a11, h10, ub1.y);
-                    hp0 = h01;
-                    hp1 = h11;
+                    float hv0[SI], hv1[SI];
+#pragma unroll
+                    for (int i = 0; i < SI; ++i) {
+                        const float2 bb = h2 ? f2(b4[i].z, b4[i].w) : f2(b4[i].x, b4[i].y);
+                        const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
+                        const float a0 = ex2(arg.x), a1 = ex2(arg.y);
+                        const float2 ub = __fmul2_rn(Ul[m], bb);
+                        hv0[i] = __fmaf_rn(a0, hp[i], ub.x);
+                        hv1[i] = __fmaf_rn(a1, hv0[i], ub.y);
+                        hp[i] = hv1[i];
+                    }
                     if (!AGG) {
-                        const float2 cc0 = h2 ? f2(c40.z, c40.w) : f2(c40.x, c40.y);
-                        const float2 cc1 = h2 ? f2(c41.z, c41.w) : f2(c41.x, c41.y);
-                        float2 r = s == 0 ? __fmul2_rn(cc0, f2(h00, h01)) : __ffma2_rn(cc0, f2(h00, h01), acc[m]);
-                        acc[m] = __ffma2_rn(cc1, f2(h10, h11), r);
+                        float2 r = acc[m];
+#pragma unroll
+                        for (int i = 0; i < SI; ++i) {
+                            const float2 cc = h2 ? f2(c4[i].z, c4[i].w) : f2(c4[i].x, c4[i].y);
+                            r = (s + i == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i])) : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r);
+                        }
+                        acc[m] = r;
                     }
                 }
                 if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
-                    ckp[s * D + kN * D] = hp0;
-                    ckp[(s + 1) * D + kN * D] = hp1;
+#pragma unroll
+                    for (int i = 0; i < SI; ++i) ckp[(s + i) * D + kN * D] = hp[i];
                 }
             }
-            h[s] = hp0;
-            h[s + 1] = hp1;
+#pragma unroll
+            for (int i = 0; i < SI; ++i) h[s + i] = hp[i];
         }
         if (!AGG) {
             // ---- E: half readouts -> full readout of this lane's 8 tokens
@@ -396,16 +406,23 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     flag_nonfinite(p.status, __fmaf_rn(yv, 0.0f, 0.0f));
 }
 
-template <typename IO, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream_t s) {
+template <typename IO, bool AGG, int MINB> int launch_fwd_v(const FwdParams& p, dim3 grid, cudaStream_t s) {
     using Ly = FwdLayout<IO>;
     static unsigned long long mask = 0;
-    auto kern = ssm_fwd_kernel<IO, AGG>;
+    auto kern = ssm_fwd_kernel<IO, AGG, MINB>;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
+    kern<<<grid, kFwdThreads, Ly::SMEM, s>>>(p);
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+template <typename IO, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream_t s) {
+    using Ly = FwdLayout<IO>;
     const int gy = AGG ? p.G - 1 : p.G;
     if (gy <= 0 || p.B == 0 || p.D == 0) return 0;
     dim3 grid((unsigned)((p.D + Ly::CH - 1) / Ly::CH), (unsigned)gy, (unsigned)p.B);
-    kern<<<grid, kFwdThreads, Ly::SMEM, s>>>(p);
-    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+    const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+    if (!AGG && p.G == 1 && ctas <= 2 * (int64_t)sm_count()) return launch_fwd_v<IO, AGG, 1>(p, grid, s);
+    return launch_fwd_v<IO, AGG, 3>(p, grid, s);
 }
 
 template <typename IO, int NSPLIT> int launch_step_t(const StepParams& p, cudaStream_t s) {
@@ -436,8 +453,9 @@ template <typename K> int blocks_per_sm(K kern, int threads, int smem, int* cach
 
 int fwd_blocks_per_sm(int io) {
     static int cache_f[64] = {0}, cache_b[64] = {0};
-    return io == 0 ? blocks_per_sm(ssm_fwd_kernel<float, false>, kFwdThreads, FwdLayout<float>::SMEM, cache_f)
-                   : blocks_per_sm(ssm_fwd_kernel<__nv_bfloat16, false>, kFwdThreads,
+    // the variant that runs whenever the grid can use more than 2 CTAs per SM
+    return io == 0 ? blocks_per_sm(ssm_fwd_kernel<float, false, 3>, kFwdThreads, FwdLayout<float>::SMEM, cache_f)
+                   : blocks_per_sm(ssm_fwd_kernel<__nv_bfloat16, false, 3>, kFwdThreads,
                                    FwdLayout<__nv_bfloat16>::SMEM, cache_b);
 }
 int fwd_channels_per_cta() { return FwdLayout<float>::CH; }
