@@ -10,13 +10,16 @@
 // C_t rows are staged into shared memory with cp.async (four tiles in
 // flight); B/C are widened to fp32 and transposed (state-major) once per
 // tile, so a half-warp reads one state's row of 4 tokens with one broadcast
-// 16-byte load. The arithmetic is packed over token pairs (f32x2).
+// 16-byte load. Delta*A, u*B and the readout are packed over token pairs
+// (f32x2); each state's update is a scalar fused multiply-add chain.
 //
 // Per tile: (A) each lane prepares Delta, u and the gate factor for its 8
 // tokens (one lane of the pair per token) and shares Delta/u with its
-// partner through shared memory; (S) per state, the 16-token recurrence and
-// the readout chain; (E) the two half-readouts of each token are added and
-// each lane gates and writes y for its 8 tokens.
+// partner through shared memory; (S) the lane's 8 state recurrences advance
+// side by side through the 16 tokens (independent chains for the scheduler)
+// while the readout chain takes the states in order; (E) the two
+// half-readouts of each token are added and each lane gates and writes y for
+// its 8 tokens.
 //
 // Canonical readout order (the step kernel evaluates the same operations):
 // each half of the states is a sequential fused multiply-add chain
