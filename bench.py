@@ -192,6 +192,23 @@ def init_dist(world, backend):
     return None
 
 
+def max_over_ranks(values, dist, device):
+    """Each value's maximum over the ranks (the job's time is its slowest
+    replica's); values unchanged on one process."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
+
+def job_value(world, token_channels, ms):
+    """Whole-job throughput in G(token*channel)/s: every rank processes its own
+    replica of the workload, so the job does world * B*L*D per step."""
+    return world * token_channels / (ms * 1e-3) / 1e9
+
+
 def visible_gpu_ids(world):
     vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
     ids = [int(v) for v in vis.split(",") if v.strip().isdigit()][:world]
@@ -352,13 +369,10 @@ def run_ours(args, w):
     tb = [e[2].elapsed_time(e[3]) for e in ev]
     ms_f, ms_b = sum(tf) / len(tf), sum(tb) / len(tb)
     ms_step = ms_f + ms_b
-    if dist:
-        t = torch.tensor([ms_f, ms_b, ms_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_f, ms_b, ms_step = [float(v) for v in t]
+    ms_f, ms_b, ms_step = max_over_ranks([ms_f, ms_b, ms_step], dist, dev)
     status = ssm.poll_status(ws)
     tc = w.B * w.L * w.D
-    value = world * tc / (ms_step * 1e-3) / 1e9
+    value = job_value(world, tc, ms_step)
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -381,11 +395,8 @@ def run_ours(args, w):
         ee.record(pipe.s_out)  # after the last step's last copy back
         pipe.synchronize()
         e2e_ms = es.elapsed_time(ee) / e2e_steps
-        if dist:
-            t = torch.tensor([e2e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t[0])
-        e2e = {"value": round(world * tc / (e2e_ms * 1e-3) / 1e9, 3), "unit": UNIT,
+        e2e_ms = max_over_ranks([e2e_ms], dist, dev)[0]
+        e2e = {"value": round(job_value(world, tc, e2e_ms), 3), "unit": UNIT,
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in host.values()),
                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in res.values()),
                "ms_per_step": round(e2e_ms, 4),
