@@ -19,8 +19,9 @@
 // the lane. Per chunk:
 //   A  each lane computes Delta, u, dp (and sigmoid(v), dy*silu'(z)) for its
 //      own channel and swaps Delta, u, dp with its partner (shuffle);
-//   S  per state: forward from the checkpoint over the 8 tokens (a_t, h_t in
-//      registers) and the reverse recurrence over them, for both channels;
+//   S  per state, the two channels side by side: forward from the
+//      checkpoint over the 8 tokens (a_t, h_t in registers) and the reverse
+//      recurrence over them;
 //      per-token state sums stay in registers; dB/dC contributions go
 //      through a per-warp shared-memory transpose every 4 states, then a
 //      per-CTA sum over warps and one vector atomic per 4 outputs;
@@ -58,6 +59,8 @@ template <typename IO> struct BwdLayout {
     // down a column and 16-byte loads along a row)
     static constexpr int SPB = 4;                  // states per transpose
     static constexpr int TBROW = SPB * 2 * T + 4;
+    // the reduction gives each lane of a half-warp one 4-float column of a row
+    static_assert(SPB * 2 * T == 16 * 4, "a transpose row must hold 16 column quads");
     static constexpr int OFF_TB = NSTAGE * STAGE;
     static constexpr int SMEM = OFF_TB + NW * 32 * TBROW * 4;
 };
