@@ -196,6 +196,42 @@ def workload_inputs(name: str, **kw) -> Inputs:
                        delta_target=w.delta_target, **kw)
 
 
+@dataclass
+class ConvInputs:
+    """One problem for the conv1d + SiLU in front of the scan: xin [B,L,D]
+    (the in_proj output), w [D,K], bias [D] (None = 0), state [B,D,K-1]
+    (None = zeros), dx [B,L,D] (the gradient arriving at the conv output)."""
+    B: int
+    L: int
+    D: int
+    K: int
+    io: str
+    xin: np.ndarray
+    w: np.ndarray
+    bias: Optional[np.ndarray]
+    state: Optional[np.ndarray]
+    dx: np.ndarray
+
+
+def make_conv_inputs(B: int, L: int, D: int, K: int = 4, *, io: str = "f32", seed: int = 0,
+                     bias: bool = True, with_state: bool = False) -> ConvInputs:
+    """Draw a conv problem: xin, dx ~ N(0,1) (bf16-rounded for bf16 I/O);
+    w ~ N(0, 1/K) (the scale of the usual 1/sqrt(fan_in) init); bias ~
+    N(0, 0.1^2) when drawn (the canonical init sets it to zero); state ~
+    N(0,1) when drawn. Per-tensor seeds come from the same SplitMix64
+    streams as make_inputs (x, dt, z, dy, h0 slots), so the draws are fixed
+    by (seed, shape)."""
+    s = tensor_seeds(seed)
+    tc = B * L * D
+    rnd = round_bf16 if io == "bf16" else (lambda a: a)
+    xin = rnd(normal_f32(s["x"], tc)).reshape(B, L, D)
+    w = normal_f32(s["dt"], D * K, 0.0, float(1.0 / np.sqrt(K))).reshape(D, K)
+    b = normal_f32(s["z"], D, 0.0, 0.1) if bias else None
+    st = normal_f32(s["h0"], B * D * (K - 1)).reshape(B, D, K - 1) if with_state and K > 1 else None
+    dx = rnd(normal_f32(s["dy"], tc)).reshape(B, L, D)
+    return ConvInputs(B, L, D, K, io, xin, w, b, st, dx)
+
+
 def recipe_text() -> str:
     lines = []
     for w in WORKLOADS.values():

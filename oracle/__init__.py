@@ -9,7 +9,10 @@ with g++ -O2 -ffp-contract=off). This module only builds that file, marshals
 numpy arrays and calls it. Parity status: every function is pinned by the
 ``-m "not gpu"`` tests in ``tests/test_oracle_pins.py`` (closed forms,
 brute-force quadratic form, special cases, finite differences, adjoint and
-step identities); none is "parity unpinned".
+step identities) and, for the conv1d + SiLU in front of the scan
+(``conv_oracle.cpp``), in ``tests/test_conv_oracle_pins.py`` (numpy's
+convolution, special kernels, causality, state chaining, finite
+differences); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -23,6 +26,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ssm_oracle.cpp")
+_SRCS = [_SRC, os.path.join(_HERE, "conv_oracle.cpp")]
 _LIB = os.path.join(_HERE, "libssm_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -33,9 +37,9 @@ CXXFLAGS = ["-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
 
 def build(force: bool = False) -> str:
     """Compile the oracle library if it is missing or older than its source."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["g++", *CXXFLAGS, _SRC, "-o", tmp])
+        subprocess.check_call(["g++", *CXXFLAGS, *_SRCS, "-o", tmp])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -56,6 +60,12 @@ class _StepArgs(ctypes.Structure):
             "x_t", "dt_t", "z_t", "Bm_t", "Cm_t", "A", "Dskip", "dt_bias", "state", "y_t")]
 
 
+class _ConvArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("L", ctypes.c_int64), ("D", ctypes.c_int64), ("K", ctypes.c_int64)] + [
+        (name, ctypes.c_void_p) for name in (
+            "xin", "w", "bias", "state", "x", "state_out", "dx", "dxin", "dw", "dbias", "dstate")]
+
+
 def lib():
     global _lib
     with _lock:
@@ -71,6 +81,11 @@ def lib():
                 f.argtypes = [ctypes.POINTER(_StepArgs)]
                 f.restype = ctypes.c_int
             _lib.ssm_oracle_hardware_threads.restype = ctypes.c_int
+            for name in ("fwd", "bwd"):
+                for dt in ("f64", "f32"):
+                    f = getattr(_lib, f"conv_oracle_{name}_{dt}")
+                    f.argtypes = [ctypes.POINTER(_ConvArgs)]
+                    f.restype = ctypes.c_int
     return _lib
 
 
@@ -157,3 +172,47 @@ def step(state: np.ndarray, x_t, dt_t, z_t, Bm_t, Cm_t, A, Dskip, dt_bias,
     if rc != 0:
         raise ValueError(f"oracle step rejected the arguments ({rc})")
     return y
+
+
+def conv_fwd(xin, w, bias=None, state=None, dtype: str = "f64") -> Dict[str, np.ndarray]:
+    """Causal depthwise conv1d + SiLU ("in_proj -> causal depthwise conv1d ->
+    SiLU"): xin [B,L,D], w [D,K], bias [D] (None = 0), state [B,D,K-1] (the
+    K-1 inputs before t = 0; None = zeros). Returns x = silu(conv) [B,L,D],
+    pre = conv before the SiLU, and state_out [B,D,K-1]."""
+    t = _NP[dtype]
+    xin = _np(xin, t)
+    B, L, D = xin.shape
+    K = int(np.asarray(w).shape[1])
+    args = _ConvArgs(B=B, L=L, D=D, K=K)
+    keep = [xin]
+    args.xin = _ptr(xin)
+    _fill(args, keep, t, w=w, bias=bias, state=state)
+    x = np.zeros((B, L, D), t)
+    so = np.zeros((B, D, max(K - 1, 0)), t)
+    args.x, args.state_out = _ptr(x), _ptr(so)
+    rc = getattr(lib(), f"conv_oracle_fwd_{dtype}")(ctypes.byref(args))
+    if rc != 0:
+        raise ValueError(f"oracle conv fwd rejected the arguments ({rc})")
+    return {"x": x, "state_out": so}
+
+
+def conv_bwd(xin, w, dx, bias=None, state=None, dtype: str = "f64") -> Dict[str, np.ndarray]:
+    """Reverse pass of conv_fwd for loss = <dx, x>. Returns dxin [B,L,D],
+    dw [D,K] and dbias [D] (summed over batch and tokens) and dstate
+    [B,D,K-1] (the gradient of the initial conv state)."""
+    t = _NP[dtype]
+    xin = _np(xin, t)
+    B, L, D = xin.shape
+    K = int(np.asarray(w).shape[1])
+    args = _ConvArgs(B=B, L=L, D=D, K=K)
+    keep = [xin]
+    args.xin = _ptr(xin)
+    _fill(args, keep, t, w=w, bias=bias, state=state, dx=dx)
+    out = {"dxin": np.zeros((B, L, D), t), "dw": np.zeros((D, K), t), "dbias": np.zeros((D,), t),
+           "dstate": np.zeros((B, D, max(K - 1, 0)), t)}
+    for k, v in out.items():
+        setattr(args, k, _ptr(v))
+    rc = getattr(lib(), f"conv_oracle_bwd_{dtype}")(ctypes.byref(args))
+    if rc != 0:
+        raise ValueError(f"oracle conv bwd rejected the arguments ({rc})")
+    return out
