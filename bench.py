@@ -15,6 +15,10 @@ the job's time is the max over ranks.
 
 --impl reference times the oracle (plain sequential C++, fp32, all host
 cores) on bounded samples of the same workload, on rank 0 only.
+
+--op conv1d times the causal depthwise conv1d + SiLU in front of the scan
+(ssm_conv1d_fwd + ssm_conv1d_bwd, K = 4) on the workload's B, L, D instead,
+with its own metric, HBM roofline and oracle baseline.
 """
 from __future__ import annotations
 
@@ -66,6 +70,23 @@ def algorithmic_bytes(w, pass_):
     # bwd: read x, z, dy (e), dt (4); write dx, dz (e), d_dt (4); read Bm, Cm (e), write dB, dC (4);
     # read A, Dskip, dt_bias; write dA, dD, d_dt_bias
     return tc * (5 * e + 8) + bl * 2 * w.N * (e + 4) + w.D * w.N * 8 + 4 * w.D * 4
+
+
+CONV_K = 4
+CONV_METRIC = "conv1d+SiLU fwd+bwd G(token·channel)/s on 1 GB300; % of HBM roofline"
+
+
+def conv_algorithmic_bytes(w, pass_, K=CONV_K):
+    """Conv bytes moved at least once: the forward reads xin and writes x; the
+    backward reads xin and dx and writes dxin (e bytes each per
+    token-channel); both read w and bias, the forward reads and writes the
+    [B, D, K-1] state, the backward writes dw, dbias and the state's gradient."""
+    e = 2 if w.io == "bf16" else 4
+    tc, small = w.B * w.L * w.D, w.D * (K + 1) * 4
+    st = w.B * w.D * (K - 1) * 4
+    if pass_ == "fwd":
+        return tc * 2 * e + small + 2 * st
+    return tc * 3 * e + 2 * small + 2 * st
 
 
 def mufu_ops(w, pass_):
@@ -454,6 +475,192 @@ def run_ours(args, w):
     return 0
 
 
+def _conv_oracle_step(c):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.conv_fwd(c.xin, c.w, c.bias, c.state, dtype="f32")
+    oracle.conv_bwd(c.xin, c.w, c.dx, c.bias, c.state, dtype="f32")
+    return time.perf_counter() - t0
+
+
+def conv_cpu_sample(w, budget_s):
+    """The conv oracle (fp32, one thread: plain loops per channel) on batch
+    row 0, all tokens, the first D_s channels sized for about budget_s."""
+    c = gen.make_conv_inputs(1, w.L, 64, CONV_K, io=w.io, seed=w.seed, with_state=True)
+    t = _conv_oracle_step(c)
+    ds = int(min(w.D, max(64, 64 * budget_s / max(t, 1e-4))) // 8 * 8)
+    return gen.make_conv_inputs(1, w.L, ds, CONV_K, io=w.io, seed=w.seed, with_state=True), ds
+
+
+def run_conv_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    c, ds = conv_cpu_sample(w, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _conv_oracle_step(c)
+    ts = [_conv_oracle_step(c) for _ in range(args.steps)]
+    total = sum(ts)
+    val = w.L * ds * len(ts) / total / 1e9
+    sample = f"per step: batch row 0, first {ds} of {w.D} channels, all {w.L} tokens, fp32 conv oracle fwd+bwd"
+    line = {
+        "impl": "reference", "metric": CONV_METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(ts), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + "-conv1d", "B": w.B, "L": w.L, "D": w.D, "K": CONV_K, "io_dtype": w.io},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_conv(args, w):
+    """The conv1d + SiLU pair on the workload's activations: one step = one
+    ssm_conv1d_fwd and one ssm_conv1d_bwd, each timed with CUDA events after
+    an L2 flush, inputs resident in HBM."""
+    import torch
+    import selective_state_space_07_gb300 as ssm
+
+    rank, world, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm.build()
+    c = gen.make_conv_inputs(w.B, w.L, w.D, CONV_K, io=w.io, seed=w.seed, with_state=True)
+    io = torch.bfloat16 if w.io == "bf16" else torch.float32
+
+    def up(a, dtype=torch.float32):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(dev, dtype)
+
+    xin, dx = up(c.xin, io), up(c.dx, io)
+    wt, bias, st = up(c.w), up(c.bias), up(c.state)
+    del c
+    x, dxin = torch.empty_like(xin), torch.empty_like(xin)
+    st_out = torch.empty_like(st)
+    ws = ssm.Workspace(1, 1, 8, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    grads = None
+
+    def fwd():
+        ssm.conv1d_fwd(xin, wt, bias, st, x=x, state_out=st_out, workspace=ws)
+        return ssm.last_launch_count()
+
+    def bwd():
+        nonlocal grads
+        grads = ssm.conv1d_bwd(xin, wt, dx, bias, st, dxin=dxin, want_dstate=True, workspace=ws)
+        return ssm.last_launch_count()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        flush.zero_()
+        bwd()
+    torch.cuda.synchronize()
+    if ssm.poll_status(ws) != 0:
+        raise RuntimeError("non-finite outputs during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        launches += fwd()
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        launches += bwd()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop(set(visible_gpu_ids(world))) if rank == 0 else None
+    ms_f = sum(e[0].elapsed_time(e[1]) for e in ev) / len(ev)
+    ms_b = sum(e[2].elapsed_time(e[3]) for e in ev) / len(ev)
+    ms_f, ms_b = max_over_ranks([ms_f, ms_b], dist, dev)
+    status = ssm.poll_status(ws)
+    tc = w.B * w.L * w.D
+    value = job_value(world, tc, ms_f + ms_b)
+
+    # end to end: pinned host inputs in, both passes, results back, one stream
+    e2e = None
+    if not args.no_e2e:
+        h_in = {"xin": xin.cpu().pin_memory(), "dx": dx.cpu().pin_memory()}
+        h_out = {"x": torch.empty_like(h_in["xin"]).pin_memory(), "dxin": torch.empty_like(h_in["xin"]).pin_memory(),
+                 "dw": torch.empty(w.D, CONV_K).pin_memory(), "dbias": torch.empty(w.D).pin_memory()}
+
+        def e2e_step():
+            xin.copy_(h_in["xin"], non_blocking=True)
+            dx.copy_(h_in["dx"], non_blocking=True)
+            fwd()
+            bwd()
+            h_out["x"].copy_(x, non_blocking=True)
+            h_out["dxin"].copy_(dxin, non_blocking=True)
+            h_out["dw"].copy_(grads["dw"], non_blocking=True)
+            h_out["dbias"].copy_(grads["dbias"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        n = max(3, min(args.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        es.record(stream)
+        for _ in range(n):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks([es.elapsed_time(ee) / n], dist, dev)[0]
+        e2e = {"value": round(job_value(world, tc, e2e_ms), 3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in h_out.values()),
+               "ms_per_step": round(e2e_ms, 4), "api": "conv1d_fwd + conv1d_bwd on one stream, pinned host copies"}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind, _ = measured_peaks()
+    rf = {}
+    for name, ms in (("fwd", ms_f), ("bwd", ms_b)):
+        ab = conv_algorithmic_bytes(w, name)
+        ach = ab / (ms * 1e-3) / 1e9
+        rf[name] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(ach / peak, 4), "peak_kind": peak_kind, "kernel": f"ssm_conv_{name}_kernel",
+                    "algorithmic_bytes_per_launch": ab, "ms_per_launch": round(ms, 5),
+                    "traffic": profiled_traffic("ssm_conv1d_" + name, w.name)}
+    dom = "bwd" if ms_b >= ms_f else "fwd"
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cs, ds = conv_cpu_sample(w, 6.0)
+        ts = []
+        while sum(ts) < 12.0 and len(ts) < 50:
+            ts.append(_conv_oracle_step(cs))
+        cpu = {"value": w.L * ds * len(ts) / sum(ts) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"batch row 0, first {ds} of {w.D} channels, all {w.L} tokens, fp32 conv oracle "
+                         f"fwd+bwd, {len(ts)} repetitions, {sum(ts):.1f} s"}
+    line = {
+        "metric": CONV_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_f + ms_b, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + "-conv1d", "B": w.B, "L": w.L, "D": w.D, "K": CONV_K, "io_dtype": w.io,
+                   "seed": w.seed, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (129 MB) and a 512 MiB write flushes L2 before every pass",
+                   "ms_fwd": round(ms_f, 5), "ms_bwd": round(ms_b, 5),
+                   "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
+        "roofline": rf[dom], "roofline_other": rf["fwd" if dom == "bwd" else "bwd"],
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk, "status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -465,10 +672,14 @@ def main():
     ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--op", choices=("scan", "conv1d"), default="scan",
+                    help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = gen.WORKLOADS[args.workload]
+    if args.op == "conv1d":
+        return run_conv_reference(args, w) if args.impl == "reference" else run_conv(args, w)
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

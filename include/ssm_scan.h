@@ -184,6 +184,57 @@ int ssm_scan_fwd_noalloc(const ssm_fwd_args* args, void* stream);
  * i < n, fp32 device arrays; dA_log may alias dA. Asynchronous on stream. */
 int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, void* stream);
 
+/* Causal depthwise conv1d + SiLU, the step in front of the scan
+ * (rustytorch commit log, "MambaBlock" S6 forward commit: "in_proj -> causal
+ * depthwise conv1d -> SiLU -> x_proj -> ..."; the MambaRecurrence commit
+ * carries the conv-ring state between steps). Per (b, d) channel, with the
+ * K-1 inputs before t = 0 in state_in (NULL = zeros):
+ *   x[t] = silu(bias[d] + sum_{k<K} w[d,k] * xin[t-(K-1)+k])
+ * xin, x [B,L,D] in the I/O dtype (SSM_F32 or SSM_BF16); w [D,K] fp32 with
+ * K in 1..4 (else SSM_ERR_UNSUPPORTED); bias [D] fp32 (NULL = 0); state_in,
+ * state_out [B,D,K-1] fp32, oldest input first (state_out, nullable, gets
+ * the last K-1 inputs). D must be a multiple of 8 and every pointer 16-byte
+ * aligned (else SSM_ERR_ALIGNMENT). x must not alias xin (chunks read the
+ * K-1 inputs before their start; SSM_ERR_INVALID_ARG). state_out may be
+ * state_in (every ring entry is read before any is written; each channel's
+ * tokens then go to one warp): with L = 1 that is the conv-ring step of
+ * decoding.
+ * workspace: nullable; when given (>= 256 bytes) non-finite outputs are
+ * latched in its status word (ssm_poll_status). Asynchronous on `stream`;
+ * the caller owns every buffer. */
+typedef struct {
+    int64_t B, L, D, K;
+    int32_t io_dtype;
+    int32_t pad_;
+    const void* xin;
+    const float* w;
+    const float* bias;
+    const float* state_in;
+    void* x;
+    float* state_out;
+    void* workspace;
+} ssm_conv_args;
+
+/* Reverse pass of ssm_conv1d_fwd for loss = <dx, x>.
+ * f: the forward's arguments (xin, w, bias, state_in are read; f.x and
+ *   f.state_out are not touched). dx [B,L,D] I/O dtype.
+ * Outputs: dxin [B,L,D] I/O dtype (must alias neither dx nor xin: chunks
+ *   read K-1 tokens past their end); dw [D,K] and dbias [D]
+ *   fp32, OVERWRITTEN (zeroed on the stream first; summed over batch and
+ *   tokens; dbias nullable); dstate_in [B,D,K-1] fp32 (nullable) = the
+ *   gradient of the initial conv state. */
+typedef struct {
+    ssm_conv_args f;
+    const void* dx;
+    void* dxin;
+    float* dw;
+    float* dbias;
+    float* dstate_in;
+} ssm_conv_bwd_args;
+
+int ssm_conv1d_fwd(const ssm_conv_args* args, void* stream);
+int ssm_conv1d_bwd(const ssm_conv_bwd_args* args, void* stream);
+
 /* Bytes of workspace a fwd or bwd call of this shape needs (>= 256). */
 size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);
 /* fp32 elements of the checkpoint buffer: B * ceil(L/8) * N * D. */

@@ -177,8 +177,8 @@ def step(state: np.ndarray, x_t, dt_t, z_t, Bm_t, Cm_t, A, Dskip, dt_bias,
 def conv_fwd(xin, w, bias=None, state=None, dtype: str = "f64") -> Dict[str, np.ndarray]:
     """Causal depthwise conv1d + SiLU ("in_proj -> causal depthwise conv1d ->
     SiLU"): xin [B,L,D], w [D,K], bias [D] (None = 0), state [B,D,K-1] (the
-    K-1 inputs before t = 0; None = zeros). Returns x = silu(conv) [B,L,D],
-    pre = conv before the SiLU, and state_out [B,D,K-1]."""
+    K-1 inputs before t = 0; None = zeros). Returns x = silu(conv) [B,L,D]
+    and state_out [B,D,K-1] (the last K-1 inputs)."""
     t = _NP[dtype]
     xin = _np(xin, t)
     B, L, D = xin.shape

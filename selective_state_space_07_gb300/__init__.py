@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "SsmError", "build", "lib", "scan_fwd", "scan_bwd", "step", "dA_log_grad", "poll_status",
     "clear_status", "workspace_bytes", "ckpt_elems", "CKPT_INTERVAL", "Workspace", "scan_fwd_bwd_host",
-    "last_launch_count", "HostPipeline",
+    "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -68,6 +68,16 @@ class StepArgs(ctypes.Structure):
         ("nsplit", ctypes.c_int32), ("pad_", ctypes.c_int32)]
 
 
+class ConvArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("L", ctypes.c_int64), ("D", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("io_dtype", ctypes.c_int32), ("pad_", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in ("xin", "w", "bias", "state_in", "x", "state_out", "workspace")]
+
+
+class ConvBwdArgs(ctypes.Structure):
+    _fields_ = [("f", ConvArgs)] + [(n, ctypes.c_void_p) for n in ("dx", "dxin", "dw", "dbias", "dstate_in")]
+
+
 EXPORTS = {
     "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
@@ -80,6 +90,8 @@ EXPORTS = {
     "ssm_clear_status": ([ctypes.c_void_p, ctypes.c_void_p], ctypes.c_int),
     "ssm_status_string": ([ctypes.c_int], ctypes.c_char_p),
     "ssm_last_launch_count": ([], ctypes.c_int),
+    "ssm_conv1d_fwd": ([ctypes.POINTER(ConvArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_conv1d_bwd": ([ctypes.POINTER(ConvBwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_dA_log_grad": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
                         ctypes.c_int),
 }
@@ -311,6 +323,77 @@ def dA_log_grad(dA, A, out=None, stream=None):
     _check(lib().ssm_dA_log_grad(_p(dA), _p(A), _p(out), A.numel(), _stream(A.device, stream)),
            "ssm_dA_log_grad")
     return out
+
+
+def _conv_struct(xin, w, bias, state_in, x, state_out, workspace):
+    if xin.dim() != 3:
+        raise ValueError("xin must be [B, L, D]")
+    B, L, D = xin.shape
+    dev, io = xin.device, xin.dtype
+    if dev.type != "cuda":
+        raise ValueError("the conv runs on a CUDA device; xin is on " + str(dev))
+    if io not in _IO:
+        raise TypeError(f"xin dtype must be float32 or bfloat16, got {io}")
+    if w.dim() != 2 or w.shape[0] != D:
+        raise ValueError("w must be [D, K]")
+    K = w.shape[1]
+    _need(xin, "xin", (B, L, D), io, dev)
+    _need(w, "w", (D, K), torch.float32, dev)
+    _opt(bias, "bias", (D,), torch.float32, dev)
+    _opt(state_in, "state_in", (B, D, K - 1), torch.float32, dev)
+    _opt(x, "x", (B, L, D), io, dev)
+    _opt(state_out, "state_out", (B, D, K - 1), torch.float32, dev)
+    return ConvArgs(B=B, L=L, D=D, K=K, io_dtype=_IO[io], xin=_p(xin), w=_p(w), bias=_p(bias),
+                    state_in=_p(state_in), x=_p(x), state_out=_p(state_out),
+                    workspace=None if workspace is None else workspace.buf.data_ptr())
+
+
+def conv1d_fwd(xin, w, bias=None, state_in=None, *, x=None, state_out=None, want_state=False, workspace=None,
+               stream=None):
+    """Causal depthwise conv1d + SiLU in front of the scan:
+    x[b,t,d] = silu(bias[d] + sum_k w[d,k] * xin[b, t-(K-1)+k, d]), with the K-1 inputs before t = 0 taken
+    from ``state_in`` [B, D, K-1] (zeros when None). xin, x [B, L, D] fp32 or bf16; w [D, K] fp32, K <= 4;
+    D a multiple of 8. Returns (x, state_out); state_out ([B, D, K-1], the last K-1 inputs) is None unless
+    given or ``want_state``."""
+    B, L, D = xin.shape
+    K = w.shape[1] if w.dim() == 2 else 0
+    x = torch.empty_like(xin) if x is None else x
+    if state_out is None and want_state:
+        state_out = torch.empty(B, D, max(K - 1, 0), dtype=torch.float32, device=xin.device)
+    args = _conv_struct(xin, w, bias, state_in, x, state_out, workspace)
+    _check(lib().ssm_conv1d_fwd(ctypes.byref(args), _stream(xin.device, stream)), "ssm_conv1d_fwd")
+    return x, state_out
+
+
+def conv1d_bwd(xin, w, dx, bias=None, state_in=None, *, dxin=None, want_dstate=False, workspace=None,
+               stream=None):
+    """Reverse pass of conv1d_fwd for loss = <dx, x>. Returns dict dxin [B, L, D] (xin's dtype), dw [D, K],
+    dbias [D] (when ``bias`` is given) and dstate_in [B, D, K-1] (when ``want_dstate``), all fp32 but dxin."""
+    B, L, D = xin.shape
+    K = w.shape[1] if w.dim() == 2 else 0
+    dev = xin.device
+    f = _conv_struct(xin, w, bias, state_in, None, None, workspace)
+    _need(dx, "dx", (B, L, D), xin.dtype, dev)
+    dxin = torch.empty_like(xin) if dxin is None else dxin
+    _need(dxin, "dxin", (B, L, D), xin.dtype, dev)
+    dw = torch.empty(D, K, dtype=torch.float32, device=dev)
+    dbias = torch.empty(D, dtype=torch.float32, device=dev) if bias is not None else None
+    dstate = torch.empty(B, D, max(K - 1, 0), dtype=torch.float32, device=dev) if want_dstate else None
+    args = ConvBwdArgs(f=f, dx=_p(dx), dxin=_p(dxin), dw=_p(dw), dbias=_p(dbias), dstate_in=_p(dstate))
+    _check(lib().ssm_conv1d_bwd(ctypes.byref(args), _stream(dev, stream)), "ssm_conv1d_bwd")
+    return {"dxin": dxin, "dw": dw, "dbias": dbias, "dstate_in": dstate}
+
+
+def conv1d_step(ring, xin_t, w, bias=None, *, x_t=None, workspace=None, stream=None):
+    """One decoding token through the conv: ``ring`` [B, D, K-1] fp32 (the last K-1 inputs, oldest first)
+    is read and then advanced in place. xin_t [B, D]; returns x_t [B, D]."""
+    if xin_t.dim() != 2:
+        raise ValueError("xin_t must be [B, D]")
+    B, D = xin_t.shape
+    xin = xin_t.view(B, 1, D)
+    x = torch.empty_like(xin) if x_t is None else x_t.view(B, 1, D)
+    conv1d_fwd(xin, w, bias, ring, x=x, state_out=ring, workspace=workspace, stream=stream)
+    return x.view(B, D)
 
 
 def poll_status(workspace, stream=None) -> int:

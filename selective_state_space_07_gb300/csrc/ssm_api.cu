@@ -262,6 +262,71 @@ int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, v
     return tally(cudaGetLastError() == cudaSuccess ? 1 : -1);
 }
 
+namespace {
+int check_conv(const ssm_conv_args* a) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->B < 0 || a->L < 0 || a->D < 0) return SSM_ERR_INVALID_ARG;
+    if (a->K < 1 || a->K > 4) return SSM_ERR_UNSUPPORTED;
+    if (a->io_dtype != SSM_F32 && a->io_dtype != SSM_BF16) return SSM_ERR_UNSUPPORTED;
+    if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
+    if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 40)) return SSM_ERR_INVALID_ARG;
+    const bool work = a->B > 0 && a->L > 0 && a->D > 0;
+    if (work && (!a->xin || !a->w)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->xin, a->w, a->bias, a->state_in, a->x, a->state_out, a->workspace};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return SSM_ERR_ALIGNMENT;
+    return SSM_OK;
+}
+}  // namespace
+
+int ssm_conv1d_fwd(const ssm_conv_args* a, void* stream) {
+    g_launches = 0;
+    int rc = check_conv(a);
+    if (rc != SSM_OK) return rc;
+    const bool work = a->B > 0 && a->L > 0 && a->D > 0;
+    if (work && (!a->x || a->x == a->xin)) return SSM_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (!work) {
+        if (a->state_out && a->B > 0 && a->D > 0 && a->K > 1 && a->state_out != a->state_in) {
+            const size_t bytes = (size_t)a->B * a->D * (a->K - 1) * sizeof(float);
+            cudaError_t e = a->state_in ? cudaMemcpyAsync(a->state_out, a->state_in, bytes, cudaMemcpyDeviceToDevice, s)
+                                        : cudaMemsetAsync(a->state_out, 0, bytes, s);
+            if (e != cudaSuccess) return SSM_ERR_CUDA;
+        }
+        return SSM_OK;
+    }
+    return tally(ssm::launch_conv(a->io_dtype, false, a->B, a->L, a->D, (int)a->K, a->xin, a->w, a->bias,
+                                  a->state_in, a->x, a->state_out, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                  (unsigned*)a->workspace, s));
+}
+
+int ssm_conv1d_bwd(const ssm_conv_bwd_args* a, void* stream) {
+    g_launches = 0;
+    if (!a) return SSM_ERR_INVALID_ARG;
+    int rc = check_conv(&a->f);
+    if (rc != SSM_OK) return rc;
+    const ssm_conv_args& f = a->f;
+    const bool work = f.B > 0 && f.L > 0 && f.D > 0;
+    if (work && (!a->dx || !a->dxin || a->dxin == a->dx || a->dxin == f.xin)) return SSM_ERR_INVALID_ARG;
+    if (f.D > 0 && !a->dw) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->dx, a->dxin, a->dw, a->dbias, a->dstate_in};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return SSM_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (f.D > 0) {  // the reductions are overwritten: zero them on the stream first
+        if (cudaMemsetAsync(a->dw, 0, (size_t)f.D * f.K * sizeof(float), s) != cudaSuccess) return SSM_ERR_CUDA;
+        if (a->dbias && cudaMemsetAsync(a->dbias, 0, (size_t)f.D * sizeof(float), s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    }
+    if (a->dstate_in && f.B > 0 && f.D > 0 && f.K > 1 && (!work))
+        if (cudaMemsetAsync(a->dstate_in, 0, (size_t)f.B * f.D * (f.K - 1) * sizeof(float), s) != cudaSuccess)
+            return SSM_ERR_CUDA;
+    if (!work) return SSM_OK;
+    return tally(ssm::launch_conv(f.io_dtype, true, f.B, f.L, f.D, (int)f.K, f.xin, f.w, f.bias, f.state_in,
+                                  nullptr, nullptr, a->dx, a->dxin, a->dw, a->dbias, a->dstate_in,
+                                  (unsigned*)f.workspace, s));
+}
+
 int ssm_step(const ssm_step_args* a, void* stream) {
     g_launches = 0;
     if (!a) return SSM_ERR_INVALID_ARG;

@@ -10,6 +10,7 @@ namespace ssm {
 constexpr unsigned kStatusNonFinite = 1u;  // workspace status bit: an output was Inf/NaN
 constexpr int kFwdThreads = 128;
 constexpr int kBwdThreads = 128;
+constexpr int kConvThreads = 128;
 
 struct FwdParams {
     int64_t B, L, D;
@@ -65,6 +66,18 @@ template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long l
     return true;
 }
 
+// Token shares per warp column of the conv: as many as one wave of
+// resident warps can take (`warps`), each at least 16 tokens, and one when
+// the call updates its state in place (the thread that reads the state at
+// the start must be the one that writes it at the end).
+inline int64_t conv_splits(int64_t cols, int64_t L, int64_t warps, bool in_place_state) {
+    if (in_place_state || cols <= 0) return 1;
+    int64_t s = warps / cols;
+    const int64_t cap = (L + 15) / 16;
+    if (s > cap) s = cap;
+    return s < 1 ? 1 : s;
+}
+
 // L-groups when the caller leaves the choice. A pass over G groups runs
 // G * ctas_per_group CTAs in waves of `capacity` (resident CTAs on the
 // device); a wave that is partly empty wastes its share, and every group but
@@ -117,6 +130,9 @@ int launch_fwd_agg(int io, const FwdParams& p, cudaStream_t s);
 int launch_carry(int64_t B, int64_t D, int G, bool reverse, const float* A, const float* start,
                  const float* aggV, const float* aggS, float* out, cudaStream_t s);
 int launch_step(int io, int nsplit, const StepParams& p, cudaStream_t s);
+int launch_conv(int io, bool bwd, int64_t B, int64_t L, int64_t D, int K, const void* xin, const float* w,
+                const float* bias, const float* state_in, void* x, float* state_out, const void* dx, void* dxin,
+                float* dw, float* dbias, float* dstate, unsigned* status, cudaStream_t s);
 int launch_bwd(int io, const BwdParams& p, cudaStream_t s);
 int launch_bwd_agg(int io, const BwdParams& p, cudaStream_t s);
 

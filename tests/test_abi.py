@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("ssm_scan_fwd", "ssm_scan_bwd", "ssm_step", "ssm_scan_workspace_bytes", "ssm_scan_ckpt_elems",
-              "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad"):
+              "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad", "ssm_conv1d_fwd", "ssm_conv1d_bwd"):
         assert n in names
 
 
@@ -118,10 +118,42 @@ def test_step_rejects_bad_arguments(ssm, over, code):
     assert ssm.lib().ssm_step(ctypes.byref(args), None) == code
 
 
+def conv_args(ssm, **over):
+    a = dict(B=2, L=300, D=16, K=4, io_dtype=1, xin=FAKE, w=FAKE + 4096, bias=None, state_in=None,
+             x=FAKE + 8192, state_out=None, workspace=None)
+    a.update(over)
+    return ssm.ConvArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=5), UNSUPPORTED), (dict(K=0), UNSUPPORTED), (dict(io_dtype=3), UNSUPPORTED), (dict(D=12), ALIGNMENT),
+    (dict(B=-1), INVALID), (dict(xin=None), INVALID), (dict(w=None), INVALID), (dict(x=None), INVALID),
+    (dict(x=FAKE), INVALID), (dict(bias=FAKE + 4), ALIGNMENT), (dict(state_in=FAKE + 8), ALIGNMENT),
+])
+def test_conv_fwd_rejects_bad_arguments(ssm, over, code):
+    args = conv_args(ssm, **over)
+    assert ssm.lib().ssm_conv1d_fwd(ctypes.byref(args), None) == code
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(dx=None), INVALID), (dict(dxin=None), INVALID), (dict(dw=None), INVALID),
+    (dict(dxin=FAKE + 16384), INVALID),  # dxin aliasing dx
+    (dict(dxin=FAKE), INVALID),          # dxin aliasing xin
+    (dict(dbias=FAKE + 2), ALIGNMENT), (dict(dstate_in=FAKE + 4), ALIGNMENT),
+])
+def test_conv_bwd_rejects_bad_arguments(ssm, over, code):
+    g = dict(dx=FAKE + 16384, dxin=FAKE + 20480, dw=FAKE + 24576, dbias=None, dstate_in=None)
+    g.update(over)
+    args = ssm.ConvBwdArgs(f=conv_args(ssm), **g)
+    assert ssm.lib().ssm_conv1d_bwd(ctypes.byref(args), None) == code
+
+
 def test_null_args_struct(ssm):
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_bwd(None, None) == INVALID
     assert ssm.lib().ssm_step(None, None) == INVALID
+    assert ssm.lib().ssm_conv1d_fwd(None, None) == INVALID
+    assert ssm.lib().ssm_conv1d_bwd(None, None) == INVALID
 
 
 def test_dA_log_rejects_bad_arguments(ssm):
