@@ -98,6 +98,13 @@ typedef struct {
     size_t workspace_bytes;
     int32_t nsplit;
     int32_t groups;
+    /* Elements from one token's Bm row to the next token's (the same for
+     * Cm); 0 = N, dense [B,L,N]. Bm and Cm may be column slices of the
+     * x_proj output [B*L, R + 2N] ("MambaBlock" S6 forward commit: x_proj
+     * emits dt_rank + 2*d_state per token), read in place with bc_stride =
+     * R + 2N. Must be >= N (else SSM_ERR_INVALID_ARG) and a multiple of 16
+     * bytes (else SSM_ERR_ALIGNMENT). dB and dC stay dense [B,L,N]. */
+    int64_t bc_stride;
 } ssm_fwd_args;
 
 /* Reverse pass for loss = <dy, y> + <dh_last, h_last> (the analytic VJP:
@@ -157,6 +164,9 @@ typedef struct {
     void* workspace;
     int32_t nsplit;
     int32_t pad_;
+    /* Elements from one batch row of Bm_t to the next (the same for Cm_t);
+     * 0 = N. Same rules as ssm_fwd_args.bc_stride. */
+    int64_t bc_stride;
 } ssm_step_args;
 
 int ssm_scan_fwd(const ssm_fwd_args* args, void* stream);

@@ -51,7 +51,8 @@ class FwdArgs(ctypes.Structure):
                 ("io_dtype", ctypes.c_int32), ("delta_softplus", ctypes.c_int32)] + [
         (n, ctypes.c_void_p) for n in ("x", "z", "Bm", "Cm", "dt", "dt_bias", "A", "Dskip", "h0", "y",
                                        "h_last", "ckpt", "workspace")] + [
-        ("workspace_bytes", ctypes.c_size_t), ("nsplit", ctypes.c_int32), ("groups", ctypes.c_int32)]
+        ("workspace_bytes", ctypes.c_size_t), ("nsplit", ctypes.c_int32), ("groups", ctypes.c_int32),
+        ("bc_stride", ctypes.c_int64)]
 
 
 class BwdArgs(ctypes.Structure):
@@ -65,7 +66,7 @@ class StepArgs(ctypes.Structure):
                 ("io_dtype", ctypes.c_int32), ("delta_softplus", ctypes.c_int32)] + [
         (n, ctypes.c_void_p) for n in ("x_t", "z_t", "Bm_t", "Cm_t", "dt_t", "dt_bias", "A", "Dskip", "state",
                                        "y_t", "workspace")] + [
-        ("nsplit", ctypes.c_int32), ("pad_", ctypes.c_int32)]
+        ("nsplit", ctypes.c_int32), ("pad_", ctypes.c_int32), ("bc_stride", ctypes.c_int64)]
 
 
 class ConvArgs(ctypes.Structure):
@@ -190,7 +191,49 @@ def _fwd_struct(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0, delta_softplus, y, h_la
     return FwdArgs(B=B, L=L, D=D, N=N, io_dtype=_IO[x.dtype], delta_softplus=int(bool(delta_softplus)),
                    x=_p(x), z=_p(z), Bm=_p(Bm), Cm=_p(Cm), dt=_p(dt), dt_bias=_p(dt_bias), A=_p(A),
                    Dskip=_p(Dskip), h0=_p(h0), y=_p(y), h_last=_p(h_last), ckpt=_p(ckpt),
-                   workspace=ws.buf.data_ptr(), workspace_bytes=ws.nbytes, nsplit=nsplit, groups=groups)
+                   workspace=ws.buf.data_ptr(), workspace_bytes=ws.nbytes, nsplit=nsplit, groups=groups,
+                   bc_stride=_bc_stride_pair(Bm, Cm, B, L, N))
+
+
+def _token_rows(t, name, lead, N, dtype, device):
+    """Check a [*lead, N] tensor whose rows (the last dim) are contiguous and evenly spaced, as in a column
+    slice of the x_proj output; returns the row stride in elements."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(lead) + (N,):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(lead) + (N,)}")
+    if t.numel() == 0:
+        return N
+    if N > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: the {N} values of a row must be contiguous")
+    # the row stride: rows of the flattened leading dims must be s elements apart
+    s, span = None, 1
+    for size, stride in zip(reversed(t.shape[:-1]), reversed(t.stride()[:-1])):
+        if size > 1:
+            if s is None:
+                s = stride
+            elif stride != s * span:
+                raise ValueError(f"{name}: rows must be evenly spaced (a slice of a [rows, width] buffer)")
+        span *= size
+    s = N if s is None else s
+    if s < N:
+        raise ValueError(f"{name}: rows overlap (row stride {s} < {N})")
+    if t.data_ptr() % 16 or (s * t.element_size()) % 16:
+        raise ValueError(f"{name} must start on a 16-byte boundary with rows a multiple of 16 bytes apart")
+    return s
+
+
+def _bc_stride_pair(Bm, Cm, *lead_and_N):
+    *lead, N = lead_and_N
+    sb = _token_rows(Bm, "Bm", lead, N, Bm.dtype, Bm.device)
+    sc = _token_rows(Cm, "Cm", lead, N, Bm.dtype, Bm.device)
+    if sb != sc:
+        raise ValueError(f"Bm and Cm must have the same row stride ({sb} != {sc})")
+    return 0 if sb == N else sb
 
 
 def _check_inputs(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0):
@@ -208,8 +251,9 @@ def _check_inputs(x, dt, A, Bm, Cm, z, Dskip, dt_bias, h0):
     _need(x, "x", (B, L, D), io, dev)
     _need(dt, "dt", (B, L, D), torch.float32, dev)
     _need(A, "A", (D, N), torch.float32, dev)
-    _need(Bm, "Bm", (B, L, N), io, dev)
-    _need(Cm, "Cm", (B, L, N), io, dev)
+    # Bm, Cm: dense [B, L, N], or column slices of the x_proj output (rows evenly spaced)
+    _token_rows(Bm, "Bm", (B, L), N, io, dev)
+    _token_rows(Cm, "Cm", (B, L), N, io, dev)
     _opt(z, "z", (B, L, D), io, dev)
     _opt(Dskip, "Dskip", (D,), torch.float32, dev)
     _opt(dt_bias, "dt_bias", (D,), torch.float32, dev)
@@ -299,8 +343,8 @@ def step(state, x_t, dt_t, A, Bm_t, Cm_t, z_t=None, Dskip=None, dt_bias=None, de
     _need(x_t, "x_t", (B, D), io, dev)
     _need(dt_t, "dt_t", (B, D), torch.float32, dev)
     _need(A, "A", (D, N), torch.float32, dev)
-    _need(Bm_t, "Bm_t", (B, N), io, dev)
-    _need(Cm_t, "Cm_t", (B, N), io, dev)
+    _token_rows(Bm_t, "Bm_t", (B,), N, io, dev)
+    _token_rows(Cm_t, "Cm_t", (B,), N, io, dev)
     _opt(z_t, "z_t", (B, D), io, dev)
     _opt(Dskip, "Dskip", (D,), torch.float32, dev)
     _opt(dt_bias, "dt_bias", (D,), torch.float32, dev)
@@ -309,7 +353,8 @@ def step(state, x_t, dt_t, A, Bm_t, Cm_t, z_t=None, Dskip=None, dt_bias=None, de
     args = StepArgs(B=B, D=D, N=N, io_dtype=_IO[io], delta_softplus=int(bool(delta_softplus)), x_t=_p(x_t),
                     z_t=_p(z_t), Bm_t=_p(Bm_t), Cm_t=_p(Cm_t), dt_t=_p(dt_t), dt_bias=_p(dt_bias), A=_p(A),
                     Dskip=_p(Dskip), state=_p(state), y_t=_p(y_t),
-                    workspace=None if workspace is None else workspace.buf.data_ptr(), nsplit=nsplit)
+                    workspace=None if workspace is None else workspace.buf.data_ptr(), nsplit=nsplit,
+                    bc_stride=_bc_stride_pair(Bm_t, Cm_t, B, N))
     _check(lib().ssm_step(ctypes.byref(args), _stream(dev, stream)), "ssm_step")
     return y_t
 

@@ -73,6 +73,8 @@ int check_fwd(const ssm_fwd_args* a, bool need_y) {
     if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
     if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 40))
         return SSM_ERR_INVALID_ARG;
+    const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
+    if (bc != SSM_OK) return bc;
     const bool work = a->B > 0 && a->L > 0 && a->D > 0;
     if (work && (!a->x || !a->dt || !a->Bm || !a->Cm || !a->A || (need_y && !a->y))) return SSM_ERR_INVALID_ARG;
     const void* ptrs[] = {a->x, a->z, a->Bm, a->Cm, a->dt, a->dt_bias, a->A, a->Dskip, a->h0, a->y, a->h_last,
@@ -173,7 +175,7 @@ int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
     FwdParams p{};
     p.B = B; p.L = L; p.D = D; p.G = G; p.Lg = Lg;
     p.has_z = a->z != nullptr; p.sp = a->delta_softplus;
-    p.x = a->x; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm;
+    p.x = a->x; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm; p.bcs = a->bc_stride ? a->bc_stride : 16;
     p.dt = a->dt; p.dt_bias = a->dt_bias; p.A = a->A; p.Dskip = a->Dskip;
     p.hstart = a->h0; p.y = a->y; p.h_last = a->h_last; p.ckpt = a->ckpt;
     p.aggH = (float*)(ws + w.aggV); p.aggS = (float*)(ws + w.aggS);
@@ -235,7 +237,7 @@ int ssm_scan_bwd(const ssm_bwd_args* a, void* stream) {
     BwdParams p{};
     p.B = B; p.L = L; p.D = D; p.G = G; p.Lg = Lg;
     p.has_z = f.z != nullptr; p.sp = f.delta_softplus;
-    p.x = f.x; p.z = f.z; p.Bm = f.Bm; p.Cm = f.Cm; p.dy = a->dy;
+    p.x = f.x; p.z = f.z; p.Bm = f.Bm; p.Cm = f.Cm; p.dy = a->dy; p.bcs = f.bc_stride ? f.bc_stride : 16;
     p.dt = f.dt; p.dt_bias = f.dt_bias; p.A = f.A; p.Dskip = f.Dskip;
     p.ckpt = f.ckpt; p.gstart = a->dh_last;
     p.dx = a->dx; p.dz = a->dz; p.ddt = a->d_dt; p.dA = a->dA; p.dD = a->dD; p.ddt_bias = a->d_dt_bias;
@@ -336,6 +338,8 @@ int ssm_step(const ssm_step_args* a, void* stream) {
     if (a->delta_softplus != 0 && a->delta_softplus != 1) return SSM_ERR_INVALID_ARG;
     if (a->nsplit != 0 && a->nsplit != 1 && a->nsplit != 2 && a->nsplit != 4) return SSM_ERR_INVALID_ARG;
     if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
+    const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
+    if (bc != SSM_OK) return bc;
     const bool work = a->B > 0 && a->D > 0;
     if (work && (!a->x_t || !a->dt_t || !a->Bm_t || !a->Cm_t || !a->A || !a->state || !a->y_t))
         return SSM_ERR_INVALID_ARG;
@@ -347,7 +351,7 @@ int ssm_step(const ssm_step_args* a, void* stream) {
     StepParams p{};
     p.B = a->B; p.D = a->D;
     p.has_z = a->z_t != nullptr; p.sp = a->delta_softplus;
-    p.x = a->x_t; p.z = a->z_t; p.Bm = a->Bm_t; p.Cm = a->Cm_t;
+    p.x = a->x_t; p.z = a->z_t; p.Bm = a->Bm_t; p.Cm = a->Cm_t; p.bcs = a->bc_stride ? a->bc_stride : 16;
     p.dt = a->dt_t; p.dt_bias = a->dt_bias; p.A = a->A; p.Dskip = a->Dskip;
     p.state = a->state; p.y = a->y_t; p.status = (unsigned*)a->workspace;
     // one lane per channel when the channels alone fill the GPU, else two

@@ -133,9 +133,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams
                         rows, vchx);
         stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
                         rows, vchd);
-        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * p.bcs * ES, p.bcs * ES, T, Ly::BCROW / 16,
                         rows, Ly::BCROW / 16);
-        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * p.bcs * ES, p.bcs * ES, T, Ly::BCROW / 16,
                         rows, Ly::BCROW / 16);
         // checkpoint tile: the 16 state rows [n][d0 .. d0+CH) of chunk t0/T
         stage_block<NT>(st + Ly::OFF_H, Ly::HROW, (const char*)(p.ckpt + ((b * nck + t0 / T) * kN) * D + d0),
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
                         rows, vchx);
         stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
                         rows, vchd);
-        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
+        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * p.bcs * ES, p.bcs * ES, T, Ly::BCROW / 16,
                         rows, Ly::BCROW / 16);
         cp_async_commit();
     };

@@ -114,10 +114,10 @@ __global__ void __launch_bounds__(kFwdThreads, MINB) ssm_fwd_kernel(const FwdPar
                             CH * ES / 16, rows, vchx);
         stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
                         rows, vchd);
-        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * kN * ES, kN * ES, T, Ly::BCROW / 16,
-                        rows, Ly::BCROW / 16);
+        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * p.bcs * ES, p.bcs * ES, T,
+                        Ly::BCROW / 16, rows, Ly::BCROW / 16);
         if (!AGG)
-            stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * kN * ES, kN * ES, T,
+            stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * p.bcs * ES, p.bcs * ES, T,
                             Ly::BCROW / 16, rows, Ly::BCROW / 16);
         cp_async_commit();
     };
@@ -366,8 +366,8 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     const int64_t D = p.D, b = blockIdx.y, d = (int64_t)blockIdx.x * CH + c;
     const bool dv = d < D;
     if (tid < kN) {
-        Bs[tid] = IOT<IO>::to_f(reinterpret_cast<const IO*>(p.Bm)[b * kN + tid]);
-        Cs[tid] = IOT<IO>::to_f(reinterpret_cast<const IO*>(p.Cm)[b * kN + tid]);
+        Bs[tid] = IOT<IO>::to_f(reinterpret_cast<const IO*>(p.Bm)[b * p.bcs + tid]);
+        Cs[tid] = IOT<IO>::to_f(reinterpret_cast<const IO*>(p.Cm)[b * p.bcs + tid]);
     }
     __syncthreads();
     const int64_t i = b * D + (dv ? d : 0);

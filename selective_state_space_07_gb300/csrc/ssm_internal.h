@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/ssm_scan.h"
+
 namespace ssm {
 
 constexpr unsigned kStatusNonFinite = 1u;  // workspace status bit: an output was Inf/NaN
@@ -18,6 +20,7 @@ struct FwdParams {
     int64_t Lg;     // tokens per group, a multiple of 16
     int has_z, sp;  // gate present; Delta = softplus(dt + dt_bias)
     const void *x, *z, *Bm, *Cm;
+    int64_t bcs;    // elements between consecutive tokens' Bm (and Cm) rows
     const float *dt, *dt_bias, *A, *Dskip;
     const float* hstart;  // G == 1: h0 [B,D,16] (nullable); G > 1: carries [B,G,D,16]
     void* y;
@@ -32,6 +35,7 @@ struct BwdParams {
     int64_t Lg;
     int has_z, sp;
     const void *x, *z, *Bm, *Cm, *dy;
+    int64_t bcs;    // elements between consecutive tokens' Bm (and Cm) rows
     const float *dt, *dt_bias, *A, *Dskip;
     const float* ckpt;    // [B, ceil(L/8), 16, D]: state before every 8th token, state-major
     const float* gstart;  // G == 1: dh_last [B,D,16] (nullable); G > 1: carries [B,G,D,16]
@@ -45,6 +49,7 @@ struct StepParams {
     int64_t B, D;
     int has_z, sp;
     const void *x, *z, *Bm, *Cm;
+    int64_t bcs;    // elements between consecutive batch rows of Bm_t (and Cm_t)
     const float *dt, *dt_bias, *A, *Dskip;
     float* state;
     void* y;
@@ -64,6 +69,16 @@ template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long l
         return false;
     mask |= bit;
     return true;
+}
+
+// The row stride of Bm / Cm in elements: 0 means dense (N); otherwise at
+// least N and a whole number of 16-byte units (cp.async stages the rows in
+// 16-byte pieces). Returns an SSM_ status code.
+inline int check_bc_stride(int64_t s, int64_t N, int io_dtype) {
+    if (s == 0) return SSM_OK;
+    if (s < N || s > (int64_t(1) << 24)) return SSM_ERR_INVALID_ARG;
+    const int64_t es = io_dtype == SSM_BF16 ? 2 : 4;
+    return (s * es) % 16 == 0 ? SSM_OK : SSM_ERR_ALIGNMENT;
 }
 
 // Token shares per warp column of the conv: as many as one wave of

@@ -89,6 +89,8 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
     if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
     if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 40))
         return SSM_ERR_INVALID_ARG;
+    const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
+    if (bc != SSM_OK) return bc;
     const int64_t B = a->B, L = a->L, D = a->D;
     const bool work = B > 0 && L > 0 && D > 0;
     if (work && (!a->x || !a->dt || !a->Bm || !a->Cm || !a->A || !a->y)) return SSM_ERR_INVALID_ARG;
@@ -138,7 +140,7 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
     ssm::FwdParams p{};
     p.B = B; p.L = L; p.D = D; p.G = G; p.Lg = Lg;
     p.has_z = a->z != nullptr; p.sp = a->delta_softplus;
-    p.x = a->x; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm;
+    p.x = a->x; p.z = a->z; p.Bm = a->Bm; p.Cm = a->Cm; p.bcs = a->bc_stride ? a->bc_stride : 16;
     p.dt = a->dt; p.dt_bias = a->dt_bias; p.A = a->A; p.Dskip = a->Dskip;
     p.hstart = a->h0; p.y = a->y; p.h_last = a->h_last; p.ckpt = a->ckpt;
     p.aggH = (float*)(scratch + kStatus);

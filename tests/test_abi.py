@@ -82,6 +82,8 @@ def fwd_args(ssm, **over):
     (dict(x=None), INVALID), (dict(y=None), INVALID), (dict(B=-1), INVALID), (dict(delta_softplus=2), INVALID),
     (dict(nsplit=3), INVALID), (dict(groups=-2), INVALID), (dict(x=FAKE + 4), ALIGNMENT),
     (dict(h0=FAKE + 8), ALIGNMENT), (dict(workspace=None), WORKSPACE), (dict(workspace_bytes=16), WORKSPACE),
+    # Bm / Cm row stride: at least N, a multiple of 16 bytes (bf16: 8 elements)
+    (dict(bc_stride=8), INVALID), (dict(bc_stride=20), ALIGNMENT), (dict(bc_stride=-16), INVALID),
 ])
 def test_fwd_rejects_bad_arguments(ssm, over, code):
     args = fwd_args(ssm, **over)
@@ -100,6 +102,14 @@ def test_bwd_rejects_bad_arguments(ssm, over, code):
     assert ssm.lib().ssm_scan_bwd(ctypes.byref(args), None) == code
 
 
+def test_bwd_checks_the_bc_stride(ssm):
+    g = dict(dy=FAKE, dx=FAKE, dz=FAKE, d_dt=FAKE, dA=FAKE, dD=FAKE, d_dt_bias=FAKE, dB=FAKE, dC=FAKE)
+    args = ssm.BwdArgs(f=fwd_args(ssm, bc_stride=12), **g)
+    assert ssm.lib().ssm_scan_bwd(ctypes.byref(args), None) == INVALID
+    args = ssm.BwdArgs(f=fwd_args(ssm, bc_stride=36), **g)
+    assert ssm.lib().ssm_scan_bwd(ctypes.byref(args), None) == ALIGNMENT
+
+
 def test_bwd_needs_the_checkpoints(ssm):
     args = ssm.BwdArgs(f=fwd_args(ssm, ckpt=None), dy=FAKE, dx=FAKE, dz=FAKE, d_dt=FAKE, dA=FAKE, dD=FAKE,
                        d_dt_bias=FAKE, dB=FAKE, dC=FAKE)
@@ -108,7 +118,8 @@ def test_bwd_needs_the_checkpoints(ssm):
 
 @pytest.mark.parametrize("over,code", [
     (dict(N=4), UNSUPPORTED), (dict(D=20), ALIGNMENT), (dict(state=None), INVALID), (dict(y_t=FAKE + 1), ALIGNMENT),
-    (dict(io_dtype=-1), UNSUPPORTED), (dict(nsplit=8), INVALID),
+    (dict(io_dtype=-1), UNSUPPORTED), (dict(nsplit=8), INVALID), (dict(bc_stride=4), INVALID),
+    (dict(bc_stride=18), ALIGNMENT),
 ])
 def test_step_rejects_bad_arguments(ssm, over, code):
     a = dict(B=2, D=16, N=16, io_dtype=0, delta_softplus=1, x_t=FAKE, z_t=None, Bm_t=FAKE, Cm_t=FAKE, dt_t=FAKE,
