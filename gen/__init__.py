@@ -232,6 +232,38 @@ def make_conv_inputs(B: int, L: int, D: int, K: int = 4, *, io: str = "f32", see
     return ConvInputs(B, L, D, K, io, xin, w, b, st, dx)
 
 
+@dataclass
+class DtProjInputs:
+    """One problem for the dt projection in front of the scan: a [B,L,R] (the
+    dt_rank columns of the x_proj output), w [D,R] (dt_proj weight), bias [D],
+    ddelta [B,L,D] (the gradient arriving at Delta)."""
+    B: int
+    L: int
+    D: int
+    R: int
+    a: np.ndarray
+    w: np.ndarray
+    bias: np.ndarray
+    ddelta: np.ndarray
+
+
+def make_dtproj_inputs(B: int, L: int, D: int, R: int, *, seed: int = 0) -> DtProjInputs:
+    """Draw a dt-projection problem with bf16 operands (the tensor-core path):
+    a ~ N(0,1) and w ~ N(0, 1/R), both bf16-rounded, so a.w ~ N(0,1); bias[d]
+    = the inverse softplus of a log-uniform Delta in [1e-3, 1e-1] (Mamba's
+    dt_proj bias init), so softplus(a.w + bias) has the scan inputs'
+    distribution; ddelta ~ N(0,1) fp32. Per-tensor seeds from the same
+    SplitMix64 streams as make_inputs (x, dt, z, dy slots)."""
+    s = tensor_seeds(seed)
+    a = round_bf16(normal_f32(s["x"], B * L * R)).reshape(B, L, R)
+    w = round_bf16(normal_f32(s["dt"], D * R, 0.0, float(1.0 / np.sqrt(R)))).reshape(D, R)
+    u = uniform53(s["z"], D)
+    delta0 = np.exp(np.log(1e-3) + u * (np.log(1e-1) - np.log(1e-3)))
+    bias = np.log(np.expm1(delta0)).astype(np.float32)
+    ddelta = normal_f32(s["dy"], B * L * D).reshape(B, L, D)
+    return DtProjInputs(B, L, D, R, a, w, bias, ddelta)
+
+
 def recipe_text() -> str:
     lines = []
     for w in WORKLOADS.values():

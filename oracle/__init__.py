@@ -12,7 +12,10 @@ brute-force quadratic form, special cases, finite differences, adjoint and
 step identities) and, for the conv1d + SiLU in front of the scan
 (``conv_oracle.cpp``), in ``tests/test_conv_oracle_pins.py`` (numpy's
 convolution, special kernels, causality, state chaining, finite
-differences); none is "parity unpinned".
+differences), and, for the dt projection with its softplus
+(``dtproj_oracle.cpp``), in ``tests/test_dtproj_oracle_pins.py`` (numpy's
+matrix product, softplus identities, finite differences); none is "parity
+unpinned".
 """
 from __future__ import annotations
 
@@ -26,7 +29,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "ssm_oracle.cpp")
-_SRCS = [_SRC, os.path.join(_HERE, "conv_oracle.cpp")]
+_SRCS = [_SRC, os.path.join(_HERE, "conv_oracle.cpp"), os.path.join(_HERE, "dtproj_oracle.cpp")]
 _LIB = os.path.join(_HERE, "libssm_oracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +69,12 @@ class _ConvArgs(ctypes.Structure):
             "xin", "w", "bias", "state", "x", "state_out", "dx", "dxin", "dw", "dbias", "dstate")]
 
 
+class _DtProjArgs(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("D", ctypes.c_int64), ("R", ctypes.c_int64),
+                ("softplus", ctypes.c_int32), ("pad_", ctypes.c_int32)] + [
+        (name, ctypes.c_void_p) for name in ("a", "w", "bias", "delta", "ddelta", "dpre", "dbias")]
+
+
 def lib():
     global _lib
     with _lock:
@@ -85,6 +94,9 @@ def lib():
                 for dt in ("f64", "f32"):
                     f = getattr(_lib, f"conv_oracle_{name}_{dt}")
                     f.argtypes = [ctypes.POINTER(_ConvArgs)]
+                    f.restype = ctypes.c_int
+                    f = getattr(_lib, f"dtproj_oracle_{name}_{dt}")
+                    f.argtypes = [ctypes.POINTER(_DtProjArgs)]
                     f.restype = ctypes.c_int
     return _lib
 
@@ -215,4 +227,42 @@ def conv_bwd(xin, w, dx, bias=None, state=None, dtype: str = "f64") -> Dict[str,
     rc = getattr(lib(), f"conv_oracle_bwd_{dtype}")(ctypes.byref(args))
     if rc != 0:
         raise ValueError(f"oracle conv bwd rejected the arguments ({rc})")
+    return out
+
+
+def dtproj_fwd(a, w, bias=None, softplus: bool = True, dtype: str = "f64") -> np.ndarray:
+    """The dt projection ("delta=softplus(dt.dt_proj+dt_bias)"): a [M,R] (the
+    dt_rank columns of the x_proj output), w [D,R], bias [D] (None = 0).
+    Returns delta [M,D] = softplus(a @ w.T + bias) (without the softplus when
+    ``softplus`` is False)."""
+    t = _NP[dtype]
+    a = _np(a, t)
+    M, R = a.shape
+    D = int(np.asarray(w).shape[0])
+    args = _DtProjArgs(M=M, D=D, R=R, softplus=int(bool(softplus)))
+    keep = [a]
+    args.a = _ptr(a)
+    _fill(args, keep, t, w=w, bias=bias)
+    out = np.zeros((M, D), t)
+    args.delta = _ptr(out)
+    if getattr(lib(), f"dtproj_oracle_fwd_{dtype}")(ctypes.byref(args)) != 0:
+        raise ValueError("oracle dt projection rejected the arguments")
+    return out
+
+
+def dtproj_bwd(a, w, ddelta, bias=None, softplus: bool = True, dtype: str = "f64") -> Dict[str, np.ndarray]:
+    """Reverse pass of dtproj_fwd up to the pre-activation: dpre [M,D] =
+    ddelta * sigmoid(pre) and dbias [D] = sum over m of dpre."""
+    t = _NP[dtype]
+    a = _np(a, t)
+    M, R = a.shape
+    D = int(np.asarray(w).shape[0])
+    args = _DtProjArgs(M=M, D=D, R=R, softplus=int(bool(softplus)))
+    keep = [a]
+    args.a = _ptr(a)
+    _fill(args, keep, t, w=w, bias=bias, ddelta=ddelta)
+    out = {"dpre": np.zeros((M, D), t), "dbias": np.zeros((D,), t)}
+    args.dpre, args.dbias = _ptr(out["dpre"]), _ptr(out["dbias"])
+    if getattr(lib(), f"dtproj_oracle_bwd_{dtype}")(ctypes.byref(args)) != 0:
+        raise ValueError("oracle dt projection backward rejected the arguments")
     return out
