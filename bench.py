@@ -19,6 +19,10 @@ cores) on bounded samples of the same workload, on rank 0 only.
 --op conv1d times the causal depthwise conv1d + SiLU in front of the scan
 (ssm_conv1d_fwd + ssm_conv1d_bwd, K = 4) on the workload's B, L, D instead,
 with its own metric, HBM roofline and oracle baseline.
+
+--op dtproj times the dt projection with its fused softplus on the tensor
+cores (ssm_dtproj_fwd + ssm_dtproj_bwd, dt_rank = D/32, a read in place from
+an x_proj-shaped buffer) on the workload's B*L tokens and D channels.
 """
 from __future__ import annotations
 
@@ -87,6 +91,22 @@ def conv_algorithmic_bytes(w, pass_, K=CONV_K):
     if pass_ == "fwd":
         return tc * 2 * e + small + 2 * st
     return tc * 3 * e + 2 * small + 2 * st
+
+
+DTPROJ_METRIC = "dt_proj+softplus fwd+bwd G(token·channel)/s on 1 GB300; % of HBM roofline"
+
+
+def dtproj_rank(w):
+    """dt_rank = d_model / 16 = D / 32 (Mamba's expand = 2)."""
+    return max(16, w.D // 32)
+
+
+def dtproj_algorithmic_bytes(w, pass_):
+    """Bytes moved at least once: a (bf16 [M,R]) and w (bf16 [D,R]) read, bias read; the forward writes
+    delta (fp32 [M,D]); the backward reads ddelta and writes dpre (fp32 [M,D]) and dbias."""
+    M, R = w.B * w.L, dtproj_rank(w)
+    ins = M * R * 2 + w.D * R * 2 + w.D * 4
+    return ins + M * w.D * 4 if pass_ == "fwd" else ins + 2 * M * w.D * 4 + w.D * 4
 
 
 def mufu_ops(w, pass_):
@@ -661,6 +681,197 @@ def run_conv(args, w):
     return 0
 
 
+def _dtproj_oracle_step(a, wt, bias, dd):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.dtproj_fwd(a, wt, bias, dtype="f32")
+    oracle.dtproj_bwd(a, wt, dd, bias, dtype="f32")
+    return time.perf_counter() - t0
+
+
+def dtproj_cpu_sample(w, budget_s):
+    """The dt-projection oracle (fp32, one thread: plain loops) on the first rows of the workload, all D
+    channels, sized for about budget_s."""
+    R = dtproj_rank(w)
+    c = gen.make_dtproj_inputs(1, 64, w.D, R, seed=w.seed)
+    t = _dtproj_oracle_step(c.a[0], c.w, c.bias, c.ddelta[0])
+    rows = int(min(w.B * w.L, max(64, 64 * budget_s / max(t, 1e-4))))
+    c = gen.make_dtproj_inputs(1, rows, w.D, R, seed=w.seed)
+    return (c.a[0], c.w, c.bias, c.ddelta[0]), rows
+
+
+def run_dtproj_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    smp, rows = dtproj_cpu_sample(w, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _dtproj_oracle_step(*smp)
+    ts = [_dtproj_oracle_step(*smp) for _ in range(args.steps)]
+    total = sum(ts)
+    val = rows * w.D * len(ts) / total / 1e9
+    sample = f"per step: the first {rows} of {w.B * w.L} token rows, all {w.D} channels, fp32 dt-projection oracle fwd+bwd"
+    line = {
+        "impl": "reference", "metric": DTPROJ_METRIC, "value": val, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(ts), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name + "-dtproj", "M": w.B * w.L, "D": w.D, "R": dtproj_rank(w)},
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_dtproj(args, w):
+    """ssm_dtproj_fwd + ssm_dtproj_bwd on the workload's tokens and channels: one step = one forward and
+    one backward call, each timed with CUDA events after an L2 flush, inputs resident in HBM."""
+    import torch
+    import selective_state_space_07_gb300 as ssm
+
+    rank, world, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm.build()
+    R = dtproj_rank(w)
+    c = gen.make_dtproj_inputs(w.B, w.L, w.D, R, seed=w.seed)
+    xp = torch.zeros(w.B, w.L, R + 32, dtype=torch.bfloat16, device=dev)  # x_proj output: dt_rank | B | C
+    xp[..., :R] = torch.from_numpy(c.a).to(dev, torch.bfloat16)
+    a = xp[..., :R]
+    wt = torch.from_numpy(c.w).to(dev, torch.bfloat16)
+    bias = torch.from_numpy(c.bias).to(dev)
+    dd = torch.from_numpy(c.ddelta).to(dev)
+    del c
+    delta = torch.empty(w.B, w.L, w.D, dtype=torch.float32, device=dev)
+    dpre = torch.empty_like(delta)
+    ws = ssm.Workspace(1, 1, 8, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+
+    def fwd():
+        ssm.dtproj_fwd(a, wt, bias, delta=delta, workspace=ws)
+        return ssm.last_launch_count()
+
+    def bwd():
+        out.update(ssm.dtproj_bwd(a, wt, dd, bias, dpre=dpre, workspace=ws))
+        return ssm.last_launch_count()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+        flush.zero_()
+        bwd()
+    torch.cuda.synchronize()
+    st = ssm.poll_status(ws)
+    if st != 0:
+        raise RuntimeError(f"status {st} during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        launches += fwd()
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        launches += bwd()
+        e[3].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop(set(visible_gpu_ids(world))) if rank == 0 else None
+    ms_f = sum(e[0].elapsed_time(e[1]) for e in ev) / len(ev)
+    ms_b = sum(e[2].elapsed_time(e[3]) for e in ev) / len(ev)
+    ms_f, ms_b = max_over_ranks([ms_f, ms_b], dist, dev)
+    status = ssm.poll_status(ws)
+    tc = w.B * w.L * w.D
+    value = job_value(world, tc, ms_f + ms_b)
+
+    e2e = None
+    if not args.no_e2e:  # the x_proj buffer and ddelta in from pinned host memory, delta, dpre and dbias back
+        h_in = {"xp": xp.cpu().pin_memory(), "dd": dd.cpu().pin_memory()}
+        h_out = {"delta": torch.empty_like(delta, device="cpu").pin_memory(),
+                 "dpre": torch.empty_like(dpre, device="cpu").pin_memory(),
+                 "dbias": torch.empty(w.D).pin_memory()}
+
+        def e2e_step():
+            xp.copy_(h_in["xp"], non_blocking=True)
+            dd.copy_(h_in["dd"], non_blocking=True)
+            fwd()
+            bwd()
+            h_out["delta"].copy_(delta, non_blocking=True)
+            h_out["dpre"].copy_(dpre, non_blocking=True)
+            h_out["dbias"].copy_(out["dbias"], non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        n = max(3, min(args.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        es.record(stream)
+        for _ in range(n):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks([es.elapsed_time(ee) / n], dist, dev)[0]
+        e2e = {"value": round(job_value(world, tc, e2e_ms), 3), "unit": UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in h_out.values()),
+               "ms_per_step": round(e2e_ms, 4), "api": "dtproj_fwd + dtproj_bwd on one stream, pinned host copies"}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind, peaks = measured_peaks()
+    flops = 2.0 * w.B * w.L * w.D * R
+    tpk = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
+    rf, tens = {}, {}
+    for name, ms in (("fwd", ms_f), ("bwd", ms_b)):
+        ab = dtproj_algorithmic_bytes(w, name)
+        ach = ab / (ms * 1e-3) / 1e9
+        rf[name] = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(ach / peak, 4), "peak_kind": peak_kind, "kernel": f"ssm_dtproj_kernel<{name == 'bwd'}>",
+                    "algorithmic_bytes_per_launch": ab, "ms_per_launch": round(ms, 5),
+                    "traffic": profiled_traffic("ssm_dtproj_" + name, w.name)}
+        tf = flops / (ms * 1e-3) / 1e12
+        tens[name] = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpk, "unit": "TFLOP/s",
+                      "frac": round(tf / tpk, 4), "peak_kind": "measured bf16 (burst)" if peaks else "fallback"}
+    dom = "bwd" if ms_b >= ms_f else "fwd"
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        smp, rows = dtproj_cpu_sample(w, 6.0)
+        ts = []
+        while sum(ts) < 12.0 and len(ts) < 50:
+            ts.append(_dtproj_oracle_step(*smp))
+        cpu = {"value": rows * w.D * len(ts) / sum(ts) / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"the first {rows} of {w.B * w.L} token rows, all {w.D} channels, fp32 dt-projection "
+                         f"oracle fwd+bwd, {len(ts)} repetitions, {sum(ts):.1f} s"}
+    line = {
+        "metric": DTPROJ_METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_f + ms_b, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name + "-dtproj", "M": w.B * w.L, "D": w.D, "R": R, "seed": w.seed,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "outputs larger than L2 (129 MB) and a 512 MiB write flushes L2 before every pass",
+                   "ms_fwd": round(ms_f, 5), "ms_bwd": round(ms_b, 5),
+                   "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
+        "roofline": rf[dom], "roofline_other": rf["fwd" if dom == "bwd" else "bwd"], "tensor_roofline": tens,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk, "status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -672,12 +883,15 @@ def main():
     ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--op", choices=("scan", "conv1d"), default="scan",
-                    help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it")
+    ap.add_argument("--op", choices=("scan", "conv1d", "dtproj"), default="scan",
+                    help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it; "
+                         "dtproj: the dt projection with its softplus")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = gen.WORKLOADS[args.workload]
+    if args.op == "dtproj":
+        return run_dtproj_reference(args, w) if args.impl == "reference" else run_dtproj(args, w)
     if args.op == "conv1d":
         return run_conv_reference(args, w) if args.impl == "reference" else run_conv(args, w)
     if args.impl == "reference":

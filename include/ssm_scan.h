@@ -59,6 +59,7 @@ enum {
     SSM_ERR_ALIGNMENT = -3,   /* D % 8 != 0 or a pointer not 16-byte aligned */
     SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */
+    SSM_ERR_TIMEOUT = -6,     /* (ssm_poll_status) a bounded wait inside a kernel ran out */
     SSM_ERR_NONFINITE = -7,   /* (ssm_poll_status) a kernel produced Inf/NaN */
     SSM_ERR_SCRATCH_LIMIT = -8 /* (ssm_scan_fwd_noalloc) carries exceed the built-in 8 MiB array */
 };
@@ -244,6 +245,48 @@ typedef struct {
 
 int ssm_conv1d_fwd(const ssm_conv_args* args, void* stream);
 int ssm_conv1d_bwd(const ssm_conv_bwd_args* args, void* stream);
+
+/* The dt projection with its softplus fused into the GEMM epilogue, on the
+ * tensor cores ("MambaBlock" S6 forward commit: "delta=softplus(dt.dt_proj
+ * +dt_bias)", dt being the first dt_rank columns of the x_proj output):
+ *   delta[m,d] = softplus(bias[d] + sum_{r<R} a[m,r] * w[d,r])    (softplus = 1)
+ *   delta[m,d] = bias[d] + sum_{r<R} a[m,r] * w[d,r]              (softplus = 0)
+ * M = batch * tokens. a [M,R] bf16, rows a_stride elements apart (0 = R), so
+ * a may be the first R columns of the x_proj output [M, R + 2N]; w [D,R]
+ * bf16 (the projection's weight); bias [D] fp32 (NULL = 0); delta [M,D]
+ * fp32, which ssm_scan_fwd then takes as dt with delta_softplus = 0 and no
+ * dt_bias. R a multiple of 16 in 16..256 (else SSM_ERR_UNSUPPORTED); D a
+ * multiple of 8, a_stride * 2 bytes and every pointer 16-byte aligned (else
+ * SSM_ERR_ALIGNMENT). Products are fp32-accumulated from the bf16 operands.
+ * workspace: nullable status word (non-finite outputs; SSM_ERR_TIMEOUT if
+ * the tensor core's completion never arrived). Asynchronous on `stream`. */
+typedef struct {
+    int64_t M, D, R;
+    int64_t a_stride;
+    int32_t softplus;
+    int32_t pad_;
+    const void* a;
+    const void* w;
+    const float* bias;
+    float* delta;
+    void* workspace;
+} ssm_dtproj_args;
+
+/* Reverse pass up to the pre-activation, for the gradient ddelta [M,D] fp32
+ * arriving at delta: dpre[m,d] = ddelta[m,d] * sigmoid(pre[m,d]) (ddelta
+ * itself when softplus = 0), the pre-activation recomputed on the tensor
+ * cores; dbias [D] (nullable) = sum over m of dpre, OVERWRITTEN. dpre may be
+ * ddelta (in place). The gradients of a and w are the plain products
+ * dpre @ w and dpre^T @ a (the caller's GEMMs). f.delta is not used. */
+typedef struct {
+    ssm_dtproj_args f;
+    const float* ddelta;
+    float* dpre;
+    float* dbias;
+} ssm_dtproj_bwd_args;
+
+int ssm_dtproj_fwd(const ssm_dtproj_args* args, void* stream);
+int ssm_dtproj_bwd(const ssm_dtproj_bwd_args* args, void* stream);
 
 /* Bytes of workspace a fwd or bwd call of this shape needs (>= 256). */
 size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N);

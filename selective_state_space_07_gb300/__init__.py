@@ -26,7 +26,7 @@ import torch
 __all__ = [
     "SsmError", "build", "lib", "scan_fwd", "scan_bwd", "step", "dA_log_grad", "poll_status",
     "clear_status", "workspace_bytes", "ckpt_elems", "CKPT_INTERVAL", "Workspace", "scan_fwd_bwd_host",
-    "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step",
+    "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -79,6 +79,16 @@ class ConvBwdArgs(ctypes.Structure):
     _fields_ = [("f", ConvArgs)] + [(n, ctypes.c_void_p) for n in ("dx", "dxin", "dw", "dbias", "dstate_in")]
 
 
+class DtProjArgs(ctypes.Structure):
+    _fields_ = [("M", ctypes.c_int64), ("D", ctypes.c_int64), ("R", ctypes.c_int64), ("a_stride", ctypes.c_int64),
+                ("softplus", ctypes.c_int32), ("pad_", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in ("a", "w", "bias", "delta", "workspace")]
+
+
+class DtProjBwdArgs(ctypes.Structure):
+    _fields_ = [("f", DtProjArgs)] + [(n, ctypes.c_void_p) for n in ("ddelta", "dpre", "dbias")]
+
+
 EXPORTS = {
     "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
@@ -93,6 +103,8 @@ EXPORTS = {
     "ssm_last_launch_count": ([], ctypes.c_int),
     "ssm_conv1d_fwd": ([ctypes.POINTER(ConvArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_conv1d_bwd": ([ctypes.POINTER(ConvBwdArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_dtproj_fwd": ([ctypes.POINTER(DtProjArgs), ctypes.c_void_p], ctypes.c_int),
+    "ssm_dtproj_bwd": ([ctypes.POINTER(DtProjBwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_dA_log_grad": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
                         ctypes.c_int),
 }
@@ -441,8 +453,58 @@ def conv1d_step(ring, xin_t, w, bias=None, *, x_t=None, workspace=None, stream=N
     return x.view(B, D)
 
 
+def _dtproj_struct(a, w, bias, softplus, delta, workspace):
+    if a.dim() < 2:
+        raise ValueError("a must be [..., R] (e.g. [B, L, R] columns of the x_proj output)")
+    dev = a.device
+    if dev.type != "cuda":
+        raise ValueError("the dt projection runs on a CUDA device; a is on " + str(dev))
+    lead, R = tuple(a.shape[:-1]), a.shape[-1]
+    M = 1
+    for v in lead:
+        M *= v
+    if w.dim() != 2 or w.shape[1] != R:
+        raise ValueError("w must be [D, R]")
+    D = w.shape[0]
+    stride = _token_rows(a, "a", lead, R, torch.bfloat16, dev)
+    _need(w, "w", (D, R), torch.bfloat16, dev)
+    _opt(bias, "bias", (D,), torch.float32, dev)
+    _opt(delta, "delta", lead + (D,), torch.float32, dev)
+    args = DtProjArgs(M=M, D=D, R=R, a_stride=0 if stride == R else stride, softplus=int(bool(softplus)),
+                      a=_p(a), w=_p(w), bias=_p(bias), delta=_p(delta),
+                      workspace=None if workspace is None else workspace.buf.data_ptr())
+    return args, lead, D
+
+
+def dtproj_fwd(a, w, bias=None, softplus=True, *, delta=None, workspace=None, stream=None):
+    """The dt projection with its softplus on the tensor cores: delta = softplus(a @ w.T + bias), fp32
+    [..., D]. a [..., R] bf16 may be the first R columns of the x_proj output (rows evenly spaced,
+    16-byte aligned); w [D, R] bf16; bias [D] fp32. Feed delta to scan_fwd as dt with
+    delta_softplus=False and no dt_bias."""
+    lead, D = tuple(a.shape[:-1]), w.shape[0]
+    delta = torch.empty(lead + (D,), dtype=torch.float32, device=a.device) if delta is None else delta
+    args, _, _ = _dtproj_struct(a, w, bias, softplus, delta, workspace)
+    _check(lib().ssm_dtproj_fwd(ctypes.byref(args), _stream(a.device, stream)), "ssm_dtproj_fwd")
+    return delta
+
+
+def dtproj_bwd(a, w, ddelta, bias=None, softplus=True, *, dpre=None, inplace=False, workspace=None, stream=None):
+    """Reverse pass up to the pre-activation: dpre = ddelta * sigmoid(a @ w.T + bias) (recomputed on the
+    tensor cores) and dbias = dpre summed over rows (None without a bias). The gradients of a and w are
+    dpre @ w and dpre^T @ a. ``inplace`` writes dpre over ddelta."""
+    args, lead, D = _dtproj_struct(a, w, bias, softplus, None, workspace)
+    _need(ddelta, "ddelta", lead + (D,), torch.float32, a.device)
+    dpre = ddelta if inplace else (torch.empty_like(ddelta) if dpre is None else dpre)
+    _need(dpre, "dpre", lead + (D,), torch.float32, a.device)
+    dbias = torch.empty(D, dtype=torch.float32, device=a.device) if bias is not None else None
+    bargs = DtProjBwdArgs(f=args, ddelta=_p(ddelta), dpre=_p(dpre), dbias=_p(dbias))
+    _check(lib().ssm_dtproj_bwd(ctypes.byref(bargs), _stream(a.device, stream)), "ssm_dtproj_bwd")
+    return {"dpre": dpre, "dbias": dbias}
+
+
 def poll_status(workspace, stream=None) -> int:
-    """Synchronise, read and clear the status word. 0 = ok, -7 = non-finite output seen."""
+    """Synchronise, read and clear the status word. 0 = ok, -7 = non-finite output seen, -6 = a bounded
+    wait inside a kernel ran out."""
     dev = workspace.buf.device
     return int(lib().ssm_poll_status(workspace.buf.data_ptr(), _stream(dev, stream)))
 

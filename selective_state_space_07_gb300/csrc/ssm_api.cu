@@ -125,6 +125,7 @@ const char* ssm_status_string(int code) {
         case SSM_ERR_WORKSPACE: return "workspace missing or smaller than ssm_scan_workspace_bytes()";
         case SSM_ERR_CUDA: return "a CUDA call or kernel launch failed";
         case SSM_ERR_NONFINITE: return "a kernel produced a non-finite value";
+        case SSM_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out (its results are not valid)";
         case SSM_ERR_SCRATCH_LIMIT:
             return "the requested L-groups need more scratch than the library's built-in 8 MiB array holds";
         default: return "unknown status";
@@ -145,6 +146,7 @@ int ssm_poll_status(void* workspace, void* stream) {
         return SSM_ERR_CUDA;
     if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), s) != cudaSuccess) return SSM_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SSM_ERR_CUDA;
+    if (v & ssm::kStatusTimeout) return SSM_ERR_TIMEOUT;
     return (v & ssm::kStatusNonFinite) ? SSM_ERR_NONFINITE : SSM_OK;
 }
 
@@ -327,6 +329,55 @@ int ssm_conv1d_bwd(const ssm_conv_bwd_args* a, void* stream) {
     return tally(ssm::launch_conv(f.io_dtype, true, f.B, f.L, f.D, (int)f.K, f.xin, f.w, f.bias, f.state_in,
                                   nullptr, nullptr, a->dx, a->dxin, a->dw, a->dbias, a->dstate_in,
                                   (unsigned*)f.workspace, s));
+}
+
+namespace {
+int check_dtproj(const ssm_dtproj_args* a) {
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->M < 0 || a->D < 0 || a->R < 0 || a->a_stride < 0) return SSM_ERR_INVALID_ARG;
+    if (a->softplus != 0 && a->softplus != 1) return SSM_ERR_INVALID_ARG;
+    if (a->R < 16 || a->R > 256 || a->R % 16 != 0) return SSM_ERR_UNSUPPORTED;
+    if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
+    const int64_t stride = a->a_stride ? a->a_stride : a->R;
+    if (stride < a->R) return SSM_ERR_INVALID_ARG;
+    if ((stride * 2) % 16 != 0) return SSM_ERR_ALIGNMENT;
+    if (a->M > (int64_t(1) << 40) || a->D > (int64_t(1) << 31) || stride > (int64_t(1) << 24)) return SSM_ERR_INVALID_ARG;
+    if (((a->M + 127) / 128) * ((a->D + 255) / 256) > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
+    const bool work = a->M > 0 && a->D > 0;
+    if (work && (!a->a || !a->w)) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->a, a->w, a->bias, a->delta, a->workspace};
+    for (const void* p : ptrs)
+        if (misaligned(p)) return SSM_ERR_ALIGNMENT;
+    return SSM_OK;
+}
+}  // namespace
+
+int ssm_dtproj_fwd(const ssm_dtproj_args* a, void* stream) {
+    g_launches = 0;
+    int rc = check_dtproj(a);
+    if (rc != SSM_OK) return rc;
+    if (a->M == 0 || a->D == 0) return SSM_OK;
+    if (!a->delta) return SSM_ERR_INVALID_ARG;
+    return tally(ssm::launch_dtproj(false, a->M, a->D, a->R, a->a_stride ? a->a_stride : a->R, a->a, a->w, a->bias,
+                                    a->delta, nullptr, nullptr, a->softplus, (unsigned*)a->workspace,
+                                    (cudaStream_t)stream));
+}
+
+int ssm_dtproj_bwd(const ssm_dtproj_bwd_args* a, void* stream) {
+    g_launches = 0;
+    if (!a) return SSM_ERR_INVALID_ARG;
+    int rc = check_dtproj(&a->f);
+    if (rc != SSM_OK) return rc;
+    const ssm_dtproj_args& f = a->f;
+    const bool work = f.M > 0 && f.D > 0;
+    if (work && (!a->ddelta || !a->dpre)) return SSM_ERR_INVALID_ARG;
+    if (misaligned(a->ddelta) || misaligned(a->dpre) || misaligned(a->dbias)) return SSM_ERR_ALIGNMENT;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (a->dbias && f.D > 0 && cudaMemsetAsync(a->dbias, 0, (size_t)f.D * sizeof(float), s) != cudaSuccess)
+        return SSM_ERR_CUDA;
+    if (!work) return SSM_OK;
+    return tally(ssm::launch_dtproj(true, f.M, f.D, f.R, f.a_stride ? f.a_stride : f.R, f.a, f.w, f.bias, a->dpre,
+                                    a->ddelta, a->dbias, f.softplus, (unsigned*)f.workspace, s));
 }
 
 int ssm_step(const ssm_step_args* a, void* stream) {

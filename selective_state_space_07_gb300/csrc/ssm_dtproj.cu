@@ -1,0 +1,294 @@
+// The dt projection in front of the S6 scan with the softplus fused into the
+// GEMM's epilogue, on the sm_103a tensor cores (tcgen05, TMEM accumulators).
+//
+// rustytorch commit log, "MambaBlock" S6 forward commit:
+// "delta=softplus(dt.dt_proj+dt_bias)", where dt is the first dt_rank
+// columns of the x_proj output. With a = those columns [M = B*L, R] (rows
+// read in place from the x_proj buffer), w the projection weight [D, R]:
+//   forward:  delta[m,d] = softplus(bias[d] + sum_r a[m,r] w[d,r])
+//   backward: dpre[m,d]  = ddelta[m,d] * sigmoid(pre[m,d]),  dbias[d] = sum_m dpre[m,d]
+// (the pre-activation is recomputed; the two weight/input gradients that
+// follow are plain GEMMs of dpre and are left to the caller's BLAS).
+//
+// One CTA computes a 128-token x 256-channel tile. Its four warps copy the
+// a rows and w rows (bf16, K-major) into shared memory with cp.async, laid
+// out as the tensor core's no-swizzle canonical layout (8-row x 16-byte core
+// matrices; LBO = 128 bytes between core matrices along K, SBO = R*16 bytes
+// between 8-row groups). One thread issues the R/16 `tcgen05.mma ...
+// kind::f16` (M = 128, N = 256, K = 16 each) into a 256-column TMEM
+// accumulator and commits them to an mbarrier; every warp then reads its 32
+// TMEM lanes (rows) with `tcgen05.ld`, transposes 32x32 blocks through
+// shared memory so that each store instruction writes whole 128-byte row
+// segments, and applies the epilogue. The op is bound by writing the fp32
+// [M, D] result (K = R is small: 2*R flops per 4 output bytes), so the
+// epilogue's stores are what the design serves.
+#include "ssm_common.cuh"
+#include "ssm_internal.h"
+
+namespace ssm {
+
+namespace {
+
+constexpr int kTM = 128;           // tokens per tile: MMA M, TMEM lanes
+constexpr int kTN = 256;           // channels per tile: MMA N, TMEM columns
+constexpr int kDPThreads = 128;    // 4 warps; warp w owns TMEM lanes 32w .. 32w+31
+constexpr int kStgRow = 36;        // floats per row of a warp's 32x32 transpose block (padded)
+constexpr int kStgBytes = 4 * 32 * kStgRow * 4;
+constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s: how long a thread waits for the MMAs
+
+struct DtProjParams {
+    int64_t M, D, R, a_stride;     // a rows are a_stride elements apart
+    int64_t tiles_n;               // tiles across D
+    const __nv_bfloat16* a;        // [M, R] (rows strided)
+    const __nv_bfloat16* w;        // [D, R]
+    const float* bias;             // [D] or null
+    float* out;                    // forward: delta [M,D]; backward: dpre [M,D]
+    const float* dout;             // backward: ddelta [M,D] (may alias out)
+    float* dbias;                  // backward: [D] (zeroed on the stream first) or null
+    int softplus;
+    unsigned* status;
+};
+
+// Every CTA holds kTN TMEM columns (half of the SM's 512), so the shared
+// memory request is at least 80 KB: two CTAs per SM at most, and
+// tcgen05.alloc never has to wait for columns.
+constexpr int kMinOperandSmem = 80 * 1024;
+__host__ __device__ constexpr int operand_bytes(int64_t R) { return (int)((kTM + kTN) * R * 2); }
+__host__ __device__ constexpr int dtproj_smem(int64_t R) {
+    return (operand_bytes(R) > kMinOperandSmem ? operand_bytes(R) : kMinOperandSmem) + kTN * 4 + 16;
+}
+static_assert(kMinOperandSmem >= kStgBytes, "the transpose blocks fit in the operand region");
+
+__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
+
+// Shared-memory matrix descriptor: no swizzle, K-major canonical layout
+// (start, LBO = core-matrix step along K, SBO = 8-row-group step), version 1.
+__device__ __forceinline__ uint64_t smem_desc(unsigned addr, unsigned lbo, unsigned sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = kTN, M = kTM.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTN >> 3) << 17) |
+                            ((uint32_t)(kTM >> 4) << 24);
+
+__device__ __forceinline__ bool mbar_test(unsigned bar, unsigned parity) {
+    unsigned ok = 0;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Wait (non-blocking polls with a short sleep) until phase `parity` of the
+// barrier completes or kWaitNs have passed; returns whether it completed.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_test(bar, parity)) {
+        if (global_ns() - t0 > kWaitNs) return false;
+        __nanosleep(64);
+    }
+    return true;
+}
+
+// Copy `rows` rows of an R-wide bf16 operand into the canonical layout:
+// 16-byte chunk kc of row r goes to (r/8)*R*16 + kc*128 + (r%8)*16.
+// Consecutive threads take consecutive rows of a core matrix, so the
+// shared-memory writes of a warp fill whole banks; rows at or past `valid`
+// are zero-filled.
+__device__ __forceinline__ void stage_operand(char* dst, const __nv_bfloat16* src, int64_t stride, int rows,
+                                              int64_t valid, int64_t R) {
+    const int kchunks = (int)(R / 8);
+    const int total = rows * kchunks;
+    for (int idx = threadIdx.x; idx < total; idx += kDPThreads) {
+        const int rr = idx & 7, kc = (idx >> 3) % kchunks, g = (idx >> 3) / kchunks;
+        const int row = g * 8 + rr;
+        const bool v = row < valid;
+        const __nv_bfloat16* s = v ? src + (int64_t)row * stride + kc * 8 : src;
+        cp_async16(dst + (int64_t)g * R * 16 + kc * 128 + rr * 16, s, v);
+    }
+}
+
+__device__ __forceinline__ float softplus_acc(float v) {
+    // max(v,0) + log1p(exp(-|v|)), CUDA's full-precision expf / log1pf
+    return fmaxf(v, 0.f) + log1pf(expf(-fabsf(v)));
+}
+__device__ __forceinline__ float sigmoid_acc(float z) { return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-z))); }
+
+template <bool BWD>
+__global__ void __launch_bounds__(kDPThreads) ssm_dtproj_kernel(const DtProjParams p) {
+    extern __shared__ __align__(128) char dp_smem[];
+    const int64_t R = p.R;
+    char* sA = dp_smem;
+    char* sB = dp_smem + (int64_t)kTM * R * 2;
+    float* stg = reinterpret_cast<float*>(dp_smem);  // reused after the MMAs have read the operands
+    float* sDB = reinterpret_cast<float*>(dp_smem + (dtproj_smem(R) - kTN * 4 - 16));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(dp_smem + (dtproj_smem(R) - 16));
+    unsigned* tslot = reinterpret_cast<unsigned*>(dp_smem + (dtproj_smem(R) - 8));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t tm = blockIdx.x / p.tiles_n, tn = blockIdx.x % p.tiles_n;
+    const int64_t m0 = tm * kTM, n0 = tn * kTN;
+
+    if (warp == 0) {  // the accumulator: 256 TMEM columns x 128 lanes of fp32
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tslot)),
+                     "r"(kTN)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    if (threadIdx.x == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_u32(bar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    if (BWD)
+        for (int i = threadIdx.x; i < kTN; i += kDPThreads) sDB[i] = 0.f;
+    stage_operand(sA, p.a + m0 * p.a_stride, p.a_stride, kTM, p.M - m0, R);
+    stage_operand(sB, p.w + n0 * R, R, kTN, p.D - n0, R);
+    cp_async_commit();
+    cp_async_wait<0>();
+    // make this thread's shared-memory writes visible to the tensor core's (async) proxy
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+    const unsigned tmem = *tslot;
+
+    if (threadIdx.x == 0) {
+        const unsigned a0 = smem_u32(sA), b0 = smem_u32(sB), sbo = (unsigned)(R * 16);
+        for (int j = 0; j < (int)(R / 16); ++j) {  // K = 16 per instruction: two core matrices along K
+            const uint64_t ad = smem_desc(a0 + j * 256, 128, sbo), bd = smem_desc(b0 + j * 256, 128, sbo);
+            const unsigned acc = j > 0;
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
+                " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem),
+                "l"(ad), "l"(bd), "r"(kIdesc), "r"(acc)
+                : "memory");
+        }
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                         smem_u32(bar))
+                     : "memory");
+    }
+    // every thread waits for the accumulator (bounded: a stuck MMA becomes an error status)
+    bool ready = mbar_wait_bounded(smem_u32(bar), 0);
+    if (!ready) {
+        // report, give the tensor core one more bounded wait before the TMEM is freed, write nothing
+        if (threadIdx.x == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+        mbar_wait_bounded(smem_u32(bar), 0);
+    }
+    asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+
+    float nf = 0.f;
+    if (ready) {
+        float* blk = stg + warp * 32 * kStgRow;
+        const int rsub = lane >> 3, cq = (lane & 7) * 4;  // coalesced phase: 4 rows x 8 float4 per instruction
+        for (int c = 0; c < kTN / 32; ++c) {
+            if (n0 + c * 32 >= p.D) break;  // uniform across the CTA
+            unsigned v[32];
+            asm volatile(
+                "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+                "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+                : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+                  "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]),
+                  "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]),
+                  "=r"(v[22]), "=r"(v[23]), "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]),
+                  "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+                : "r"(tmem + ((unsigned)(warp * 32) << 16) + (unsigned)(c * 32)));
+            asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+            // lane = row: write the row's 32 accumulators into the transpose block
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(blk + lane * kStgRow + 4 * q) =
+                    make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            __syncwarp();
+            const int64_t col = n0 + c * 32 + cq;
+            const bool cv = col < p.D;
+            const float4 b4 = (p.bias && cv) ? __ldg(reinterpret_cast<const float4*>(p.bias + col))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+            float4 db = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = 4 * i + rsub;
+                const int64_t m = m0 + warp * 32 + r;
+                const float4 acc = *reinterpret_cast<const float4*>(blk + r * kStgRow + cq);
+                if (m < p.M && cv) {
+                    const float4 pre = make_float4(acc.x + b4.x, acc.y + b4.y, acc.z + b4.z, acc.w + b4.w);
+                    float4 o;
+                    if (!BWD) {
+                        o = p.softplus ? make_float4(softplus_acc(pre.x), softplus_acc(pre.y), softplus_acc(pre.z),
+                                                     softplus_acc(pre.w))
+                                       : pre;
+                    } else {
+                        const float4 g = *reinterpret_cast<const float4*>(p.dout + m * p.D + col);
+                        o = p.softplus ? make_float4(g.x * sigmoid_acc(pre.x), g.y * sigmoid_acc(pre.y),
+                                                     g.z * sigmoid_acc(pre.z), g.w * sigmoid_acc(pre.w))
+                                       : g;
+                        db.x += o.x; db.y += o.y; db.z += o.z; db.w += o.w;
+                    }
+                    *reinterpret_cast<float4*>(p.out + m * p.D + col) = o;
+                    nf = __fmaf_rn(o.x + o.y + o.z + o.w, 0.0f, nf);
+                }
+            }
+            if (BWD) {  // the 4 lanes holding these 4 columns (lane % 8 equal) sum their rows
+#pragma unroll
+                for (int s = 8; s < 32; s <<= 1) {
+                    db.x += __shfl_xor_sync(0xffffffffu, db.x, s);
+                    db.y += __shfl_xor_sync(0xffffffffu, db.y, s);
+                    db.z += __shfl_xor_sync(0xffffffffu, db.z, s);
+                    db.w += __shfl_xor_sync(0xffffffffu, db.w, s);
+                }
+                if (lane < 8) {
+                    float* d = sDB + c * 32 + cq;
+                    atomicAdd(d, db.x); atomicAdd(d + 1, db.y); atomicAdd(d + 2, db.z); atomicAdd(d + 3, db.w);
+                }
+            }
+            __syncwarp();  // the block is rewritten by the next chunk
+        }
+    }
+    flag_nonfinite(p.status, nf);
+    asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+    __syncthreads();
+    if (BWD && ready && p.dbias)
+        for (int i = threadIdx.x; i < kTN; i += kDPThreads)
+            if (n0 + i < p.D) atomicAdd(p.dbias + n0 + i, sDB[i]);
+    if (warp == 0) {
+        asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kTN) : "memory");
+    }
+}
+
+}  // namespace
+
+int dtproj_smem_bytes(int64_t R) { return dtproj_smem(R); }
+
+int launch_dtproj(bool bwd, int64_t M, int64_t D, int64_t R, int64_t a_stride, const void* a, const void* w,
+                  const float* bias, float* out, const float* dout, float* dbias, int softplus, unsigned* status,
+                  cudaStream_t s) {
+    if (M == 0 || D == 0) return 0;
+    DtProjParams p{};
+    p.M = M; p.D = D; p.R = R; p.a_stride = a_stride;
+    p.tiles_n = (D + kTN - 1) / kTN;
+    p.a = reinterpret_cast<const __nv_bfloat16*>(a);
+    p.w = reinterpret_cast<const __nv_bfloat16*>(w);
+    p.bias = bias; p.out = out; p.dout = dout; p.dbias = dbias; p.softplus = softplus; p.status = status;
+    const int64_t tiles = ((M + kTM - 1) / kTM) * p.tiles_n;
+    const int smem = dtproj_smem(R);
+    // the limit is set once per device, so it is set for the largest R (256)
+    static unsigned long long mask_f = 0, mask_b = 0;
+    if (bwd) {
+        if (!ensure_smem(ssm_dtproj_kernel<true>, dtproj_smem(256), mask_b)) return -1;
+        ssm_dtproj_kernel<true><<<(unsigned)tiles, kDPThreads, smem, s>>>(p);
+    } else {
+        if (!ensure_smem(ssm_dtproj_kernel<false>, dtproj_smem(256), mask_f)) return -1;
+        ssm_dtproj_kernel<false><<<(unsigned)tiles, kDPThreads, smem, s>>>(p);
+    }
+    return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+}  // namespace ssm

@@ -10,6 +10,7 @@
 namespace ssm {
 
 constexpr unsigned kStatusNonFinite = 1u;  // workspace status bit: an output was Inf/NaN
+constexpr unsigned kStatusTimeout = 2u;    // workspace status bit: a bounded wait inside a kernel ran out
 constexpr int kFwdThreads = 128;
 constexpr int kBwdThreads = 128;
 constexpr int kConvThreads = 128;
@@ -149,6 +150,10 @@ int launch_conv(int io, bool bwd, int64_t B, int64_t L, int64_t D, int K, const 
                 const float* bias, const float* state_in, void* x, float* state_out, const void* dx, void* dxin,
                 float* dw, float* dbias, float* dstate, unsigned* status, cudaStream_t s);
 int launch_bwd(int io, const BwdParams& p, cudaStream_t s);
+int dtproj_smem_bytes(int64_t R);
+int launch_dtproj(bool bwd, int64_t M, int64_t D, int64_t R, int64_t a_stride, const void* a, const void* w,
+                  const float* bias, float* out, const float* dout, float* dbias, int softplus, unsigned* status,
+                  cudaStream_t s);
 int launch_bwd_agg(int io, const BwdParams& p, cudaStream_t s);
 
 }  // namespace ssm

@@ -33,7 +33,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("ssm_scan_fwd", "ssm_scan_bwd", "ssm_step", "ssm_scan_workspace_bytes", "ssm_scan_ckpt_elems",
-              "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad", "ssm_conv1d_fwd", "ssm_conv1d_bwd"):
+              "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad", "ssm_conv1d_fwd", "ssm_conv1d_bwd",
+              "ssm_dtproj_fwd", "ssm_dtproj_bwd"):
         assert n in names
 
 
@@ -159,12 +160,42 @@ def test_conv_bwd_rejects_bad_arguments(ssm, over, code):
     assert ssm.lib().ssm_conv1d_bwd(ctypes.byref(args), None) == code
 
 
+def dtproj_args(ssm, **over):
+    a = dict(M=300, D=1048, R=64, a_stride=96, softplus=1, a=FAKE, w=FAKE + 4096, bias=None, delta=FAKE + 8192,
+             workspace=None)
+    a.update(over)
+    return ssm.DtProjArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(R=24), UNSUPPORTED), (dict(R=0), UNSUPPORTED), (dict(R=272), UNSUPPORTED), (dict(D=1044), ALIGNMENT),
+    (dict(a_stride=60), INVALID), (dict(a_stride=100), ALIGNMENT), (dict(softplus=2), INVALID),
+    (dict(a=None), INVALID), (dict(w=None), INVALID), (dict(delta=None), INVALID), (dict(bias=FAKE + 4), ALIGNMENT),
+    (dict(M=-1), INVALID),
+])
+def test_dtproj_rejects_bad_arguments(ssm, over, code):
+    args = dtproj_args(ssm, **over)
+    assert ssm.lib().ssm_dtproj_fwd(ctypes.byref(args), None) == code
+
+
+def test_dtproj_bwd_rejects_bad_arguments(ssm):
+    for over, code in ((dict(ddelta=None), INVALID), (dict(dpre=None), INVALID), (dict(dbias=FAKE + 8), ALIGNMENT)):
+        g = dict(ddelta=FAKE + 16384, dpre=FAKE + 20480, dbias=None)
+        g.update(over)
+        args = ssm.DtProjBwdArgs(f=dtproj_args(ssm), **g)
+        assert ssm.lib().ssm_dtproj_bwd(ctypes.byref(args), None) == code
+    args = ssm.DtProjBwdArgs(f=dtproj_args(ssm, R=8), ddelta=FAKE, dpre=FAKE)
+    assert ssm.lib().ssm_dtproj_bwd(ctypes.byref(args), None) == UNSUPPORTED
+
+
 def test_null_args_struct(ssm):
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_bwd(None, None) == INVALID
     assert ssm.lib().ssm_step(None, None) == INVALID
     assert ssm.lib().ssm_conv1d_fwd(None, None) == INVALID
     assert ssm.lib().ssm_conv1d_bwd(None, None) == INVALID
+    assert ssm.lib().ssm_dtproj_fwd(None, None) == INVALID
+    assert ssm.lib().ssm_dtproj_bwd(None, None) == INVALID
 
 
 def test_dA_log_rejects_bad_arguments(ssm):
