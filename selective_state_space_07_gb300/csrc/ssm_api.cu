@@ -341,7 +341,8 @@ int check_dtproj(const ssm_dtproj_args* a) {
     const int64_t stride = a->a_stride ? a->a_stride : a->R;
     if (stride < a->R) return SSM_ERR_INVALID_ARG;
     if ((stride * 2) % 16 != 0) return SSM_ERR_ALIGNMENT;
-    if (a->M > (int64_t(1) << 40) || a->D > (int64_t(1) << 31) || stride > (int64_t(1) << 24)) return SSM_ERR_INVALID_ARG;
+    // the copies address rows with 32-bit coordinates
+    if (a->M > 0x7fffffff || a->D > 0x7fffffff || stride > (int64_t(1) << 24)) return SSM_ERR_INVALID_ARG;
     if (((a->M + 127) / 128) * ((a->D + 255) / 256) > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
     const bool work = a->M > 0 && a->D > 0;
     if (work && (!a->a || !a->w)) return SSM_ERR_INVALID_ARG;
