@@ -128,10 +128,22 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback", {}
 
 
-def kernel_source_hash():
+# The device sources each C-ABI call's kernels are compiled from: a committed
+# DRAM-traffic figure is used only while these files are unchanged.
+CALL_SOURCES = {
+    "ssm_scan_fwd": ("ssm_fwd.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "ssm_scan_bwd": ("ssm_bwd.cu", "ssm_fwd.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "ssm_conv1d_fwd": ("ssm_conv.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "ssm_conv1d_bwd": ("ssm_conv.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "ssm_dtproj_fwd": ("ssm_dtproj.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "ssm_dtproj_bwd": ("ssm_dtproj.cu", "ssm_common.cuh", "ssm_internal.h"),
+}
+
+
+def kernel_source_hash(call):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "selective_state_space_07_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
+    for fn in CALL_SOURCES[call]:
         with open(os.path.join(d, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -154,7 +166,7 @@ def profiled_traffic(kernel, workload):
         with open(p) as f:
             d = json.load(f)
         ent = d.get(kernel, {}).get(workload)
-        if ent and ent.get("source_hash") == kernel_source_hash():
+        if ent and ent.get("source_hash") == kernel_source_hash(kernel):
             return float(ent["dram_bytes_per_launch"])
     except Exception:
         pass

@@ -10,7 +10,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, NONFINITE = 0, -1, -2, -3, -4, -5, -7
+OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, TIMEOUT, NONFINITE = 0, -1, -2, -3, -4, -5, -6, -7
 
 
 @pytest.fixture(scope="module")
@@ -63,8 +63,10 @@ def test_sizes(ssm):
 
 
 def test_status_strings(ssm):
-    for code in (OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, NONFINITE, 12345):
+    for code in (OK, INVALID, UNSUPPORTED, ALIGNMENT, WORKSPACE, CUDA, TIMEOUT, NONFINITE, 12345):
         assert isinstance(ssm.lib().ssm_status_string(code), bytes)
+    assert b"wait" in ssm.lib().ssm_status_string(TIMEOUT)
+    assert ssm.lib().ssm_status_string(TIMEOUT) != ssm.lib().ssm_status_string(12345)
 
 
 FAKE = 1 << 20  # a 16-byte aligned address; never dereferenced: every case fails validation first
