@@ -41,7 +41,9 @@ constexpr int kTM = 128;           // tokens per tile: MMA M, TMEM lanes
 // spill). Warp w >= 1 reads TMEM lanes 32(w%4) .. +31 and every (EW/4)-th
 // 32-column chunk starting at (w-1)/4.
 template <bool BWD> __host__ __device__ constexpr int epi_warps() { return BWD ? 8 : 16; }
-template <bool BWD> __host__ __device__ constexpr int dp_threads() { return 32 * (1 + epi_warps<BWD>()); }  // + warp 0: TMA, MMA
+// + warp 0 (operand TMA, MMA issue) and, in the backward, a last warp that streams ddelta with TMA
+template <bool BWD> __host__ __device__ constexpr int dp_threads() { return 32 * (1 + epi_warps<BWD>() + (BWD ? 1 : 0)); }
+constexpr int kChunkBytes = kTM * 32 * 4;  // one ddelta chunk: 128 rows x 32 fp32 columns
 constexpr int kStgRow = 36;        // floats per row of a warp's 32x32 transpose block (padded)
 constexpr int kStgWarpBytes = 32 * kStgRow * 4;
 constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s: how long a thread waits on an mbarrier
@@ -50,9 +52,10 @@ constexpr int kMaxSmem = 227 * 1024;
 // so the two accumulators (2*TN of the SM's 512 TMEM columns) are always free.
 constexpr int kMinSmem = 116 * 1024;
 
-// Tile geometry for TN channels per tile (MMA N) and EW epilogue warps.
-// Shared memory: operands (A then B) | transpose blocks | 5 mbarriers + the TMEM address.
-template <int TN, int EW> struct DpGeom {
+// Tile geometry for TN channels per tile (MMA N), EW epilogue warps and RS
+// ddelta ring slots (backward). Shared memory: operands (A then B) | ddelta
+// ring | transpose blocks | mbarriers + the TMEM address.
+template <int TN, int EW, int RS> struct DpGeom {
     static_assert(TN == 128 || TN == 256, "N of the MMA");
     // kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, N = TN, M = kTM
     static constexpr uint32_t idesc =
@@ -61,8 +64,12 @@ template <int TN, int EW> struct DpGeom {
     __host__ __device__ static constexpr int atoms(int64_t R) { return (int)((R + 63) / 64); }
     __host__ __device__ static constexpr int operand_bytes(int64_t R) { return atoms(R) * (kTM + TN) * 128; }
     static constexpr int stg_bytes = EW * kStgWarpBytes;
+    static constexpr int ring_bytes = RS * kChunkBytes;
+    static constexpr int nbars = 5 + 2 * RS;  // op_full, tmem_full[2], tmem_empty[2], ring full[RS], ring empty[RS]
     // + 1 KB: the operand atoms start on a 1024-byte boundary (the swizzle's period)
-    __host__ __device__ static constexpr int need(int64_t R) { return operand_bytes(R) + stg_bytes + 64 + 1024; }
+    __host__ __device__ static constexpr int need(int64_t R) {
+        return operand_bytes(R) + ring_bytes + stg_bytes + 8 * nbars + 16 + 1024;
+    }
     __host__ __device__ static constexpr int smem(int64_t R) { return need(R) > kMinSmem ? need(R) : kMinSmem; }
     __host__ __device__ static constexpr bool fits(int64_t R) { return need(R) <= kMaxSmem; }
 };
@@ -147,22 +154,24 @@ __device__ __forceinline__ float4 dsoftplus4(float4 g, float4 v) {
 // warps finished reading accumulator b). Every wait is bounded by the global
 // timer; a wait that runs out sets the timeout status and ends that role's
 // loop (the others run out the same way), and the TMEM is freed at the end.
-template <int TN, bool BWD>
+template <int TN, bool BWD, int RS>
 __global__ void __launch_bounds__(dp_threads<BWD>(), 1)
     ssm_dtproj_kernel(const DtProjParams p, const __grid_constant__ CUtensorMap tmA,
-                      const __grid_constant__ CUtensorMap tmB) {
+                      const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmG) {
     extern __shared__ __align__(1024) char dp_smem_raw[];
     // the swizzled atoms need 1024-byte alignment; the request has 1 KB of slack for it
     char* dp_smem = dp_smem_raw + ((1024u - (smem_u32(dp_smem_raw) & 1023u)) & 1023u);
     constexpr int EW = epi_warps<BWD>();
-    using G = DpGeom<TN, EW>;
+    using G = DpGeom<TN, EW, RS>;
     const int64_t R = p.R;
     char* sA = dp_smem;
     char* sB = dp_smem + G::atoms(R) * kTM * 128;
-    float* stg = reinterpret_cast<float*>(dp_smem + G::operand_bytes(R));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(dp_smem + G::operand_bytes(R) + G::stg_bytes);
+    char* ring = dp_smem + G::operand_bytes(R);  // ddelta chunks, row-major [128][32] fp32 each
+    float* stg = reinterpret_cast<float*>(ring + G::ring_bytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<char*>(stg) + G::stg_bytes);
     const unsigned op_full = smem_u32(bars), tfull0 = smem_u32(bars + 1), tempty0 = smem_u32(bars + 3);
-    unsigned* tslot = reinterpret_cast<unsigned*>(bars + 5);
+    const unsigned rfull0 = smem_u32(bars + 5), rempty0 = smem_u32(bars + 5 + RS);
+    unsigned* tslot = reinterpret_cast<unsigned*>(bars + G::nbars);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = p.tiles_m * p.tiles_n;
 
@@ -178,6 +187,10 @@ __global__ void __launch_bounds__(dp_threads<BWD>(), 1)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(tfull0 + 8 * b) : "memory");
             asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(tempty0 + 8 * b), "r"(EW)
                          : "memory");
+        }
+        for (int b = 0; b < RS; ++b) {  // a ddelta chunk is read by one epilogue warp per TMEM lane quarter
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(rfull0 + 8 * b) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 4;\n" ::"r"(rempty0 + 8 * b) : "memory");
         }
         asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     }
@@ -233,41 +246,56 @@ __global__ void __launch_bounds__(dp_threads<BWD>(), 1)
             }
         }
         __syncwarp();
+    } else if (BWD && warp == EW + 1) {
+        // ddelta producer: the chunks of every tile in order, through the RS-slot ring
+        if (lane == 0) {
+            int64_t q = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+                const int64_t m0 = (t / p.tiles_n) * kTM, n0 = (t % p.tiles_n) * TN;
+                for (int c = 0; c < TN / 32 && n0 + c * 32 < p.D; ++c, ++q) {
+                    const int slot = (int)(q % RS);
+                    const int64_t k = q / RS;
+                    if (k > 0 && !mbar_wait_bounded(rempty0 + 8 * slot, (unsigned)((k - 1) & 1))) {
+                        if (p.status) atomicOr(p.status, kStatusTimeout);
+                        ok = false;
+                        break;
+                    }
+                    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(rfull0 + 8 * slot),
+                                 "r"((unsigned)kChunkBytes)
+                                 : "memory");
+                    // x = a column multiple of 32 (128 bytes); rows past M read as zero
+                    tma_load_2d(ring + slot * kChunkBytes, &tmG, (int)(n0 + c * 32), (int)m0, rfull0 + 8 * slot);
+                }
+            }
+        }
+        __syncwarp();
     } else {
         constexpr int step = EW / 4;  // warps per TMEM lane quarter
         const int ew = warp - 1, quarter = warp & 3, first = ew >> 2;  // TMEM lanes 32*quarter.., chunks first, first+step, ..
         float* blk = stg + ew * 32 * kStgRow;
         const int rsub = lane >> 3, cq = (lane & 7) * 4;  // coalesced phase: 4 rows x 8 float4 per instruction
-        int64_t it = 0;
-        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++it) {
+        int64_t it = 0, qbase = 0;  // qbase: ddelta chunks of the earlier tiles (the producer's count)
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++it) {
             const int64_t m0 = (t / p.tiles_n) * kTM, n0 = (t % p.tiles_n) * TN;
             const int buf = (int)(it & 1);
             const int64_t mrow = m0 + quarter * 32;
-            // backward: ddelta of a chunk is loaded one chunk ahead, before any
-            // store of this thread (dpre may be ddelta: read, then written, by the same thread)
-            float4 gcur[8], gnext[8];
-            auto load_g = [&](int c, float4 (&g)[8]) {
-                const int64_t col = n0 + c * 32 + cq;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int64_t m = mrow + 4 * i + rsub;
-                    g[i] = (c < TN / 32 && m < p.M && col < p.D)
-                               ? *reinterpret_cast<const float4*>(p.dout + m * p.D + col)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-            };
-            if (BWD) load_g(first, gnext);
+            const int nch = (int)min64(TN / 32, (p.D - n0 + 31) / 32);
             if (!mbar_wait_bounded(tfull0 + 8 * buf, (unsigned)((it >> 1) & 1))) {
                 if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeout);
                 break;
             }
             asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-            for (int c = first; c < TN / 32; c += step) {
-                if (n0 + c * 32 >= p.D) break;  // uniform across the warp
-                if (BWD) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) gcur[i] = gnext[i];
-                    load_g(c + step, gnext);
+            for (int c = first; c < nch; c += step) {
+                // backward: this chunk's ddelta, 128 rows x 32 columns, in ring slot q % RS
+                const int64_t q = qbase + c;
+                const float* gch = reinterpret_cast<const float*>(ring + (int)(q % (RS > 0 ? RS : 1)) * kChunkBytes);
+                if (BWD && !mbar_wait_bounded(rfull0 + 8 * (int)(q % (RS > 0 ? RS : 1)),
+                                              (unsigned)((q / (RS > 0 ? RS : 1)) & 1))) {
+                    if (lane == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+                    ok = false;
+                    break;
                 }
                 unsigned v[32];
                 asm volatile(
@@ -303,7 +331,8 @@ __global__ void __launch_bounds__(dp_threads<BWD>(), 1)
                         if (!BWD) {
                             o = p.softplus ? softplus4(pre) : pre;
                         } else {
-                            o = p.softplus ? dsoftplus4(gcur[i], pre) : gcur[i];
+                            const float4 g = *reinterpret_cast<const float4*>(gch + (quarter * 32 + r) * 32 + cq);
+                            o = p.softplus ? dsoftplus4(g, pre) : g;
                             db.x += o.x; db.y += o.y; db.z += o.z; db.w += o.w;
                         }
                         *reinterpret_cast<float4*>(p.out + m * p.D + col) = o;
@@ -320,8 +349,12 @@ __global__ void __launch_bounds__(dp_threads<BWD>(), 1)
                     }
                     if (lane < 8 && cv && p.dbias) red_add_v4(p.dbias + col, db);
                 }
-                __syncwarp();  // the block is rewritten by the next chunk
+                __syncwarp();  // the block is rewritten by the next chunk; the ring slot is read
+                if (BWD && lane == 0)
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(rempty0 + 8 * (int)(q % (RS > 0 ? RS : 1)))
+                                 : "memory");
             }
+            qbase += nch;
             asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(tempty0 + 8 * buf) : "memory");
@@ -339,7 +372,7 @@ __global__ void __launch_bounds__(dp_threads<BWD>(), 1)
 }  // namespace
 
 int dtproj_smem_bytes(int64_t R) {
-    return DpGeom<256, 16>::fits(R) ? DpGeom<256, 16>::smem(R) : DpGeom<128, 16>::smem(R);
+    return DpGeom<256, 16, 0>::fits(R) ? DpGeom<256, 16, 0>::smem(R) : DpGeom<128, 16, 0>::smem(R);
 }
 
 namespace {
@@ -356,41 +389,60 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// A [rows, R] bf16 matrix with rows `stride` elements apart, copied in boxes
-// of 64 elements (128 bytes, 128-byte swizzle) x box_rows rows; rows and
-// columns past the end read as zero.
-bool encode_rows(CUtensorMap* map, const void* base, int64_t R, int64_t rows, int64_t stride, int box_rows) {
+// A 2D [rows, cols] matrix with rows `stride_bytes` apart, copied in boxes
+// of box_cols x box_rows; rows and columns past the end read as zero.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
+               int64_t stride_bytes, int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
     const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)R, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)(stride * 2)};
-    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return enc(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// a bf16 operand [rows, R]: boxes of one 64-wide K atom (128 bytes, 128-byte swizzle) x box_rows
+bool encode_operand(CUtensorMap* map, const void* base, int64_t R, int64_t rows, int64_t stride, int box_rows) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, R, rows, stride * 2, 64, box_rows,
+                     CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-template <int TN, bool BWD> int launch_dtproj_t(const DtProjParams& p0, int64_t a_stride, cudaStream_t s) {
+template <int TN, bool BWD, int RS> int launch_dtproj_t(const DtProjParams& p0, int64_t a_stride, cudaStream_t s) {
     DtProjParams p = p0;
     p.tiles_m = (p.M + kTM - 1) / kTM;
     p.tiles_n = (p.D + TN - 1) / TN;
     const int64_t tiles = p.tiles_m * p.tiles_n;
-    const int smem = DpGeom<TN, epi_warps<BWD>()>::smem(p.R);
-    CUtensorMap ta, tb;
-    if (!encode_rows(&ta, p.a, p.R, p.M, a_stride, kTM) || !encode_rows(&tb, p.w, p.R, p.D, p.R, TN)) return -1;
+    const int smem = DpGeom<TN, epi_warps<BWD>(), RS>::smem(p.R);
+    CUtensorMap ta, tb, tg;
+    if (!encode_operand(&ta, p.a, p.R, p.M, a_stride, kTM) || !encode_operand(&tb, p.w, p.R, p.D, p.R, TN))
+        return -1;
+    if (BWD) {  // ddelta [M, D] fp32 in chunks of 32 columns (128 bytes) x 128 rows
+        if (!encode_2d(&tg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dout, p.D, p.M, p.D * 4, 32, kTM,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+            return -1;
+    } else {
+        tg = ta;  // not read by the forward
+    }
     const unsigned grid = (unsigned)min64(tiles, (int64_t)sm_count());  // persistent: one CTA per SM
     // the limit is set once per device, so it is set to the largest request
     static unsigned long long mask = 0;
-    if (!ensure_smem(ssm_dtproj_kernel<TN, BWD>, kMaxSmem, mask)) return -1;
-    ssm_dtproj_kernel<TN, BWD><<<grid, dp_threads<BWD>(), smem, s>>>(p, ta, tb);
+    if (!ensure_smem(ssm_dtproj_kernel<TN, BWD, RS>, kMaxSmem, mask)) return -1;
+    ssm_dtproj_kernel<TN, BWD, RS><<<grid, dp_threads<BWD>(), smem, s>>>(p, ta, tb, tg);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
-template <bool BWD> int launch_dtproj_b(const DtProjParams& p, int64_t a_stride, cudaStream_t s) {
+int launch_dtproj_fwd(const DtProjParams& p, int64_t a_stride, cudaStream_t s) {
     // 256-channel tiles while their operands fit next to the transpose blocks, else 128
-    return DpGeom<256, epi_warps<BWD>()>::fits(p.R) ? launch_dtproj_t<256, BWD>(p, a_stride, s)
-                                                    : launch_dtproj_t<128, BWD>(p, a_stride, s);
+    return DpGeom<256, epi_warps<false>(), 0>::fits(p.R) ? launch_dtproj_t<256, false, 0>(p, a_stride, s)
+                                                         : launch_dtproj_t<128, false, 0>(p, a_stride, s);
+}
+int launch_dtproj_bwd(const DtProjParams& p, int64_t a_stride, cudaStream_t s) {
+    // the widest tile, then the deepest ddelta ring, that fit
+    constexpr int EW = epi_warps<true>();
+    if (DpGeom<256, EW, 4>::fits(p.R)) return launch_dtproj_t<256, true, 4>(p, a_stride, s);
+    if (DpGeom<128, EW, 4>::fits(p.R)) return launch_dtproj_t<128, true, 4>(p, a_stride, s);
+    return launch_dtproj_t<128, true, 2>(p, a_stride, s);
 }
 
 }  // namespace
@@ -404,7 +456,7 @@ int launch_dtproj(bool bwd, int64_t M, int64_t D, int64_t R, int64_t a_stride, c
     p.a = reinterpret_cast<const __nv_bfloat16*>(a);
     p.w = reinterpret_cast<const __nv_bfloat16*>(w);
     p.bias = bias; p.out = out; p.dout = dout; p.dbias = dbias; p.softplus = softplus; p.status = status;
-    return bwd ? launch_dtproj_b<true>(p, a_stride, s) : launch_dtproj_b<false>(p, a_stride, s);
+    return bwd ? launch_dtproj_bwd(p, a_stride, s) : launch_dtproj_fwd(p, a_stride, s);
 }
 
 }  // namespace ssm
