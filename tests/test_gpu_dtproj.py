@@ -59,6 +59,33 @@ def test_parity_against_the_oracle(ssm, shape, softplus):
     assert rel_err(to_np(g["dbias"]), rg["dbias"]) <= TOL_BWD
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 264, 16), (1, 3, 8, 32), (3, 1, 4096, 128), (1, 129, 8, 256)])
+def test_decode_and_narrow_shapes(ssm, shape):
+    # one token (decoding), fewer tiles than SMs, a single 8-channel column,
+    # the widest rank: every persistent CTA without a tile must still leave cleanly
+    B, L, D, R = shape
+    c = gen.make_dtproj_inputs(B, L, D, R, seed=B * 1000 + L + D + R)
+    a = xproj_buffer(c.a)
+    w, bias = dev(c.w, torch.bfloat16), dev(c.bias)
+    delta = ssm.dtproj_fwd(a, w, bias)
+    g = ssm.dtproj_bwd(a, w, dev(c.ddelta), bias)
+    torch.cuda.synchronize()
+    a2 = c.a.reshape(-1, R)
+    assert rel_err(to_np(delta).reshape(-1, D), oracle.dtproj_fwd(a2, c.w, c.bias)) <= TOL_FWD
+    rg = oracle.dtproj_bwd(a2, c.w, c.ddelta.reshape(-1, D), c.bias)
+    assert rel_err(to_np(g["dpre"]).reshape(-1, D), rg["dpre"]) <= TOL_BWD
+    assert rel_err(to_np(g["dbias"]), rg["dbias"]) <= TOL_BWD
+
+
+def test_empty_rows(ssm):
+    w = torch.zeros(256, 64, dtype=torch.bfloat16, device="cuda")
+    a = torch.zeros(2, 0, 64, dtype=torch.bfloat16, device="cuda")
+    assert ssm.dtproj_fwd(a, w).shape == (2, 0, 256)
+    g = ssm.dtproj_bwd(a, w, torch.zeros(2, 0, 256, device="cuda"), torch.zeros(256, device="cuda"))
+    torch.cuda.synchronize()
+    assert not torch.any(g["dbias"])
+
+
 def test_dense_a_without_bias_and_in_place_backward(ssm):
     c = gen.make_dtproj_inputs(2, 100, 256, 32, seed=5)
     a, w = dev(c.a, torch.bfloat16), dev(c.w, torch.bfloat16)
