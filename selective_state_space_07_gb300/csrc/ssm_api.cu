@@ -6,8 +6,39 @@
 #include <algorithm>
 #include <cstdint>
 
+#include <cudaTypedefs.h>
+
 #include "../../include/ssm_scan.h"
 #include "ssm_internal.h"
+
+namespace ssm {
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            f = nullptr;
+        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }();
+    return fn;
+}
+}  // namespace
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
+               int64_t stride_bytes, int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
+    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || cols <= 0 || rows <= 0) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)stride_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace ssm
 
 namespace {
 
@@ -75,6 +106,8 @@ int check_fwd(const ssm_fwd_args* a, bool need_y) {
         return SSM_ERR_INVALID_ARG;
     const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
     if (bc != SSM_OK) return bc;
+    // the tiles are addressed by 32-bit token rows of the flattened [B*L] tensors
+    if (a->B * a->L > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
     const bool work = a->B > 0 && a->L > 0 && a->D > 0;
     if (work && (!a->x || !a->dt || !a->Bm || !a->Cm || !a->A || (need_y && !a->y))) return SSM_ERR_INVALID_ARG;
     const void* ptrs[] = {a->x, a->z, a->Bm, a->Cm, a->dt, a->dt_bias, a->A, a->Dskip, a->h0, a->y, a->h_last,

@@ -25,9 +25,6 @@
 // epilogue. The op is bound by writing the fp32 [M, D] result (K = R is
 // small: 2*R flops per 4 output bytes), so the design keeps the epilogue's
 // stores going while the next tile is loaded and multiplied.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
 
@@ -46,7 +43,6 @@ template <bool BWD> __host__ __device__ constexpr int dp_threads() { return 32 *
 constexpr int kChunkBytes = kTM * 32 * 4;  // one ddelta chunk: 128 rows x 32 fp32 columns
 constexpr int kStgRow = 36;        // floats per row of a warp's 32x32 transpose block (padded)
 constexpr int kStgWarpBytes = 32 * kStgRow * 4;
-constexpr unsigned long long kWaitNs = 1000000000ull;  // 1 s: how long a thread waits on an mbarrier
 constexpr int kMaxSmem = 227 * 1024;
 // The shared-memory request is above half an SM's 228 KB: one CTA per SM,
 // so the two accumulators (2*TN of the SM's 512 TMEM columns) are always free.
@@ -88,7 +84,6 @@ struct DtProjParams {
     unsigned* status;
 };
 
-__device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)__cvta_generic_to_shared(p); }
 
 // Shared-memory matrix descriptor of a K-major operand in the 128-byte
 // swizzled canonical layout: atoms of 8 rows x 128 bytes (64 bf16 of K), the
@@ -99,39 +94,6 @@ __device__ __forceinline__ unsigned smem_u32(const void* p) { return (unsigned)_
 __device__ __forceinline__ uint64_t smem_desc_sw128(unsigned addr) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
            (2ull << 61);
-}
-
-__device__ __forceinline__ bool mbar_test(unsigned bar, unsigned parity) {
-    unsigned ok = 0;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-    return t;
-}
-// Wait (non-blocking polls with a short sleep) until phase `parity` of the
-// barrier completes or kWaitNs have passed; returns whether it completed.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity) {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_test(bar, parity)) {
-        if (global_ns() - t0 > kWaitNs) return false;
-        __nanosleep(64);
-    }
-    return true;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, unsigned bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
-        : "memory");
 }
 
 // The bf16-operand path uses the scan's MUFU forms of softplus and sigmoid
@@ -376,32 +338,6 @@ int dtproj_smem_bytes(int64_t R) {
 }
 
 namespace {
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-        void* f = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
-                cudaSuccess ||
-            q != cudaDriverEntryPointSuccess)
-            f = nullptr;
-        return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }();
-    return fn;
-}
-
-// A 2D [rows, cols] matrix with rows `stride_bytes` apart, copied in boxes
-// of box_cols x box_rows; rows and columns past the end read as zero.
-bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
-               int64_t stride_bytes, int box_cols, int box_rows, CUtensorMapSwizzle swizzle) {
-    const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)stride_bytes};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 // a bf16 operand [rows, R]: boxes of one 64-wide K atom (128 bytes, 128-byte swizzle) x box_rows
 bool encode_operand(CUtensorMap* map, const void* base, int64_t R, int64_t rows, int64_t stride, int box_rows) {
     return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, R, rows, stride * 2, 64, box_rows,

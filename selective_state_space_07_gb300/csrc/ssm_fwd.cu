@@ -52,22 +52,35 @@ template <typename IO> struct FwdLayout {
     static constexpr int OFF_C = OFF_B + kCK * BCROW;
     static constexpr int STAGE = OFF_C + kCK * BCROW;
     static constexpr int NSTAGE = 4;              // tiles in flight
-    static constexpr int SMEM = NSTAGE * STAGE;   // dynamic shared memory
+    static constexpr int SMEM = NSTAGE * STAGE + 128;  // dynamic shared memory (+ slack for 128-byte alignment)
+    static_assert(OFF_Z % 128 == 0 && OFF_DT % 128 == 0 && OFF_B % 128 == 0 && OFF_C % 128 == 0 &&
+                      STAGE % 128 == 0, "TMA destinations on 128-byte boundaries");
     static constexpr int ROW = 2 * kCK + 4;       // per-channel row of DU / PB (floats, padded)
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// TMA descriptors of a tile's inputs: x, z, dt [B*L, D] in boxes of CH
+// channels x 16 tokens; B, C [B*L, 16] (rows bcs elements apart) in boxes of
+// 16 x 16. Elements past the last token or channel read as zero.
+struct FwdMaps {
+    CUtensorMap x, z, dt, b, c;
+};
 
 // MINB: resident CTAs per SM the register budget is cut for (3 when the grid
 // can use a third CTA per SM; 1 -- no cut -- when one L-group's grid fits in
 // two CTAs per SM, which leaves the scheduler registers for the interleaved
 // state chains).
 template <typename IO, bool AGG, int MINB>
-__global__ void __launch_bounds__(kFwdThreads, MINB) ssm_fwd_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kFwdThreads, MINB)
+    ssm_fwd_kernel(const FwdParams p, const __grid_constant__ FwdMaps mp) {
     using Ly = FwdLayout<IO>;
     constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
     constexpr bool FAST = IOT<IO>::kFast;
-    extern __shared__ __align__(16) char smem[];
+    extern __shared__ __align__(128) char smem_raw[];
+    char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
+    __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];       // a stage's copies landed
+    __shared__ int aborted;                                    // a copy did not arrive within the time bound
     __shared__ __align__(16) float BT[kN * T];                 // B^T of the tile [state][token]
     __shared__ __align__(16) float CT[AGG ? 4 : kN * T];
     __shared__ __align__(16) float DU[CH * Ly::ROW];           // per channel [Delta 0..15 | u 0..15]
@@ -101,47 +114,49 @@ __global__ void __launch_bounds__(kFwdThreads, MINB) ssm_fwd_kernel(const FwdPar
     const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
     const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
 
-    const int vchx = (int)(min64(CH, D - d0) * ES / 16);  // valid 16-byte chunks per x row
-    const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
-    auto issue = [&](int j, char* st) {
-        const int64_t t0 = tb0 + (int64_t)j * T;
-        const int rows = (int)min64(T, tb1 - t0);
-        const int64_t row0 = b * L + t0;
-        stage_block<NT>(st + Ly::OFF_X, Ly::XROW, (const char*)p.x + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
-                        rows, vchx);
-        if (has_z)
-            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, T,
-                            CH * ES / 16, rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
-                        rows, vchd);
-        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * p.bcs * ES, p.bcs * ES, T,
-                        Ly::BCROW / 16, rows, Ly::BCROW / 16);
-        if (!AGG)
-            stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * p.bcs * ES, p.bcs * ES, T,
-                            Ly::BCROW / 16, rows, Ly::BCROW / 16);
-        cp_async_commit();
+    // one thread loads a tile's inputs with TMA onto the stage's mbarrier;
+    // rows past the group's last token are loaded too (or read as zero past
+    // the tensor's end) and ignored: they act as identity tokens below
+    const unsigned stage_bytes =
+        (unsigned)(T * (Ly::XROW * (has_z ? 2 : 1) + Ly::DTROW + Ly::BCROW * (AGG ? 1 : 2)));
+    auto issue = [&](int j) {
+        if (tid != 0) return;
+        const int slot = j % Ly::NSTAGE;
+        char* st = smem + slot * Ly::STAGE;
+        const int y = (int)(b * L + tb0 + (int64_t)j * T);  // first token row of the tile in [B*L]
+        const unsigned bar = smem_u32(&fullb[slot]);
+        mbar_expect_tx(bar, stage_bytes);
+        tma_load_2d(st + Ly::OFF_X, &mp.x, (int)d0, y, bar);
+        if (has_z) tma_load_2d(st + Ly::OFF_Z, &mp.z, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_DT, &mp.dt, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_B, &mp.b, 0, y, bar);
+        if (!AGG) tma_load_2d(st + Ly::OFF_C, &mp.c, 0, y, bar);
     };
+    if (tid == 0) {
+        for (int q = 0; q < Ly::NSTAGE; ++q) mbar_init(smem_u32(&fullb[q]), 1);
+        mbar_fence_init();
+        aborted = 0;
+    }
+    __syncthreads();
 
     float* du = DU + c * Ly::ROW;
     float* pb = PB + c * Ly::ROW;
     float nf = 0.f;     // Inf/NaN detector
     float ssum = 0.f;   // AGG: this lane's part of the sum of Delta over the group
 
-    // prologue: tiles 0 .. NSTAGE-2 in flight (one commit group per tile,
-    // empty groups past the end keep the group count uniform)
+    // prologue: tiles 0 .. NSTAGE-2 in flight
 #pragma unroll
-    for (int q = 0; q < Ly::NSTAGE - 1; ++q) {
-        if (q < ntile) issue(q, smem + q * Ly::STAGE);
-        else cp_async_commit();
-    }
+    for (int q = 0; q < Ly::NSTAGE - 1; ++q)
+        if (q < ntile) issue(q);
     for (int j = 0; j < ntile; ++j) {
         char* st = smem + (j % Ly::NSTAGE) * Ly::STAGE;
-        {
-            const int jn = j + Ly::NSTAGE - 1;  // refill the slot tile j-1 used
-            if (jn < ntile) issue(jn, smem + (jn % Ly::NSTAGE) * Ly::STAGE);
-            else cp_async_commit();
+        if (j + Ly::NSTAGE - 1 < ntile) issue(j + Ly::NSTAGE - 1);  // refill the slot tile j-1 used
+        // every thread waits for the tile (bounded); after a timeout the block
+        // stops waiting but keeps the barrier sequence (its results are flagged invalid)
+        if (!aborted && !mbar_wait_bounded(smem_u32(&fullb[j % Ly::NSTAGE]), (unsigned)((j / Ly::NSTAGE) & 1))) {
+            aborted = 1;
+            if (p.status) atomicOr(p.status, kStatusTimeout);
         }
-        cp_async_wait<Ly::NSTAGE - 1>();
         __syncthreads();
         const int64_t t0 = tb0 + (int64_t)j * T;
         const int rows = (int)min64(T, tb1 - t0);
@@ -409,23 +424,42 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     flag_nonfinite(p.status, __fmaf_rn(yv, 0.0f, 0.0f));
 }
 
-template <typename IO, bool AGG, int MINB> int launch_fwd_v(const FwdParams& p, dim3 grid, cudaStream_t s) {
+template <typename IO, bool AGG, int MINB>
+int launch_fwd_v(const FwdParams& p, const FwdMaps& mp, dim3 grid, cudaStream_t s) {
     using Ly = FwdLayout<IO>;
     static unsigned long long mask = 0;
     auto kern = ssm_fwd_kernel<IO, AGG, MINB>;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
-    kern<<<grid, kFwdThreads, Ly::SMEM, s>>>(p);
+    kern<<<grid, kFwdThreads, Ly::SMEM, s>>>(p, mp);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
+}
+
+template <typename IO> bool encode_fwd_maps(const FwdParams& p, bool with_c, FwdMaps* mp) {
+    using Ly = FwdLayout<IO>;
+    const CUtensorMapDataType io = sizeof(IO) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const int64_t rows = p.B * p.L, ES = sizeof(IO);
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    if (!encode_2d(&mp->x, io, p.x, p.D, rows, p.D * ES, Ly::CH, kCK, none) ||
+        !encode_2d(&mp->dt, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.dt, p.D, rows, p.D * 4, Ly::CH, kCK, none) ||
+        !encode_2d(&mp->b, io, p.Bm, kN, rows, p.bcs * ES, kN, kCK, none))
+        return false;
+    mp->z = mp->x;
+    mp->c = mp->b;
+    if (p.has_z && !encode_2d(&mp->z, io, p.z, p.D, rows, p.D * ES, Ly::CH, kCK, none)) return false;
+    if (with_c && !encode_2d(&mp->c, io, p.Cm, kN, rows, p.bcs * ES, kN, kCK, none)) return false;
+    return true;
 }
 
 template <typename IO, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream_t s) {
     using Ly = FwdLayout<IO>;
     const int gy = AGG ? p.G - 1 : p.G;
     if (gy <= 0 || p.B == 0 || p.D == 0) return 0;
+    FwdMaps mp;
+    if (!encode_fwd_maps<IO>(p, !AGG, &mp)) return -1;
     dim3 grid((unsigned)((p.D + Ly::CH - 1) / Ly::CH), (unsigned)gy, (unsigned)p.B);
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
-    if (!AGG && p.G == 1 && ctas <= 2 * (int64_t)sm_count()) return launch_fwd_v<IO, AGG, 1>(p, grid, s);
-    return launch_fwd_v<IO, AGG, 3>(p, grid, s);
+    if (!AGG && p.G == 1 && ctas <= 2 * (int64_t)sm_count()) return launch_fwd_v<IO, AGG, 1>(p, mp, grid, s);
+    return launch_fwd_v<IO, AGG, 3>(p, mp, grid, s);
 }
 
 template <typename IO, int NSPLIT> int launch_step_t(const StepParams& p, cudaStream_t s) {

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libssmscan.so:
 // kernel parameter blocks and the launchers ssm_api.cu calls.
 #pragma once
+#include <cuda.h>  // CUtensorMap (built through the runtime's driver entry point; no libcuda link)
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -151,6 +152,11 @@ int launch_conv(int io, bool bwd, int64_t B, int64_t L, int64_t D, int K, const 
                 float* dw, float* dbias, float* dstate, unsigned* status, cudaStream_t s);
 int launch_bwd(int io, const BwdParams& p, cudaStream_t s);
 int dtproj_smem_bytes(int64_t R);
+// A TMA descriptor of a 2D [rows, cols] tensor whose rows are stride_bytes
+// apart, copied in boxes of box_cols x box_rows; elements past either end
+// read as zero. False when the driver lacks the encoder or rejects the shape.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType type, const void* base, int64_t cols, int64_t rows,
+               int64_t stride_bytes, int box_cols, int box_rows, CUtensorMapSwizzle swizzle);
 int launch_dtproj(bool bwd, int64_t M, int64_t D, int64_t R, int64_t a_stride, const void* a, const void* w,
                   const float* bias, float* out, const float* dout, float* dbias, int softplus, unsigned* status,
                   cudaStream_t s);

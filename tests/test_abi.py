@@ -87,6 +87,7 @@ def fwd_args(ssm, **over):
     (dict(h0=FAKE + 8), ALIGNMENT), (dict(workspace=None), WORKSPACE), (dict(workspace_bytes=16), WORKSPACE),
     # Bm / Cm row stride: at least N, a multiple of 16 bytes (bf16: 8 elements)
     (dict(bc_stride=8), INVALID), (dict(bc_stride=20), ALIGNMENT), (dict(bc_stride=-16), INVALID),
+    (dict(B=2, L=1 << 30), UNSUPPORTED),  # 2^31 token rows: past the 32-bit row coordinates of the copies
 ])
 def test_fwd_rejects_bad_arguments(ssm, over, code):
     args = fwd_args(ssm, **over)
