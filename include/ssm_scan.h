@@ -55,7 +55,7 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
 enum {
     SSM_OK = 0,
     SSM_ERR_INVALID_ARG = -1, /* null required pointer, negative size, bad flag */
-    SSM_ERR_UNSUPPORTED = -2, /* N != 16, unknown dtype, B*L >= 2^31 */
+    SSM_ERR_UNSUPPORTED = -2, /* N != 16, unknown dtype, B*L > 2^30 */
     SSM_ERR_ALIGNMENT = -3,   /* D % 8 != 0 or a pointer not 16-byte aligned */
     SSM_ERR_WORKSPACE = -4,   /* workspace missing or smaller than ssm_scan_workspace_bytes */
     SSM_ERR_CUDA = -5,        /* a CUDA runtime call or launch failed */

@@ -62,18 +62,32 @@ template <typename IO> struct BwdLayout {
     // the reduction gives each lane of a half-warp one 4-float column of a row
     static_assert(SPB * 2 * T == 16 * 4, "a transpose row must hold 16 column quads");
     static constexpr int OFF_TB = NSTAGE * STAGE;
-    static constexpr int SMEM = OFF_TB + NW * 32 * TBROW * 4;
+    static constexpr int SMEM = OFF_TB + NW * 32 * TBROW * 4 + 128;  // + slack for 128-byte alignment
+    static_assert(OFF_Z % 128 == 0 && OFF_DY % 128 == 0 && OFF_DT % 128 == 0 && OFF_B % 128 == 0 &&
+                      OFF_C % 128 == 0 && OFF_H % 128 == 0 && STAGE % 128 == 0, "TMA destinations on 128-byte boundaries");
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// TMA descriptors of a chunk's inputs: x, z, dy, dt [B*L, D] in boxes of CH
+// channels x T tokens; B, C [B*L, 16] (rows bcs elements apart) in boxes of
+// 16 x T; the checkpoints [B*ceil(L/8)*16, D] in boxes of CH x 16 states.
+// Elements past the last token or channel read as zero.
+struct BwdMaps {
+    CUtensorMap x, z, dy, dt, b, c, h;
+};
+
 template <typename IO>
-__global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 2)
+    ssm_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps mp) {
     using Ly = BwdLayout<IO>;
     constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = Ly::T, SPB = Ly::SPB;
     constexpr int NS = kN / 2;  // states per lane
     constexpr bool FAST = IOT<IO>::kFast;
-    extern __shared__ __align__(16) char smem[];
+    extern __shared__ __align__(128) char smem_raw[];
+    char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
+    __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];      // a chunk's copies landed
+    __shared__ int aborted;                                   // a copy did not arrive within the time bound
     __shared__ __align__(16) float AT[kN * CH];               // A^T of the CTA's channels
     __shared__ __align__(16) float BT[kN * T];                // B^T, C^T of the chunk (fp32)
     __shared__ __align__(16) float CT[kN * T];
@@ -118,40 +132,44 @@ __global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams
     const float bias = (vO && p.dt_bias) ? p.dt_bias[dO] : 0.f;
     float dDacc = 0.f, dbacc = 0.f, nf = 0.f;
 
-    const int vchx = (int)(min64(CH, D - d0) * ES / 16);
-    const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
-    auto issue = [&](int s, char* st) {
+    // one thread loads a chunk's inputs with TMA onto the buffer's mbarrier;
+    // rows past the group's last token are loaded too (or read as zero past
+    // the tensor's end) and ignored: they act as identity tokens below
+    const unsigned chunk_bytes =
+        (unsigned)(T * (Ly::XROW * (has_z ? 3 : 2) + Ly::DTROW + 2 * Ly::BCROW) + kN * Ly::HROW);
+    auto issue = [&](int s, int buf) {
+        if (tid != 0) return;
+        char* st = smem + buf * Ly::STAGE;
         const int64_t t0 = tb0 + (int64_t)s * T;
-        const int rows = (int)min64(T, tb1 - t0);
-        const int64_t row0 = b * L + t0;
-        stage_block<NT>(st + Ly::OFF_X, Ly::XROW, (const char*)p.x + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
-                        rows, vchx);
-        if (has_z)
-            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, T,
-                            CH * ES / 16, rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DY, Ly::XROW, (const char*)p.dy + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
-                        rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
-                        rows, vchd);
-        stage_block<NT>(st + Ly::OFF_B, Ly::BCROW, (const char*)p.Bm + row0 * p.bcs * ES, p.bcs * ES, T, Ly::BCROW / 16,
-                        rows, Ly::BCROW / 16);
-        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * p.bcs * ES, p.bcs * ES, T, Ly::BCROW / 16,
-                        rows, Ly::BCROW / 16);
-        // checkpoint tile: the 16 state rows [n][d0 .. d0+CH) of chunk t0/T
-        stage_block<NT>(st + Ly::OFF_H, Ly::HROW, (const char*)(p.ckpt + ((b * nck + t0 / T) * kN) * D + d0),
-                        D * 4, kN, CH * 4 / 16, kN, vchd);
-        cp_async_commit();
+        const int y = (int)(b * L + t0);                 // the chunk's first token row in [B*L]
+        const int yh = (int)((b * nck + t0 / T) * kN);  // its checkpoint's first state row
+        const unsigned bar = smem_u32(&fullb[buf]);
+        mbar_expect_tx(bar, chunk_bytes);
+        tma_load_2d(st + Ly::OFF_X, &mp.x, (int)d0, y, bar);
+        if (has_z) tma_load_2d(st + Ly::OFF_Z, &mp.z, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_DY, &mp.dy, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_DT, &mp.dt, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_B, &mp.b, 0, y, bar);
+        tma_load_2d(st + Ly::OFF_C, &mp.c, 0, y, bar);
+        tma_load_2d(st + Ly::OFF_H, &mp.h, (int)d0, yh, bar);
     };
+    if (tid == 0) {
+        for (int q = 0; q < Ly::NSTAGE; ++q) mbar_init(smem_u32(&fullb[q]), 1);
+        mbar_fence_init();
+        aborted = 0;
+    }
+    __syncthreads();
 
-    if (nsub > 0) issue(nsub - 1, smem);
+    if (nsub > 0) issue(nsub - 1, 0);
     for (int it = 0; it < nsub; ++it) {
         const int s_ = nsub - 1 - it;
         char* st = smem + (it & 1) * Ly::STAGE;
-        if (s_ > 0) {
-            issue(s_ - 1, smem + ((it + 1) & 1) * Ly::STAGE);
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
+        if (s_ > 0) issue(s_ - 1, (it + 1) & 1);  // into the buffer chunk it-1 used
+        // every thread waits for the chunk (bounded); after a timeout the block
+        // stops waiting but keeps the barrier sequence (its results are flagged invalid)
+        if (!aborted && !mbar_wait_bounded(smem_u32(&fullb[it & 1]), (unsigned)((it >> 1) & 1))) {
+            aborted = 1;
+            if (p.status) atomicOr(p.status, kStatusTimeout);
         }
         __syncthreads();
         const int64_t t0 = tb0 + (int64_t)s_ * T;
@@ -161,8 +179,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2) ssm_bwd_kernel(const BwdParams
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
             for (int i = tid; i < kN * T; i += NT) {
                 const int n = i / T, tok = i - n * T;
-                BT[i] = IOT<IO>::to_f(Braw[tok * kN + n]);
-                CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
+                const bool live = tok < rows;  // rows past the end belong to other tokens: zero, not read
+                BT[i] = live ? IOT<IO>::to_f(Braw[tok * kN + n]) : 0.f;
+                CT[i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
             }
         }
 
@@ -405,16 +424,27 @@ template <typename IO> struct BwdAggLayout {
     static constexpr int OFF_Z = 0, OFF_DY = kCK * XROW, OFF_DT = 2 * kCK * XROW, OFF_C = OFF_DT + kCK * DTROW;
     static constexpr int STAGE = OFF_C + kCK * BCROW;
     static constexpr int NSTAGE = 3;
-    static constexpr int SMEM = NSTAGE * STAGE;
+    static constexpr int SMEM = NSTAGE * STAGE + 128;  // + slack for 128-byte alignment
     static constexpr int ROW = 2 * kCK + 4;  // per-channel row [Delta 0..15 | dp 0..15], padded
+    static_assert(OFF_DY % 128 == 0 && OFF_DT % 128 == 0 && OFF_C % 128 == 0 && STAGE % 128 == 0,
+                  "TMA destinations on 128-byte boundaries");
+};
+
+// TMA descriptors of a tile's inputs: z, dy, dt [B*L, D] in boxes of CH
+// channels x 16 tokens, C [B*L, 16] in boxes of 16 x 16.
+struct AggMaps {
+    CUtensorMap z, dy, dt, c;
 };
 
 template <typename IO>
-__global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParams p, const __grid_constant__ AggMaps mp) {
     using Ly = BwdAggLayout<IO>;
     constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
     constexpr bool FAST = IOT<IO>::kFast;
-    extern __shared__ __align__(16) char smem[];
+    extern __shared__ __align__(128) char smem_raw[];
+    char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
+    __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];
+    __shared__ int aborted;
     __shared__ __align__(16) float CT[kN * T];
     __shared__ __align__(16) float DP[CH * Ly::ROW];
 
@@ -438,38 +468,37 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
         an[s] = 1.f;
     }
     const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
-    const int vchx = (int)(min64(CH, D - d0) * ES / 16);
-    const int vchd = (int)(min64(CH, D - d0) * 4 / 16);
-    auto issue = [&](int j, char* st) {  // tile j counted from the group's end
-        const int64_t t0 = tb0 + (int64_t)(ntile - 1 - j) * T;
-        const int rows = (int)min64(T, tb1 - t0);
-        const int64_t row0 = b * L + t0;
-        if (has_z)
-            stage_block<NT>(st + Ly::OFF_Z, Ly::XROW, (const char*)p.z + (row0 * D + d0) * ES, D * ES, T,
-                            CH * ES / 16, rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DY, Ly::XROW, (const char*)p.dy + (row0 * D + d0) * ES, D * ES, T, CH * ES / 16,
-                        rows, vchx);
-        stage_block<NT>(st + Ly::OFF_DT, Ly::DTROW, (const char*)p.dt + (row0 * D + d0) * 4, D * 4, T, CH * 4 / 16,
-                        rows, vchd);
-        stage_block<NT>(st + Ly::OFF_C, Ly::BCROW, (const char*)p.Cm + row0 * p.bcs * ES, p.bcs * ES, T, Ly::BCROW / 16,
-                        rows, Ly::BCROW / 16);
-        cp_async_commit();
+    const unsigned tile_bytes = (unsigned)(T * (Ly::XROW * (has_z ? 2 : 1) + Ly::DTROW + Ly::BCROW));
+    auto issue = [&](int j) {  // tile j counted from the group's end
+        if (tid != 0) return;
+        const int slot = j % Ly::NSTAGE;
+        char* st = smem + slot * Ly::STAGE;
+        const int y = (int)(b * L + tb0 + (int64_t)(ntile - 1 - j) * T);
+        const unsigned bar = smem_u32(&fullb[slot]);
+        mbar_expect_tx(bar, tile_bytes);
+        if (has_z) tma_load_2d(st + Ly::OFF_Z, &mp.z, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_DY, &mp.dy, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_DT, &mp.dt, (int)d0, y, bar);
+        tma_load_2d(st + Ly::OFF_C, &mp.c, 0, y, bar);
     };
+    if (tid == 0) {
+        for (int q = 0; q < Ly::NSTAGE; ++q) mbar_init(smem_u32(&fullb[q]), 1);
+        mbar_fence_init();
+        aborted = 0;
+    }
+    __syncthreads();
     float* dp = DP + c * Ly::ROW;
     float ssum = 0.f;
 #pragma unroll
-    for (int q = 0; q < Ly::NSTAGE - 1; ++q) {
-        if (q < ntile) issue(q, smem + q * Ly::STAGE);
-        else cp_async_commit();
-    }
+    for (int q = 0; q < Ly::NSTAGE - 1; ++q)
+        if (q < ntile) issue(q);
     for (int j = 0; j < ntile; ++j) {
         char* st = smem + (j % Ly::NSTAGE) * Ly::STAGE;
-        {
-            const int jn = j + Ly::NSTAGE - 1;
-            if (jn < ntile) issue(jn, smem + (jn % Ly::NSTAGE) * Ly::STAGE);
-            else cp_async_commit();
+        if (j + Ly::NSTAGE - 1 < ntile) issue(j + Ly::NSTAGE - 1);
+        if (!aborted && !mbar_wait_bounded(smem_u32(&fullb[j % Ly::NSTAGE]), (unsigned)((j / Ly::NSTAGE) & 1))) {
+            aborted = 1;
+            if (p.status) atomicOr(p.status, kStatusTimeout);
         }
-        cp_async_wait<Ly::NSTAGE - 1>();
         __syncthreads();
         const int64_t t0 = tb0 + (int64_t)(ntile - 1 - j) * T;
         const int rows = (int)min64(T, tb1 - t0);
@@ -477,7 +506,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
             for (int i = tid; i < kN * T; i += NT) {
                 const int n = i / T, tok = i - n * T;
-                CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
+                CT[i] = tok < rows ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;  // rows past the end: zero
             }
         }
         {
@@ -553,14 +582,31 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
     }
 }
 
+template <typename IO> constexpr CUtensorMapDataType io_map_type() {
+    return sizeof(IO) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+}
+
 template <typename IO> int launch_bwd_t(const BwdParams& p, cudaStream_t s) {
     using Ly = BwdLayout<IO>;
     auto kern = ssm_bwd_kernel<IO>;
     static unsigned long long mask = 0;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
     if (p.B == 0 || p.D == 0 || p.G == 0) return 0;
+    const CUtensorMapDataType io = io_map_type<IO>(), f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const int64_t rows = p.B * p.L, ES = sizeof(IO), hrows = p.B * ((p.L + Ly::T - 1) / Ly::T) * kN;
+    BwdMaps mp;
+    if (!encode_2d(&mp.x, io, p.x, p.D, rows, p.D * ES, Ly::CH, Ly::T, none) ||
+        !encode_2d(&mp.dy, io, p.dy, p.D, rows, p.D * ES, Ly::CH, Ly::T, none) ||
+        !encode_2d(&mp.dt, f32, p.dt, p.D, rows, p.D * 4, Ly::CH, Ly::T, none) ||
+        !encode_2d(&mp.b, io, p.Bm, kN, rows, p.bcs * ES, kN, Ly::T, none) ||
+        !encode_2d(&mp.c, io, p.Cm, kN, rows, p.bcs * ES, kN, Ly::T, none) ||
+        !encode_2d(&mp.h, f32, p.ckpt, p.D, hrows, p.D * 4, Ly::CH, kN, none))
+        return -1;
+    mp.z = mp.x;
+    if (p.has_z && !encode_2d(&mp.z, io, p.z, p.D, rows, p.D * ES, Ly::CH, Ly::T, none)) return -1;
     dim3 grid((unsigned)((p.D + Ly::CH - 1) / Ly::CH), (unsigned)p.G, (unsigned)p.B);
-    kern<<<grid, kBwdThreads, Ly::SMEM, s>>>(p);
+    kern<<<grid, kBwdThreads, Ly::SMEM, s>>>(p, mp);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -570,8 +616,18 @@ template <typename IO> int launch_bwd_agg_t(const BwdParams& p, cudaStream_t s) 
     static unsigned long long mask = 0;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
     if (p.B == 0 || p.D == 0 || p.G <= 1) return 0;
+    const CUtensorMapDataType io = io_map_type<IO>(), f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
+    const int64_t rows = p.B * p.L, ES = sizeof(IO);
+    AggMaps mp;
+    if (!encode_2d(&mp.dy, io, p.dy, p.D, rows, p.D * ES, Ly::CH, kCK, none) ||
+        !encode_2d(&mp.dt, f32, p.dt, p.D, rows, p.D * 4, Ly::CH, kCK, none) ||
+        !encode_2d(&mp.c, io, p.Cm, kN, rows, p.bcs * ES, kN, kCK, none))
+        return -1;
+    mp.z = mp.dy;
+    if (p.has_z && !encode_2d(&mp.z, io, p.z, p.D, rows, p.D * ES, Ly::CH, kCK, none)) return -1;
     dim3 grid((unsigned)((p.D + Ly::CH - 1) / Ly::CH), (unsigned)(p.G - 1), (unsigned)p.B);
-    kern<<<grid, kBwdThreads, Ly::SMEM, s>>>(p);
+    kern<<<grid, kBwdThreads, Ly::SMEM, s>>>(p, mp);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 

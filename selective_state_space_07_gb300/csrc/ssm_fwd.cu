@@ -167,8 +167,9 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
             for (int i = tid; i < kN * T; i += NT) {
                 const int n = i / T, tok = i - n * T;
-                BT[i] = IOT<IO>::to_f(Braw[tok * kN + n]);
-                if (!AGG) CT[i] = IOT<IO>::to_f(Craw[tok * kN + n]);
+                const bool live = tok < rows;  // rows past the end belong to other tokens: zero, not read
+                BT[i] = live ? IOT<IO>::to_f(Braw[tok * kN + n]) : 0.f;
+                if (!AGG) CT[i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
             }
         }
         // ---- A: Delta, u and the gate factor of this lane's 8 tokens;

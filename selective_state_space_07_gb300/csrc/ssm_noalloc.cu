@@ -91,8 +91,9 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
         return SSM_ERR_INVALID_ARG;
     const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
     if (bc != SSM_OK) return bc;
-    // the tiles are addressed by 32-bit token rows of the flattened [B*L] tensors
-    if (a->B * a->L > 0x7fffffff) return SSM_ERR_UNSUPPORTED;
+    // the tiles are addressed by 32-bit rows of the flattened [B*L] tensors and of the
+    // checkpoints (2 rows per token: 16 states every 8 tokens)
+    if (a->B * a->L > (int64_t(1) << 30)) return SSM_ERR_UNSUPPORTED;
     const int64_t B = a->B, L = a->L, D = a->D;
     const bool work = B > 0 && L > 0 && D > 0;
     if (work && (!a->x || !a->dt || !a->Bm || !a->Cm || !a->A || !a->y)) return SSM_ERR_INVALID_ARG;

@@ -88,6 +88,7 @@ def fwd_args(ssm, **over):
     # Bm / Cm row stride: at least N, a multiple of 16 bytes (bf16: 8 elements)
     (dict(bc_stride=8), INVALID), (dict(bc_stride=20), ALIGNMENT), (dict(bc_stride=-16), INVALID),
     (dict(B=2, L=1 << 30), UNSUPPORTED),  # 2^31 token rows: past the 32-bit row coordinates of the copies
+    (dict(B=1, L=(1 << 30) + 1), UNSUPPORTED),
 ])
 def test_fwd_rejects_bad_arguments(ssm, over, code):
     args = fwd_args(ssm, **over)
