@@ -21,7 +21,8 @@
 //      own channel and swaps Delta, u, dp with its partner (shuffle);
 //   S  per state, the two channels side by side: forward from the
 //      checkpoint over the 8 tokens (a_t, h_t in registers) and the reverse
-//      recurrence over them;
+//      recurrence over them, the forward of state n+1 interleaved with the
+//      reverse of state n (four independent chains in flight);
 //      per-token state sums stay in registers; dB/dC contributions go
 //      through a per-warp shared-memory transpose every 4 states, then a
 //      per-CTA sum over warps and one vector atomic per 4 outputs;
@@ -81,7 +82,7 @@ template <typename IO>
 __global__ void __launch_bounds__(kBwdThreads, 2)
     ssm_bwd_kernel(const BwdParams p, const __grid_constant__ BwdMaps mp) {
     using Ly = BwdLayout<IO>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = Ly::T, SPB = Ly::SPB;
+    constexpr int NT = Ly::NT, CH = Ly::CH, T = Ly::T, SPB = Ly::SPB;
     constexpr int NS = kN / 2;  // states per lane
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(128) char smem_raw[];
@@ -229,43 +230,53 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
             for (int m = 0; m < T / 2; ++m) S1[sl][m] = S2[sl][m] = S3[sl][m] = f2(0.f, 0.f);
         const float* hck = reinterpret_cast<const float*>(st + Ly::OFF_H);
 
-#pragma unroll
-        for (int s = 0; s < NS; ++s) {
-            const int n = NS * hk + s;
+        // the forward recomputation of state s+1 runs interleaved with the
+        // reverse recurrence of state s (independent chains for the scheduler)
+        float2 aS[2][2][T / 2], hS[2][2][T / 2], bS[2][T / 2];  // [state parity][channel slot][token pair]
+        float A2s[2][2], hps[2][2];
+        auto load_state = [&](int n, int k) {
             const float4 b4a = *reinterpret_cast<const float4*>(BT + n * T);
             const float4 b4b = *reinterpret_cast<const float4*>(BT + n * T + 4);
-            const float4 c4a = *reinterpret_cast<const float4*>(CT + n * T);
-            const float4 c4b = *reinterpret_cast<const float4*>(CT + n * T + 4);
-            const float2 bb[4] = {f2(b4a.x, b4a.y), f2(b4a.z, b4a.w), f2(b4b.x, b4b.y), f2(b4b.z, b4b.w)};
-            const float2 cc[4] = {f2(c4a.x, c4a.y), f2(c4a.z, c4a.w), f2(c4b.x, c4b.y), f2(c4b.z, c4b.w)};
-            float2 vb[T / 2], vc[T / 2];
-            // both channels advance together (independent chains for the scheduler)
-            float An[2], hp[2];
-            float2 A2p[2], Ap[2];
+            bS[k][0] = f2(b4a.x, b4a.y); bS[k][1] = f2(b4a.z, b4a.w);
+            bS[k][2] = f2(b4b.x, b4b.y); bS[k][3] = f2(b4b.z, b4b.w);
 #pragma unroll
             for (int sl = 0; sl < 2; ++sl) {
                 const int c = sl ? cP : cO;
-                An[sl] = AT[n * CH + c];
-                const float A2 = __fmul_rn(An[sl], kLog2e);
-                A2p[sl] = f2(A2, A2);
-                Ap[sl] = f2(An[sl], An[sl]);
-                hp[sl] = hck[n * CH + c];
+                A2s[k][sl] = __fmul_rn(AT[n * CH + c], kLog2e);
+                hps[k][sl] = hck[n * CH + c];
             }
-            // forward from the checkpoint over the chunk
-            float2 a[2][T / 2], hh[2][T / 2];
+        };
+        auto fwd_pair = [&](int k, int m) {
 #pragma unroll
-            for (int m = 0; m < T / 2; ++m) {
-#pragma unroll
-                for (int sl = 0; sl < 2; ++sl) {
-                    const float2 arg = __fmul2_rn(Dl[sl][m], A2p[sl]);
-                    a[sl][m] = f2(ex2(arg.x), ex2(arg.y));
-                    const float2 ub = __fmul2_rn(Ul[sl][m], bb[m]);
-                    const float h0v = __fmaf_rn(a[sl][m].x, hp[sl], ub.x);
-                    const float h1v = __fmaf_rn(a[sl][m].y, h0v, ub.y);
-                    hp[sl] = h1v;
-                    hh[sl][m] = f2(h0v, h1v);
-                }
+            for (int sl = 0; sl < 2; ++sl) {
+                const float2 arg = __fmul2_rn(Dl[sl][m], f2(A2s[k][sl], A2s[k][sl]));
+                aS[k][sl][m] = f2(ex2(arg.x), ex2(arg.y));
+                const float2 ub = __fmul2_rn(Ul[sl][m], bS[k][m]);
+                const float h0v = __fmaf_rn(aS[k][sl][m].x, hps[k][sl], ub.x);
+                const float h1v = __fmaf_rn(aS[k][sl][m].y, h0v, ub.y);
+                hps[k][sl] = h1v;
+                hS[k][sl][m] = f2(h0v, h1v);
             }
+        };
+        load_state(NS * hk, 0);
+#pragma unroll
+        for (int m = 0; m < T / 2; ++m) fwd_pair(0, m);
+
+#pragma unroll
+        for (int s = 0; s < NS; ++s) {
+            const int n = NS * hk + s, k = s & 1;
+            const bool more = s + 1 < NS;
+            const float4 c4a = *reinterpret_cast<const float4*>(CT + n * T);
+            const float4 c4b = *reinterpret_cast<const float4*>(CT + n * T + 4);
+            const float2 cc[4] = {f2(c4a.x, c4a.y), f2(c4a.z, c4a.w), f2(c4b.x, c4b.y), f2(c4b.z, c4b.w)};
+            float2 Ap[2];
+#pragma unroll
+            for (int sl = 0; sl < 2; ++sl) {
+                const float An = AT[n * CH + (sl ? cP : cO)];
+                Ap[sl] = f2(An, An);
+            }
+            if (more) load_state(n + 1, k ^ 1);
+            float2 vb[T / 2], vc[T / 2];
             // reverse: E_t = a_{t+1} E_{t+1} + dp_t C_t, carry Gc = a_{t+1} E_{t+1}
             float E[2] = {Gc[0][s], Gc[1][s]}, anext[2] = {1.f, 1.f};
             float2 dAp[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
@@ -275,25 +286,26 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
                 for (int sl = 0; sl < 2; ++sl) {
                     const float2 rr = __fmul2_rn(Pl[sl][m], cc[m]);
                     const float e1 = __fmaf_rn(anext[sl], E[sl], rr.y);
-                    const float e0 = __fmaf_rn(a[sl][m].y, e1, rr.x);
+                    const float e0 = __fmaf_rn(aS[k][sl][m].y, e1, rr.x);
                     E[sl] = e0;
-                    anext[sl] = a[sl][m].x;
+                    anext[sl] = aS[k][sl][m].x;
                     const float2 E2 = f2(e0, e1);
                     if (sl == 0) {
                         vb[m] = __fmul2_rn(E2, Ul[0][m]);
-                        vc[m] = __fmul2_rn(Pl[0][m], hh[0][m]);
+                        vc[m] = __fmul2_rn(Pl[0][m], hS[k][0][m]);
                     } else {
                         vb[m] = __ffma2_rn(E2, Ul[1][m], vb[m]);
-                        vc[m] = __ffma2_rn(Pl[1][m], hh[1][m], vc[m]);
+                        vc[m] = __ffma2_rn(Pl[1][m], hS[k][1][m], vc[m]);
                     }
-                    S1[sl][m] = __ffma2_rn(E2, bb[m], S1[sl][m]);
+                    S1[sl][m] = __ffma2_rn(E2, bS[k][m], S1[sl][m]);
                     // a_t h_{t-1} = h_t - u_t B_t
-                    const float2 q = __ffma2_rn(f2(-Ul[sl][m].x, -Ul[sl][m].y), bb[m], hh[sl][m]);
+                    const float2 q = __ffma2_rn(f2(-Ul[sl][m].x, -Ul[sl][m].y), bS[k][m], hS[k][sl][m]);
                     const float2 w = __fmul2_rn(E2, q);
                     dAp[sl] = __ffma2_rn(Dl[sl][m], w, dAp[sl]);
                     S2[sl][m] = __ffma2_rn(Ap[sl], w, S2[sl][m]);
-                    S3[sl][m] = __ffma2_rn(cc[m], hh[sl][m], S3[sl][m]);
+                    S3[sl][m] = __ffma2_rn(cc[m], hS[k][sl][m], S3[sl][m]);
                 }
+                if (more) fwd_pair(k ^ 1, T / 2 - 1 - m);
             }
 #pragma unroll
             for (int sl = 0; sl < 2; ++sl) {
@@ -439,7 +451,7 @@ struct AggMaps {
 template <typename IO>
 __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParams p, const __grid_constant__ AggMaps mp) {
     using Ly = BwdAggLayout<IO>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
+    constexpr int NT = Ly::NT, CH = Ly::CH, T = kCK, NS = kN / 2;
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(128) char smem_raw[];
     char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
