@@ -49,6 +49,15 @@ def test_partial_channel_tiles(ssm, D):
         compare(ssm, inp, "bf16", dict(nsplit=ns), dict(nsplit=ns))
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_single_group_forward_over_a_wide_channel_grid(ssm, io):
+    # 2 x 7656 channels: 240 forward CTAs of 64 channels in one L-group
+    # (between one and two per SM on a 152-SM GB300), the last CTA of each
+    # batch row ragged (40 of its 64 channels live)
+    inp = gen.make_inputs(2, 40, 7656, 16, io=io, seed=77, with_h0=True, with_dh_last=True)
+    compare(ssm, inp, io, dict(groups=0), dict(groups=0))
+
+
 @pytest.mark.parametrize("gate,skip,bias", [(False, True, True), (True, False, True), (True, True, False),
                                             (False, False, False)])
 def test_optional_inputs_absent(ssm, gate, skip, bias):

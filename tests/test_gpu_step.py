@@ -46,6 +46,20 @@ def test_step_from_zero_is_bitwise_the_forward(ssm, fwd_split, step_split, io):
     assert torch.equal(state, h_last)
 
 
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_step_from_zero_is_bitwise_a_wide_single_group_forward(ssm, io):
+    # one L-group over 2 x 7656 channels (240 forward CTAs, the last of each
+    # batch row ragged): the step form reproduces it bit for bit
+    inp = gen.make_inputs(2, 24, 7656, 16, io=io, seed=78)
+    dv = to_dev(inp)
+    y, h_last, _, _ = run_fwd(ssm, dv, inp, groups=1)
+    state = torch.zeros(inp.B, inp.D, 16, device="cuda")
+    ys = step_through(ssm, dv, state, 0, inp.L, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(ys, y), float((ys.float() - y.float()).abs().max())
+    assert torch.equal(state, h_last)
+
+
 def test_step_from_every_checkpoint_is_bitwise_the_forward(ssm):
     # A forward split into 3 L-groups of 32 tokens: stepping from any saved
     # checkpoint (one every 8 tokens, stored state-major [B, L/8, N, D])
