@@ -140,12 +140,40 @@ CALL_SOURCES = {
 }
 
 
+def strip_c_comments(src: str) -> str:
+    """C/C++ source with comments removed and whitespace runs collapsed to
+    one space (string and character literals kept as written)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash(call):
+    """Hash of the code (comments and layout ignored) of the sources a call's
+    kernels are built from: stored counters stay valid across documentation
+    edits and lapse with any change to the code."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "selective_state_space_07_gb300", "csrc")
     for fn in CALL_SOURCES[call]:
-        with open(os.path.join(d, fn), "rb") as f:
-            h.update(fn.encode() + f.read())
+        with open(os.path.join(d, fn), encoding="utf-8") as f:
+            h.update((fn + "\n" + strip_c_comments(f.read())).encode())
     return h.hexdigest()[:16]
 
 

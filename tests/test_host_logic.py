@@ -41,3 +41,17 @@ def test_backward_groups(choices):
     assert bwd[:3] == [7, 3, 19]
     assert bwd[3] == 1                               # the cap wins
     assert bwd[4] == 1                               # a grid of many waves needs no groups
+
+
+def test_kernel_source_hash_ignores_comments_and_layout_only():
+    # the stored ncu counters are keyed by this hash: documentation edits
+    # keep them, any change to the code (literals included) drops them
+    import bench
+    strip = bench.strip_c_comments
+    code = 'int f(int a) { return a + 1; }\nconst char* s = "x // y";'
+    assert strip(code) == strip("// lead\n" + code.replace("{ ", "{\n    /* note */ ") + "  // tail\n")
+    assert strip(code) != strip(code.replace("a + 1", "a + 2"))
+    assert "// y" in strip(code)  # inside a string literal: kept
+    assert strip("char c = '\\''; // q") == "char c = '\\'';"
+    for call in bench.CALL_SOURCES:
+        assert len(bench.kernel_source_hash(call)) == 16
