@@ -7,8 +7,9 @@
 // recurrence in t. Lanes l and l^16 of a warp share one channel: lane l
 // holds states 8*(l>>4) .. 8*(l>>4)+7 in registers and walks the tokens in
 // order. Tiles of 16 tokens x 64 channels of x, z, dt and the 16-wide B_t /
-// C_t rows are staged into shared memory with cp.async (four tiles in
-// flight); B/C are widened to fp32 and transposed (state-major) once per
+// C_t rows are staged into shared memory by TMA (one thread issues a tile's
+// boxes onto the stage's mbarrier; four tiles in flight); B/C are widened to
+// fp32 and transposed (state-major) once per
 // tile, so a half-warp reads one state's row of 4 tokens with one broadcast
 // 16-byte load. Delta*A, u*B and the readout are packed over token pairs
 // (f32x2); each state's update is a scalar fused multiply-add chain.

@@ -74,8 +74,9 @@ template <typename K> inline bool ensure_smem(K kern, int bytes, unsigned long l
 }
 
 // The row stride of Bm / Cm in elements: 0 means dense (N); otherwise at
-// least N and a whole number of 16-byte units (cp.async stages the rows in
-// 16-byte pieces). Returns an SSM_ status code.
+// least N and a whole number of 16-byte units (the TMA tensor maps that stage
+// the rows need a row pitch that is a multiple of 16 bytes). Returns an SSM_
+// status code.
 inline int check_bc_stride(int64_t s, int64_t N, int io_dtype) {
     if (s == 0) return SSM_OK;
     if (s < N || s > (int64_t(1) << 24)) return SSM_ERR_INVALID_ARG;
