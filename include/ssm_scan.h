@@ -25,8 +25,8 @@
  *     A, dA                               [D, N]
  *     Dskip, dt_bias, dD, d_dt_bias       [D]
  *     h0, h_last, dh_last, dh0, state     [B, D, N]
- *     ckpt                                [B, ceil(L/8), N, D]  (state before tokens 0, 8, 16, ...;
- *                                          state-major: one row of D channels per state)
+ *     ckpt                                [B, ceil(L/8), N/2, D, 2]  (state before tokens 0, 8, 16,
+ *                                          ...; state n of channel d at [.., n/2, d, n%2])
  * - Types: x, z, Bm, Cm, y, dy, dx, dz (and the step's x_t, z_t, Bm_t, Cm_t,
  *   y_t) use the I/O dtype (SSM_F32 or SSM_BF16). Everything else is fp32.
  *   All arithmetic and the recurrent state are fp32.
@@ -75,8 +75,8 @@ enum {
  * nsplit / groups: launch shape; 0 = automatic. groups = number of
  *   L-segments scanned in parallel, joined by chunk carries (0: chosen from
  *   the device's occupancy). The forward kernel has one lane layout (two
- *   lanes per channel, 8 states each): nsplit must be 0, 1, 2 or 4 and is
- *   otherwise ignored here. Results are the same up to rounding for every
+ *   lanes share a pair of channels, 8 states each): nsplit must be 0, 1, 2
+ *   or 4 and is otherwise ignored here. Results are the same up to rounding for every
  *   choice; with groups == 1 the forward is bitwise equal to stepping
  *   ssm_step through the sequence. */
 typedef struct {
@@ -295,15 +295,28 @@ int64_t ssm_scan_ckpt_elems(int64_t B, int64_t L, int64_t D, int64_t N);
 /* Tokens between checkpoints (8). */
 int ssm_scan_ckpt_interval(void);
 /* Synchronises `stream`, reads and clears the workspace status word.
- * Returns SSM_OK, SSM_ERR_NONFINITE, or SSM_ERR_CUDA. */
+ * Returns SSM_OK, SSM_ERR_TIMEOUT, SSM_ERR_NONFINITE, or SSM_ERR_CUDA. */
 int ssm_poll_status(void* workspace, void* stream);
 /* Zeroes the workspace status word on `stream` (asynchronous). */
 int ssm_clear_status(void* workspace, void* stream);
 /* Static English description of a status code. */
 const char* ssm_status_string(int code);
 /* Launches of the library's own kernels made by the most recent
- * fwd / bwd / step / dA_log call on this host thread. */
+ * fwd / bwd / step / dA_log / conv / dtproj / noalloc call on this host
+ * thread. */
 int ssm_last_launch_count(void);
+
+/* Testing hook for the bounded waits (no counterpart on the pages). Arms,
+ * for the next ssm_scan_fwd call on this host thread only, a staging fault
+ * in its main forward kernel: every warp arms the barrier of its tile `tile`
+ * (counted from the start of its L-group) without issuing that tile's
+ * copies, and every wait of that kernel gives up after wait_ns nanoseconds
+ * (0: the default of one second). The call returns SSM_OK; the warps stop at
+ * that tile, wait (bounded) for the copies they still have in flight and
+ * leave, y / h_last / ckpt are not valid, and ssm_poll_status then returns
+ * SSM_ERR_TIMEOUT. tile < 0 disarms. Returns SSM_ERR_INVALID_ARG for
+ * wait_ns above 10 s. */
+int ssm_debug_arm_wait_fault(int64_t tile, uint64_t wait_ns);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,8 @@ import torch
 
 __all__ = [
     "SsmError", "build", "lib", "scan_fwd", "scan_bwd", "step", "dA_log_grad", "poll_status",
-    "clear_status", "workspace_bytes", "ckpt_elems", "CKPT_INTERVAL", "Workspace", "scan_fwd_bwd_host",
+    "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
+    "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
 ]
 
@@ -107,6 +108,7 @@ EXPORTS = {
     "ssm_dtproj_bwd": ([ctypes.POINTER(DtProjBwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_dA_log_grad": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
                         ctypes.c_int),
+    "ssm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
 }
 
 
@@ -168,6 +170,20 @@ def workspace_bytes(B: int, L: int, D: int, N: int = 16) -> int:
 
 def ckpt_elems(B: int, L: int, D: int, N: int = 16) -> int:
     return int(lib().ssm_scan_ckpt_elems(B, L, D, N))
+
+
+def ckpt_states(ckpt: torch.Tensor, B: int, L: int, D: int, N: int = 16) -> torch.Tensor:
+    """The checkpoint buffer as states [B, ceil(L/8), D, N] (a copy): entry [b, k] is the state [D, N]
+    before token 8k of batch row b. The buffer itself is laid out [B, ceil(L/8), N/2, D, 2]."""
+    nck = (L + CKPT_INTERVAL - 1) // CKPT_INTERVAL
+    v = ckpt[: B * nck * N * D].view(B, nck, N // 2, D, 2)
+    return v.permute(0, 1, 3, 2, 4).reshape(B, nck, D, N)
+
+
+def arm_wait_fault(tile: int, wait_ns: int) -> None:
+    """Testing hook: the next scan_fwd on this thread stages tile ``tile`` of every warp without issuing its
+    copies and bounds its waits by ``wait_ns``; poll_status then reports the timeout."""
+    _check(lib().ssm_debug_arm_wait_fault(int(tile), int(wait_ns)), "ssm_debug_arm_wait_fault")
 
 
 def last_launch_count() -> int:

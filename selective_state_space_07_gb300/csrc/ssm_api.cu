@@ -52,6 +52,9 @@ constexpr int64_t kGroupBudget = 131072;  // cap on B*D*groups held in the carry
 constexpr size_t kStatusBytes = 256;
 
 thread_local int g_launches = 0;
+// One-shot staging fault for the next ssm_scan_fwd of this thread (tests).
+thread_local int64_t g_fault_tile1 = 0;
+thread_local unsigned long long g_fault_wait_ns = 0;
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -133,6 +136,11 @@ int tally(int r) {
 
 }  // namespace
 
+namespace ssm {
+void reset_launches() { g_launches = 0; }
+int count_launches(int r) { return tally(r); }
+}  // namespace ssm
+
 extern "C" {
 
 size_t ssm_scan_workspace_bytes(int64_t B, int64_t L, int64_t D, int64_t N) {
@@ -149,6 +157,13 @@ int64_t ssm_scan_ckpt_elems(int64_t B, int64_t L, int64_t D, int64_t N) {
 int ssm_scan_ckpt_interval(void) { return (int)kCkpt; }
 
 int ssm_last_launch_count(void) { return g_launches; }
+
+int ssm_debug_arm_wait_fault(int64_t tile, uint64_t wait_ns) {
+    if (wait_ns > 10000000000ull) return SSM_ERR_INVALID_ARG;
+    g_fault_tile1 = tile < 0 ? 0 : tile + 1;
+    g_fault_wait_ns = tile < 0 ? 0 : wait_ns;
+    return SSM_OK;
+}
 
 const char* ssm_status_string(int code) {
     switch (code) {
@@ -186,6 +201,11 @@ int ssm_poll_status(void* workspace, void* stream) {
 
 int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
     g_launches = 0;
+    // a fault armed by ssm_debug_arm_wait_fault applies to this call only
+    const int64_t fault_tile1 = g_fault_tile1;
+    const unsigned long long fault_wait_ns = g_fault_wait_ns;
+    g_fault_tile1 = 0;
+    g_fault_wait_ns = 0;
     int rc = check_fwd(a, true);
     if (rc != SSM_OK) return rc;
     cudaStream_t s = (cudaStream_t)stream;
@@ -223,6 +243,8 @@ int ssm_scan_fwd(const ssm_fwd_args* a, void* stream) {
             return rc;
         p.hstart = (const float*)(ws + w.carry);
     }
+    p.fault_tile1 = fault_tile1;
+    p.wait_ns = fault_wait_ns;
     return tally(ssm::launch_fwd(a->io_dtype, p, s));
 }
 

@@ -70,9 +70,14 @@ template <typename IO> struct BwdLayout {
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
+// Column c of two consecutive staged rows (`row` bytes apart) as fp32.
+template <typename IO> __device__ __forceinline__ float2 ld_pair(const char* p, int row, int c) {
+    return f2(IOT<IO>::to_f(reinterpret_cast<const IO*>(p)[c]), IOT<IO>::to_f(reinterpret_cast<const IO*>(p + row)[c]));
+}
+
 // TMA descriptors of a chunk's inputs: x, z, dy, dt [B*L, D] in boxes of CH
 // channels x T tokens; B, C [B*L, 16] (rows bcs elements apart) in boxes of
-// 16 x T; the checkpoints [B*ceil(L/8)*16, D] in boxes of CH x 16 states.
+// 16 x T; the checkpoints [B*ceil(L/8)*8, 2D] (state pairs) in boxes of 2CH x 8.
 // Elements past the last token or channel read as zero.
 struct BwdMaps {
     CUtensorMap x, z, dy, dt, b, c, h;
@@ -131,7 +136,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
     }
     const float Dd = (vO && p.Dskip) ? p.Dskip[dO] : 0.f;
     const float bias = (vO && p.dt_bias) ? p.dt_bias[dO] : 0.f;
-    float dDacc = 0.f, dbacc = 0.f, nf = 0.f;
+    const float2 D2 = f2(Dd, Dd), bias2 = f2(bias, bias);
+    float2 dD2 = f2(0.f, 0.f), db2 = f2(0.f, 0.f), nf2 = f2(0.f, 0.f);  // even / odd tokens
 
     // one thread loads a chunk's inputs with TMA onto the buffer's mbarrier;
     // rows past the group's last token are loaded too (or read as zero past
@@ -143,7 +149,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         char* st = smem + buf * Ly::STAGE;
         const int64_t t0 = tb0 + (int64_t)s * T;
         const int y = (int)(b * L + t0);                 // the chunk's first token row in [B*L]
-        const int yh = (int)((b * nck + t0 / T) * kN);  // its checkpoint's first state row
+        const int yh = (int)((b * nck + t0 / T) * (kN / 2));  // its checkpoint's first state-pair row
         const unsigned bar = smem_u32(&fullb[buf]);
         mbar_expect_tx(bar, chunk_bytes);
         tma_load_2d(st + Ly::OFF_X, &mp.x, (int)d0, y, bar);
@@ -152,7 +158,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         tma_load_2d(st + Ly::OFF_DT, &mp.dt, (int)d0, y, bar);
         tma_load_2d(st + Ly::OFF_B, &mp.b, 0, y, bar);
         tma_load_2d(st + Ly::OFF_C, &mp.c, 0, y, bar);
-        tma_load_2d(st + Ly::OFF_H, &mp.h, (int)d0, yh, bar);
+        tma_load_2d(st + Ly::OFF_H, &mp.h, (int)(2 * d0), yh, bar);
     };
     if (tid == 0) {
         for (int q = 0; q < Ly::NSTAGE; ++q) mbar_init(smem_u32(&fullb[q]), 1);
@@ -186,33 +192,43 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
             }
         }
 
-        // ---- A: per-token quantities of the own channel; tokens past the
-        // end act as identity (a = 1, no input, no adjoint input)
+        // ---- A: per-token quantities of the own channel, a token pair at a
+        // time (packed f32x2); tokens past the end act as identity (a = 1, no
+        // input, no adjoint input, nothing accumulated)
+        const bool full = rows == T;
         float2 Dl[2][T / 2], Ul[2][T / 2], Pl[2][T / 2];
-        float sg[T], dd[T];
+        float2 sgp[T / 2], ddp[T / 2];
 #pragma unroll
-        for (int t = 0; t < T; ++t) {
-            const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[cO]);
-            const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + t * Ly::XROW)[cO]);
-            const float v = __fadd_rn(reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[cO], bias);
-            float sgv = 1.f, delta = v;
-            if (sp) delta = softplus_sig<FAST>(v, &sgv);
-            float dpv = dyv, dyds = 0.f;
+        for (int m = 0; m < T / 2; ++m) {
+            const int t = 2 * m;
+            const float2 xv = ld_pair<IO>(st + Ly::OFF_X + t * Ly::XROW, Ly::XROW, cO);
+            const float2 dyv = ld_pair<IO>(st + Ly::OFF_DY + t * Ly::XROW, Ly::XROW, cO);
+            const float2 dtv = ld_pair<float>(st + Ly::OFF_DT + t * Ly::DTROW, Ly::DTROW, cO);
+            float2 sgv;
+            float2 dl = delta_sig2<FAST>(dtv, bias2, sp, &sgv);
+            float2 pl = dyv, dyds = f2(0.f, 0.f);
             if (has_z) {
-                const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[cO]);
-                const float sz = sigmoid<FAST>(zv);
-                dpv = __fmul_rn(dyv, __fmul_rn(zv, sz));
-                dyds = dyv * (sz * (1.0f + zv * (1.0f - sz)));
+                const float2 zv = ld_pair<IO>(st + Ly::OFF_Z + t * Ly::XROW, Ly::XROW, cO);
+                const float2 sz = sigmoid2<FAST>(zv);
+                pl = __fmul2_rn(dyv, __fmul2_rn(zv, sz));
+                // dy * silu'(z) = dy * s (1 + z (1 - s))
+                const float2 one = f2(1.f, 1.f);
+                dyds = __fmul2_rn(dyv, __fmul2_rn(sz, __ffma2_rn(zv, __fadd2_rn(one, f2(-sz.x, -sz.y)), one)));
             }
-            const bool live = t < rows;
-            const float dl = live ? delta : 0.f, ul = live ? __fmul_rn(delta, xv) : 0.f, pl = live ? dpv : 0.f;
-            if (t & 1) {
-                Dl[0][t / 2].y = dl; Ul[0][t / 2].y = ul; Pl[0][t / 2].y = pl;
-            } else {
-                Dl[0][t / 2].x = dl; Ul[0][t / 2].x = ul; Pl[0][t / 2].x = pl;
+            float2 ul = __fmul2_rn(dl, xv);
+            if (!full) {
+                const bool l0 = t < rows, l1 = t + 1 < rows;
+                dl = f2(l0 ? dl.x : 0.f, l1 ? dl.y : 0.f);
+                ul = f2(l0 ? ul.x : 0.f, l1 ? ul.y : 0.f);
+                pl = f2(l0 ? pl.x : 0.f, l1 ? pl.y : 0.f);
+                sgv = f2(l0 ? sgv.x : 0.f, l1 ? sgv.y : 0.f);
+                dyds = f2(l0 ? dyds.x : 0.f, l1 ? dyds.y : 0.f);
             }
-            sg[t] = sgv;
-            dd[t] = dyds;
+            Dl[0][m] = dl;
+            Ul[0][m] = ul;
+            Pl[0][m] = pl;
+            sgp[m] = sgv;
+            ddp[m] = dyds;
         }
 #pragma unroll
         for (int m = 0; m < T / 2; ++m) {
@@ -243,7 +259,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
             for (int sl = 0; sl < 2; ++sl) {
                 const int c = sl ? cP : cO;
                 A2s[k][sl] = __fmul_rn(AT[n * CH + c], kLog2e);
-                hps[k][sl] = hck[n * CH + c];
+                hps[k][sl] = hck[((n >> 1) * CH + c) * 2 + (n & 1)];  // [state pair][channel][2]
             }
         };
         auto fwd_pair = [&](int k, int m) {
@@ -356,31 +372,35 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         }
         if (vO) {
 #pragma unroll
-            for (int t = 0; t < T; ++t) {
-                if (t < rows) {
-                    const int m = t / 2;
-                    const bool odd = t & 1;
-                    const float s1 = odd ? S1[0][m].y : S1[0][m].x;
-                    const float s2 = odd ? S2[0][m].y : S2[0][m].x;
-                    const float s3 = odd ? S3[0][m].y : S3[0][m].x;
-                    const float delta = odd ? Dl[0][m].y : Dl[0][m].x;
-                    const float dpv = odd ? Pl[0][m].y : Pl[0][m].x;
-                    const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[cO]);
-                    const int64_t off = (b * L + t0 + t) * D + dO;
-                    if (has_z) {
-                        const float dzv = __fmaf_rn(Dd, xv, s3) * dd[t];
-                        nf = __fmaf_rn(dzv, 0.0f, nf);
-                        reinterpret_cast<IO*>(p.dz)[off] = IOT<IO>::from_f(dzv);
-                    }
-                    const float dxv = __fmaf_rn(dpv, Dd, delta * s1);
-                    const float ddelta = __fmaf_rn(xv, s1, s2);
-                    const float ddtv = sp ? ddelta * sg[t] : ddelta;
-                    dDacc = __fmaf_rn(dpv, xv, dDacc);
-                    dbacc += ddtv;
-                    nf = __fmaf_rn(dxv, 0.0f, nf);
-                    nf = __fmaf_rn(ddtv, 0.0f, nf);
-                    reinterpret_cast<IO*>(p.dx)[off] = IOT<IO>::from_f(dxv);
-                    p.ddt[off] = ddtv;
+            for (int m = 0; m < T / 2; ++m) {
+                const int t = 2 * m;
+                float2 xv = ld_pair<IO>(st + Ly::OFF_X + t * Ly::XROW, Ly::XROW, cO);
+                if (!full) xv = f2(t < rows ? xv.x : 0.f, t + 1 < rows ? xv.y : 0.f);
+                const float2 s1 = S1[0][m], s2 = S2[0][m];
+                const float2 dxv = __ffma2_rn(Pl[0][m], D2, __fmul2_rn(Dl[0][m], s1));
+                const float2 ddelta = __ffma2_rn(xv, s1, s2);
+                float2 ddtv = sp ? __fmul2_rn(ddelta, sgp[m]) : ddelta;
+                if (!full) ddtv = f2(t < rows ? ddtv.x : 0.f, t + 1 < rows ? ddtv.y : 0.f);
+                dD2 = __ffma2_rn(Pl[0][m], xv, dD2);
+                db2 = __fadd2_rn(db2, ddtv);
+                nf2 = __ffma2_rn(dxv, f2(0.f, 0.f), __ffma2_rn(ddtv, f2(0.f, 0.f), nf2));
+                IO* dxp = reinterpret_cast<IO*>(p.dx) + (b * L + t0 + t) * D + dO;
+                float* ddp_ = p.ddt + (b * L + t0 + t) * D + dO;
+                IO* dzp = reinterpret_cast<IO*>(p.dz) + (b * L + t0 + t) * D + dO;
+                float2 dzv = f2(0.f, 0.f);
+                if (has_z) {
+                    dzv = __fmul2_rn(__ffma2_rn(D2, xv, S3[0][m]), ddp[m]);
+                    nf2 = __ffma2_rn(dzv, f2(0.f, 0.f), nf2);
+                }
+                if (full || t < rows) {
+                    dxp[0] = IOT<IO>::from_f(dxv.x);
+                    ddp_[0] = ddtv.x;
+                    if (has_z) dzp[0] = IOT<IO>::from_f(dzv.x);
+                }
+                if (full || t + 1 < rows) {
+                    dxp[D] = IOT<IO>::from_f(dxv.y);
+                    ddp_[D] = ddtv.y;
+                    if (has_z) dzp[D] = IOT<IO>::from_f(dzv.y);
                 }
             }
         }
@@ -414,10 +434,10 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         }
     }
     if (vO) {
-        atomicAdd(p.dD + dO, dDacc);
-        atomicAdd(p.ddt_bias + dO, dbacc);
+        atomicAdd(p.dD + dO, __fadd_rn(dD2.x, dD2.y));
+        atomicAdd(p.ddt_bias + dO, __fadd_rn(db2.x, db2.y));
     }
-    flag_nonfinite(p.status, nf);
+    flag_nonfinite(p.status, __fadd_rn(nf2.x, nf2.y));
 }
 
 // Chunk aggregate of the reverse recurrence for groups 1..G-1: with the
@@ -606,14 +626,14 @@ template <typename IO> int launch_bwd_t(const BwdParams& p, cudaStream_t s) {
     if (p.B == 0 || p.D == 0 || p.G == 0) return 0;
     const CUtensorMapDataType io = io_map_type<IO>(), f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
     const CUtensorMapSwizzle none = CU_TENSOR_MAP_SWIZZLE_NONE;
-    const int64_t rows = p.B * p.L, ES = sizeof(IO), hrows = p.B * ((p.L + Ly::T - 1) / Ly::T) * kN;
+    const int64_t rows = p.B * p.L, ES = sizeof(IO), hrows = p.B * ((p.L + Ly::T - 1) / Ly::T) * (kN / 2);
     BwdMaps mp;
     if (!encode_2d(&mp.x, io, p.x, p.D, rows, p.D * ES, Ly::CH, Ly::T, none) ||
         !encode_2d(&mp.dy, io, p.dy, p.D, rows, p.D * ES, Ly::CH, Ly::T, none) ||
         !encode_2d(&mp.dt, f32, p.dt, p.D, rows, p.D * 4, Ly::CH, Ly::T, none) ||
         !encode_2d(&mp.b, io, p.Bm, kN, rows, p.bcs * ES, kN, Ly::T, none) ||
         !encode_2d(&mp.c, io, p.Cm, kN, rows, p.bcs * ES, kN, Ly::T, none) ||
-        !encode_2d(&mp.h, f32, p.ckpt, p.D, hrows, p.D * 4, Ly::CH, kN, none))
+        !encode_2d(&mp.h, f32, p.ckpt, 2 * p.D, hrows, p.D * 8, 2 * Ly::CH, kN / 2, none))
         return -1;
     mp.z = mp.x;
     if (p.has_z && !encode_2d(&mp.z, io, p.z, p.D, rows, p.D * ES, Ly::CH, Ly::T, none)) return -1;

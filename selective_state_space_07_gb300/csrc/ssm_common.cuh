@@ -134,6 +134,69 @@ __device__ __forceinline__ float gate_out(float p, float Dd, float xv, float zv,
     return __fmul_rn(pp, __fmul_rn(zv, sigmoid<FAST>(zv)));
 }
 
+// ------------------------------------------------------------ channel-pair (f32x2) forms
+// The same roundings as the scalar helpers above, applied to two channels at
+// once with packed fp32 instructions (each half of a packed add, multiply or
+// fused multiply-add rounds exactly as the scalar instruction does), so a
+// kernel using these and one using the scalar forms get identical bits.
+__device__ __forceinline__ float2 pk(float a, float b) { return make_float2(a, b); }
+
+template <bool FAST>
+__device__ __forceinline__ float2 delta2(float2 dtv, float2 bias, bool sp) {
+    const float2 v = __fadd2_rn(dtv, bias);
+    if (!sp) return v;
+    if (FAST) {
+        const float2 arg = __fmul2_rn(pk(-fabsf(v.x), -fabsf(v.y)), pk(kLog2e, kLog2e));
+        const float2 w = __fadd2_rn(pk(1.0f, 1.0f), pk(ex2(arg.x), ex2(arg.y)));
+        return __ffma2_rn(pk(kLn2, kLn2), pk(lg2(w.x), lg2(w.y)), pk(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f)));
+    }
+    return pk(softplus<false>(v.x), softplus<false>(v.y));
+}
+// Delta and sigmoid(dt + bias) of two channels (the backward's d(dt) factor).
+template <bool FAST>
+__device__ __forceinline__ float2 delta_sig2(float2 dtv, float2 bias, bool sp, float2* sig) {
+    const float2 v = __fadd2_rn(dtv, bias);
+    if (!sp) {
+        *sig = pk(1.0f, 1.0f);
+        return v;
+    }
+    if (FAST) {
+        const float2 arg = __fmul2_rn(pk(-fabsf(v.x), -fabsf(v.y)), pk(kLog2e, kLog2e));
+        const float2 e = pk(ex2(arg.x), ex2(arg.y));
+        const float2 w = __fadd2_rn(pk(1.0f, 1.0f), e);
+        const float2 r = pk(rcp(w.x), rcp(w.y));
+        const float2 er = __fmul2_rn(e, r);
+        *sig = pk(v.x >= 0.0f ? r.x : er.x, v.y >= 0.0f ? r.y : er.y);
+        return __ffma2_rn(pk(kLn2, kLn2), pk(lg2(w.x), lg2(w.y)), pk(fmaxf(v.x, 0.0f), fmaxf(v.y, 0.0f)));
+    }
+    float s0, s1;
+    const float d0 = softplus_sig<false>(v.x, &s0), d1 = softplus_sig<false>(v.y, &s1);
+    *sig = pk(s0, s1);
+    return pk(d0, d1);
+}
+template <bool FAST> __device__ __forceinline__ float2 sigmoid2(float2 z) {
+    if (FAST) {
+        const float2 arg = __fmul2_rn(pk(-z.x, -z.y), pk(kLog2e, kLog2e));
+        const float2 w = __fadd2_rn(pk(1.0f, 1.0f), pk(ex2(arg.x), ex2(arg.y)));
+        return pk(rcp(w.x), rcp(w.y));
+    }
+    return pk(sigmoid<false>(z.x), sigmoid<false>(z.y));
+}
+
+// Two adjacent channels of a staged row (byte offset `off`) as fp32, and the
+// store of two adjacent outputs in the I/O dtype.
+template <typename IO> __device__ __forceinline__ float2 ld2(const char* p);
+template <> __device__ __forceinline__ float2 ld2<float>(const char* p) { return *reinterpret_cast<const float2*>(p); }
+template <> __device__ __forceinline__ float2 ld2<__nv_bfloat16>(const char* p) {
+    const unsigned w = *reinterpret_cast<const unsigned*>(p);  // low half: the first channel
+    return pk(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+template <typename IO> __device__ __forceinline__ void st2(IO* p, float2 v);
+template <> __device__ __forceinline__ void st2<float>(float* p, float2 v) { *reinterpret_cast<float2*>(p) = v; }
+template <> __device__ __forceinline__ void st2<__nv_bfloat16>(__nv_bfloat16* p, float2 v) {
+    *reinterpret_cast<__nv_bfloat162*>(p) = __floats2bfloat162_rn(v.x, v.y);
+}
+
 __device__ __forceinline__ void flag_nonfinite(unsigned* status, float acc) {
     // acc accumulates y*0 over the outputs: 0 unless one of them was Inf/NaN.
     const bool bad = !(acc == 0.0f);
@@ -167,12 +230,14 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 // Wait (non-blocking polls with a short sleep) until phase `parity` of the
-// barrier completes or kWaitNs have passed; returns whether it completed.
-__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity) {
+// barrier completes or `limit_ns` have passed; returns whether it completed.
+__device__ __forceinline__ bool mbar_wait_bounded(unsigned bar, unsigned parity,
+                                                  unsigned long long limit_ns = kWaitNs) {
+    if (mbar_test(bar, parity)) return true;
     const unsigned long long t0 = global_ns();
     while (!mbar_test(bar, parity)) {
-        if (global_ns() - t0 > kWaitNs) return false;
-        __nanosleep(64);
+        if (global_ns() - t0 > limit_ns) return false;
+        __nanosleep(32);
     }
     return true;
 }

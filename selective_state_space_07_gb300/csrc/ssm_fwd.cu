@@ -15,12 +15,19 @@
 // (f32x2); each state's update is a scalar fused multiply-add chain.
 //
 // Per tile: (A) each lane prepares Delta, u and the gate factor for its 8
-// tokens (one lane of the pair per token) and shares Delta/u with its
-// partner through shared memory; (S) the lane's 8 state recurrences advance
-// side by side through the 16 tokens (independent chains for the scheduler)
-// while the readout chain takes the states in order; (E) the two
-// half-readouts of each token are added and each lane gates and writes y for
-// its 8 tokens.
+// tokens (one lane of the pair per token, two tokens per packed f32x2
+// operation) and shares Delta/u with its partner through shared memory;
+// (S) the lane's 8 state recurrences advance side by side through the 16
+// tokens (independent chains for the scheduler) while the readout chain
+// takes the states in order; (E) the two half-readouts of each token are
+// added and each lane gates and writes y for its 8 tokens.
+//
+// One block barrier per tile: the tables a tile writes (B^T, C^T, Delta/u)
+// are double-buffered by tile parity, so the barrier after (A) of tile j
+// also orders every write of tile j+1 after the reads of tile j-1; the
+// stage a tile used is refilled at the top of the next tile, after that
+// barrier. The per-warp half-readout exchange of (E) synchronises the warp
+// only.
 //
 // Canonical readout order (the step kernel evaluates the same operations):
 // each half of the states is a sequential fused multiply-add chain
@@ -80,12 +87,13 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
     constexpr bool FAST = IOT<IO>::kFast;
     extern __shared__ __align__(128) char smem_raw[];
     char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
-    __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];       // a stage's copies landed
-    __shared__ int aborted;                                    // a copy did not arrive within the time bound
-    __shared__ __align__(16) float BT[kN * T];                 // B^T of the tile [state][token]
-    __shared__ __align__(16) float CT[AGG ? 4 : kN * T];
-    __shared__ __align__(16) float DU[CH * Ly::ROW];           // per channel [Delta 0..15 | u 0..15]
-    __shared__ __align__(16) float PB[AGG ? 4 : CH * Ly::ROW]; // per channel [half-0 readouts | half-1]
+    __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];          // a stage's copies landed
+    // tables of a tile, double-buffered by tile parity so that one barrier
+    // per tile orders every write after the reads of two tiles before
+    __shared__ __align__(16) float BT[2][kN * T];                 // B^T of the tile [state][token]
+    __shared__ __align__(16) float CT[2][AGG ? 4 : kN * T];
+    __shared__ __align__(16) float DU[2][CH * Ly::ROW];           // per channel [Delta 0..15 | u 0..15]
+    __shared__ __align__(16) float PB[AGG ? 4 : CH * Ly::ROW];    // per channel [half-0 readouts | half-1]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hk = lane >> 4;                 // states 8*hk .. 8*hk+7; tokens 8*hk .. 8*hk+7 of the tile
@@ -115,18 +123,21 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
     const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
     const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
 
+    const float2 D2 = f2(Dd, Dd), bias2 = f2(bias, bias);
+    const unsigned long long wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
+
     // one thread loads a tile's inputs with TMA onto the stage's mbarrier;
     // rows past the group's last token are loaded too (or read as zero past
     // the tensor's end) and ignored: they act as identity tokens below
     const unsigned stage_bytes =
         (unsigned)(T * (Ly::XROW * (has_z ? 2 : 1) + Ly::DTROW + Ly::BCROW * (AGG ? 1 : 2)));
     auto issue = [&](int j) {
-        if (tid != 0) return;
         const int slot = j % Ly::NSTAGE;
         char* st = smem + slot * Ly::STAGE;
         const int y = (int)(b * L + tb0 + (int64_t)j * T);  // first token row of the tile in [B*L]
         const unsigned bar = smem_u32(&fullb[slot]);
         mbar_expect_tx(bar, stage_bytes);
+        if (j + 1 == p.fault_tile1) return;  // test hook: the barrier is armed, the copies never come
         tma_load_2d(st + Ly::OFF_X, &mp.x, (int)d0, y, bar);
         if (has_z) tma_load_2d(st + Ly::OFF_Z, &mp.z, (int)d0, y, bar);
         tma_load_2d(st + Ly::OFF_DT, &mp.dt, (int)d0, y, bar);
@@ -136,29 +147,26 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
     if (tid == 0) {
         for (int q = 0; q < Ly::NSTAGE; ++q) mbar_init(smem_u32(&fullb[q]), 1);
         mbar_fence_init();
-        aborted = 0;
     }
     __syncthreads();
 
-    float* du = DU + c * Ly::ROW;
-    float* pb = PB + c * Ly::ROW;
     float nf = 0.f;     // Inf/NaN detector
     float ssum = 0.f;   // AGG: this lane's part of the sum of Delta over the group
 
     // prologue: tiles 0 .. NSTAGE-2 in flight
-#pragma unroll
-    for (int q = 0; q < Ly::NSTAGE - 1; ++q)
-        if (q < ntile) issue(q);
-    for (int j = 0; j < ntile; ++j) {
-        char* st = smem + (j % Ly::NSTAGE) * Ly::STAGE;
-        if (j + Ly::NSTAGE - 1 < ntile) issue(j + Ly::NSTAGE - 1);  // refill the slot tile j-1 used
-        // every thread waits for the tile (bounded); after a timeout the block
-        // stops waiting but keeps the barrier sequence (its results are flagged invalid)
-        if (!aborted && !mbar_wait_bounded(smem_u32(&fullb[j % Ly::NSTAGE]), (unsigned)((j / Ly::NSTAGE) & 1))) {
-            aborted = 1;
-            if (p.status) atomicOr(p.status, kStatusTimeout);
-        }
-        __syncthreads();
+    if (tid == 0)
+        for (int q = 0; q < Ly::NSTAGE - 1 && q < ntile; ++q) issue(q);
+    int j = 0;
+    bool aborted = false;
+    for (; j < ntile; ++j) {
+        const int buf = j & 1;
+        const char* st = smem + (j % Ly::NSTAGE) * Ly::STAGE;
+        // refill the slot tile j-1 used: every thread passed tile j-1's
+        // barrier, after its last read of that stage
+        if (tid == 0 && j + Ly::NSTAGE - 1 < ntile) issue(j + Ly::NSTAGE - 1);
+        // every thread waits for the tile itself (bounded); the barrier below
+        // tells every thread whether any wait ran out
+        const bool late = !mbar_wait_bounded(smem_u32(&fullb[j % Ly::NSTAGE]), (unsigned)((j / Ly::NSTAGE) & 1), wait_ns);
         const int64_t t0 = tb0 + (int64_t)j * T;
         const int rows = (int)min64(T, tb1 - t0);
 
@@ -169,37 +177,47 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
             for (int i = tid; i < kN * T; i += NT) {
                 const int n = i / T, tok = i - n * T;
                 const bool live = tok < rows;  // rows past the end belong to other tokens: zero, not read
-                BT[i] = live ? IOT<IO>::to_f(Braw[tok * kN + n]) : 0.f;
-                if (!AGG) CT[i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
+                BT[buf][i] = live ? IOT<IO>::to_f(Braw[tok * kN + n]) : 0.f;
+                if (!AGG) CT[buf][i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
             }
         }
-        // ---- A: Delta, u and the gate factor of this lane's 8 tokens;
-        // tokens past the end act as identity (Delta = u = 0)
-        float xo[NS], gz[NS];
+        // ---- A: Delta, u and the gate factor of this lane's 8 tokens, a
+        // token pair at a time; tokens past the end act as identity (Delta = u = 0)
+        float* du = DU[buf] + c * Ly::ROW;
+        float2 xo[NS / 2], gz[NS / 2];
         {
-            float dl[NS], ul[NS];
+            float2 dl[NS / 2], ul[NS / 2];
 #pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                const int t = NS * hk + i;
-                const float xv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_X + t * Ly::XROW)[c]);
-                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[c];
-                const float delta = token_delta<FAST>(dtv, bias, sp);
-                const bool live = t < rows;
-                dl[i] = live ? delta : 0.f;
-                ul[i] = live ? __fmul_rn(delta, xv) : 0.f;
+            for (int i = 0; i < NS / 2; ++i) {
+                const int t = NS * hk + 2 * i;
+                const char* xr = st + Ly::OFF_X + t * Ly::XROW;
+                const float2 xv = f2(IOT<IO>::to_f(reinterpret_cast<const IO*>(xr)[c]),
+                                     IOT<IO>::to_f(reinterpret_cast<const IO*>(xr + Ly::XROW)[c]));
+                const char* dr = st + Ly::OFF_DT + t * Ly::DTROW;
+                const float2 dtv = f2(reinterpret_cast<const float*>(dr)[c], reinterpret_cast<const float*>(dr + Ly::DTROW)[c]);
+                const float2 delta = delta2<FAST>(dtv, bias2, sp);
+                const bool l0 = t < rows, l1 = t + 1 < rows;
+                dl[i] = f2(l0 ? delta.x : 0.f, l1 ? delta.y : 0.f);
+                const float2 u = __fmul2_rn(delta, xv);
+                ul[i] = f2(l0 ? u.x : 0.f, l1 ? u.y : 0.f);
                 xo[i] = xv;
-                if (AGG) ssum = __fadd_rn(ssum, dl[i]);
+                if (AGG) ssum = __fadd_rn(__fadd_rn(ssum, dl[i].x), dl[i].y);
                 if (has_z) {
-                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[c]);
-                    gz[i] = __fmul_rn(zv, sigmoid<FAST>(zv));
+                    const char* zr = st + Ly::OFF_Z + t * Ly::XROW;
+                    const float2 zv = f2(IOT<IO>::to_f(reinterpret_cast<const IO*>(zr)[c]),
+                                         IOT<IO>::to_f(reinterpret_cast<const IO*>(zr + Ly::XROW)[c]));
+                    gz[i] = __fmul2_rn(zv, sigmoid2<FAST>(zv));
                 }
             }
-            *reinterpret_cast<float4*>(du + NS * hk) = make_float4(dl[0], dl[1], dl[2], dl[3]);
-            *reinterpret_cast<float4*>(du + NS * hk + 4) = make_float4(dl[4], dl[5], dl[6], dl[7]);
-            *reinterpret_cast<float4*>(du + T + NS * hk) = make_float4(ul[0], ul[1], ul[2], ul[3]);
-            *reinterpret_cast<float4*>(du + T + NS * hk + 4) = make_float4(ul[4], ul[5], ul[6], ul[7]);
+            *reinterpret_cast<float4*>(du + NS * hk) = make_float4(dl[0].x, dl[0].y, dl[1].x, dl[1].y);
+            *reinterpret_cast<float4*>(du + NS * hk + 4) = make_float4(dl[2].x, dl[2].y, dl[3].x, dl[3].y);
+            *reinterpret_cast<float4*>(du + T + NS * hk) = make_float4(ul[0].x, ul[0].y, ul[1].x, ul[1].y);
+            *reinterpret_cast<float4*>(du + T + NS * hk + 4) = make_float4(ul[2].x, ul[2].y, ul[3].x, ul[3].y);
         }
-        __syncthreads();
+        if (__syncthreads_or(late)) {  // the tables of this tile are ready -- unless a copy never came
+            aborted = true;
+            break;
+        }
         float2 Dl[T / 2], Ul[T / 2];
 #pragma unroll
         for (int q = 0; q < T / 4; ++q) {
@@ -214,7 +232,10 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
         // ---- S: per state, the tile's 16 tokens; the readout chain runs
         // over this lane's 8 states
         const bool ck = !AGG && p.ckpt && dv;
-        float* ckp = ck ? p.ckpt + ((b * nck + t0 / kCkpt) * kN + NS * hk) * D + d : nullptr;
+        // checkpoint [B][nck][8 state pairs][D][2]: pair (n, n+1) of channel d
+        float* ckp = ck ? p.ckpt + (((b * nck + t0 / kCkpt) * (kN / 2) + NS * hk / 2) * D + d) * 2 : nullptr;
+        const float* BTb = BT[buf];
+        const float* CTb = CT[buf];
         float2 acc[T / 2];
         // SI states advance together through the tokens (independent chains
         // for the scheduler); the readout chain still takes the states in order
@@ -228,15 +249,18 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
             for (int i = 0; i < SI; ++i) {
                 A2p[i] = f2(A2[s + i], A2[s + i]);
                 hp[i] = h[s + i];
-                if (ck) ckp[(s + i) * D] = hp[i];  // states before token t0
+            }
+            if (ck) {  // states before token t0
+#pragma unroll
+                for (int i = 0; i < SI; i += 2) *reinterpret_cast<float2*>(ckp + (int64_t)((s + i) / 2) * D * 2) = f2(hp[i], hp[i + 1]);
             }
 #pragma unroll
             for (int q = 0; q < T / 4; ++q) {
                 float4 b4[SI], c4[SI];
 #pragma unroll
                 for (int i = 0; i < SI; ++i) {
-                    b4[i] = *reinterpret_cast<const float4*>(BT + (n + i) * T + 4 * q);
-                    if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CT + (n + i) * T + 4 * q);
+                    b4[i] = *reinterpret_cast<const float4*>(BTb + (n + i) * T + 4 * q);
+                    if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CTb + (n + i) * T + 4 * q);
                 }
 #pragma unroll
                 for (int h2 = 0; h2 < 2; ++h2) {
@@ -264,7 +288,8 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
                 }
                 if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
 #pragma unroll
-                    for (int i = 0; i < SI; ++i) ckp[(s + i) * D + kN * D] = hp[i];
+                    for (int i = 0; i < SI; i += 2)
+                        *reinterpret_cast<float2*>(ckp + (int64_t)((s + i) / 2) * D * 2 + (int64_t)kN * D) = f2(hp[i], hp[i + 1]);
                 }
             }
 #pragma unroll
@@ -272,6 +297,8 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
         }
         if (!AGG) {
             // ---- E: half readouts -> full readout of this lane's 8 tokens
+            float* pb = PB + c * Ly::ROW;
+            __syncwarp();  // the previous tile's reads of PB are done
             *reinterpret_cast<float4*>(pb + T * hk) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
             *reinterpret_cast<float4*>(pb + T * hk + 4) = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
             *reinterpret_cast<float4*>(pb + T * hk + 8) = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
@@ -281,24 +308,38 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
             const float4 p0b = *reinterpret_cast<const float4*>(pb + NS * hk + 4);
             const float4 p1a = *reinterpret_cast<const float4*>(pb + T + NS * hk);
             const float4 p1b = *reinterpret_cast<const float4*>(pb + T + NS * hk + 4);
-            const float P0[NS] = {p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, p0b.y, p0b.z, p0b.w};
-            const float P1[NS] = {p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, p1b.y, p1b.z, p1b.w};
+            const float2 P0[NS / 2] = {f2(p0a.x, p0a.y), f2(p0a.z, p0a.w), f2(p0b.x, p0b.y), f2(p0b.z, p0b.w)};
+            const float2 P1[NS / 2] = {f2(p1a.x, p1a.y), f2(p1a.z, p1a.w), f2(p1b.x, p1b.y), f2(p1b.z, p1b.w)};
             IO* yrow = reinterpret_cast<IO*>(p.y) + (b * L + t0) * D + d;
 #pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                const int t = NS * hk + i;
-                const float pr = __fadd_rn(P0[i], P1[i]);
-                const float pp = __fmaf_rn(Dd, xo[i], pr);
-                const float yv = has_z ? __fmul_rn(pp, gz[i]) : pp;
+            for (int i = 0; i < NS / 2; ++i) {
+                const int t = NS * hk + 2 * i;
+                const float2 pr = __fadd2_rn(P0[i], P1[i]);
+                const float2 pp = __ffma2_rn(D2, xo[i], pr);
+                const float2 yv = has_z ? __fmul2_rn(pp, gz[i]) : pp;
                 if (dv && t < rows) {
-                    nf = __fmaf_rn(yv, 0.0f, nf);
-                    yrow[(int64_t)t * D] = IOT<IO>::from_f(yv);
+                    nf = __fmaf_rn(yv.x, 0.0f, nf);
+                    yrow[(int64_t)t * D] = IOT<IO>::from_f(yv.x);
+                }
+                if (dv && t + 1 < rows) {
+                    nf = __fmaf_rn(yv.y, 0.0f, nf);
+                    yrow[(int64_t)(t + 1) * D] = IOT<IO>::from_f(yv.y);
                 }
             }
         }
-        __syncthreads();
     }
 
+    if (aborted) {
+        // every thread stops at tile j; thread 0 waits (bounded) for the
+        // copies still in flight (tiles j .. j + NSTAGE - 1) before the block leaves
+        if (tid == 0) {
+            const int last = min(j + Ly::NSTAGE - 1, ntile - 1);
+            for (int jj = j; jj <= last; ++jj)
+                (void)mbar_wait_bounded(smem_u32(&fullb[jj % Ly::NSTAGE]), (unsigned)((jj / Ly::NSTAGE) & 1), wait_ns);
+            if (p.status) atomicOr(p.status, kStatusTimeout);
+        }
+        return;
+    }
     if (AGG) {
         ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, 16));
         if (dv) {

@@ -12,7 +12,15 @@ namespace ssm {
 
 constexpr unsigned kStatusNonFinite = 1u;  // workspace status bit: an output was Inf/NaN
 constexpr unsigned kStatusTimeout = 2u;    // workspace status bit: a bounded wait inside a kernel ran out
-constexpr int kFwdThreads = 128;
+constexpr int kFwdThreads = 128;  // ssm_step_kernel
+#ifndef SSM_FWD_SL
+#define SSM_FWD_SL 4
+#endif
+#ifndef SSM_FWD_WARPS
+#define SSM_FWD_WARPS 2
+#endif
+constexpr int kFwdSL = SSM_FWD_SL;        // forward: states per lane of each of its two channels (2, 4 or 8)
+constexpr int kFwdWarps = SSM_FWD_WARPS;  // warps per forward CTA (each warp scans its channels on its own)
 constexpr int kBwdThreads = 128;
 constexpr int kConvThreads = 128;
 
@@ -29,6 +37,12 @@ struct FwdParams {
     float *h_last, *ckpt;
     float *aggH, *aggS;   // chunk aggregates [B,G,D,16] and [B,G,D]
     unsigned* status;
+    // Bounded waits give up after wait_ns (0: one second). fault_tile1 > 0
+    // (tests only) makes the staging of tile fault_tile1 - 1 (counted per
+    // warp from its group's start) arm its barrier without issuing the
+    // copies, so that its wait runs out.
+    unsigned long long wait_ns;
+    int64_t fault_tile1;
 };
 
 struct BwdParams {
@@ -39,7 +53,7 @@ struct BwdParams {
     const void *x, *z, *Bm, *Cm, *dy;
     int64_t bcs;    // elements between consecutive tokens' Bm (and Cm) rows
     const float *dt, *dt_bias, *A, *Dskip;
-    const float* ckpt;    // [B, ceil(L/8), 16, D]: state before every 8th token, state-major
+    const float* ckpt;    // [B, ceil(L/8), 8, D, 2]: state before every 8th token, pairs of states per channel
     const float* gstart;  // G == 1: dh_last [B,D,16] (nullable); G > 1: carries [B,G,D,16]
     void *dx, *dz;
     float *ddt, *dA, *dD, *ddt_bias, *dB, *dC, *dh0;
@@ -162,5 +176,11 @@ int launch_dtproj(bool bwd, int64_t M, int64_t D, int64_t R, int64_t a_stride, c
                   const float* bias, float* out, const float* dout, float* dbias, int softplus, unsigned* status,
                   cudaStream_t s);
 int launch_bwd_agg(int io, const BwdParams& p, cudaStream_t s);
+
+// The per-thread launch count that ssm_last_launch_count reports: reset at
+// the start of an entry point; count_launches adds a launcher's result and
+// maps a failed launch (r < 0) to SSM_ERR_CUDA.
+void reset_launches();
+int count_launches(int r);
 
 }  // namespace ssm

@@ -124,6 +124,26 @@ def test_nonfinite_outputs_are_flagged(ssm):
     assert ssm.poll_status(ws2) == 0
 
 
+@pytest.mark.parametrize("groups", [1, 3])
+def test_bounded_wait_expiry_is_reported_and_the_context_stays_usable(ssm, groups):
+    # The testing hook arms tile 1 of every warp of the next forward's main
+    # kernel without issuing its copies and bounds the waits by 1 ms: the
+    # waits run out, the warps drain the copies they have in flight and
+    # leave, and the status word says so. The same workspace then serves a
+    # normal call, whose results are exact again.
+    inp = gen.make_inputs(2, 160, 64, 16, io="f32", seed=21, with_h0=True)
+    dv = to_dev(inp)
+    y_ref, h_ref, _, ws = run_fwd(ssm, dv, inp, groups=groups)
+    assert ssm.poll_status(ws) == 0
+    ssm.arm_wait_fault(1, 1_000_000)
+    run_fwd(ssm, dv, inp, groups=groups, workspace=ws)
+    assert ssm.poll_status(ws) == -6
+    assert ssm.poll_status(ws) == 0  # polling clears the word
+    y, h_last, _, ws = run_fwd(ssm, dv, inp, groups=groups, workspace=ws)  # the hook was one-shot
+    assert ssm.poll_status(ws) == 0
+    assert torch.equal(y, y_ref) and torch.equal(h_last, h_ref)
+
+
 def test_canonical_init_is_finite_at_length_4096(ssm):
     inp = gen.make_inputs(1, 4096, 64, 16, io="bf16", seed=4, dt_std=1.0, delta_target=0.01)
     dv = to_dev(inp)
@@ -137,12 +157,18 @@ def test_canonical_init_is_finite_at_length_4096(ssm):
 
 
 def test_dA_log_chain_rule(ssm):
-    A_log = torch.log(torch.arange(1, 17, dtype=torch.float32, device="cuda")).repeat(32, 1)
-    A = -torch.exp(A_log)
-    dA = torch.randn(32, 16, device="cuda")
-    out = ssm.dA_log_grad(dA, A)
-    torch.cuda.synchronize()
-    assert torch.equal(out, dA * A)
+    # dA_log = dA * A (A = -exp(A_log)): the GPU's dA of a real backward,
+    # taken through ssm_dA_log_grad, against the fp64 oracle's dA times A
+    inp = gen.make_inputs(2, 200, 48, 16, io="f32", seed=9, with_h0=True, with_dh_last=True)
+    dv = to_dev(inp)
+    _, _, ckpt, ws = run_fwd(ssm, dv, inp)
+    g = run_bwd(ssm, dv, inp, ckpt, workspace=ws)
+    out = ssm.dA_log_grad(g["dA"], dv["A"])
+    ref = oracle.bwd(inp)["dA"] * inp.A.astype(np.float64)
+    assert rel_err(to_np(out), ref) <= TOL[("f32", "bwd")]
+    # elementwise it is one rounded product, in place too
+    dA = g["dA"].clone()
+    assert torch.equal(ssm.dA_log_grad(dA, dv["A"], out=dA), g["dA"] * dv["A"])
 
 
 def test_launch_counts(ssm):

@@ -62,7 +62,7 @@ def test_step_from_zero_is_bitwise_a_wide_single_group_forward(ssm, io):
 
 def test_step_from_every_checkpoint_is_bitwise_the_forward(ssm):
     # A forward split into 3 L-groups of 32 tokens: stepping from any saved
-    # checkpoint (one every 8 tokens, stored state-major [B, L/8, N, D])
+    # checkpoint (one every 8 tokens; ckpt_states gives them as [B, L/8, D, N])
     # reproduces those tokens' outputs exactly, and the state it reaches
     # equals the next checkpoint exactly inside a group. A group's first
     # checkpoint comes from the carry scan over groups, which re-associates
@@ -72,7 +72,7 @@ def test_step_from_every_checkpoint_is_bitwise_the_forward(ssm):
     dv = to_dev(inp)
     y, h_last, ckpt, _ = run_fwd(ssm, dv, inp, nsplit=2, groups=3)
     nck = 96 // K
-    ck = ckpt[: ssm.ckpt_elems(2, 96, 64)].view(2, nck, 16, 64).transpose(2, 3)  # -> [B, nck, D, N]
+    ck = ssm.ckpt_states(ckpt, 2, 96, 64)  # -> [B, nck, D, N]
     group_starts = {0, 32 // K, 64 // K}
     for c in range(nck):
         state = ck[:, c].contiguous().clone()
