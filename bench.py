@@ -216,7 +216,7 @@ class ClockSampler:
         try:
             self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
                                          stdout=self.tmp, stderr=subprocess.DEVNULL)
         except Exception as ex:  # nvidia-smi missing: report no clocks
             log("clock sampling unavailable:", ex)
@@ -297,6 +297,59 @@ def visible_gpu_ids(world):
 
 
 # ------------------------------------------------------------------ cpu work
+def decode_throughput(ssm, dv, w, dev, stream, n_tok=64):
+    """ssm_step at the workload's B and D (one token of every channel per
+    call), timed over n_tok consecutive tokens of the resident inputs: as
+    n_tok eager calls, and replayed from one CUDA graph that holds the same
+    n_tok calls (launch cost out of the way)."""
+    import torch
+    state = torch.zeros(w.B, w.D, w.N, dtype=torch.float32, device=dev)
+    cols = [{k: dv[k][:, t].contiguous() for k in ("x", "dt", "z", "Bm", "Cm")} for t in range(n_tok)]
+    ys = [torch.empty(w.B, w.D, dtype=dv["x"].dtype, device=dev) for _ in range(n_tok)]
+
+    def run():
+        for t in range(n_tok):
+            c = cols[t]
+            ssm.step(state, c["x"], c["dt"], dv["A"], c["Bm"], c["Cm"], c["z"], dv["Dskip"], dv["dt_bias"],
+                     y_t=ys[t])
+
+    def timed(fn, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        a.record(cur)
+        for _ in range(reps):
+            fn()
+        b.record(cur)
+        b.synchronize()
+        return a.elapsed_time(b) / reps / n_tok
+
+    run()
+    eager_ms = timed(run, 5)
+    graph_ms = None
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        g.replay()
+        graph_ms = timed(g.replay, 20)
+    except Exception as ex:  # a torch without graph capture: report the eager number only
+        log("decode graph capture failed:", ex)
+    e = 2 if w.io == "bf16" else 4
+    per_call = w.B * w.D * (3 * e + 4) + w.B * 2 * w.N * e + w.B * w.D * w.N * 8 + w.D * (w.N + 2) * 4
+    best = graph_ms if graph_ms is not None else eager_ms
+    return {"what": f"ssm_step, one token for all {w.B}x{w.D} channels per call",
+            "us_per_call_eager": round(eager_ms * 1e3, 3),
+            "us_per_call_graph": None if graph_ms is None else round(graph_ms * 1e3, 3),
+            "tokens_per_s": round(w.B / (best * 1e-3), 1),
+            "algorithmic_bytes_per_call": per_call,
+            "achieved_gbs": round(per_call / (best * 1e-3) / 1e9, 1)}
+
+
 def _row(w):
     """Batch row 0 of the workload (the generator is indexed by position, so
     a one-row draw equals the first row of the full draw)."""
@@ -455,6 +508,24 @@ def run_ours(args, w):
     tc = w.B * w.L * w.D
     value = job_value(world, tc, ms_step)
 
+    # ---- the forward without checkpoints (inference: y and the last state only)
+    ms_inf = None
+    if not args.no_extras:
+        h_last = torch.empty(w.B, w.D, w.N, dtype=torch.float32, device=dev)
+        ts = []
+        for k in range(max(3, min(args.steps, 50)) + 3):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            ssm.scan_fwd(dv["x"], dv["dt"], dv["A"], dv["Bm"], dv["Cm"], dv["z"], dv["Dskip"], dv["dt_bias"],
+                         y=y, h_last=h_last, save_ckpt=False, workspace=ws, **kw)
+            b_.record(stream)
+            b_.synchronize()
+            if k >= 3:
+                ts.append(a_.elapsed_time(b_))
+        ms_inf = max_over_ranks([sum(ts) / len(ts)], dist, dev)[0]
+    decode = decode_throughput(ssm, dv, w, dev, stream) if not args.no_extras else None
+
     # ---- end to end through the public API with host buffers
     e2e = None
     if not args.no_e2e:
@@ -521,6 +592,10 @@ def run_ours(args, w):
                    "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
         "roofline": rf[dom],
         "roofline_other": rf["fwd" if dom == "bwd" else "bwd"],
+        "fwd_inference": None if ms_inf is None else {
+            "ms": round(ms_inf, 5), "what": "ssm_scan_fwd with ckpt = NULL (y and h_last only)",
+            "hbm_frac": round(algorithmic_bytes(w, "fwd") / (ms_inf * 1e-3) / 1e9 / peak, 4)},
+        "decode": decode,
         "sfu_roofline": sfu,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -923,6 +998,7 @@ def main():
     ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the inference-forward and decode timings")
     ap.add_argument("--op", choices=("scan", "conv1d", "dtproj"), default="scan",
                     help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it; "
                          "dtproj: the dt projection with its softplus")

@@ -185,9 +185,11 @@ int ssm_step(const ssm_step_args* args, void* stream);
  * workspace is optional and, when given (>= 256 bytes), only receives the
  * status word; groups == 0 picks at most the L-groups whose carries fit the
  * array; an explicit groups that does not fit returns SSM_ERR_SCRATCH_LIMIT
- * before anything runs. The first call on a device looks up the array's
- * address; make it before any stream capture. All calls share the array:
- * calls that overlap on the GPU race and must be serialised. */
+ * before anything runs. The first call in each CUDA context (for the
+ * runtime's primary contexts: once per device) looks up the array's address
+ * with that device current; make it before any stream capture. All calls
+ * share the array: calls that overlap on the GPU race and must be
+ * serialised. */
 int ssm_scan_fwd_noalloc(const ssm_fwd_args* args, void* stream);
 
 /* Gradient of A_log for A = -exp(A_log) (the analytic-VJP commit: "A_log

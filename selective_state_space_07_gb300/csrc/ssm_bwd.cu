@@ -542,27 +542,29 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             }
         }
         {
-            float dl[NS], pl[NS];
+            // Delta and dp of this lane's 8 tokens, a token pair at a time
+            const float2 bias2 = make_float2(bias, bias);
+            float2 dl[NS / 2], pl[NS / 2];
 #pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                const int t = NS * hk + i;
-                const float dtv = reinterpret_cast<const float*>(st + Ly::OFF_DT + t * Ly::DTROW)[c];
-                const float dyv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_DY + t * Ly::XROW)[c]);
-                const float delta = token_delta<FAST>(dtv, bias, sp);
-                float dpv = dyv;
+            for (int i = 0; i < NS / 2; ++i) {
+                const int t = NS * hk + 2 * i;
+                const float2 dtv = ld_pair<float>(st + Ly::OFF_DT + t * Ly::DTROW, Ly::DTROW, c);
+                const float2 dyv = ld_pair<IO>(st + Ly::OFF_DY + t * Ly::XROW, Ly::XROW, c);
+                const float2 delta = delta2<FAST>(dtv, bias2, sp);
+                float2 dpv = dyv;
                 if (has_z) {
-                    const float zv = IOT<IO>::to_f(reinterpret_cast<const IO*>(st + Ly::OFF_Z + t * Ly::XROW)[c]);
-                    dpv = __fmul_rn(dyv, __fmul_rn(zv, sigmoid<FAST>(zv)));
+                    const float2 zv = ld_pair<IO>(st + Ly::OFF_Z + t * Ly::XROW, Ly::XROW, c);
+                    dpv = __fmul2_rn(dyv, __fmul2_rn(zv, sigmoid2<FAST>(zv)));
                 }
-                const bool live = t < rows;  // tokens past the end: a = 1, no adjoint input
-                dl[i] = live ? delta : 0.f;
-                pl[i] = live ? dpv : 0.f;
-                ssum = __fadd_rn(ssum, dl[i]);
+                const bool l0 = t < rows, l1 = t + 1 < rows;  // tokens past the end: a = 1, no adjoint input
+                dl[i] = make_float2(l0 ? delta.x : 0.f, l1 ? delta.y : 0.f);
+                pl[i] = make_float2(l0 ? dpv.x : 0.f, l1 ? dpv.y : 0.f);
+                ssum = __fadd_rn(__fadd_rn(ssum, dl[i].x), dl[i].y);
             }
-            *reinterpret_cast<float4*>(dp + NS * hk) = make_float4(dl[0], dl[1], dl[2], dl[3]);
-            *reinterpret_cast<float4*>(dp + NS * hk + 4) = make_float4(dl[4], dl[5], dl[6], dl[7]);
-            *reinterpret_cast<float4*>(dp + T + NS * hk) = make_float4(pl[0], pl[1], pl[2], pl[3]);
-            *reinterpret_cast<float4*>(dp + T + NS * hk + 4) = make_float4(pl[4], pl[5], pl[6], pl[7]);
+            *reinterpret_cast<float4*>(dp + NS * hk) = make_float4(dl[0].x, dl[0].y, dl[1].x, dl[1].y);
+            *reinterpret_cast<float4*>(dp + NS * hk + 4) = make_float4(dl[2].x, dl[2].y, dl[3].x, dl[3].y);
+            *reinterpret_cast<float4*>(dp + T + NS * hk) = make_float4(pl[0].x, pl[0].y, pl[1].x, pl[1].y);
+            *reinterpret_cast<float4*>(dp + T + NS * hk + 4) = make_float4(pl[2].x, pl[2].y, pl[3].x, pl[3].y);
         }
         __syncthreads();
         float2 Dl[T / 2], Pl[T / 2];
@@ -576,32 +578,44 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             Pl[2 * q + 1] = make_float2(pq.z, pq.w);
         }
 #pragma unroll
-        for (int s = 0; s < NS; s += 2) {
+        // SA states at a time: independent adjoint chains for the scheduler
+        constexpr int SA = 4;
+#pragma unroll
+        for (int s = 0; s < NS; s += SA) {
             const int n = NS * hk + s;
-            const float2 A2p0 = make_float2(A2[s], A2[s]), A2p1 = make_float2(A2[s + 1], A2[s + 1]);
-            float E0 = E[s], E1 = E[s + 1], n0 = an[s], n1 = an[s + 1];
+            float2 A2p[SA];
+            float Ev[SA], nx[SA];
+#pragma unroll
+            for (int i = 0; i < SA; ++i) {
+                A2p[i] = make_float2(A2[s + i], A2[s + i]);
+                Ev[i] = E[s + i];
+                nx[i] = an[s + i];
+            }
 #pragma unroll
             for (int q = T / 4 - 1; q >= 0; --q) {
-                const float4 c40 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
-                const float4 c41 = *reinterpret_cast<const float4*>(CT + (n + 1) * T + 4 * q);
+                float4 c4[SA];
+#pragma unroll
+                for (int i = 0; i < SA; ++i) c4[i] = *reinterpret_cast<const float4*>(CT + (n + i) * T + 4 * q);
 #pragma unroll
                 for (int h2 = 1; h2 >= 0; --h2) {
                     const int m = 2 * q + h2;
-                    const float2 cc0 = h2 ? make_float2(c40.z, c40.w) : make_float2(c40.x, c40.y);
-                    const float2 cc1 = h2 ? make_float2(c41.z, c41.w) : make_float2(c41.x, c41.y);
-                    const float2 arg0 = __fmul2_rn(Dl[m], A2p0), arg1 = __fmul2_rn(Dl[m], A2p1);
-                    const float2 r0 = __fmul2_rn(Pl[m], cc0), r1 = __fmul2_rn(Pl[m], cc1);
-                    const float a01 = ex2(arg0.y), a11 = ex2(arg1.y);
-                    E0 = __fmaf_rn(n0, E0, r0.y);
-                    E1 = __fmaf_rn(n1, E1, r1.y);
-                    const float a00 = ex2(arg0.x), a10 = ex2(arg1.x);
-                    E0 = __fmaf_rn(a01, E0, r0.x);
-                    E1 = __fmaf_rn(a11, E1, r1.x);
-                    n0 = a00;
-                    n1 = a10;
+#pragma unroll
+                    for (int i = 0; i < SA; ++i) {
+                        const float2 cc = h2 ? make_float2(c4[i].z, c4[i].w) : make_float2(c4[i].x, c4[i].y);
+                        const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
+                        const float2 r = __fmul2_rn(Pl[m], cc);
+                        const float a1 = ex2(arg.y), a0 = ex2(arg.x);
+                        Ev[i] = __fmaf_rn(nx[i], Ev[i], r.y);
+                        Ev[i] = __fmaf_rn(a1, Ev[i], r.x);
+                        nx[i] = a0;
+                    }
                 }
             }
-            E[s] = E0; E[s + 1] = E1; an[s] = n0; an[s + 1] = n1;
+#pragma unroll
+            for (int i = 0; i < SA; ++i) {
+                E[s + i] = Ev[i];
+                an[s + i] = nx[i];
+            }
         }
         __syncthreads();
     }

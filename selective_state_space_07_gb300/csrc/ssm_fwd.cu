@@ -4,9 +4,10 @@
 // Recurrence (rustytorch commit log, "MambaBlock" S6 forward commit:
 // "sequential scan h=dA.h+dBu, y=sum C.h + D.u -> gate by SiLU(z)"):
 // per (b, d) channel the 16 states are an independent first-order linear
-// recurrence in t. Lanes l and l^16 of a warp share one channel: lane l
-// holds states 8*(l>>4) .. 8*(l>>4)+7 in registers and walks the tokens in
-// order. Tiles of 16 tokens x 64 channels of x, z, dt and the 16-wide B_t /
+// recurrence in t. kFwdLPC lanes of a warp share one channel (lanes l,
+// l + 32/kFwdLPC, ...): each holds 16/kFwdLPC of its states in registers and
+// walks the tokens in order. Tiles of 16 tokens x 32 channels of x, z, dt and
+// the 16-wide B_t /
 // C_t rows are staged into shared memory by TMA (one thread issues a tile's
 // boxes onto the stage's mbarrier; four tiles in flight); B/C are widened to
 // fp32 and transposed (state-major) once per
@@ -14,13 +15,13 @@
 // 16-byte load. Delta*A, u*B and the readout are packed over token pairs
 // (f32x2); each state's update is a scalar fused multiply-add chain.
 //
-// Per tile: (A) each lane prepares Delta, u and the gate factor for its 8
-// tokens (one lane of the pair per token, two tokens per packed f32x2
-// operation) and shares Delta/u with its partner through shared memory;
-// (S) the lane's 8 state recurrences advance side by side through the 16
-// tokens (independent chains for the scheduler) while the readout chain
-// takes the states in order; (E) the two half-readouts of each token are
-// added and each lane gates and writes y for its 8 tokens.
+// Per tile: (A) each lane prepares Delta, u and the gate factor for its
+// share of the tokens (one lane of the channel per token, two tokens per
+// packed f32x2 operation) and shares Delta/u with the channel's other lanes
+// through shared memory; (S) the lane's state recurrences advance side by
+// side through the 16 tokens (independent chains for the scheduler) while
+// its readout chain takes them in order; (E) the partial readouts of each
+// token are summed and each lane gates and writes y for its tokens.
 //
 // One block barrier per tile: the tables a tile writes (B^T, C^T, Delta/u)
 // are double-buffered by tile parity, so the barrier after (A) of tile j
@@ -30,9 +31,11 @@
 // only.
 //
 // Canonical readout order (the step kernel evaluates the same operations):
-// each half of the states is a sequential fused multiply-add chain
-// C_0 h_0 -> fma(C_1, h_1, .) -> ... -> fma(C_7, h_7, .), and the two halves
-// are added; p + D x is fused, then multiplied by z * sigmoid(z).
+// the states split into kFwdLPC blocks of 16/kFwdLPC consecutive states; each
+// block is a sequential fused multiply-add chain C_n h_n -> fma(C_n+1,
+// h_n+1, .) -> ...; the blocks are summed as a balanced binary tree in state
+// order ((b0 + b1) + (b2 + b3) for four blocks); p + D x is fused, then
+// multiplied by z * sigmoid(z).
 //
 // Parallelism along L: the sequence splits into G groups. A first pass
 // (AGG) runs every group but the last from a zero state and publishes its
@@ -46,9 +49,15 @@ namespace ssm {
 
 namespace {
 
+// Lane layout: the kFwdLPC lanes l, l + 32/kFwdLPC, ... of a warp share one
+// channel; each holds NS = 16/kFwdLPC of its states and does the per-token
+// work of TPL = 16/kFwdLPC of a tile's tokens.
+constexpr int kLPC = kFwdLPC;
+constexpr int kCPW = 32 / kLPC;  // channels per warp
+
 template <typename IO> struct FwdLayout {
-    static constexpr int NT = kFwdThreads;
-    static constexpr int CH = NT / 2;             // channels per CTA (a lane pair per channel)
+    static constexpr int NT = kFwdCtaThreads;
+    static constexpr int CH = NT / kLPC;          // channels per CTA
     static constexpr int ES = sizeof(IO);
     static constexpr int XROW = CH * ES;          // staged row of x / z (bytes)
     static constexpr int DTROW = CH * 4;          // staged row of dt
@@ -63,10 +72,21 @@ template <typename IO> struct FwdLayout {
     static constexpr int SMEM = NSTAGE * STAGE + 128;  // dynamic shared memory (+ slack for 128-byte alignment)
     static_assert(OFF_Z % 128 == 0 && OFF_DT % 128 == 0 && OFF_B % 128 == 0 && OFF_C % 128 == 0 &&
                       STAGE % 128 == 0, "TMA destinations on 128-byte boundaries");
-    static constexpr int ROW = 2 * kCK + 4;       // per-channel row of DU / PB (floats, padded)
+    static constexpr int ROW = 2 * kCK + 4;       // per-channel row of DU: [Delta 0..15 | u 0..15], padded
+    static constexpr int PROW = kLPC * kCK + 4;   // per-channel row of PB: one 16-token row per lane, padded
 };
 
 __device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
+
+// Sum of a channel's kLPC partial readouts in the canonical order: a
+// balanced binary tree over the lanes' state blocks, in state order.
+template <int P> __device__ __forceinline__ float2 tree2(const float2* q) {
+    if constexpr (P == 1) {
+        return q[0];
+    } else {
+        return __fadd2_rn(tree2<P / 2>(q), tree2<P / 2>(q + P / 2));
+    }
+}
 
 // TMA descriptors of a tile's inputs: x, z, dt [B*L, D] in boxes of CH
 // channels x 16 tokens; B, C [B*L, 16] (rows bcs elements apart) in boxes of
@@ -75,16 +95,14 @@ struct FwdMaps {
     CUtensorMap x, z, dt, b, c;
 };
 
-// MINB: resident CTAs per SM the register budget is cut for (3 when the grid
-// can use a third CTA per SM; 1 -- no cut -- when one L-group's grid fits in
-// two CTAs per SM, which leaves the scheduler registers for the interleaved
-// state chains).
+// MINB: resident CTAs per SM the register budget is cut for.
 template <typename IO, bool AGG, int MINB>
-__global__ void __launch_bounds__(kFwdThreads, MINB)
+__global__ void __launch_bounds__(kFwdCtaThreads, MINB)
     ssm_fwd_kernel(const FwdParams p, const __grid_constant__ FwdMaps mp) {
     using Ly = FwdLayout<IO>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, ES = Ly::ES, T = kCK, NS = kN / 2;
+    constexpr int NT = Ly::NT, CH = Ly::CH, T = kCK, NS = kN / kLPC, TPL = kCK / kLPC;
     constexpr bool FAST = IOT<IO>::kFast;
+    static_assert(NS % 2 == 0 && TPL % 4 == 0, "states and tokens per lane in pairs / quads");
     extern __shared__ __align__(128) char smem_raw[];
     char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
     __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];          // a stage's copies landed
@@ -93,11 +111,11 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
     __shared__ __align__(16) float BT[2][kN * T];                 // B^T of the tile [state][token]
     __shared__ __align__(16) float CT[2][AGG ? 4 : kN * T];
     __shared__ __align__(16) float DU[2][CH * Ly::ROW];           // per channel [Delta 0..15 | u 0..15]
-    __shared__ __align__(16) float PB[AGG ? 4 : CH * Ly::ROW];    // per channel [half-0 readouts | half-1]
+    __shared__ __align__(16) float PB[AGG ? 4 : CH * Ly::PROW];   // per channel, per lane: partial readouts
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int hk = lane >> 4;                 // states 8*hk .. 8*hk+7; tokens 8*hk .. 8*hk+7 of the tile
-    const int c = warp * 16 + (lane & 15);    // channel within the CTA
+    const int hk = lane / kCPW;                    // states NS*hk ..; tokens TPL*hk .. of the tile
+    const int c = warp * kCPW + (lane % kCPW);     // channel within the CTA
     const int64_t D = p.D, L = p.L;
     const int64_t d0 = (int64_t)blockIdx.x * CH, d = d0 + c;
     const bool dv = d < D;
@@ -122,7 +140,6 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
     }
     const float Dd = (dv && p.Dskip) ? p.Dskip[d] : 0.f;
     const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
-
     const float2 D2 = f2(Dd, Dd), bias2 = f2(bias, bias);
     const unsigned long long wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
 
@@ -181,15 +198,15 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
                 if (!AGG) CT[buf][i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
             }
         }
-        // ---- A: Delta, u and the gate factor of this lane's 8 tokens, a
+        // ---- A: Delta, u and the gate factor of this lane's TPL tokens, a
         // token pair at a time; tokens past the end act as identity (Delta = u = 0)
         float* du = DU[buf] + c * Ly::ROW;
-        float2 xo[NS / 2], gz[NS / 2];
+        float2 xo[TPL / 2], gz[TPL / 2];
         {
-            float2 dl[NS / 2], ul[NS / 2];
+            float2 dl[TPL / 2], ul[TPL / 2];
 #pragma unroll
-            for (int i = 0; i < NS / 2; ++i) {
-                const int t = NS * hk + 2 * i;
+            for (int i = 0; i < TPL / 2; ++i) {
+                const int t = TPL * hk + 2 * i;
                 const char* xr = st + Ly::OFF_X + t * Ly::XROW;
                 const float2 xv = f2(IOT<IO>::to_f(reinterpret_cast<const IO*>(xr)[c]),
                                      IOT<IO>::to_f(reinterpret_cast<const IO*>(xr + Ly::XROW)[c]));
@@ -209,10 +226,13 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
                     gz[i] = __fmul2_rn(zv, sigmoid2<FAST>(zv));
                 }
             }
-            *reinterpret_cast<float4*>(du + NS * hk) = make_float4(dl[0].x, dl[0].y, dl[1].x, dl[1].y);
-            *reinterpret_cast<float4*>(du + NS * hk + 4) = make_float4(dl[2].x, dl[2].y, dl[3].x, dl[3].y);
-            *reinterpret_cast<float4*>(du + T + NS * hk) = make_float4(ul[0].x, ul[0].y, ul[1].x, ul[1].y);
-            *reinterpret_cast<float4*>(du + T + NS * hk + 4) = make_float4(ul[2].x, ul[2].y, ul[3].x, ul[3].y);
+#pragma unroll
+            for (int i = 0; i < TPL / 4; ++i) {
+                *reinterpret_cast<float4*>(du + TPL * hk + 4 * i) =
+                    make_float4(dl[2 * i].x, dl[2 * i].y, dl[2 * i + 1].x, dl[2 * i + 1].y);
+                *reinterpret_cast<float4*>(du + T + TPL * hk + 4 * i) =
+                    make_float4(ul[2 * i].x, ul[2 * i].y, ul[2 * i + 1].x, ul[2 * i + 1].y);
+            }
         }
         if (__syncthreads_or(late)) {  // the tables of this tile are ready -- unless a copy never came
             aborted = true;
@@ -229,101 +249,99 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
             Ul[2 * q + 1] = f2(uq.z, uq.w);
         }
 
-        // ---- S: per state, the tile's 16 tokens; the readout chain runs
-        // over this lane's 8 states
+        // ---- S: this lane's NS states advance together through the tile's
+        // 16 tokens; the readout chain takes them in order
         const bool ck = !AGG && p.ckpt && dv;
         // checkpoint [B][nck][8 state pairs][D][2]: pair (n, n+1) of channel d
         float* ckp = ck ? p.ckpt + (((b * nck + t0 / kCkpt) * (kN / 2) + NS * hk / 2) * D + d) * 2 : nullptr;
         const float* BTb = BT[buf];
         const float* CTb = CT[buf];
+        const int n0 = NS * hk;
         float2 acc[T / 2];
-        // SI states advance together through the tokens (independent chains
-        // for the scheduler); the readout chain still takes the states in order
-        constexpr int SI = 8;
+        float2 A2p[NS];
+        float hp[NS];
 #pragma unroll
-        for (int s = 0; s < NS; s += SI) {
-            const int n = NS * hk + s;
-            float2 A2p[SI];
-            float hp[SI];
-#pragma unroll
-            for (int i = 0; i < SI; ++i) {
-                A2p[i] = f2(A2[s + i], A2[s + i]);
-                hp[i] = h[s + i];
-            }
-            if (ck) {  // states before token t0
-#pragma unroll
-                for (int i = 0; i < SI; i += 2) *reinterpret_cast<float2*>(ckp + (int64_t)((s + i) / 2) * D * 2) = f2(hp[i], hp[i + 1]);
-            }
-#pragma unroll
-            for (int q = 0; q < T / 4; ++q) {
-                float4 b4[SI], c4[SI];
-#pragma unroll
-                for (int i = 0; i < SI; ++i) {
-                    b4[i] = *reinterpret_cast<const float4*>(BTb + (n + i) * T + 4 * q);
-                    if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CTb + (n + i) * T + 4 * q);
-                }
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int m = 2 * q + h2;
-                    float hv0[SI], hv1[SI];
-#pragma unroll
-                    for (int i = 0; i < SI; ++i) {
-                        const float2 bb = h2 ? f2(b4[i].z, b4[i].w) : f2(b4[i].x, b4[i].y);
-                        const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
-                        const float a0 = ex2(arg.x), a1 = ex2(arg.y);
-                        const float2 ub = __fmul2_rn(Ul[m], bb);
-                        hv0[i] = __fmaf_rn(a0, hp[i], ub.x);
-                        hv1[i] = __fmaf_rn(a1, hv0[i], ub.y);
-                        hp[i] = hv1[i];
-                    }
-                    if (!AGG) {
-                        float2 r = acc[m];
-#pragma unroll
-                        for (int i = 0; i < SI; ++i) {
-                            const float2 cc = h2 ? f2(c4[i].z, c4[i].w) : f2(c4[i].x, c4[i].y);
-                            r = (s + i == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i])) : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r);
-                        }
-                        acc[m] = r;
-                    }
-                }
-                if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
-#pragma unroll
-                    for (int i = 0; i < SI; i += 2)
-                        *reinterpret_cast<float2*>(ckp + (int64_t)((s + i) / 2) * D * 2 + (int64_t)kN * D) = f2(hp[i], hp[i + 1]);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < SI; ++i) h[s + i] = hp[i];
+        for (int i = 0; i < NS; ++i) {
+            A2p[i] = f2(A2[i], A2[i]);
+            hp[i] = h[i];
         }
+        if (ck) {  // states before token t0
+#pragma unroll
+            for (int i = 0; i < NS; i += 2) *reinterpret_cast<float2*>(ckp + (int64_t)(i / 2) * D * 2) = f2(hp[i], hp[i + 1]);
+        }
+#pragma unroll
+        for (int q = 0; q < T / 4; ++q) {
+            float4 b4[NS], c4[NS];
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                b4[i] = *reinterpret_cast<const float4*>(BTb + (n0 + i) * T + 4 * q);
+                if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CTb + (n0 + i) * T + 4 * q);
+            }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int m = 2 * q + h2;
+                float hv0[NS], hv1[NS];
+#pragma unroll
+                for (int i = 0; i < NS; ++i) {
+                    const float2 bb = h2 ? f2(b4[i].z, b4[i].w) : f2(b4[i].x, b4[i].y);
+                    const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
+                    const float a0 = ex2(arg.x), a1 = ex2(arg.y);
+                    const float2 ub = __fmul2_rn(Ul[m], bb);
+                    hv0[i] = __fmaf_rn(a0, hp[i], ub.x);
+                    hv1[i] = __fmaf_rn(a1, hv0[i], ub.y);
+                    hp[i] = hv1[i];
+                }
+                if (!AGG) {
+                    float2 r = f2(0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < NS; ++i) {
+                        const float2 cc = h2 ? f2(c4[i].z, c4[i].w) : f2(c4[i].x, c4[i].y);
+                        r = (i == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i])) : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r);
+                    }
+                    acc[m] = r;
+                }
+            }
+            if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
+#pragma unroll
+                for (int i = 0; i < NS; i += 2)
+                    *reinterpret_cast<float2*>(ckp + (int64_t)(i / 2) * D * 2 + (int64_t)kN * D) = f2(hp[i], hp[i + 1]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < NS; ++i) h[i] = hp[i];
         if (!AGG) {
-            // ---- E: half readouts -> full readout of this lane's 8 tokens
-            float* pb = PB + c * Ly::ROW;
+            // ---- E: the kLPC partial readouts of this lane's TPL tokens
+            float* pb = PB + c * Ly::PROW;
             __syncwarp();  // the previous tile's reads of PB are done
-            *reinterpret_cast<float4*>(pb + T * hk) = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
-            *reinterpret_cast<float4*>(pb + T * hk + 4) = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
-            *reinterpret_cast<float4*>(pb + T * hk + 8) = make_float4(acc[4].x, acc[4].y, acc[5].x, acc[5].y);
-            *reinterpret_cast<float4*>(pb + T * hk + 12) = make_float4(acc[6].x, acc[6].y, acc[7].x, acc[7].y);
+#pragma unroll
+            for (int q = 0; q < T / 4; ++q)
+                *reinterpret_cast<float4*>(pb + T * hk + 4 * q) =
+                    make_float4(acc[2 * q].x, acc[2 * q].y, acc[2 * q + 1].x, acc[2 * q + 1].y);
             __syncwarp();
-            const float4 p0a = *reinterpret_cast<const float4*>(pb + NS * hk);
-            const float4 p0b = *reinterpret_cast<const float4*>(pb + NS * hk + 4);
-            const float4 p1a = *reinterpret_cast<const float4*>(pb + T + NS * hk);
-            const float4 p1b = *reinterpret_cast<const float4*>(pb + T + NS * hk + 4);
-            const float2 P0[NS / 2] = {f2(p0a.x, p0a.y), f2(p0a.z, p0a.w), f2(p0b.x, p0b.y), f2(p0b.z, p0b.w)};
-            const float2 P1[NS / 2] = {f2(p1a.x, p1a.y), f2(p1a.z, p1a.w), f2(p1b.x, p1b.y), f2(p1b.z, p1b.w)};
             IO* yrow = reinterpret_cast<IO*>(p.y) + (b * L + t0) * D + d;
 #pragma unroll
-            for (int i = 0; i < NS / 2; ++i) {
-                const int t = NS * hk + 2 * i;
-                const float2 pr = __fadd2_rn(P0[i], P1[i]);
-                const float2 pp = __ffma2_rn(D2, xo[i], pr);
-                const float2 yv = has_z ? __fmul2_rn(pp, gz[i]) : pp;
-                if (dv && t < rows) {
-                    nf = __fmaf_rn(yv.x, 0.0f, nf);
-                    yrow[(int64_t)t * D] = IOT<IO>::from_f(yv.x);
+            for (int i = 0; i < TPL / 4; ++i) {
+                float2 qa[kLPC], qb[kLPC];  // tokens TPL*hk + 4i + (0, 1) and (2, 3), one per lane block
+#pragma unroll
+                for (int r = 0; r < kLPC; ++r) {
+                    const float4 v = *reinterpret_cast<const float4*>(pb + T * r + TPL * hk + 4 * i);
+                    qa[r] = f2(v.x, v.y);
+                    qb[r] = f2(v.z, v.w);
                 }
-                if (dv && t + 1 < rows) {
-                    nf = __fmaf_rn(yv.y, 0.0f, nf);
-                    yrow[(int64_t)(t + 1) * D] = IOT<IO>::from_f(yv.y);
+                const float2 pr[2] = {tree2<kLPC>(qa), tree2<kLPC>(qb)};
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int t = TPL * hk + 4 * i + 2 * k2;
+                    const float2 pp = __ffma2_rn(D2, xo[2 * i + k2], pr[k2]);
+                    const float2 yv = has_z ? __fmul2_rn(pp, gz[2 * i + k2]) : pp;
+                    if (dv && t < rows) {
+                        nf = __fmaf_rn(yv.x, 0.0f, nf);
+                        yrow[(int64_t)t * D] = IOT<IO>::from_f(yv.x);
+                    }
+                    if (dv && t + 1 < rows) {
+                        nf = __fmaf_rn(yv.y, 0.0f, nf);
+                        yrow[(int64_t)(t + 1) * D] = IOT<IO>::from_f(yv.y);
+                    }
                 }
             }
         }
@@ -341,7 +359,8 @@ __global__ void __launch_bounds__(kFwdThreads, MINB)
         return;
     }
     if (AGG) {
-        ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, 16));
+#pragma unroll
+        for (int off = kCPW; off < 32; off <<= 1) ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, off));
         if (dv) {
             float* H = p.aggH + ((b * p.G + g) * D + d) * kN + NS * hk;
 #pragma unroll
@@ -436,14 +455,21 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     const float delta = token_delta<FAST>(dtv, bias, p.sp != 0);
     const float u = __fmul_rn(delta, xv);
     float* st = p.state + (b * D + (dv ? d : 0)) * kN;
-    float half[2] = {0.f, 0.f};
+    // the forward's readout order: blocks of BS states, each a sequential
+    // fused multiply-add chain C_0 h_0 -> fma(C_1, h_1, .) -> ...; the blocks
+    // summed as a balanced binary tree in state order (its top level: one
+    // half of the blocks + the other)
+    constexpr int BS = kN / kLPC, NB = kLPC, HB = NB / 2;
+    float part[NB];
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        if (NSPLIT == 2 && hf != k) continue;
+    for (int blk = 0; blk < NB; ++blk) part[blk] = 0.f;
+#pragma unroll
+    for (int blk = 0; blk < NB; ++blk) {
+        if (NSPLIT == 2 && blk / HB != k) continue;
         float acc = 0.f;
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-            const int n = 8 * hf + s;
+        for (int s = 0; s < BS; ++s) {
+            const int n = BS * blk + s;
             const float A2 = dv ? __fmul_rn(p.A[d * kN + n], kLog2e) : 0.f;
             const float a = ex2(__fmul_rn(delta, A2));
             const float ub = __fmul_rn(u, Bs[n]);
@@ -451,13 +477,17 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
             if (dv) st[n] = hv;
             acc = s == 0 ? __fmul_rn(Cs[n], hv) : __fmaf_rn(Cs[n], hv, acc);
         }
-        half[hf] = acc;
+        part[blk] = acc;
     }
+#pragma unroll
+    for (int w = 1; w < HB; w <<= 1)
+#pragma unroll
+        for (int i = 0; i < NB; i += 2 * w) part[i] = __fadd_rn(part[i], part[i + w]);
     float pr;
     if (NSPLIT == 1) {
-        pr = __fadd_rn(half[0], half[1]);
+        pr = __fadd_rn(part[0], part[HB]);
     } else {
-        const float mine = half[k];
+        const float mine = part[k * HB];
         pr = __fadd_rn(mine, __shfl_xor_sync(0xffffffffu, mine, 1));  // addition commutes: same bits in both lanes
     }
     const bool has_z = p.has_z != 0;
@@ -473,7 +503,7 @@ int launch_fwd_v(const FwdParams& p, const FwdMaps& mp, dim3 grid, cudaStream_t 
     static unsigned long long mask = 0;
     auto kern = ssm_fwd_kernel<IO, AGG, MINB>;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
-    kern<<<grid, kFwdThreads, Ly::SMEM, s>>>(p, mp);
+    kern<<<grid, kFwdCtaThreads, Ly::SMEM, s>>>(p, mp);
     return cudaGetLastError() == cudaSuccess ? 1 : -1;
 }
 
@@ -501,6 +531,9 @@ template <typename IO, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream
     if (!encode_fwd_maps<IO>(p, !AGG, &mp)) return -1;
     dim3 grid((unsigned)((p.D + Ly::CH - 1) / Ly::CH), (unsigned)gy, (unsigned)p.B);
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
+    // the register budget: uncut when one L-group's grid fits in two CTAs
+    // per SM (the scheduler gets registers for the interleaved state
+    // chains), else cut to three CTAs per SM
     if (!AGG && p.G == 1 && ctas <= 2 * (int64_t)sm_count()) return launch_fwd_v<IO, AGG, 1>(p, mp, grid, s);
     return launch_fwd_v<IO, AGG, 3>(p, mp, grid, s);
 }
@@ -534,8 +567,9 @@ template <typename K> int blocks_per_sm(K kern, int threads, int smem, int* cach
 int fwd_blocks_per_sm(int io) {
     static int cache_f[64] = {0}, cache_b[64] = {0};
     // the variant that runs whenever the grid can use more than 2 CTAs per SM
-    return io == 0 ? blocks_per_sm(ssm_fwd_kernel<float, false, 3>, kFwdThreads, FwdLayout<float>::SMEM, cache_f)
-                   : blocks_per_sm(ssm_fwd_kernel<__nv_bfloat16, false, 3>, kFwdThreads,
+    // the variant that runs whenever the grid can use more than 2 CTAs per SM
+    return io == 0 ? blocks_per_sm(ssm_fwd_kernel<float, false, 3>, kFwdCtaThreads, FwdLayout<float>::SMEM, cache_f)
+                   : blocks_per_sm(ssm_fwd_kernel<__nv_bfloat16, false, 3>, kFwdCtaThreads,
                                    FwdLayout<__nv_bfloat16>::SMEM, cache_b);
 }
 int fwd_channels_per_cta() { return FwdLayout<float>::CH; }

@@ -13,14 +13,14 @@ namespace ssm {
 constexpr unsigned kStatusNonFinite = 1u;  // workspace status bit: an output was Inf/NaN
 constexpr unsigned kStatusTimeout = 2u;    // workspace status bit: a bounded wait inside a kernel ran out
 constexpr int kFwdThreads = 128;  // ssm_step_kernel
-#ifndef SSM_FWD_SL
-#define SSM_FWD_SL 4
+#ifndef SSM_FWD_LPC
+#define SSM_FWD_LPC 2
 #endif
+constexpr int kFwdLPC = SSM_FWD_LPC;  // forward: lanes sharing one channel (16/kFwdLPC states each)
 #ifndef SSM_FWD_WARPS
-#define SSM_FWD_WARPS 2
+#define SSM_FWD_WARPS 4
 #endif
-constexpr int kFwdSL = SSM_FWD_SL;        // forward: states per lane of each of its two channels (2, 4 or 8)
-constexpr int kFwdWarps = SSM_FWD_WARPS;  // warps per forward CTA (each warp scans its channels on its own)
+constexpr int kFwdCtaThreads = 32 * SSM_FWD_WARPS;  // threads of a forward / aggregate CTA
 constexpr int kBwdThreads = 128;
 constexpr int kConvThreads = 128;
 

@@ -17,9 +17,13 @@
 //   ssm_scan_fwd does, but never more than the array can hold; an explicit
 //   groups whose carries do not fit is rejected with SSM_ERR_SCRATCH_LIMIT
 //   before anything is launched.
-// - The first call on each device looks up the array's device address
-//   (cudaGetSymbolAddress, with that device current) and caches it; make
-//   that first call before any stream capture.
+// - The first call in each CUDA context (one per device for the runtime's
+//   primary contexts) looks up the array's device address
+//   (cudaGetSymbolAddress, with that device current) and caches it under
+//   the context's unique ID; make that first call before any stream
+//   capture. A context that is destroyed and created again (after
+//   cudaDeviceReset, say) gets a new ID, so the address is looked up again
+//   instead of reusing one from the old context.
 // - All calls share the array and it keeps the last call's contents. The
 //   kernels overwrite every carry they read, and the status word is zeroed
 //   at the start of each call. Calls whose work overlaps on the GPU (other
@@ -28,6 +32,7 @@
 //   passes one (>= 256 bytes, read it with ssm_poll_status); otherwise they
 //   are latched in the array, which the caller cannot read.
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <cstdint>
@@ -47,20 +52,57 @@ constexpr size_t kStatus = 256;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[256] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up once
-// per device with that device current). nullptr on failure.
+// Unique ID of the calling thread's current CUDA context (the driver's
+// cuCtxGetId, reached through the runtime's entry-point query so that the
+// library needs no link to libcuda); false when it is not available.
+bool current_context_id(unsigned long long* id) {
+    static const auto fns = [] {
+        void* get = nullptr;
+        void* gid = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &get, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            get = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &gid, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            gid = nullptr;
+        return std::make_pair(reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(get),
+                              reinterpret_cast<PFN_cuCtxGetId_v12000>(gid));
+    }();
+    if (!fns.first || !fns.second) return false;
+    CUcontext ctx = nullptr;
+    if (fns.first(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return fns.second(ctx, id) == CUDA_SUCCESS;
+}
+
+// Looked-up addresses, keyed by context ID (or, when the driver gives no
+// context IDs, by device ordinal + 1 with the top bit set).
+struct ScratchEntry {
+    unsigned long long key;
+    void* addr;
+};
+ScratchEntry g_scratch_cache[64] = {};
+int g_scratch_next = 0;
+
+// Device address of g_noalloc_scratch in the current context (looked up
+// once per context, with the device current). nullptr on failure.
 void* scratch_on_current_device() {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return nullptr;
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
-        g_scratch_addr[dev] = p;
-    }
-    return g_scratch_addr[dev];
+    unsigned long long key = 0;
+    bool have = current_context_id(&key);
+    if (have)
+        for (const ScratchEntry& e : g_scratch_cache)
+            if (e.addr && e.key == key) return e.addr;
+    void* p = nullptr;  // (the lookup also brings up the device's primary context when it has none yet)
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    if (!have) have = current_context_id(&key);
+    if (!have) key = (1ull << 63) | (unsigned long long)(dev + 1);
+    g_scratch_cache[g_scratch_next] = ScratchEntry{key, p};
+    g_scratch_next = (g_scratch_next + 1) % 64;
+    return p;
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -79,6 +121,7 @@ bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 1
 }  // namespace
 
 extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
+    ssm::reset_launches();
     if (!a) return SSM_ERR_INVALID_ARG;
     if (a->B < 0 || a->L < 0 || a->D < 0 || a->N < 0) return SSM_ERR_INVALID_ARG;
     if (a->N != 16) return SSM_ERR_UNSUPPORTED;
@@ -149,11 +192,14 @@ extern "C" int ssm_scan_fwd_noalloc(const ssm_fwd_args* a, void* stream) {
     p.aggH = (float*)(scratch + kStatus);
     p.aggS = (float*)(scratch + kStatus + nv);
     p.status = status;
+    int rc;
     if (G > 1) {
         float* carry = (float*)(scratch + kStatus + nv + ns);
-        if (ssm::launch_fwd_agg(a->io_dtype, p, s) < 0) return SSM_ERR_CUDA;
-        if (ssm::launch_carry(B, D, G, false, a->A, a->h0, p.aggH, p.aggS, carry, s) < 0) return SSM_ERR_CUDA;
+        if ((rc = ssm::count_launches(ssm::launch_fwd_agg(a->io_dtype, p, s))) != SSM_OK) return rc;
+        if ((rc = ssm::count_launches(ssm::launch_carry(B, D, G, false, a->A, a->h0, p.aggH, p.aggS, carry, s))) !=
+            SSM_OK)
+            return rc;
         p.hstart = carry;
     }
-    return ssm::launch_fwd(a->io_dtype, p, s) < 0 ? SSM_ERR_CUDA : SSM_OK;
+    return ssm::count_launches(ssm::launch_fwd(a->io_dtype, p, s));
 }
