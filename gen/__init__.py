@@ -264,6 +264,62 @@ def make_dtproj_inputs(B: int, L: int, D: int, R: int, *, seed: int = 0) -> DtPr
     return DtProjInputs(B, L, D, R, a, w, bias, ddelta)
 
 
+@dataclass
+class Gdn2Inputs:
+    """One problem for the Gated DeltaNet-2 chunkwise forward (layout
+    [batch, heads, time, dim] as on its page): q, k, g, b [B,H,T,K]; v, w
+    [B,H,T,V]; state [B,H,K,V]; scale."""
+    B: int
+    H: int
+    T: int
+    K: int
+    V: int
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    g: np.ndarray
+    b: np.ndarray
+    w: np.ndarray
+    state: np.ndarray
+    scale: float
+
+
+GDN2_WORKLOADS = {
+    # name: (B, H, T, K, V, seed); chunks of 64 tokens
+    "gdn2-small": (1, 2, 200, 32, 32, 11),
+    "gdn2-1.3b-like": (8, 16, 2048, 128, 128, 12),
+}
+
+
+def make_gdn2_inputs(B: int, H: int, T: int, K: int, V: int, *, seed: int = 0, io: str = "bf16",
+                     with_state: bool = True, key_uniform_gates: bool = False) -> Gdn2Inputs:
+    """Draw a Gated DeltaNet-2 problem: q, k ~ N(0, 1/K) (so q.k ~ N(0,1));
+    v ~ N(0,1); the log-gates g uniform in [-0.3, -0.001] per (token, key
+    channel) (one value per token, shared by all key channels, with
+    key_uniform_gates); the erase gates b and write gates w uniform in
+    (0, 1); the initial state ~ N(0, 0.1^2) (zeros without with_state);
+    scale = 1/sqrt(K). With io = "bf16", q, k, v, b, w are rounded to
+    bfloat16 once; g and the state stay float32. Per-tensor seeds from the
+    same SplitMix64 streams as make_inputs (x, z, Bm, Cm, dt, dy, h0, dh_last
+    slots in order)."""
+    s = tensor_seeds(seed)
+    nk, nv = B * H * T * K, B * H * T * V
+    rnd = round_bf16 if io == "bf16" else (lambda a: np.asarray(a, np.float32))
+    q = rnd(normal_f32(s["x"], nk, 0.0, float(1.0 / np.sqrt(K)))).reshape(B, H, T, K)
+    k = rnd(normal_f32(s["z"], nk, 0.0, float(1.0 / np.sqrt(K)))).reshape(B, H, T, K)
+    v = rnd(normal_f32(s["Bm"], nv)).reshape(B, H, T, V)
+    if key_uniform_gates:
+        gt = (-0.001 - 0.299 * uniform53(s["Cm"], B * H * T)).astype(np.float32).reshape(B, H, T, 1)
+        g = np.ascontiguousarray(np.broadcast_to(gt, (B, H, T, K)))
+    else:
+        g = (-0.001 - 0.299 * uniform53(s["Cm"], nk)).astype(np.float32).reshape(B, H, T, K)
+    b = rnd(uniform53(s["dt"], nk).astype(np.float32)).reshape(B, H, T, K)
+    w = rnd(uniform53(s["dy"], nv).astype(np.float32)).reshape(B, H, T, V)
+    state = (normal_f32(s["h0"], B * H * K * V, 0.0, 0.1).reshape(B, H, K, V) if with_state
+             else np.zeros((B, H, K, V), np.float32))
+    return Gdn2Inputs(B, H, T, K, V, q, k, v, g, b, w, state, float(1.0 / np.sqrt(K)))
+
+
 def recipe_text() -> str:
     lines = []
     for w in WORKLOADS.values():
