@@ -286,7 +286,7 @@ class Gdn2Inputs:
 
 GDN2_WORKLOADS = {
     # name: (B, H, T, K, V, seed); chunks of 64 tokens
-    "gdn2-small": (1, 2, 200, 32, 32, 11),
+    "gdn2-small": (1, 2, 200, 128, 128, 11),
     "gdn2-1.3b-like": (8, 16, 2048, 128, 128, 12),
 }
 

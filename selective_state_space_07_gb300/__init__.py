@@ -28,6 +28,7 @@ __all__ = [
     "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
     "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
+    "gdn2_fwd", "GDN2_CHUNK",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -90,6 +91,14 @@ class DtProjBwdArgs(ctypes.Structure):
     _fields_ = [("f", DtProjArgs)] + [(n, ctypes.c_void_p) for n in ("ddelta", "dpre", "dbias")]
 
 
+class Gdn2Args(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("V", ctypes.c_int64), ("chunk", ctypes.c_int32), ("scale", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "b", "w", "state_in", "out", "state_out", "workspace")]
+
+
+GDN2_CHUNK = 64
+
 EXPORTS = {
     "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
@@ -109,6 +118,7 @@ EXPORTS = {
     "ssm_dA_log_grad": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
                         ctypes.c_int),
     "ssm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
+    "gdn2_chunk_fwd": ([ctypes.POINTER(Gdn2Args), ctypes.c_void_p], ctypes.c_int),
 }
 
 
@@ -516,6 +526,40 @@ def dtproj_bwd(a, w, ddelta, bias=None, softplus=True, *, dpre=None, inplace=Fal
     bargs = DtProjBwdArgs(f=args, ddelta=_p(ddelta), dpre=_p(dpre), dbias=_p(dbias))
     _check(lib().ssm_dtproj_bwd(ctypes.byref(bargs), _stream(a.device, stream)), "ssm_dtproj_bwd")
     return {"dpre": dpre, "dbias": dbias}
+
+
+def gdn2_fwd(q, k, v, g, b, w, state=None, scale=None, *, out=None, state_out=None, want_state=True,
+             workspace=None, stream=None):
+    """Gated DeltaNet-2 chunkwise forward (C ABI in ``include/gdn2.h``; docs.rs, burn-gdn2 0.1.4,
+    src/forward.rs, chunk_wy_forward) on the tensor cores, chunks of 64 tokens.
+    q, k, b [B, H, T, 128] bf16; g [B, H, T, 128] fp32 log-gates; v, w [B, H, T, 128] bf16;
+    state [B, H, 128, 128] fp32 or None (zeros); scale defaults to 1/sqrt(K).
+    Returns (out [B, H, T, V] bf16, final state [B, H, K, V] fp32 or None)."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, K]")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("the GDN2 forward runs on a CUDA device; q is on " + str(dev))
+    Bn, H, T, K = q.shape
+    V = v.shape[-1] if v.dim() == 4 else -1
+    bf, f32 = torch.bfloat16, torch.float32
+    for t, n in ((q, "q"), (k, "k"), (b, "b")):
+        _need(t, n, (Bn, H, T, K), bf, dev)
+    _need(g, "g", (Bn, H, T, K), f32, dev)
+    for t, n in ((v, "v"), (w, "w")):
+        _need(t, n, (Bn, H, T, V), bf, dev)
+    _opt(state, "state", (Bn, H, K, V), f32, dev)
+    out = torch.empty((Bn, H, T, V), dtype=bf, device=dev) if out is None else out
+    _need(out, "out", (Bn, H, T, V), bf, dev)
+    if want_state and state_out is None:
+        state_out = torch.empty((Bn, H, K, V), dtype=f32, device=dev)
+    _opt(state_out, "state_out", (Bn, H, K, V), f32, dev)
+    args = Gdn2Args(B=Bn, H=H, T=T, K=K, V=V, chunk=GDN2_CHUNK,
+                    scale=float(K ** -0.5 if scale is None else scale),
+                    q=_p(q), k=_p(k), v=_p(v), g=_p(g), b=_p(b), w=_p(w), state_in=_p(state), out=_p(out),
+                    state_out=_p(state_out), workspace=None if workspace is None else workspace.buf.data_ptr())
+    _check(lib().gdn2_chunk_fwd(ctypes.byref(args), _stream(dev, stream)), "gdn2_chunk_fwd")
+    return out, state_out
 
 
 def poll_status(workspace, stream=None) -> int:

@@ -26,7 +26,7 @@ def declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b(ssm_\w+)\s*\(", text, flags=re.M))
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b((?:ssm|gdn2)_\w+)\s*\(", text, flags=re.M))
     return names
 
 
@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("ssm_scan_fwd", "ssm_scan_bwd", "ssm_step", "ssm_scan_workspace_bytes", "ssm_scan_ckpt_elems",
               "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad", "ssm_conv1d_fwd", "ssm_conv1d_bwd",
-              "ssm_dtproj_fwd", "ssm_dtproj_bwd"):
+              "ssm_dtproj_fwd", "ssm_dtproj_bwd", "gdn2_chunk_fwd"):
         assert n in names
 
 
@@ -192,7 +192,27 @@ def test_dtproj_bwd_rejects_bad_arguments(ssm):
     assert ssm.lib().ssm_dtproj_bwd(ctypes.byref(args), None) == UNSUPPORTED
 
 
+def gdn2_args(ssm, **over):
+    a = dict(B=2, H=3, T=100, K=128, V=128, chunk=64, scale=0.088, q=FAKE, k=FAKE + 4096, v=FAKE + 8192,
+             g=FAKE + 12288, b=FAKE + 16384, w=FAKE + 20480, state_in=None, out=FAKE + 24576, state_out=None,
+             workspace=None)
+    a.update(over)
+    return ssm.Gdn2Args(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), UNSUPPORTED), (dict(V=256), UNSUPPORTED), (dict(chunk=32), UNSUPPORTED), (dict(B=-1), INVALID),
+    (dict(T=-5), INVALID), (dict(q=None), INVALID), (dict(g=None), INVALID), (dict(out=None), INVALID),
+    (dict(w=FAKE + 2), ALIGNMENT), (dict(state_in=FAKE + 8), ALIGNMENT), (dict(state_out=FAKE + 4), ALIGNMENT),
+    (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+])
+def test_gdn2_rejects_bad_arguments(ssm, over, code):
+    args = gdn2_args(ssm, **over)
+    assert ssm.lib().gdn2_chunk_fwd(ctypes.byref(args), None) == code
+
+
 def test_null_args_struct(ssm):
+    assert ssm.lib().gdn2_chunk_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_bwd(None, None) == INVALID
     assert ssm.lib().ssm_step(None, None) == INVALID
