@@ -23,6 +23,10 @@ with its own metric, HBM roofline and oracle baseline.
 --op dtproj times the dt projection with its fused softplus on the tensor
 cores (ssm_dtproj_fwd + ssm_dtproj_bwd, dt_rank = D/32, a read in place from
 an x_proj-shaped buffer) on the workload's B*L tokens and D channels.
+
+--op gdn2 times the Gated DeltaNet-2 chunkwise forward (gdn2_chunk_fwd) on
+a GDN2 workload (default gdn2-1.3b-like: 8 x 16 heads x 2048 tokens,
+K = V = 128, chunks of 64): one step = one forward call.
 """
 from __future__ import annotations
 
@@ -137,6 +141,7 @@ CALL_SOURCES = {
     "ssm_conv1d_bwd": ("ssm_conv.cu", "ssm_common.cuh", "ssm_internal.h"),
     "ssm_dtproj_fwd": ("ssm_dtproj.cu", "ssm_common.cuh", "ssm_internal.h"),
     "ssm_dtproj_bwd": ("ssm_dtproj.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "gdn2_chunk_fwd": ("gdn2.cu", "ssm_common.cuh", "ssm_internal.h"),
 }
 
 
@@ -987,24 +992,227 @@ def run_dtproj(args, w):
     return 0
 
 
+# ------------------------------------------------------------------ gdn2
+GDN2_METRIC = "gdn2 chunkwise forward M(token·head)/s on 1 GB300; % of HBM roofline"
+GDN2_UNIT = "M(token·head)/s"
+GDN2_CHUNK = 64
+
+
+def gdn2_algorithmic_bytes(B, H, T, K, V):
+    """Bytes the forward moves at least once: q, k, b (bf16) and g (fp32) per
+    key channel, v and w (bf16) per value channel, out (bf16) per value
+    channel, for every (token, head); the fp32 state read and written once
+    per (batch, head)."""
+    return B * H * T * (K * (3 * 2 + 4) + V * (2 * 2 + 2)) + 2 * B * H * K * V * 4
+
+
+def gdn2_flops(B, H, T, K, V, c=GDN2_CHUNK):
+    """The method's multiply-add work per full chunk, 2 flops each: q k^T and
+    (b k) k^T (2 c^2 K), the key-mean decay as a product (c^2 K), the WY rows
+    W and U from the inverse (c^2 K + c^2 V), W S (c K V), the output's two
+    terms (c^2 V + c K V) and the state update (c K V)."""
+    per_chunk = 2 * (2 * c * c * K + c * c * K + c * c * (K + V) + 3 * c * K * V + c * c * V)
+    return B * H * (T / c) * per_chunk
+
+
+def _gdn2_oracle_step(x, tmax):
+    from oracle import gdn2_oracle
+    sl = lambda a: a[:1, :1, :tmax]  # noqa: E731
+    t0 = time.perf_counter()
+    gdn2_oracle.chunk_wy_forward(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.b), sl(x.w), x.state[:1, :1], x.scale,
+                                 chunk=GDN2_CHUNK)
+    return time.perf_counter() - t0
+
+
+def gdn2_cpu_sample(name, budget_s):
+    """The float64 GDN2 oracle (numpy) on head (0, 0) of the workload, the
+    first tokens (whole chunks), sized for about budget_s."""
+    B, H, T, K, V, seed = gen.GDN2_WORKLOADS[name]
+    x = gen.make_gdn2_inputs(1, 1, T, K, V, seed=seed)
+    t = _gdn2_oracle_step(x, GDN2_CHUNK)
+    tmax = int(min(T, max(GDN2_CHUNK, GDN2_CHUNK * budget_s / max(t, 1e-4))) // GDN2_CHUNK * GDN2_CHUNK)
+    return x, tmax
+
+
+def gdn2_name(args):
+    return args.workload if args.workload in gen.GDN2_WORKLOADS else "gdn2-1.3b-like"
+
+
+def run_gdn2_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    name = gdn2_name(args)
+    B, H, T, K, V, seed = gen.GDN2_WORKLOADS[name]
+    x, tmax = gdn2_cpu_sample(name, 150.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        _gdn2_oracle_step(x, tmax)
+    ts = [_gdn2_oracle_step(x, tmax) for _ in range(args.steps)]
+    total = sum(ts)
+    val = tmax * len(ts) / total / 1e6
+    sample = (f"per step: head (0, 0), the first {tmax} of {T} tokens, float64 numpy oracle of the chunked forward "
+              f"(numpy's BLAS may thread its products over the host's cores)")
+    line = {
+        "impl": "reference", "metric": GDN2_METRIC, "value": val, "unit": GDN2_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(ts), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": GDN2_CHUNK},
+        "cpu_baseline": {"value": val, "unit": GDN2_UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": GDN2_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gdn2(args):
+    """gdn2_chunk_fwd on a GDN2 workload: one step = one forward call timed with
+    CUDA events after an L2 flush, inputs resident in HBM."""
+    import torch
+    import selective_state_space_07_gb300 as ssm
+
+    rank, world, local = dist_env()
+    dist = init_dist(world, "nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    ssm.build()
+    name = gdn2_name(args)
+    B, H, T, K, V, seed = gen.GDN2_WORKLOADS[name]
+    x = gen.make_gdn2_inputs(B, H, T, K, V, seed=seed)
+    bf, f32 = torch.bfloat16, torch.float32
+    t = {n: torch.from_numpy(getattr(x, n)).to(dev, bf) for n in ("q", "k", "v", "b", "w")}
+    t["g"] = torch.from_numpy(x.g).to(dev, f32)
+    t["state"] = torch.from_numpy(x.state).to(dev, f32)
+    del x
+    out = torch.empty(B, H, T, V, dtype=bf, device=dev)
+    st = torch.empty(B, H, K, V, dtype=f32, device=dev)
+    ws = ssm.Workspace(1, 1, 8, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    scale = K ** -0.5
+
+    def fwd():
+        ssm.gdn2_fwd(t["q"], t["k"], t["v"], t["g"], t["b"], t["w"], t["state"], scale, out=out, state_out=st,
+                     workspace=ws)
+        return ssm.last_launch_count()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fwd()
+    torch.cuda.synchronize()
+    if ssm.poll_status(ws) != 0:
+        raise RuntimeError("non-zero status during warm-up")
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler()
+    if rank == 0:
+        clocks.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches = 0
+    for e in ev:
+        flush.zero_()
+        e[0].record(stream)
+        launches += fwd()
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop(set(visible_gpu_ids(world))) if rank == 0 else None
+    ms = max_over_ranks([sum(e[0].elapsed_time(e[1]) for e in ev) / len(ev)], dist, dev)[0]
+    status = ssm.poll_status(ws)
+    units = B * H * T
+    value = world * units / (ms * 1e-3) / 1e6
+
+    e2e = None
+    if not args.no_e2e:  # inputs in from pinned host memory, the output and the final state back
+        h_in = {n: v.cpu().pin_memory() for n, v in t.items()}
+        h_out = {"out": torch.empty_like(out, device="cpu").pin_memory(),
+                 "state": torch.empty_like(st, device="cpu").pin_memory()}
+
+        def e2e_step():
+            for n, v in h_in.items():
+                t[n].copy_(v, non_blocking=True)
+            fwd()
+            h_out["out"].copy_(out, non_blocking=True)
+            h_out["state"].copy_(st, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        n = max(3, min(args.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        es.record(stream)
+        for _ in range(n):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks([es.elapsed_time(ee) / n], dist, dev)[0]
+        e2e = {"value": round(world * units / (e2e_ms * 1e-3) / 1e6, 3), "unit": GDN2_UNIT,
+               "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
+               "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in h_out.values()),
+               "ms_per_step": round(e2e_ms, 4), "api": "gdn2_fwd on one stream, pinned host copies"}
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+    peak, peak_kind, peaks = measured_peaks()
+    ab = gdn2_algorithmic_bytes(B, H, T, K, V)
+    ach = ab / (ms * 1e-3) / 1e9
+    rf = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+          "peak_kind": peak_kind, "kernel": "gdn2_chunk_fwd_kernel", "algorithmic_bytes_per_launch": ab,
+          "ms_per_launch": round(ms, 5), "traffic": profiled_traffic("gdn2_chunk_fwd", name)}
+    fl = gdn2_flops(B, H, T, K, V)
+    tpk = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
+    tf = fl / (ms * 1e-3) / 1e12
+    tens = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpk, "unit": "TFLOP/s", "frac": round(tf / tpk, 4),
+            "peak_kind": "measured bf16 (burst)" if peaks else "fallback", "flops_per_launch": fl}
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        x1, tmax = gdn2_cpu_sample(name, 6.0)
+        ts = []
+        while sum(ts) < 12.0 and len(ts) < 50:
+            ts.append(_gdn2_oracle_step(x1, tmax))
+        cpu = {"value": tmax * len(ts) / sum(ts) / 1e6, "unit": GDN2_UNIT, "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"head (0, 0), the first {tmax} of {T} tokens, float64 numpy oracle (its BLAS may thread "
+                         f"over the host's cores), {len(ts)} repetitions, {sum(ts):.1f} s"}
+    line = {
+        "metric": GDN2_METRIC, "value": round(value, 3), "unit": GDN2_UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": GDN2_CHUNK, "seed": seed,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (129 MB) and a 512 MiB write flushes L2 before every call"},
+        "roofline": rf, "tensor_roofline": tens, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+        "clocks": clk, "status": status,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=gen.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(gen.WORKLOAD_ORDER) + list(gen.GDN2_WORKLOADS))
     ap.add_argument("--nsplit", type=int, default=0, help="lanes per channel (0 = library's choice)")
     ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the inference-forward and decode timings")
-    ap.add_argument("--op", choices=("scan", "conv1d", "dtproj"), default="scan",
+    ap.add_argument("--op", choices=("scan", "conv1d", "dtproj", "gdn2"), default="scan",
                     help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it; "
-                         "dtproj: the dt projection with its softplus")
+                         "dtproj: the dt projection with its softplus; gdn2: the Gated DeltaNet-2 chunkwise forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.op == "gdn2":
+        return run_gdn2_reference(args) if args.impl == "reference" else run_gdn2(args)
+    if args.workload in gen.GDN2_WORKLOADS:
+        ap.error("a GDN2 workload needs --op gdn2")
     w = gen.WORKLOADS[args.workload]
     if args.op == "dtproj":
         return run_dtproj_reference(args, w) if args.impl == "reference" else run_dtproj(args, w)

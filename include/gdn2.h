@@ -27,7 +27,9 @@
  * (0 means 64) are required (else SSM_ERR_UNSUPPORTED); every pointer must
  * be 16-byte aligned (else SSM_ERR_ALIGNMENT); q, k, v, g, b, w and out
  * must be non-null when B*H*T > 0, sizes non-negative, B*H below 2^31 and
- * scale finite (else SSM_ERR_INVALID_ARG). state_in NULL means a zero
+ * scale finite (else SSM_ERR_INVALID_ARG); B*H*T must stay below
+ * 2^31 - 128 token rows (else SSM_ERR_UNSUPPORTED: copies address rows with
+ * 32-bit coordinates). state_in NULL means a zero
  * initial state; state_out NULL skips the final state. With T = 0 the
  * final state is the initial one (copied, or zeroed).
  *

@@ -8,29 +8,36 @@
 // fp32 accumulation, M = 128) whose operands one thread points at in shared
 // memory in the tensor core's 128-byte-swizzled K-major layout (rows of
 // 128 bytes = 64 bf16 of K, 8-row groups 1024 bytes apart, the 16-byte
-// chunks of row r permuted by r % 8); the CTA's threads write those
-// operands with ordinary stores, then fence them to the async proxy.
+// chunks of row r permuted by r % 8).
+//
+// Inputs arrive by TMA, one chunk ahead: q, k and b straight into the first
+// product's operands (128-byte swizzled boxes, which is that layout), g, v
+// and w into staging buffers; each copy is issued as soon as the buffer it
+// lands in has been read for the current chunk, so it runs under the
+// current chunk's work.
 //
 // Per chunk (the page's steps, with the products arranged so that M = 128):
-//  1. load q, k, b*k (bf16) and w*v; the column threads form G = cumsum of
-//     g, and from it E+ = exp(G - G[m]), E- = exp(G[m] - G) about the
-//     middle token m, q*exp(G)*scale, (b*k*exp(G))^T and
-//     (k*exp(G[last] - G))^T;
-//  2. MMA [q; b*k] k^T and [E+; E+] E-^T (the second / K is the key-mean
-//     of exp(G[i] - G[j]) = the decay, in both lane halves);
-//  3. aqk = qk * decay * scale (j <= i) and akk = (bk)k^T * decay (j < i);
-//  4. T = (I + akk)^-1 by forward substitution, one column per thread
-//     (unit lower-triangular); then MMA W^T = (b*k*exp(G))^T T^T and
+//  0. b*k in place; column pass (thread = one key channel, 32 tokens):
+//     G = cumsum of g; E+ = exp(G - G[m]) about the middle token m (fp32,
+//     in place of g); (b*k*exp G)^T and (k*exp(G[last] - G))^T. Row pass:
+//     [E+; E-] with E- = 1/E+, and q*exp(G)*scale;
+//  1. MMA [q; b*k] k^T and [E+; E-] E-^T (the first 64 lanes of the second
+//     are K * decay: the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K);
+//  2. aqk = qk * decay * scale (j <= i); akk = (bk)k^T * decay (j < i), the
+//     decay passed between lane halves through shared memory;
+//  3. T = (I + akk)^-1 by forward substitution, one thread per column, while
+//     other warps form (w*v)^T; MMA W = T (b*k*exp G) in row layout and
 //     U^T = (w*v)^T T^T (the page's row-by-row WY substitution, as
 //     (I + akk) W = rhs);
-//  5. MMA (W S)^T = S^T W^T; v_new = U - W S;
-//  6. MMA out^T = v_new^T aqk^T + S^T (q*exp(G)*scale)^T, and, after S^T
+//  4. MMA (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T;
+//  5. MMA out^T = v_new^T aqk^T + S^T (q*exp(G)*scale)^T, and, after S^T
 //     is scaled column-wise by exp(G[last]), S^T += v_new^T (k*exp(G[last]-G)).
 // The state's bf16 copy that the products read is refreshed from TMEM
 // after every chunk.
 //
-// Every wait on a tensor-core completion is bounded (1 s); a wait that runs
-// out sets the timeout status bit and the CTA stops.
+// Every wait (copies, tensor-core completions) is bounded (1 s); a wait that
+// runs out sets the timeout status bit, the CTA waits (bounded) for its
+// copies still in flight and stops.
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
 #include "../../include/gdn2.h"
@@ -46,25 +53,30 @@ constexpr int kGThreads = 256;
 
 // Shared-memory regions (bytes from a 1024-byte aligned base). Regions used
 // in disjoint phases of a chunk share space.
-constexpr int kA1 = 0;                  // [q; b*k]            128 rows x K=128
-constexpr int kB1 = kA1 + 32768;        // k                    64 rows x K=128   (then akk^T fp32 [64][64])
-constexpr int kA2 = kB1 + 16384;        // [E+; E+]            128 rows x K=128   (then W, v_new^T)
-constexpr int kB2 = kA2 + 32768;        // E-                   64 rows x K=128   (then aqk, T)
-constexpr int kA3 = kB2 + 16384;        // (b*k*exp G)^T       128 rows x K=64
-constexpr int kA4 = kA3 + 16384;        // (w*v)^T             128 rows x K=64
+constexpr int kA1 = 0;                  // [q; b*k]            128 rows x K=128 (q, b by TMA)
+constexpr int kB1 = kA1 + 32768;        // k                    64 rows x K=128 (TMA)
+constexpr int kA2 = kB1 + 16384;        // [E+; E-]            128 rows x K=128 (E- = rows 64.. as a B operand)
+constexpr int kA3 = kA2 + 32768;        // (b*k*exp G)^T       128 rows x K=64  (then v_new^T)
+constexpr int kA4 = kA3 + 16384;        // w staging [64][128] (TMA), then (w*v)^T 128 rows x K=64
 constexpr int kA5 = kA4 + 16384;        // S^T (bf16)          128 rows x K=128
 constexpr int kB7 = kA5 + 32768;        // q*exp(G)*scale       64 rows x K=128
 constexpr int kB8 = kB7 + 16384;        // (k*exp(Glast-G))^T  128 rows x K=64
-constexpr int kMisc = kB8 + 16384;      // gsum[128], glast[128] (fp32), mbarrier, TMEM slot
-constexpr int kB5 = kA2;                // W                    64 rows x K=128
-constexpr int kA6 = kA2 + 16384;        // v_new^T             128 rows x K=64
-constexpr int kB6 = kB2;                // aqk                  64 rows x K=64
-constexpr int kB3 = kB2 + 8192;         // T                    64 rows x K=64
-constexpr int kAKK = kB1;               // akk^T fp32 [64][64]
-constexpr int kGSmem = kMisc + 2048 + 1024;  // misc (1040 bytes used) + slack for the 1024-byte alignment
+constexpr int kGS = kB8 + 16384;        // g staging fp32 [64][128] (TMA) -> E+; then the decay fp32 [64][64]
+constexpr int kVS = kGS + 32768;        // v staging [64][128] bf16 (TMA)
+constexpr int kMisc = kVS + 16384;      // em, egl [128] fp32; mbarriers; TMEM slot
+constexpr int kB6 = kA2;                // aqk                  64 rows x K=64
+constexpr int kB3 = kA2 + 8192;         // T                    64 rows x K=64 (as A: 128 rows, the rest unused)
+constexpr int kAKK = kA2 + 16384;       // akk^T fp32 [column][row]
+constexpr int kB5 = kA2 + 16384;        // W                    64 rows x K=128
+constexpr int kA6 = kA3;                // v_new^T             128 rows x K=64
+constexpr int kGSmem = kMisc + 1024 + 64 + 1024;  // + slack for the 1024-byte alignment
+static_assert(kGSmem <= 227 * 1024, "shared memory");
+constexpr unsigned kQkbBytes = 3 * 2 * 64 * 128;  // q, b, k: two 64-column boxes each
+constexpr unsigned kGBytes = kGC * kGK * 4, kVBytes = kGC * kGV * 2;
 
-// TMEM columns
-constexpr unsigned kTS = 0, kTD1 = 128, kTD2 = 192, kTDW = 256, kTDU = 320, kTDWS = 384, kTDOUT = 448;
+// TMEM columns: S^T, then per chunk qk|bkk and the decay, whose columns W
+// (row layout, 128 columns) reuses once they are read.
+constexpr unsigned kTS = 0, kTD1 = 128, kTD2 = 192, kTDW = 128, kTDU = 256, kTDWS = 320, kTDOUT = 384;
 
 // Byte offset of element (row, col) in a K-major, 128-byte-swizzled bf16
 // operand of `rows` rows.
@@ -84,7 +96,8 @@ __host__ __device__ constexpr uint32_t idesc_m128(int n) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
 }
 
-// D[128 x n] (+)= A[128 x kdim] B[n x kdim]^T, both operands K-major swizzled in shared memory.
+// D[128 x n] (+)= A[128 x kdim] B[n x kdim]^T, both operands K-major swizzled
+// in shared memory; b_rows is the row count B's 64-wide K atoms are laid out for.
 __device__ __forceinline__ void mma_issue(unsigned d_tmem, unsigned a, unsigned b, int b_rows, int n, int kdim,
                                           bool accumulate) {
     const uint32_t id = idesc_m128(n);
@@ -137,16 +150,14 @@ __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.a
 __device__ __forceinline__ void tc_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
 
+__device__ __forceinline__ unsigned pack_bf2(float a, float b) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<unsigned*>(&h);
+}
 // 8 consecutive bf16 of a K-major swizzled row (one 16-byte chunk): col % 8 == 0.
 __device__ __forceinline__ void st8(char* base, int row, int col, int rows, const float* v) {
-    uint4 u;
-    __nv_bfloat162 p0 = __floats2bfloat162_rn(v[0], v[1]), p1 = __floats2bfloat162_rn(v[2], v[3]),
-                   p2 = __floats2bfloat162_rn(v[4], v[5]), p3 = __floats2bfloat162_rn(v[6], v[7]);
-    u.x = *reinterpret_cast<unsigned*>(&p0);
-    u.y = *reinterpret_cast<unsigned*>(&p1);
-    u.z = *reinterpret_cast<unsigned*>(&p2);
-    u.w = *reinterpret_cast<unsigned*>(&p3);
-    *reinterpret_cast<uint4*>(base + swz(row, col, rows)) = u;
+    *reinterpret_cast<uint4*>(base + swz(row, col, rows)) =
+        make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
 }
 __device__ __forceinline__ void st1(char* base, int row, int col, int rows, float v) {
     *reinterpret_cast<__nv_bfloat16*>(base + swz(row, col, rows)) = __float2bfloat16_rn(v);
@@ -162,25 +173,81 @@ __device__ __forceinline__ void unpack8(uint4 u, float* f) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
 }
+__device__ __forceinline__ void ld8(const char* base, int row, int col, int rows, float* f) {
+    unpack8(*reinterpret_cast<const uint4*>(base + swz(row, col, rows)), f);
+}
+__device__ __forceinline__ float bf(__nv_bfloat16 h) { return __bfloat162float(h); }
+
+
+// Wait until phase `parity` of the barrier completes (mbarrier.try_wait,
+// which suspends the thread for a while in hardware between checks), at most
+// kWaitNs; returns whether it completed.
+__device__ __forceinline__ bool mbar_wait_try(unsigned bar, unsigned parity) {
+    const unsigned long long t0 = global_ns();
+    while (true) {
+        unsigned done = 0;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (done) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
+    }
+}
+
+// T = (I + akk)^-1 (akk strictly lower triangular, 64 x 64) by forward
+// substitution, one thread per column `col`, written to `tb` as the K-major
+// operand T (rows r, K = column). akk is read as its transpose, fp32
+// [column][row], so that step i reads a contiguous broadcast run; rows are
+// updated in pairs with packed fused multiply-adds. Kept out of line: its
+// unrolled steps then draw on registers of their own.
+__device__ __noinline__ void triangular_inverse(const float* akkT, char* tb, int col) {
+    float2 x[kGC / 2];  // rows 2m, 2m+1
+#pragma unroll
+    for (int m = 0; m < kGC / 2; ++m) x[m] = make_float2(2 * m == col ? 1.f : 0.f, 2 * m + 1 == col ? 1.f : 0.f);
+#pragma unroll
+    for (int i = 0; i < kGC - 1; ++i) {
+        const float xi = (i & 1) ? x[i >> 1].y : x[i >> 1].x;  // final: every earlier step has updated it
+        const float2 nx = make_float2(-xi, -xi);
+        const float* a = akkT + i * kGC;  // akk[r][i], r = 0..63
+        if (!(i & 1)) x[i >> 1].y = __fmaf_rn(-a[i + 1], xi, x[i >> 1].y);  // row i+1 shares the pair
+#pragma unroll
+        for (int q4 = ((i >> 1) + 1) >> 1; q4 < kGC / 4; ++q4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(a + 4 * q4);
+            if (2 * (2 * q4) > i) x[2 * q4] = __ffma2_rn(make_float2(a4.x, a4.y), nx, x[2 * q4]);
+            if (2 * (2 * q4 + 1) > i) x[2 * q4 + 1] = __ffma2_rn(make_float2(a4.z, a4.w), nx, x[2 * q4 + 1]);
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kGC / 2; ++m) {
+        st1(tb, 2 * m, col, 64, x[m].x);  // T[r][col]
+        st1(tb, 2 * m + 1, col, 64, x[m].y);
+    }
+}
 
 struct Gdn2Params {
     int64_t B, H, T;
     float scale;
-    const __nv_bfloat16 *q, *k, *v, *b, *w;
-    const float* g;
-    const float* state_in;
-    __nv_bfloat16* out;
-    float* state_out;
     unsigned* status;
 };
+struct Gdn2Maps {
+    CUtensorMap q, k, b, g, v, w;  // rows = B*H*T tokens; q, k, b: 64-column swizzled boxes; g, v, w: whole rows
+};
 
-__global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2Params p) {
+__global__ void __launch_bounds__(kGThreads, 1)
+    gdn2_chunk_fwd_kernel(const Gdn2Params p, const float* __restrict__ state_in, __nv_bfloat16* __restrict__ out,
+                          float* __restrict__ state_out, const __grid_constant__ Gdn2Maps mp) {
     extern __shared__ __align__(1024) char g_smem_raw[];
     char* sm = g_smem_raw + ((1024u - (smem_u32(g_smem_raw) & 1023u)) & 1023u);
-    float* gsum = reinterpret_cast<float*>(sm + kMisc);
-    float* glast = gsum + kGK;                       // exp(G[last]) per key channel
-    uint64_t* bar = reinterpret_cast<uint64_t*>(glast + kGK);
-    unsigned* tslot = reinterpret_cast<unsigned*>(bar + 1);
+    float* s_em = reinterpret_cast<float*>(sm + kMisc);  // exp(G[m]) per key channel
+    float* s_egl = s_em + kGK;                           // exp(G[last])
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_egl + kGK);  // mma, qkb, g, v, w
+    unsigned* tslot = reinterpret_cast<unsigned*>(bars + 5);
+    float* s_gm = reinterpret_cast<float*>(sm + kA2);    // column-pass exchange (A2 is written after it)
+    float* s_gl = s_gm + kGK;
+    float* s_e = reinterpret_cast<float*>(sm + kGS);     // g, then E+ [64][128]; then the decay [64][64]
+    float* s_akkT = reinterpret_cast<float*>(sm + kAKK);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, whalf = warp >> 2;  // TMEM lanes 32*quarter..; column half
@@ -188,7 +255,9 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
     const int64_t T = p.T;
     const int nchunks = (int)((T + kGC - 1) / kGC);
     const unsigned sbase = smem_u32(sm);
-    const unsigned mbar = smem_u32(bar);
+    const unsigned mbar = smem_u32(bars), bar_qkb = smem_u32(bars + 1), bar_g = smem_u32(bars + 2),
+                   bar_v = smem_u32(bars + 3), bar_w = smem_u32(bars + 4);
+    constexpr float L2E = 1.4426950408889634f;
 
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tslot)),
@@ -196,9 +265,33 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
+    // the copies of chunk cj (thread 0); rows past the end of the whole
+    // tensor read as zero, rows of the next (batch, head) are zeroed or
+    // ignored on the ragged last chunk
+    auto row_of = [&](int cj) { return (int)(bh * T + (int64_t)cj * kGC); };
+    auto issue_qkb = [&](int cj) {
+        const int y = row_of(cj);
+        mbar_expect_tx(bar_qkb, kQkbBytes);
+#pragma unroll
+        for (int at = 0; at < 2; ++at) {  // x = 0, 64: 128-byte aligned
+            tma_load_2d(sm + kA1 + at * 16384, &mp.q, at * 64, y, bar_qkb);
+            tma_load_2d(sm + kA1 + at * 16384 + 8192, &mp.b, at * 64, y, bar_qkb);
+            tma_load_2d(sm + kB1 + at * 8192, &mp.k, at * 64, y, bar_qkb);
+        }
+    };
+    auto issue_one = [&](unsigned bar, int off, const CUtensorMap* m, unsigned bytes, int cj) {
+        mbar_expect_tx(bar, bytes);
+        tma_load_2d(sm + off, m, 0, row_of(cj), bar);
+    };
     if (tid == 0) {
-        mbar_init(mbar, 1);
+        for (int b = 0; b < 5; ++b) mbar_init(smem_u32(bars + b), 1);
         mbar_fence_init();
+        if (nchunks > 0) {
+            issue_qkb(0);
+            issue_one(bar_g, kGS, &mp.g, kGBytes, 0);
+            issue_one(bar_v, kVS, &mp.v, kVBytes, 0);
+            issue_one(bar_w, kA4, &mp.w, kVBytes, 0);
+        }
     }
     tc_before();
     __syncthreads();
@@ -209,7 +302,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
 
     // ---- the initial state: S^T into TMEM (lane v, column n) and its bf16 copy
     {
-        const float* s0 = p.state_in ? p.state_in + bh * kGK * kGV : nullptr;
+        const float* s0 = state_in ? state_in + bh * kGK * kGV : nullptr;
         for (int c = 0; c < 2; ++c) {
             const int n0 = whalf * 64 + c * 32;
             float vals[32];
@@ -226,16 +319,39 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
     __syncthreads();
 
     unsigned phase = 0;
+    // copies issued / waited for, per barrier (qkb, g, v, w); uniform over the CTA
+    int issued[4] = {nchunks > 0, nchunks > 0, nchunks > 0, nchunks > 0}, waited[4] = {0, 0, 0, 0};
+    const unsigned tbar[4] = {bar_qkb, bar_g, bar_v, bar_w};
     float nf = 0.f;
+    auto fail = [&]() {
+        if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+    };
     auto mma_wait = [&]() -> bool {  // every thread waits for the last commit; false if it never came
-        const bool ok = mbar_wait_bounded(mbar, phase & 1u);
+        const bool ok = mbar_wait_try(mbar, phase & 1u);
         phase++;
-        if (!ok && tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
+        if (!ok) fail();
+        return __syncthreads_and(ok) != 0;
+    };
+    auto copy_wait = [&](int b) -> bool {  // every thread waits for copy b of the current chunk
+        const bool ok = mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1));
+        if (ok) waited[b]++;
+        if (!ok) fail();
         return __syncthreads_and(ok) != 0;
     };
     auto commit = [&]() {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
                      : "memory");
+    };
+    auto refill = [&](int b, int cj) {  // next chunk's copy into a buffer all threads are done reading
+        if (cj >= nchunks) return;
+        if (tid == 0) {
+            fence_async_smem();
+            if (b == 0) issue_qkb(cj);
+            else if (b == 1) issue_one(bar_g, kGS, &mp.g, kGBytes, cj);
+            else if (b == 2) issue_one(bar_v, kVS, &mp.v, kVBytes, cj);
+            else issue_one(bar_w, kA4, &mp.w, kVBytes, cj);
+        }
+        issued[b]++;
     };
 
     bool ok = true;
@@ -244,168 +360,198 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
         const int c = (int)min64(kGC, T - t0);  // live tokens; rows c..63 are zero (identity tokens)
         const int64_t row0 = bh * T + t0;      // first token row of the chunk in [B*H*T]
 
-        // ---- 1a. q, k, b*k into the product operands; (w*v)^T
-        for (int e = tid; e < kGC * (kGK / 8); e += kGThreads) {
+        // ---- 0a. b*k in place; rows past the chunk's tokens zeroed
+        if (!(ok = copy_wait(0))) break;
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + it * kGThreads;
             const int r = e >> 4, cc = (e & 15) * 8;
-            float qv[8], kv[8], bv[8];
+            char* pb = sm + kA1 + swz(64 + r, cc, 128);
+            char* pk = sm + kB1 + swz(r, cc, 64);
             if (r < c) {
-                const int64_t off = (row0 + r) * kGK + cc;
-                unpack8(*reinterpret_cast<const uint4*>(p.q + off), qv);
-                unpack8(*reinterpret_cast<const uint4*>(p.k + off), kv);
-                unpack8(*reinterpret_cast<const uint4*>(p.b + off), bv);
+                float bv[8], kv[8];
+                unpack8(*reinterpret_cast<const uint4*>(pb), bv);
+                unpack8(*reinterpret_cast<const uint4*>(pk), kv);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) bv[i] *= kv[i];
+                *reinterpret_cast<uint4*>(pb) = make_uint4(pack_bf2(bv[0], bv[1]), pack_bf2(bv[2], bv[3]),
+                                                           pack_bf2(bv[4], bv[5]), pack_bf2(bv[6], bv[7]));
             } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) qv[i] = kv[i] = bv[i] = 0.f;
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(pb) = z;
+                *reinterpret_cast<uint4*>(pk) = z;
+                *reinterpret_cast<uint4*>(sm + kA1 + swz(r, cc, 128)) = z;
             }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) bv[i] *= kv[i];
-            st8(sm + kA1, r, cc, 128, qv);
-            st8(sm + kA1, 64 + r, cc, 128, bv);
-            st8(sm + kB1, r, cc, 64, kv);
         }
-        for (int e = tid; e < kGC * (kGV / 8); e += kGThreads) {
-            const int r = e >> 4, cc = (e & 15) * 8;
-            float vv[8], wv[8];
-            if (r < c) {
-                const int64_t off = (row0 + r) * kGV + cc;
-                unpack8(*reinterpret_cast<const uint4*>(p.v + off), vv);
-                unpack8(*reinterpret_cast<const uint4*>(p.w + off), wv);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) vv[i] = wv[i] = 0.f;
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) st1(sm + kA4, cc + i, r, 128, vv[i] * wv[i]);  // (w*v)^T: row v, column j
-        }
-        // ---- 1b. the column threads: G = cumsum(g) over the chunk's tokens,
-        // rows 32*half .. +31 of key channel kc
-        const int kc = tid & (kGK - 1), half = tid >> 7;
+        // ---- 0b. column pass (thread = key channel n, tokens 32*hf ..+31)
+        if (!(ok = copy_wait(1))) break;  // g (also orders 0a's stores before the reads below)
+        const int n = tid & (kGK - 1), hf = tid >> 7, j0 = hf * 32;
         float G[32];
         {
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int r = half * 32 + i;
-                const float gv = r < c ? p.g[(row0 + r) * kGK + kc] : 0.f;
+                const float gv = j0 + i < c ? s_e[(j0 + i) * kGK + n] : 0.f;
                 acc = __fadd_rn(acc, gv);
                 G[i] = acc;
             }
-            if (half == 0) gsum[kc] = acc;  // G at the middle token m = 31
+            if (hf == 0) s_gm[n] = acc;  // G at the middle token m = 31
         }
-        __syncthreads();  // gsum; the q / k / b*k operands
-        const float Gm = gsum[kc];
-        if (half == 1) {
+        __syncthreads();
+        const float Gm = s_gm[n];
+        if (hf == 1) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) G[i] = __fadd_rn(G[i], Gm);
-            glast[kc] = G[31];  // G at the last row (= the last live token: later rows add zeros)
+            s_gl[n] = G[31];  // G at the last row (= the last live token: later rows add zeros)
         }
         __syncthreads();
         {
-            const float Gl = glast[kc];
-            const float em = expf(Gm), elm = expf(Gl - Gm);  // exp(G[m]), exp(G[last] - G[m])
+            const float Gl = s_gl[n];
+            const float em = ex2(Gm * L2E);
+            const float elm = ex2((Gl - Gm) * L2E);  // exp(G[last] - G[m])
+            if (hf == 0) {
+                s_em[n] = em;
+                s_egl[n] = ex2(Gl * L2E);
+            }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int r = half * 32 + i;
-                const float ep = expf(G[i] - Gm);    // E+ = exp(G - G[m])
-                const float en = expf(Gm - G[i]);    // E- = exp(G[m] - G)
-                const float eg = ep * em;            // exp(G)
-                st1(sm + kA2, r, kc, 128, ep);
-                st1(sm + kA2, 64 + r, kc, 128, ep);
-                st1(sm + kB2, r, kc, 64, en);
-                st1(sm + kB7, r, kc, 64, ld1(sm + kA1, r, kc, 128) * eg * p.scale);   // q * exp(G) * scale
-                st1(sm + kA3, kc, r, 128, ld1(sm + kA1, 64 + r, kc, 128) * eg);       // (b*k*exp G)^T
-                st1(sm + kB8, kc, r, 128, ld1(sm + kB1, r, kc, 64) * (elm * en));     // (k*exp(Glast - G))^T
+            for (int i0 = 0; i0 < 32; i0 += 8) {
+                float a3[8], b8[8];
+#pragma unroll
+                for (int ii = 0; ii < 8; ++ii) {
+                    const int i = i0 + ii, j = j0 + i;
+                    const float ep = ex2((G[i] - Gm) * L2E);  // E+ = exp(G - G[m])
+                    const float en = rcp(ep);                  // E- = exp(G[m] - G)
+                    s_e[j * kGK + n] = ep;                     // in place of g (same thread)
+                    a3[ii] = ld1(sm + kA1, 64 + j, n, 128) * (ep * em);  // b*k*exp(G)
+                    b8[ii] = ld1(sm + kB1, j, n, 64) * (en * elm);       // k*exp(G[last] - G)
+                }
+                st8(sm + kA3, n, j0 + i0, 128, a3);
+                st8(sm + kB8, n, j0 + i0, 128, b8);
             }
         }
-        __syncthreads();
-        if (half == 0) glast[kc] = expf(glast[kc]);  // from here on: exp(G[last])
+        __syncthreads();  // E+; exp tables
+        // ---- 0c. row pass: [E+; E-] and q*exp(G)*scale
+#pragma unroll 2
+        for (int it = 0; it < 4; ++it) {
+            const int e = tid + it * kGThreads;
+            const int r = e >> 4, cc = (e & 15) * 8;
+            float ep[8], en[8], qv[8], em8[8];
+            *reinterpret_cast<float4*>(ep) = *reinterpret_cast<const float4*>(s_e + r * kGK + cc);
+            *reinterpret_cast<float4*>(ep + 4) = *reinterpret_cast<const float4*>(s_e + r * kGK + cc + 4);
+            *reinterpret_cast<float4*>(em8) = *reinterpret_cast<const float4*>(s_em + cc);
+            *reinterpret_cast<float4*>(em8 + 4) = *reinterpret_cast<const float4*>(s_em + cc + 4);
+            ld8(sm + kA1, r, cc, 128, qv);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                en[i] = rcp(ep[i]);
+                qv[i] = qv[i] * ep[i] * em8[i] * p.scale;
+            }
+            st8(sm + kA2, r, cc, 128, ep);
+            st8(sm + kA2, 64 + r, cc, 128, en);
+            st8(sm + kB7, r, cc, 64, qv);
+        }
         fence_async_smem();
         tc_before();
         __syncthreads();
 
-        // ---- 2. qk^T and (bk)k^T in one product; the decay (x K) in both lane halves
+        // ---- 1. qk^T | (bk)k^T, and E+ E-^T (= K * decay in lanes 0-63)
         if (tid == 0) {
             tc_after();
             mma_issue(tmem + kTD1, sbase + kA1, sbase + kB1, 64, 64, kGK, false);
-            mma_issue(tmem + kTD2, sbase + kA2, sbase + kB2, 64, 64, kGK, false);
+            mma_issue(tmem + kTD2, sbase + kA2, sbase + kA2 + 8192, 128, 64, kGK, false);
             commit();
         }
         if (!(ok = mma_wait())) break;
         tc_after();
+        refill(0, ci + 1);  // q, k, b have been read
 
-        // ---- 3. aqk (rows 0-63) and akk^T (rows 64-127, fp32, transposed)
+        // ---- 2. aqk (lanes 0-63) and akk (lanes 64-127; the decay through shared memory)
         {
-            float d1[32], d2[32];
-            const int j0 = whalf * 32;
-            tmem_ld32(tmem + tlane + kTD1 + (unsigned)j0, d1);
-            tmem_ld32(tmem + tlane + kTD2 + (unsigned)j0, d2);
-            if (vrow < 64) {
+            const int jb = whalf * 32;
+            float d1[32];
+            tmem_ld32(tmem + tlane + kTD1 + (unsigned)jb, d1);
+            float* s_dec = s_e;  // [64][64]
+            if (quarter < 2) {
                 const int i = vrow;
-                float a[32];
+                float d2[32];
+                tmem_ld32(tmem + tlane + kTD2 + (unsigned)jb, d2);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) a[jj] = (j0 + jj <= i) ? d1[jj] * d2[jj] * (p.scale / kGK) : 0.f;
+                for (int jj = 0; jj < 32; ++jj) {
+                    const float dec = d2[jj] * (1.f / kGK);
+                    d2[jj] = dec;
+                    d1[jj] = (jb + jj <= i) ? d1[jj] * dec * p.scale : 0.f;
+                }
 #pragma unroll
-                for (int jj = 0; jj < 32; jj += 8) st8(sm + kB6, i, j0 + jj, 64, a + jj);
-            } else {
-                const int i = vrow - 64;
-                float* akkT = reinterpret_cast<float*>(sm + kAKK);
+                for (int jj = 0; jj < 32; jj += 4)
+                    *reinterpret_cast<float4*>(s_dec + i * kGC + jb + jj) =
+                        make_float4(d2[jj], d2[jj + 1], d2[jj + 2], d2[jj + 3]);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) akkT[(j0 + jj) * kGC + i] = (j0 + jj < i) ? d1[jj] * d2[jj] * (1.f / kGK) : 0.f;
+                for (int jj = 0; jj < 32; jj += 8) st8(sm + kB6, i, jb + jj, 64, d1 + jj);
             }
-        }
-        tc_before();
-        __syncthreads();
-
-        // ---- 4. T = (I + akk)^-1 by forward substitution: four threads per
-        // column (column tid/4, rows 16*(tid%4) ..+15); at step i the owner of
-        // x[i] passes it to the other three, which update their later rows
-        {
-            const float* akkT = reinterpret_cast<const float*>(sm + kAKK);
-            const int col = tid >> 2, part = tid & 3, r0 = part * 16;
-            float x[16];
+            __syncthreads();
+            if (quarter >= 2) {
+                const int i = vrow - 64;
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) x[rr] = (r0 + rr == col) ? 1.f : 0.f;
+                for (int jj = 0; jj < 32; jj += 4) {
+                    const float4 dec = *reinterpret_cast<const float4*>(s_dec + i * kGC + jb + jj);
+                    const float dv[4] = {dec.x, dec.y, dec.z, dec.w};
 #pragma unroll
-            for (int i = 0; i < kGC - 1; ++i) {
-                const float xi = __shfl_sync(0xffffffffu, x[i & 15], (lane & ~3) | (i >> 4));
-                if (r0 + 15 > i) {
-                    const float4* row = reinterpret_cast<const float4*>(akkT + i * kGC + r0);  // akk[r0.., i]
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        const float4 a4 = row[q4];
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            if (r0 + 4 * q4 + e > i) x[4 * q4 + e] = __fmaf_rn(-av[e], xi, x[4 * q4 + e]);
+                    for (int e = 0; e < 4; ++e) {
+                        const int j = jb + jj + e;
+                        s_akkT[j * kGC + i] = (j < i) ? d1[jj + e] * dv[e] : 0.f;
                     }
                 }
             }
+        }
+        tc_before();
+        __syncthreads();
+        refill(1, ci + 1);  // g / E+ / the decay have been read
+        if (!(ok = copy_wait(2))) break;  // v
+        if (!(ok = copy_wait(3))) break;  // w
+
+        // ---- 3. T = (I + akk)^-1 (warps 0-1) while warps 4-7 form (w*v)^T
+        if (warp < 2) {
+            triangular_inverse(s_akkT, sm + kB3, tid);
+        } else if (warp >= 4) {
+            const int vn = tid - 128;  // value channel
+            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + kVS);
+            const __nv_bfloat16* sw = reinterpret_cast<const __nv_bfloat16*>(sm + kA4);
+            float wv[kGC];
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) st1(sm + kB3, r0 + rr, col, 64, x[rr]);  // T[r][col]
+            for (int j = 0; j < kGC; ++j) wv[j] = j < c ? bf(sv[j * kGV + vn]) * bf(sw[j * kGV + vn]) : 0.f;
+            asm volatile("bar.sync 1, 128;\n" ::: "memory");  // w read by all four warps before A4 is rewritten
+#pragma unroll
+            for (int j = 0; j < kGC; j += 8) st8(sm + kA4, vn, j, 128, wv + j);
         }
         fence_async_smem();
         tc_before();
         __syncthreads();
+        refill(2, ci + 1);  // v has been read
         if (tid == 0) {
             tc_after();
-            mma_issue(tmem + kTDW, sbase + kA3, sbase + kB3, 64, 64, kGC, false);  // W^T = rhs_k^T T^T
-            mma_issue(tmem + kTDU, sbase + kA4, sbase + kB3, 64, 64, kGC, false);  // U^T = rhs_v^T T^T
+            // W = T (b*k*exp G): rows i in lanes 0-63, 128 columns; A = T as a 128-row operand
+            mma_issue(tmem + kTDW, sbase + kB3, sbase + kA3, 128, 128, kGC, false);
+            mma_issue(tmem + kTDU, sbase + kA4, sbase + kB3, 64, 64, kGC, false);  // U^T = (w*v)^T T^T
             commit();
         }
         if (!(ok = mma_wait())) break;
         tc_after();
-        {   // W (rows i, K = n) from W^T (lane n, column i)
-            float wt[32];
-            const int i0 = whalf * 32;
-            tmem_ld32(tmem + tlane + kTDW + (unsigned)i0, wt);
+        refill(3, ci + 1);  // (w*v)^T has been read: the next w can land in A4
+        if (quarter < 2) {  // W (rows i, K = n) from lanes 0-63
 #pragma unroll
-            for (int ii = 0; ii < 32; ++ii) st1(sm + kB5, i0 + ii, vrow, 64, wt[ii]);
+            for (int cc = 0; cc < 2; ++cc) {
+                const int n0 = whalf * 64 + cc * 32;
+                float wr[32];
+                tmem_ld32(tmem + tlane + kTDW + (unsigned)n0, wr);
+#pragma unroll
+                for (int nn = 0; nn < 32; nn += 8) st8(sm + kB5, vrow, n0 + nn, 64, wr + nn);
+            }
         }
         fence_async_smem();
         tc_before();
         __syncthreads();
 
-        // ---- 5. (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T
+        // ---- 4. (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T
         if (tid == 0) {
             tc_after();
             mma_issue(tmem + kTDWS, sbase + kA5, sbase + kB5, 64, 64, kGK, false);
@@ -428,7 +574,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
                 float s[32];
                 tmem_ld32(tmem + tlane + kTS + (unsigned)n0, s);
 #pragma unroll
-                for (int nn = 0; nn < 32; ++nn) s[nn] *= glast[n0 + nn];
+                for (int nn = 0; nn < 32; ++nn) s[nn] *= s_egl[n0 + nn];
                 tmem_st32(tmem + tlane + kTS + (unsigned)n0, s);
             }
             asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
@@ -437,7 +583,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
         tc_before();
         __syncthreads();
 
-        // ---- 6. out^T = v_new^T aqk^T + S^T (q exp(G) scale)^T;  S^T += v_new^T (k exp(Glast - G))
+        // ---- 5. out^T = v_new^T aqk^T + S^T (q exp(G) scale)^T;  S^T += v_new^T (k exp(Glast - G))
         if (tid == 0) {
             tc_after();
             mma_issue(tmem + kTDOUT, sbase + kA6, sbase + kB6, 64, 64, kGC, false);
@@ -455,7 +601,7 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
             for (int ii = 0; ii < 32; ++ii) {
                 if (i0 + ii < c) {
                     nf = __fmaf_rn(o[ii], 0.f, nf);
-                    p.out[(row0 + i0 + ii) * kGV + vrow] = __float2bfloat16_rn(o[ii]);
+                    out[(row0 + i0 + ii) * kGV + vrow] = __float2bfloat16_rn(o[ii]);
                 }
             }
             // the bf16 copy of the updated state for the next chunk's products
@@ -472,8 +618,13 @@ __global__ void __launch_bounds__(kGThreads, 1) gdn2_chunk_fwd_kernel(const Gdn2
         __syncthreads();
     }
 
-    if (ok && p.state_out) {
-        float* so = p.state_out + bh * kGK * kGV;
+    if (!ok) {  // a wait ran out: let the copies still in flight land before the CTA exits
+        if (tid == 0)
+            for (int b = 0; b < 4; ++b)
+                for (; waited[b] < issued[b]; ++waited[b])
+                    if (!mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1))) break;
+    } else if (state_out) {
+        float* so = state_out + bh * kGK * kGV;
         for (int cc = 0; cc < 2; ++cc) {
             const int n0 = whalf * 64 + cc * 32;
             float s[32];
@@ -502,7 +653,9 @@ extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
     if (a->B < 0 || a->H < 0 || a->T < 0) return SSM_ERR_INVALID_ARG;
     if (a->K != ssm::kGK || a->V != ssm::kGV || (a->chunk != 0 && a->chunk != ssm::kGC)) return SSM_ERR_UNSUPPORTED;
     if (!(fabsf(a->scale) <= 3.0e38f)) return SSM_ERR_INVALID_ARG;  // NaN or infinite scale
-    if (a->B * a->H > 0x7fffffff || a->B * a->H * a->T > (int64_t(1) << 40)) return SSM_ERR_INVALID_ARG;
+    if (a->B * a->H > 0x7fffffff) return SSM_ERR_INVALID_ARG;
+    // token rows are addressed by 32-bit copy coordinates
+    if (a->B * a->H * a->T > 0x7fffffff - 2 * ssm::kGC) return SSM_ERR_UNSUPPORTED;
     const bool work = a->B > 0 && a->H > 0 && a->T > 0;
     if (work && (!a->q || !a->k || !a->v || !a->g || !a->b || !a->w || !a->out)) return SSM_ERR_INVALID_ARG;
     const void* ptrs[] = {a->q, a->k, a->v, a->g, a->b, a->w, a->state_in, a->out, a->state_out, a->workspace};
@@ -523,10 +676,19 @@ extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
     if (!ssm::ensure_smem(ssm::gdn2_chunk_fwd_kernel, ssm::kGSmem, mask)) return SSM_ERR_CUDA;
     ssm::Gdn2Params p{};
     p.B = a->B; p.H = a->H; p.T = a->T; p.scale = a->scale;
-    p.q = (const __nv_bfloat16*)a->q; p.k = (const __nv_bfloat16*)a->k; p.v = (const __nv_bfloat16*)a->v;
-    p.b = (const __nv_bfloat16*)a->b; p.w = (const __nv_bfloat16*)a->w; p.g = a->g;
-    p.state_in = a->state_in; p.out = (__nv_bfloat16*)a->out; p.state_out = a->state_out;
     p.status = (unsigned*)a->workspace;
-    ssm::gdn2_chunk_fwd_kernel<<<(unsigned)BH, ssm::kGThreads, ssm::kGSmem, s>>>(p);
+    const int64_t rows = BH * a->T;
+    ssm::Gdn2Maps mp{};
+    const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    const bool enc =
+        ssm::encode_2d(&mp.q, bf, a->q, ssm::kGK, rows, ssm::kGK * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        ssm::encode_2d(&mp.k, bf, a->k, ssm::kGK, rows, ssm::kGK * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        ssm::encode_2d(&mp.b, bf, a->b, ssm::kGK, rows, ssm::kGK * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        ssm::encode_2d(&mp.g, f32, a->g, ssm::kGK, rows, ssm::kGK * 4, ssm::kGK, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        ssm::encode_2d(&mp.v, bf, a->v, ssm::kGV, rows, ssm::kGV * 2, ssm::kGV, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_NONE) &&
+        ssm::encode_2d(&mp.w, bf, a->w, ssm::kGV, rows, ssm::kGV * 2, ssm::kGV, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!enc) return SSM_ERR_CUDA;
+    ssm::gdn2_chunk_fwd_kernel<<<(unsigned)BH, ssm::kGThreads, ssm::kGSmem, s>>>(
+        p, a->state_in, (__nv_bfloat16*)a->out, a->state_out, mp);
     return ssm::count_launches(cudaGetLastError() == cudaSuccess ? 1 : -1);
 }

@@ -577,9 +577,11 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             Pl[2 * q] = make_float2(pq.x, pq.y);
             Pl[2 * q + 1] = make_float2(pq.z, pq.w);
         }
-#pragma unroll
         // SA states at a time: independent adjoint chains for the scheduler
-        constexpr int SA = 4;
+#ifndef SSM_AGG_SA
+#define SSM_AGG_SA 4
+#endif
+        constexpr int SA = SSM_AGG_SA;
 #pragma unroll
         for (int s = 0; s < NS; s += SA) {
             const int n = NS * hk + s;

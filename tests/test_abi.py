@@ -205,6 +205,7 @@ def gdn2_args(ssm, **over):
     (dict(T=-5), INVALID), (dict(q=None), INVALID), (dict(g=None), INVALID), (dict(out=None), INVALID),
     (dict(w=FAKE + 2), ALIGNMENT), (dict(state_in=FAKE + 8), ALIGNMENT), (dict(state_out=FAKE + 4), ALIGNMENT),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(B=1, H=1, T=1 << 31), UNSUPPORTED), (dict(B=4, H=8, T=1 << 26), UNSUPPORTED),
 ])
 def test_gdn2_rejects_bad_arguments(ssm, over, code):
     args = gdn2_args(ssm, **over)
