@@ -25,8 +25,10 @@
 //     are K * decay: the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K);
 //  2. aqk = qk * decay * scale (j <= i); akk = (bk)k^T * decay (j < i), the
 //     decay passed between lane halves through shared memory;
-//  3. T = (I + akk)^-1 by forward substitution, one thread per column, while
-//     other warps form (w*v)^T; MMA W = T (b*k*exp G) in row layout and
+//  3. T = (I + akk)^-1 by 2 x 2 block inversion (16 x 16 diagonal blocks
+//     by forward substitution, the off-diagonal blocks as warp-level tf32
+//     products: T is rounded to bf16 for the products that use it);
+//     MMA W = T (b*k*exp G) in row layout and
 //     U^T = (w*v)^T T^T (the page's row-by-row WY substitution, as
 //     (I + akk) W = rhs);
 //  4. MMA (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T;
@@ -66,7 +68,7 @@ constexpr int kVS = kGS + 32768;        // v staging [64][128] bf16 (TMA)
 constexpr int kMisc = kVS + 16384;      // em, egl [128] fp32; mbarriers; TMEM slot
 constexpr int kB6 = kA2;                // aqk                  64 rows x K=64
 constexpr int kB3 = kA2 + 8192;         // T                    64 rows x K=64 (as A: 128 rows, the rest unused)
-constexpr int kAKK = kA2 + 16384;       // akk^T fp32 [column][row]
+constexpr int kAKK = kA2 + 16384;       // akk fp32 [64][64], row-major, float4 chunks permuted per row
 constexpr int kB5 = kA2 + 16384;        // W                    64 rows x K=128
 constexpr int kA6 = kA3;                // v_new^T             128 rows x K=64
 constexpr int kGSmem = kMisc + 1024 + 64 + 1024;  // + slack for the 1024-byte alignment
@@ -179,6 +181,22 @@ __device__ __forceinline__ void ld8(const char* base, int row, int col, int rows
 __device__ __forceinline__ float bf(__nv_bfloat16 h) { return __bfloat162float(h); }
 
 
+// D[16 x 8] += A[16 x 8] B[8 x 8] on the warp's tensor-core path (tf32
+// operands, fp32 accumulation); g = lane / 4, t = lane % 4 hold
+// a = {A[g][t], A[g+8][t], A[g][t+4], A[g+8][t+4]}, b = {B[t][g], B[t+4][g]},
+// d = {D[g][2t], D[g][2t+1], D[g+8][2t], D[g+8][2t+1]}.
+__device__ __forceinline__ unsigned tf32(float x) {
+    unsigned u;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(x));
+    return u;
+}
+__device__ __forceinline__ void mma_tf32(float* d, const float* a, const float* b) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(tf32(a[0])), "r"(tf32(a[1])), "r"(tf32(a[2])), "r"(tf32(a[3])), "r"(tf32(b[0])), "r"(tf32(b[1])));
+}
+
 // Wait until phase `parity` of the barrier completes (mbarrier.try_wait,
 // which suspends the thread for a while in hardware between checks), at most
 // kWaitNs; returns whether it completed.
@@ -193,36 +211,6 @@ __device__ __forceinline__ bool mbar_wait_try(unsigned bar, unsigned parity) {
             : "memory");
         if (done) return true;
         if (global_ns() - t0 > kWaitNs) return false;
-    }
-}
-
-// T = (I + akk)^-1 (akk strictly lower triangular, 64 x 64) by forward
-// substitution, one thread per column `col`, written to `tb` as the K-major
-// operand T (rows r, K = column). akk is read as its transpose, fp32
-// [column][row], so that step i reads a contiguous broadcast run; rows are
-// updated in pairs with packed fused multiply-adds. Kept out of line: its
-// unrolled steps then draw on registers of their own.
-__device__ __noinline__ void triangular_inverse(const float* akkT, char* tb, int col) {
-    float2 x[kGC / 2];  // rows 2m, 2m+1
-#pragma unroll
-    for (int m = 0; m < kGC / 2; ++m) x[m] = make_float2(2 * m == col ? 1.f : 0.f, 2 * m + 1 == col ? 1.f : 0.f);
-#pragma unroll
-    for (int i = 0; i < kGC - 1; ++i) {
-        const float xi = (i & 1) ? x[i >> 1].y : x[i >> 1].x;  // final: every earlier step has updated it
-        const float2 nx = make_float2(-xi, -xi);
-        const float* a = akkT + i * kGC;  // akk[r][i], r = 0..63
-        if (!(i & 1)) x[i >> 1].y = __fmaf_rn(-a[i + 1], xi, x[i >> 1].y);  // row i+1 shares the pair
-#pragma unroll
-        for (int q4 = ((i >> 1) + 1) >> 1; q4 < kGC / 4; ++q4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(a + 4 * q4);
-            if (2 * (2 * q4) > i) x[2 * q4] = __ffma2_rn(make_float2(a4.x, a4.y), nx, x[2 * q4]);
-            if (2 * (2 * q4 + 1) > i) x[2 * q4 + 1] = __ffma2_rn(make_float2(a4.z, a4.w), nx, x[2 * q4 + 1]);
-        }
-    }
-#pragma unroll
-    for (int m = 0; m < kGC / 2; ++m) {
-        st1(tb, 2 * m, col, 64, x[m].x);  // T[r][col]
-        st1(tb, 2 * m + 1, col, 64, x[m].y);
     }
 }
 
@@ -247,7 +235,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     float* s_gm = reinterpret_cast<float*>(sm + kA2);    // column-pass exchange (A2 is written after it)
     float* s_gl = s_gm + kGK;
     float* s_e = reinterpret_cast<float*>(sm + kGS);     // g, then E+ [64][128]; then the decay [64][64]
-    float* s_akkT = reinterpret_cast<float*>(sm + kAKK);
+    float* s_akk = reinterpret_cast<float*>(sm + kAKK);
+    // akk[i][j]: row i, its float4 chunks permuted by i % 16 (conflict-free row and column access)
+    auto akk_at = [&](int i, int j) -> float* { return s_akk + i * kGC + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3)); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quarter = warp & 3, whalf = warp >> 2;  // TMEM lanes 32*quarter..; column half
@@ -283,9 +273,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
         mbar_expect_tx(bar, bytes);
         tma_load_2d(sm + off, m, 0, row_of(cj), bar);
     };
+    // thread kTmaThread (warp 2, idle while the first two lane quarters run the
+    // epilogues) issues the copies; thread 0 issues the products
+    constexpr int kTmaThread = 64;
+    if (tid == kTmaThread) {
+        const CUtensorMap* maps[6] = {&mp.q, &mp.k, &mp.b, &mp.g, &mp.v, &mp.w};
+        for (int m = 0; m < 6; ++m)
+            asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(maps[m])) : "memory");
+    }
     if (tid == 0) {
         for (int b = 0; b < 5; ++b) mbar_init(smem_u32(bars + b), 1);
         mbar_fence_init();
+    }
+    __syncthreads();
+    if (tid == kTmaThread) {
         if (nchunks > 0) {
             issue_qkb(0);
             issue_one(bar_g, kGS, &mp.g, kGBytes, 0);
@@ -332,11 +333,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (!ok) fail();
         return __syncthreads_and(ok) != 0;
     };
-    auto copy_wait = [&](int b) -> bool {  // every thread waits for copy b of the current chunk
-        const bool ok = mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1));
-        if (ok) waited[b]++;
+    auto copies_wait = [&](int b0, int b1) -> bool {  // copies b0..b1 of the current chunk, one CTA barrier
+        bool ok = true;
+        for (int b = b0; b <= b1; ++b) ok = ok && mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1));
         if (!ok) fail();
-        return __syncthreads_and(ok) != 0;
+        const bool all = __syncthreads_and(ok) != 0;
+        if (all)
+            for (int b = b0; b <= b1; ++b) waited[b]++;
+        return all;
     };
     auto commit = [&]() {
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     };
     auto refill = [&](int b, int cj) {  // next chunk's copy into a buffer all threads are done reading
         if (cj >= nchunks) return;
-        if (tid == 0) {
+        if (tid == kTmaThread) {
             fence_async_smem();
             if (b == 0) issue_qkb(cj);
             else if (b == 1) issue_one(bar_g, kGS, &mp.g, kGBytes, cj);
@@ -360,39 +364,24 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int c = (int)min64(kGC, T - t0);  // live tokens; rows c..63 are zero (identity tokens)
         const int64_t row0 = bh * T + t0;      // first token row of the chunk in [B*H*T]
 
-        // ---- 0a. b*k in place; rows past the chunk's tokens zeroed
-        if (!(ok = copy_wait(0))) break;
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int e = tid + it * kGThreads;
-            const int r = e >> 4, cc = (e & 15) * 8;
-            char* pb = sm + kA1 + swz(64 + r, cc, 128);
-            char* pk = sm + kB1 + swz(r, cc, 64);
-            if (r < c) {
-                float bv[8], kv[8];
-                unpack8(*reinterpret_cast<const uint4*>(pb), bv);
-                unpack8(*reinterpret_cast<const uint4*>(pk), kv);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) bv[i] *= kv[i];
-                *reinterpret_cast<uint4*>(pb) = make_uint4(pack_bf2(bv[0], bv[1]), pack_bf2(bv[2], bv[3]),
-                                                           pack_bf2(bv[4], bv[5]), pack_bf2(bv[6], bv[7]));
-            } else {
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(pb) = z;
-                *reinterpret_cast<uint4*>(pk) = z;
-                *reinterpret_cast<uint4*>(sm + kA1 + swz(r, cc, 128)) = z;
-            }
-        }
-        // ---- 0b. column pass (thread = key channel n, tokens 32*hf ..+31)
-        if (!(ok = copy_wait(1))) break;  // g (also orders 0a's stores before the reads below)
+        // ---- 0. column pass (thread = channel n, tokens 32*hf ..+31) over all
+        // four copies of the chunk: G = cumsum(g) and E+ in place of g; b*k
+        // in place of b; (b*k*exp G)^T, (k*exp(G[last] - G))^T and (w*v)^T.
+        // Rows past the chunk's tokens: b*k and k zeroed (identity tokens);
+        // q's rows there only reach outputs that are not stored.
+        if (!(ok = copies_wait(0, 3))) break;
         const int n = tid & (kGK - 1), hf = tid >> 7, j0 = hf * 32;
-        float G[32];
+        float G[32], wv[32];
         {
+            // w is read here and (w*v)^T written over it after two CTA barriers
+            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + kVS);
+            const __nv_bfloat16* sw = reinterpret_cast<const __nv_bfloat16*>(sm + kA4);
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float gv = j0 + i < c ? s_e[(j0 + i) * kGK + n] : 0.f;
-                acc = __fadd_rn(acc, gv);
+                const int j = j0 + i;
+                wv[i] = j < c ? bf(sv[j * kGV + n]) * bf(sw[j * kGV + n]) : 0.f;
+                acc = __fadd_rn(acc, j < c ? s_e[j * kGK + n] : 0.f);
                 G[i] = acc;
             }
             if (hf == 0) s_gm[n] = acc;  // G at the middle token m = 31
@@ -422,14 +411,22 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     const float ep = ex2((G[i] - Gm) * L2E);  // E+ = exp(G - G[m])
                     const float en = rcp(ep);                  // E- = exp(G[m] - G)
                     s_e[j * kGK + n] = ep;                     // in place of g (same thread)
-                    a3[ii] = ld1(sm + kA1, 64 + j, n, 128) * (ep * em);  // b*k*exp(G)
-                    b8[ii] = ld1(sm + kB1, j, n, 64) * (en * elm);       // k*exp(G[last] - G)
+                    const bool live = j < c;
+                    const float kk = live ? ld1(sm + kB1, j, n, 64) : 0.f;
+                    const float bk = live ? ld1(sm + kA1, 64 + j, n, 128) * kk : 0.f;
+                    st1(sm + kA1, 64 + j, n, 128, bk);  // b*k in place of b
+                    if (!live) st1(sm + kB1, j, n, 64, 0.f);
+                    a3[ii] = bk * (ep * em);   // b*k*exp(G)
+                    b8[ii] = kk * (en * elm);  // k*exp(G[last] - G)
                 }
                 st8(sm + kA3, n, j0 + i0, 128, a3);
                 st8(sm + kB8, n, j0 + i0, 128, b8);
             }
+#pragma unroll
+            for (int i0 = 0; i0 < 32; i0 += 8) st8(sm + kA4, n, j0 + i0, 128, wv + i0);  // (w*v)^T
         }
-        __syncthreads();  // E+; exp tables
+        __syncthreads();  // E+; exp tables; the operands
+        refill(2, ci + 1);  // v has been read
         // ---- 0c. row pass: [E+; E-] and q*exp(G)*scale
 #pragma unroll 2
         for (int it = 0; it < 4; ++it) {
@@ -470,7 +467,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int jb = whalf * 32;
             float d1[32];
             tmem_ld32(tmem + tlane + kTD1 + (unsigned)jb, d1);
-            float* s_dec = s_e;  // [64][64]
+            // the decay [64][64] fp32, float4 chunks permuted per row as in akk
+            auto dec_at = [&](int i, int j) -> float* { return s_e + i * kGC + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3)); };
             if (quarter < 2) {
                 const int i = vrow;
                 float d2[32];
@@ -483,8 +481,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 4)
-                    *reinterpret_cast<float4*>(s_dec + i * kGC + jb + jj) =
-                        make_float4(d2[jj], d2[jj + 1], d2[jj + 2], d2[jj + 3]);
+                    *reinterpret_cast<float4*>(dec_at(i, jb + jj)) = make_float4(d2[jj], d2[jj + 1], d2[jj + 2], d2[jj + 3]);
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 8) st8(sm + kB6, i, jb + jj, 64, d1 + jj);
             }
@@ -493,40 +490,132 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 const int i = vrow - 64;
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 4) {
-                    const float4 dec = *reinterpret_cast<const float4*>(s_dec + i * kGC + jb + jj);
+                    const float4 dec = *reinterpret_cast<const float4*>(dec_at(i, jb + jj));
                     const float dv[4] = {dec.x, dec.y, dec.z, dec.w};
+                    float a4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int j = jb + jj + e;
-                        s_akkT[j * kGC + i] = (j < i) ? d1[jj + e] * dv[e] : 0.f;
-                    }
+                    for (int e = 0; e < 4; ++e) a4[e] = (jb + jj + e < i) ? d1[jj + e] * dv[e] : 0.f;
+                    *reinterpret_cast<float4*>(akk_at(i, jb + jj)) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                 }
             }
         }
         tc_before();
         __syncthreads();
-        refill(1, ci + 1);  // g / E+ / the decay have been read
-        if (!(ok = copy_wait(2))) break;  // v
-        if (!(ok = copy_wait(3))) break;  // w
-
-        // ---- 3. T = (I + akk)^-1 (warps 0-1) while warps 4-7 form (w*v)^T
-        if (warp < 2) {
-            triangular_inverse(s_akkT, sm + kB3, tid);
-        } else if (warp >= 4) {
-            const int vn = tid - 128;  // value channel
-            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + kVS);
-            const __nv_bfloat16* sw = reinterpret_cast<const __nv_bfloat16*>(sm + kA4);
-            float wv[kGC];
+        // ---- 3. T = (I + akk)^-1 by blocks; then W and U^T
+        // The inverse of the unit lower-triangular I + akk by blocks: for
+        // [[A, 0], [C, B]] the inverse is [[A^-1, 0], [-B^-1 C A^-1, B^-1]].
+        // (a) the four diagonal 16 x 16 blocks by forward substitution (one
+        // thread per column); (b) the two off-diagonal 16 x 16 blocks inside
+        // the 32 x 32 halves; (c) the lower 32 x 32 block. fp32 throughout.
+        constexpr int TS = kGC + 4;   // row stride of T: rows 4 banks apart
+        float* TT = s_e;              // T fp32 [64][TS], row-major (g's staging buffer is free)
+        float* TY = s_e + kGC * TS;   // scratch products
+        if (tid < kGC) {
+            const int base = (tid >> 4) * 16, cl = tid & 15;
+            float x[16];
 #pragma unroll
-            for (int j = 0; j < kGC; ++j) wv[j] = j < c ? bf(sv[j * kGV + vn]) * bf(sw[j * kGV + vn]) : 0.f;
-            asm volatile("bar.sync 1, 128;\n" ::: "memory");  // w read by all four warps before A4 is rewritten
+            for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < kGC; j += 8) st8(sm + kA4, vn, j, 128, wv + j);
+            for (int i = 0; i < 15; ++i) {
+#pragma unroll
+                for (int r = i + 1; r < 16; ++r) x[r] = __fmaf_rn(-*akk_at(base + r, base + i), x[i], x[r]);
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) TT[(base + r) * TS + base + cl] = x[r];
+        } else {  // zeros above the diagonal blocks: blocks (0,1), (2,3) and the upper 32 x 32
+            for (int e = tid - kGC; e < 1024 + 512; e += kGThreads - kGC) {
+                int r, cc;
+                if (e < 1024) {  // rows 0-31, columns 32-63
+                    r = e >> 5;
+                    cc = 32 + (e & 31);
+                } else {         // block (0,1) (rows 0-15, columns 16-31) or (2,3) (rows 32-47, columns 48-63)
+                    const int f = e - 1024, blk = f >> 8;
+                    r = 32 * blk + ((f >> 4) & 15);
+                    cc = 32 * blk + 16 + (f & 15);
+                }
+                TT[r * TS + cc] = 0.f;
+            }
+        }
+        __syncthreads();
+        {   // (b) T[R0+r][C0+c] = -D_hi (L D_lo), R0 = 16 + 32p, C0 = 32p: warps 0-3,
+            // problem p = warp / 2, 8-column tile nj = warp % 2, two k-steps of 8
+            const int g = lane >> 2, t = lane & 3;
+            const int pb = (warp >> 1) & 1, nj = warp & 1;
+            const int R0 = 16 + 32 * pb, C0 = 32 * pb;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            if (warp < 4) {
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks;
+                    const float av[4] = {*akk_at(R0 + g, C0 + k0 + t), *akk_at(R0 + g + 8, C0 + k0 + t),
+                                         *akk_at(R0 + g, C0 + k0 + t + 4), *akk_at(R0 + g + 8, C0 + k0 + t + 4)};
+                    const float bv[2] = {TT[(C0 + k0 + t) * TS + C0 + 8 * nj + g],
+                                         TT[(C0 + k0 + t + 4) * TS + C0 + 8 * nj + g]};
+                    mma_tf32(d, av, bv);
+                }
+                float* y = TY + pb * 256 + 8 * nj + 2 * t;  // Y [16][16] per problem
+                y[g * 16] = d[0]; y[g * 16 + 1] = d[1]; y[(g + 8) * 16] = d[2]; y[(g + 8) * 16 + 1] = d[3];
+            }
+            __syncthreads();
+            if (warp < 4) {
+                d[0] = d[1] = d[2] = d[3] = 0.f;
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    const int k0 = 8 * ks;
+                    const float* dh = TT + (R0 + g) * TS + R0 + k0 + t;
+                    const float av[4] = {-dh[0], -dh[8 * TS], -dh[4], -dh[8 * TS + 4]};
+                    const float* yb = TY + pb * 256 + (k0 + t) * 16 + 8 * nj + g;
+                    const float bv[2] = {yb[0], yb[4 * 16]};
+                    mma_tf32(d, av, bv);
+                }
+                float* o = TT + (R0 + g) * TS + C0 + 8 * nj + 2 * t;
+                o[0] = d[0]; o[1] = d[1]; o[8 * TS] = d[2]; o[8 * TS + 1] = d[3];
+            }
+        }
+        __syncthreads();
+        {   // (c) T[32+r][c] = -E1 (L E0), E0 = T[0:32][0:32], E1 = T[32:64][32:64]:
+            // 16-row tile mi = warp / 4, 8-column tile nj = warp % 4, four k-steps
+            const int g = lane >> 2, t = lane & 3;
+            const int mi = warp >> 2, nj = warp & 3;
+            const int r0 = 16 * mi, cc = 8 * nj;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int k0 = 8 * ks;
+                const float av[4] = {*akk_at(32 + r0 + g, k0 + t), *akk_at(32 + r0 + g + 8, k0 + t),
+                                     *akk_at(32 + r0 + g, k0 + t + 4), *akk_at(32 + r0 + g + 8, k0 + t + 4)};
+                const float bv[2] = {TT[(k0 + t) * TS + cc + g], TT[(k0 + t + 4) * TS + cc + g]};
+                mma_tf32(d, av, bv);
+            }
+            float* y = TY + (r0 + g) * 32 + cc + 2 * t;  // Y [32][32]
+            y[0] = d[0]; y[1] = d[1]; y[8 * 32] = d[2]; y[8 * 32 + 1] = d[3];
+            __syncthreads();
+            d[0] = d[1] = d[2] = d[3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int k0 = 8 * ks;
+                const float* e1 = TT + (32 + r0 + g) * TS + 32 + k0 + t;
+                const float av[4] = {-e1[0], -e1[8 * TS], -e1[4], -e1[8 * TS + 4]};
+                const float bv[2] = {TY[(k0 + t) * 32 + cc + g], TY[(k0 + t + 4) * 32 + cc + g]};
+                mma_tf32(d, av, bv);
+            }
+            float* o = TT + (32 + r0 + g) * TS + cc + 2 * t;
+            o[0] = d[0]; o[1] = d[1]; o[8 * TS] = d[2]; o[8 * TS + 1] = d[3];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int it = 0; it < 2; ++it) {  // T into the K-major operand (rows r, K = column)
+            const int e = tid + it * kGThreads;
+            const int r = e >> 3, cc = (e & 7) * 8;
+            float tv[8];
+            *reinterpret_cast<float4*>(tv) = *reinterpret_cast<const float4*>(TT + r * TS + cc);
+            *reinterpret_cast<float4*>(tv + 4) = *reinterpret_cast<const float4*>(TT + r * TS + cc + 4);
+            st8(sm + kB3, r, cc, 64, tv);
         }
         fence_async_smem();
         tc_before();
         __syncthreads();
-        refill(2, ci + 1);  // v has been read
+        refill(1, ci + 1);  // g's buffer (E+, the decay, T) has been read
         if (tid == 0) {
             tc_after();
             // W = T (b*k*exp G): rows i in lanes 0-63, 128 columns; A = T as a 128-row operand
@@ -619,7 +708,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 
     if (!ok) {  // a wait ran out: let the copies still in flight land before the CTA exits
-        if (tid == 0)
+        if (tid == kTmaThread)
             for (int b = 0; b < 4; ++b)
                 for (; waited[b] < issued[b]; ++waited[b])
                     if (!mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1))) break;
