@@ -6,21 +6,24 @@
 // its transpose S^T in 128 TMEM columns (lane = value channel v, column =
 // key channel n). Every product is a tcgen05.mma (kind::f16: bf16 operands,
 // fp32 accumulation, M = 128) whose operands one thread points at in shared
-// memory in the tensor core's 128-byte-swizzled K-major layout (rows of
-// 128 bytes = 64 bf16 of K, 8-row groups 1024 bytes apart, the 16-byte
-// chunks of row r permuted by r % 8).
+// memory in the tensor core's 128-byte-swizzled layouts (rows of 128 bytes =
+// 64 bf16, 8-row groups 1024 bytes apart, the 16-byte chunks of row r
+// permuted by r % 8; rows along M or N for K-major operands, along K for
+// MN-major ones).
 //
 // Inputs arrive by TMA, one chunk ahead: q, k and b straight into the first
-// product's operands (128-byte swizzled boxes, which is that layout), g, v
-// and w into staging buffers; each copy is issued as soon as the buffer it
+// product's operands, v and w as the same 128-byte-swizzled 64-column boxes,
+// g into a staging buffer; each copy is issued as soon as the buffer it
 // lands in has been read for the current chunk, so it runs under the
-// current chunk's work.
+// current chunk's work. Operands whose contraction runs over tokens (b*k*
+// exp G, k*exp(G[last] - G), w*v) are kept row-major, token by channel, and
+// handed to the tensor core as MN-major operands -- no transposes.
 //
 // Per chunk (the page's steps, with the products arranged so that M = 128):
-//  0. b*k in place; column pass (thread = one key channel, 32 tokens):
-//     G = cumsum of g; E+ = exp(G - G[m]) about the middle token m (fp32,
-//     in place of g); (b*k*exp G)^T and (k*exp(G[last] - G))^T. Row pass:
-//     [E+; E-] with E- = 1/E+, and q*exp(G)*scale;
+//  0. column pass (thread = one key channel, 32 tokens): G = cumsum of g,
+//     E+ = exp(G - G[m]) about the middle token m (fp32, in place of g).
+//     Row pass (thread = 8 channels of a token): [E+; E-] with E- = 1/E+,
+//     q*exp(G)*scale, b*k, b*k*exp(G), k*exp(G[last] - G), w*v;
 //  1. MMA [q; b*k] k^T and [E+; E-] E-^T (the first 64 lanes of the second
 //     are K * decay: the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K);
 //  2. aqk = qk * decay * scale (j <= i); akk = (bk)k^T * decay (j < i), the
@@ -28,9 +31,8 @@
 //  3. T = (I + akk)^-1 by 2 x 2 block inversion (16 x 16 diagonal blocks
 //     by forward substitution, the off-diagonal blocks as warp-level tf32
 //     products: T is rounded to bf16 for the products that use it);
-//     MMA W = T (b*k*exp G) in row layout and
-//     U^T = (w*v)^T T^T (the page's row-by-row WY substitution, as
-//     (I + akk) W = rhs);
+//     MMA W = T (b*k*exp G) in row layout and U^T = (w*v)^T T^T (the
+//     page's row-by-row WY substitution, as (I + akk) W = rhs);
 //  4. MMA (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T;
 //  5. MMA out^T = v_new^T aqk^T + S^T (q*exp(G)*scale)^T, and, after S^T
 //     is scaled column-wise by exp(G[last]), S^T += v_new^T (k*exp(G[last]-G)).
@@ -58,20 +60,20 @@ constexpr int kGThreads = 256;
 constexpr int kA1 = 0;                  // [q; b*k]            128 rows x K=128 (q, b by TMA)
 constexpr int kB1 = kA1 + 32768;        // k                    64 rows x K=128 (TMA)
 constexpr int kA2 = kB1 + 16384;        // [E+; E-]            128 rows x K=128 (E- = rows 64.. as a B operand)
-constexpr int kA3 = kA2 + 32768;        // (b*k*exp G)^T       128 rows x K=64  (then v_new^T)
-constexpr int kA4 = kA3 + 16384;        // w staging [64][128] (TMA), then (w*v)^T 128 rows x K=64
+constexpr int kA3 = kA2 + 32768;        // b*k*exp(G)          MN-major [64 tokens][128]  (then v_new^T)
+constexpr int kA4 = kA3 + 16384;        // w (TMA), then w*v   MN-major [64 tokens][128]
 constexpr int kA5 = kA4 + 16384;        // S^T (bf16)          128 rows x K=128
 constexpr int kB7 = kA5 + 32768;        // q*exp(G)*scale       64 rows x K=128
-constexpr int kB8 = kB7 + 16384;        // (k*exp(Glast-G))^T  128 rows x K=64
+constexpr int kB8 = kB7 + 16384;        // k*exp(Glast-G)      MN-major [64 tokens][128]
 constexpr int kGS = kB8 + 16384;        // g staging fp32 [64][128] (TMA) -> E+; then the decay fp32 [64][64]
-constexpr int kVS = kGS + 32768;        // v staging [64][128] bf16 (TMA)
-constexpr int kMisc = kVS + 16384;      // em, egl [128] fp32; mbarriers; TMEM slot
+constexpr int kVS = kGS + 32768;        // v staging, swz(token, channel, 64) image (TMA)
+constexpr int kMisc = kVS + 16384;      // em, egl, elm [128] fp32; mbarriers; TMEM slot
 constexpr int kB6 = kA2;                // aqk                  64 rows x K=64
 constexpr int kB3 = kA2 + 8192;         // T                    64 rows x K=64 (as A: 128 rows, the rest unused)
 constexpr int kAKK = kA2 + 16384;       // akk fp32 [64][64], row-major, float4 chunks permuted per row
 constexpr int kB5 = kA2 + 16384;        // W                    64 rows x K=128
 constexpr int kA6 = kA3;                // v_new^T             128 rows x K=64
-constexpr int kGSmem = kMisc + 1024 + 64 + 1024;  // + slack for the 1024-byte alignment
+constexpr int kGSmem = kMisc + 1536 + 64 + 1024;  // + slack for the 1024-byte alignment
 static_assert(kGSmem <= 227 * 1024, "shared memory");
 constexpr unsigned kQkbBytes = 3 * 2 * 64 * 128;  // q, b, k: two 64-column boxes each
 constexpr unsigned kGBytes = kGC * kGK * 4, kVBytes = kGC * kGV * 2;
@@ -87,25 +89,40 @@ __device__ __forceinline__ int swz(int row, int col, int rows) {
            ((col & 7) << 1);
 }
 
-// Shared-memory matrix descriptor: 128-byte swizzled K-major layout, SBO 1024.
+// Shared-memory matrix descriptors, 128-byte swizzle. K-major: 8-row groups
+// 1024 bytes apart (SBO), K advancing inside the 128-byte rows. MN-major
+// (the operand stored as rows of K, M or N contiguous): the same 1024-byte
+// atoms with the roles swapped -- a 128-byte row holds 64 elements of M or
+// N, 8 rows of K make an atom; SBO = 1024 between 8-row groups of K, LBO =
+// 8192 between the 64-element blocks of M or N. That is the image
+// swz(k, mn, 64) writes, and what a 128-byte-swizzled TMA box of 64 columns
+// x 64 rows lands as.
 __device__ __forceinline__ uint64_t desc_sw128(unsigned addr) {
     return (uint64_t)((addr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
            (2ull << 61);
 }
-
-// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, both K-major, M = 128, N = n.
-__host__ __device__ constexpr uint32_t idesc_m128(int n) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+__device__ __forceinline__ uint64_t desc_sw128_mn(unsigned addr) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(8192 >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           (1ull << 46) | (2ull << 61);
 }
 
-// D[128 x n] (+)= A[128 x kdim] B[n x kdim]^T, both operands K-major swizzled
-// in shared memory; b_rows is the row count B's 64-wide K atoms are laid out for.
+// kind::f16 instruction descriptor: fp32 accumulator, bf16 A and B, M = 128,
+// N = n; A and B K-major unless a_mn / b_mn (bits 15 / 16: MN-major).
+__host__ __device__ constexpr uint32_t idesc_m128(int n, bool a_mn = false, bool b_mn = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+
+// D[128 x n] (+)= A[128 x kdim] B[kdim x n]. A K-major (128 rows) or, with
+// a_mn, MN-major (the swz(k, m, 64) image); B K-major with its 64-wide K
+// atoms laid out for b_rows rows or, with b_mn, MN-major (swz(k, n, 64)).
 __device__ __forceinline__ void mma_issue(unsigned d_tmem, unsigned a, unsigned b, int b_rows, int n, int kdim,
-                                          bool accumulate) {
-    const uint32_t id = idesc_m128(n);
-    for (int j = 0; j < kdim / 16; ++j) {  // K = 16 per instruction: atom j/4, 32-byte step j%4
-        const uint64_t ad = desc_sw128(a + (j >> 2) * 128 * 128 + (j & 3) * 32);
-        const uint64_t bd = desc_sw128(b + (j >> 2) * b_rows * 128 + (j & 3) * 32);
+                                          bool accumulate, bool a_mn = false, bool b_mn = false) {
+    const uint32_t id = idesc_m128(n, a_mn, b_mn);
+    for (int j = 0; j < kdim / 16; ++j) {  // K = 16 per instruction
+        // K-major: atom j/4, 32-byte step j%4; MN-major: two 8-row K groups per step
+        const uint64_t ad = a_mn ? desc_sw128_mn(a + j * 2048) : desc_sw128(a + (j >> 2) * 128 * 128 + (j & 3) * 32);
+        const uint64_t bd = b_mn ? desc_sw128_mn(b + j * 2048) : desc_sw128(b + (j >> 2) * b_rows * 128 + (j & 3) * 32);
         const unsigned acc = (accumulate || j > 0) ? 1u : 0u;
         asm volatile(
             "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n"
@@ -161,12 +178,6 @@ __device__ __forceinline__ void st8(char* base, int row, int col, int rows, cons
     *reinterpret_cast<uint4*>(base + swz(row, col, rows)) =
         make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
 }
-__device__ __forceinline__ void st1(char* base, int row, int col, int rows, float v) {
-    *reinterpret_cast<__nv_bfloat16*>(base + swz(row, col, rows)) = __float2bfloat16_rn(v);
-}
-__device__ __forceinline__ float ld1(const char* base, int row, int col, int rows) {
-    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(base + swz(row, col, rows)));
-}
 __device__ __forceinline__ void unpack8(uint4 u, float* f) {
     const unsigned w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -178,7 +189,6 @@ __device__ __forceinline__ void unpack8(uint4 u, float* f) {
 __device__ __forceinline__ void ld8(const char* base, int row, int col, int rows, float* f) {
     unpack8(*reinterpret_cast<const uint4*>(base + swz(row, col, rows)), f);
 }
-__device__ __forceinline__ float bf(__nv_bfloat16 h) { return __bfloat162float(h); }
 
 
 // D[16 x 8] += A[16 x 8] B[8 x 8] on the warp's tensor-core path (tf32
@@ -220,7 +230,7 @@ struct Gdn2Params {
     unsigned* status;
 };
 struct Gdn2Maps {
-    CUtensorMap q, k, b, g, v, w;  // rows = B*H*T tokens; q, k, b: 64-column swizzled boxes; g, v, w: whole rows
+    CUtensorMap q, k, b, g, v, w;  // rows = B*H*T tokens; q, k, b, v, w: 64-column swizzled boxes; g: whole rows
 };
 
 __global__ void __launch_bounds__(kGThreads, 1)
@@ -230,10 +240,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     char* sm = g_smem_raw + ((1024u - (smem_u32(g_smem_raw) & 1023u)) & 1023u);
     float* s_em = reinterpret_cast<float*>(sm + kMisc);  // exp(G[m]) per key channel
     float* s_egl = s_em + kGK;                           // exp(G[last])
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_egl + kGK);  // mma, qkb, g, v, w
+    float* s_elm = s_egl + kGK;                          // exp(G[last] - G[m])
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_elm + kGK);  // mma, qkb, g, v, w
     unsigned* tslot = reinterpret_cast<unsigned*>(bars + 5);
     float* s_gm = reinterpret_cast<float*>(sm + kA2);    // column-pass exchange (A2 is written after it)
-    float* s_gl = s_gm + kGK;
     float* s_e = reinterpret_cast<float*>(sm + kGS);     // g, then E+ [64][128]; then the decay [64][64]
     float* s_akk = reinterpret_cast<float*>(sm + kAKK);
     // akk[i][j]: row i, its float4 chunks permuted by i % 16 (conflict-free row and column access)
@@ -273,6 +283,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
         mbar_expect_tx(bar, bytes);
         tma_load_2d(sm + off, m, 0, row_of(cj), bar);
     };
+    auto issue_sw = [&](unsigned bar, int off, const CUtensorMap* m, int cj) {  // two 64-column swizzled boxes
+        mbar_expect_tx(bar, kVBytes);
+        tma_load_2d(sm + off, m, 0, row_of(cj), bar);
+        tma_load_2d(sm + off + 8192, m, 64, row_of(cj), bar);
+    };
     // thread kTmaThread (warp 2, idle while the first two lane quarters run the
     // epilogues) issues the copies; thread 0 issues the products
     constexpr int kTmaThread = 64;
@@ -290,8 +305,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (nchunks > 0) {
             issue_qkb(0);
             issue_one(bar_g, kGS, &mp.g, kGBytes, 0);
-            issue_one(bar_v, kVS, &mp.v, kVBytes, 0);
-            issue_one(bar_w, kA4, &mp.w, kVBytes, 0);
+            issue_sw(bar_v, kVS, &mp.v, 0);
+            issue_sw(bar_w, kA4, &mp.w, 0);
         }
     }
     tc_before();
@@ -352,8 +367,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             fence_async_smem();
             if (b == 0) issue_qkb(cj);
             else if (b == 1) issue_one(bar_g, kGS, &mp.g, kGBytes, cj);
-            else if (b == 2) issue_one(bar_v, kVS, &mp.v, kVBytes, cj);
-            else issue_one(bar_w, kA4, &mp.w, kVBytes, cj);
+            else if (b == 2) issue_sw(bar_v, kVS, &mp.v, cj);
+            else issue_sw(bar_w, kA4, &mp.w, cj);
         }
         issued[b]++;
     };
@@ -364,92 +379,82 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const int c = (int)min64(kGC, T - t0);  // live tokens; rows c..63 are zero (identity tokens)
         const int64_t row0 = bh * T + t0;      // first token row of the chunk in [B*H*T]
 
-        // ---- 0. column pass (thread = channel n, tokens 32*hf ..+31) over all
-        // four copies of the chunk: G = cumsum(g) and E+ in place of g; b*k
-        // in place of b; (b*k*exp G)^T, (k*exp(G[last] - G))^T and (w*v)^T.
-        // Rows past the chunk's tokens: b*k and k zeroed (identity tokens);
-        // q's rows there only reach outputs that are not stored.
+        // ---- 0. column pass (thread = key channel n, tokens 32*hf ..+31):
+        // G = cumsum(g) and E+ = exp(G - G[m]) in place of g; per-channel
+        // exp(G[m]), exp(G[last]), exp(G[last] - G[m])
         if (!(ok = copies_wait(0, 3))) break;
-        const int n = tid & (kGK - 1), hf = tid >> 7, j0 = hf * 32;
-        float G[32], wv[32];
         {
-            // w is read here and (w*v)^T written over it after two CTA barriers
-            const __nv_bfloat16* sv = reinterpret_cast<const __nv_bfloat16*>(sm + kVS);
-            const __nv_bfloat16* sw = reinterpret_cast<const __nv_bfloat16*>(sm + kA4);
+            const int n = tid & (kGK - 1), hf = tid >> 7, j0 = hf * 32;
+            float G[32];
             float acc = 0.f;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const int j = j0 + i;
-                wv[i] = j < c ? bf(sv[j * kGV + n]) * bf(sw[j * kGV + n]) : 0.f;
-                acc = __fadd_rn(acc, j < c ? s_e[j * kGK + n] : 0.f);
+                acc = __fadd_rn(acc, j0 + i < c ? s_e[(j0 + i) * kGK + n] : 0.f);
                 G[i] = acc;
             }
             if (hf == 0) s_gm[n] = acc;  // G at the middle token m = 31
-        }
-        __syncthreads();
-        const float Gm = s_gm[n];
-        if (hf == 1) {
+            __syncthreads();
+            const float Gm = s_gm[n];
+            if (hf == 1) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) G[i] = __fadd_rn(G[i], Gm);
-            s_gl[n] = G[31];  // G at the last row (= the last live token: later rows add zeros)
-        }
-        __syncthreads();
-        {
-            const float Gl = s_gl[n];
-            const float em = ex2(Gm * L2E);
-            const float elm = ex2((Gl - Gm) * L2E);  // exp(G[last] - G[m])
-            if (hf == 0) {
-                s_em[n] = em;
+                for (int i = 0; i < 32; ++i) G[i] = __fadd_rn(G[i], Gm);
+                const float Gl = G[31];  // G at the last row (= the last live token: later rows add zeros)
+                s_em[n] = ex2(Gm * L2E);
                 s_egl[n] = ex2(Gl * L2E);
+                s_elm[n] = ex2((Gl - Gm) * L2E);
             }
 #pragma unroll
-            for (int i0 = 0; i0 < 32; i0 += 8) {
-                float a3[8], b8[8];
-#pragma unroll
-                for (int ii = 0; ii < 8; ++ii) {
-                    const int i = i0 + ii, j = j0 + i;
-                    const float ep = ex2((G[i] - Gm) * L2E);  // E+ = exp(G - G[m])
-                    const float en = rcp(ep);                  // E- = exp(G[m] - G)
-                    s_e[j * kGK + n] = ep;                     // in place of g (same thread)
-                    const bool live = j < c;
-                    const float kk = live ? ld1(sm + kB1, j, n, 64) : 0.f;
-                    const float bk = live ? ld1(sm + kA1, 64 + j, n, 128) * kk : 0.f;
-                    st1(sm + kA1, 64 + j, n, 128, bk);  // b*k in place of b
-                    if (!live) st1(sm + kB1, j, n, 64, 0.f);
-                    a3[ii] = bk * (ep * em);   // b*k*exp(G)
-                    b8[ii] = kk * (en * elm);  // k*exp(G[last] - G)
-                }
-                st8(sm + kA3, n, j0 + i0, 128, a3);
-                st8(sm + kB8, n, j0 + i0, 128, b8);
-            }
-#pragma unroll
-            for (int i0 = 0; i0 < 32; i0 += 8) st8(sm + kA4, n, j0 + i0, 128, wv + i0);  // (w*v)^T
+            for (int i = 0; i < 32; ++i) s_e[(j0 + i) * kGK + n] = ex2((G[i] - Gm) * L2E);  // same thread's entries
         }
-        __syncthreads();  // E+; exp tables; the operands
-        refill(2, ci + 1);  // v has been read
-        // ---- 0c. row pass: [E+; E-] and q*exp(G)*scale
+        __syncthreads();  // E+; the exp tables
+        // ---- 0c. row pass (thread = token r, channels cc..cc+7): [E+; E-],
+        // q*exp(G)*scale, b*k in place of b, and the MN-major operands
+        // b*k*exp(G), k*exp(G[last] - G), w*v (in place of w). Rows past the
+        // chunk's tokens: b*k, k, w*v zeroed (identity tokens); q's rows there
+        // only reach outputs that are not stored.
 #pragma unroll 2
         for (int it = 0; it < 4; ++it) {
             const int e = tid + it * kGThreads;
             const int r = e >> 4, cc = (e & 15) * 8;
-            float ep[8], en[8], qv[8], em8[8];
+            const bool live = r < c;
+            float ep[8], en[8], qv[8], kv[8], bv[8], wv[8], vv[8], em8[8], elm8[8];
             *reinterpret_cast<float4*>(ep) = *reinterpret_cast<const float4*>(s_e + r * kGK + cc);
             *reinterpret_cast<float4*>(ep + 4) = *reinterpret_cast<const float4*>(s_e + r * kGK + cc + 4);
             *reinterpret_cast<float4*>(em8) = *reinterpret_cast<const float4*>(s_em + cc);
             *reinterpret_cast<float4*>(em8 + 4) = *reinterpret_cast<const float4*>(s_em + cc + 4);
+            *reinterpret_cast<float4*>(elm8) = *reinterpret_cast<const float4*>(s_elm + cc);
+            *reinterpret_cast<float4*>(elm8 + 4) = *reinterpret_cast<const float4*>(s_elm + cc + 4);
             ld8(sm + kA1, r, cc, 128, qv);
+            ld8(sm + kA1, 64 + r, cc, 128, bv);
+            ld8(sm + kB1, r, cc, 64, kv);
+            ld8(sm + kA4, r, cc, 64, wv);
+            ld8(sm + kVS, r, cc, 64, vv);
+            float qg[8], bk[8], rk[8], kp[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 en[i] = rcp(ep[i]);
-                qv[i] = qv[i] * ep[i] * em8[i] * p.scale;
+                const float eg = ep[i] * em8[i];  // exp(G)
+                qg[i] = qv[i] * eg * p.scale;
+                const float kk = live ? kv[i] : 0.f;
+                kv[i] = kk;
+                bk[i] = live ? bv[i] * kk : 0.f;
+                rk[i] = bk[i] * eg;
+                kp[i] = kk * (en[i] * elm8[i]);  // k*exp(G[last] - G)
+                wv[i] = live ? wv[i] * vv[i] : 0.f;
             }
             st8(sm + kA2, r, cc, 128, ep);
             st8(sm + kA2, 64 + r, cc, 128, en);
-            st8(sm + kB7, r, cc, 64, qv);
+            st8(sm + kB7, r, cc, 64, qg);
+            st8(sm + kA1, 64 + r, cc, 128, bk);
+            if (!live) st8(sm + kB1, r, cc, 64, kv);
+            st8(sm + kA3, r, cc, 64, rk);
+            st8(sm + kB8, r, cc, 64, kp);
+            st8(sm + kA4, r, cc, 64, wv);
         }
         fence_async_smem();
         tc_before();
         __syncthreads();
+        refill(2, ci + 1);  // v has been read
 
         // ---- 1. qk^T | (bk)k^T, and E+ E-^T (= K * decay in lanes 0-63)
         if (tid == 0) {
@@ -619,8 +624,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (tid == 0) {
             tc_after();
             // W = T (b*k*exp G): rows i in lanes 0-63, 128 columns; A = T as a 128-row operand
-            mma_issue(tmem + kTDW, sbase + kB3, sbase + kA3, 128, 128, kGC, false);
-            mma_issue(tmem + kTDU, sbase + kA4, sbase + kB3, 64, 64, kGC, false);  // U^T = (w*v)^T T^T
+            mma_issue(tmem + kTDW, sbase + kB3, sbase + kA3, 0, 128, kGC, false, false, true);
+            mma_issue(tmem + kTDU, sbase + kA4, sbase + kB3, 64, 64, kGC, false, true, false);  // U^T = (w*v)^T T^T
             commit();
         }
         if (!(ok = mma_wait())) break;
@@ -677,7 +682,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tc_after();
             mma_issue(tmem + kTDOUT, sbase + kA6, sbase + kB6, 64, 64, kGC, false);
             mma_issue(tmem + kTDOUT, sbase + kA5, sbase + kB7, 64, 64, kGK, true);
-            mma_issue(tmem + kTS, sbase + kA6, sbase + kB8, 128, 128, kGC, true);
+            mma_issue(tmem + kTS, sbase + kA6, sbase + kB8, 0, 128, kGC, true, false, true);
             commit();
         }
         if (!(ok = mma_wait())) break;
@@ -774,8 +779,8 @@ extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
         ssm::encode_2d(&mp.k, bf, a->k, ssm::kGK, rows, ssm::kGK * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B) &&
         ssm::encode_2d(&mp.b, bf, a->b, ssm::kGK, rows, ssm::kGK * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B) &&
         ssm::encode_2d(&mp.g, f32, a->g, ssm::kGK, rows, ssm::kGK * 4, ssm::kGK, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-        ssm::encode_2d(&mp.v, bf, a->v, ssm::kGV, rows, ssm::kGV * 2, ssm::kGV, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-        ssm::encode_2d(&mp.w, bf, a->w, ssm::kGV, rows, ssm::kGV * 2, ssm::kGV, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_NONE);
+        ssm::encode_2d(&mp.v, bf, a->v, ssm::kGV, rows, ssm::kGV * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+        ssm::encode_2d(&mp.w, bf, a->w, ssm::kGV, rows, ssm::kGV * 2, 64, ssm::kGC, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!enc) return SSM_ERR_CUDA;
     ssm::gdn2_chunk_fwd_kernel<<<(unsigned)BH, ssm::kGThreads, ssm::kGSmem, s>>>(
         p, a->state_in, (__nv_bfloat16*)a->out, a->state_out, mp);
