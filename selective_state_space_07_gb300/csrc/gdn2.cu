@@ -25,7 +25,8 @@
 //     Row pass (thread = 8 channels of a token): [E+; E-] with E- = 1/E+,
 //     q*exp(G)*scale, b*k, b*k*exp(G), k*exp(G[last] - G), w*v;
 //  1. MMA [q; b*k] k^T and [E+; E-] E-^T (the first 64 lanes of the second
-//     are K * decay: the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K);
+//     are K * decay: the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K),
+//     and the output's inter-chunk term out^T = S^T (q*exp(G)*scale)^T;
 //  2. aqk = qk * decay * scale (j <= i); akk = (bk)k^T * decay (j < i), the
 //     decay passed between lane halves through shared memory;
 //  3. T = (I + akk)^-1 by 2 x 2 block inversion (16 x 16 diagonal blocks
@@ -34,8 +35,8 @@
 //     MMA W = T (b*k*exp G) in row layout and U^T = (w*v)^T T^T (the
 //     page's row-by-row WY substitution, as (I + akk) W = rhs);
 //  4. MMA (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T;
-//  5. MMA out^T = v_new^T aqk^T + S^T (q*exp(G)*scale)^T, and, after S^T
-//     is scaled column-wise by exp(G[last]), S^T += v_new^T (k*exp(G[last]-G)).
+//  5. MMA out^T += v_new^T aqk^T, and, after S^T is scaled column-wise by
+//     exp(G[last]), S^T += v_new^T (k*exp(G[last]-G)).
 // The state's bf16 copy that the products read is refreshed from TMEM
 // after every chunk.
 //
@@ -412,18 +413,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
         // b*k*exp(G), k*exp(G[last] - G), w*v (in place of w). Rows past the
         // chunk's tokens: b*k, k, w*v zeroed (identity tokens); q's rows there
         // only reach outputs that are not stored.
+        {
+        const int cc = (tid & 15) * 8;  // the thread's channels, the same for its four tokens
+        float em8[8], elm8[8];
+        *reinterpret_cast<float4*>(em8) = *reinterpret_cast<const float4*>(s_em + cc);
+        *reinterpret_cast<float4*>(em8 + 4) = *reinterpret_cast<const float4*>(s_em + cc + 4);
+        *reinterpret_cast<float4*>(elm8) = *reinterpret_cast<const float4*>(s_elm + cc);
+        *reinterpret_cast<float4*>(elm8 + 4) = *reinterpret_cast<const float4*>(s_elm + cc + 4);
 #pragma unroll 2
         for (int it = 0; it < 4; ++it) {
-            const int e = tid + it * kGThreads;
-            const int r = e >> 4, cc = (e & 15) * 8;
+            const int r = (tid >> 4) + it * (kGThreads >> 4);
             const bool live = r < c;
-            float ep[8], en[8], qv[8], kv[8], bv[8], wv[8], vv[8], em8[8], elm8[8];
+            float ep[8], en[8], qv[8], kv[8], bv[8], wv[8], vv[8];
             *reinterpret_cast<float4*>(ep) = *reinterpret_cast<const float4*>(s_e + r * kGK + cc);
             *reinterpret_cast<float4*>(ep + 4) = *reinterpret_cast<const float4*>(s_e + r * kGK + cc + 4);
-            *reinterpret_cast<float4*>(em8) = *reinterpret_cast<const float4*>(s_em + cc);
-            *reinterpret_cast<float4*>(em8 + 4) = *reinterpret_cast<const float4*>(s_em + cc + 4);
-            *reinterpret_cast<float4*>(elm8) = *reinterpret_cast<const float4*>(s_elm + cc);
-            *reinterpret_cast<float4*>(elm8 + 4) = *reinterpret_cast<const float4*>(s_elm + cc + 4);
             ld8(sm + kA1, r, cc, 128, qv);
             ld8(sm + kA1, 64 + r, cc, 128, bv);
             ld8(sm + kB1, r, cc, 64, kv);
@@ -451,6 +454,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             st8(sm + kB8, r, cc, 64, kp);
             st8(sm + kA4, r, cc, 64, wv);
         }
+        }
         fence_async_smem();
         tc_before();
         __syncthreads();
@@ -461,6 +465,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tc_after();
             mma_issue(tmem + kTD1, sbase + kA1, sbase + kB1, 64, 64, kGK, false);
             mma_issue(tmem + kTD2, sbase + kA2, sbase + kA2 + 8192, 128, 64, kGK, false);
+            // the output's inter-chunk term S^T (q exp(G) scale)^T needs only the state before the chunk
+            mma_issue(tmem + kTDOUT, sbase + kA5, sbase + kB7, 64, 64, kGK, false);
             commit();
         }
         if (!(ok = mma_wait())) break;
@@ -677,11 +683,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
         tc_before();
         __syncthreads();
 
-        // ---- 5. out^T = v_new^T aqk^T + S^T (q exp(G) scale)^T;  S^T += v_new^T (k exp(Glast - G))
+        // ---- 5. out^T += v_new^T aqk^T (the inter-chunk term is in already);  S^T += v_new^T (k exp(Glast - G))
         if (tid == 0) {
             tc_after();
-            mma_issue(tmem + kTDOUT, sbase + kA6, sbase + kB6, 64, 64, kGC, false);
-            mma_issue(tmem + kTDOUT, sbase + kA5, sbase + kB7, 64, 64, kGK, true);
+            mma_issue(tmem + kTDOUT, sbase + kA6, sbase + kB6, 64, 64, kGC, true);
             mma_issue(tmem + kTS, sbase + kA6, sbase + kB8, 0, 128, kGC, true, false, true);
             commit();
         }
