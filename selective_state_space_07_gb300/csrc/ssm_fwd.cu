@@ -100,7 +100,8 @@ template <typename IO, bool AGG, int MINB>
 __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
     ssm_fwd_kernel(const FwdParams p, const __grid_constant__ FwdMaps mp) {
     using Ly = FwdLayout<IO>;
-    constexpr int NT = Ly::NT, CH = Ly::CH, T = kCK, NS = kN / kLPC, TPL = kCK / kLPC;
+    constexpr int NT = Ly::NT, CH = Ly::CH, T = kCK, NS = kN / kLPC, TPL = kCK / kLPC, RB = kReadBlock;
+    static_assert(NS % RB == 0, "whole readout blocks per lane");
     constexpr bool FAST = IOT<IO>::kFast;
     static_assert(NS % 2 == 0 && TPL % 4 == 0, "states and tokens per lane in pairs / quads");
     extern __shared__ __align__(128) char smem_raw[];
@@ -292,13 +293,16 @@ __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
                     hp[i] = hv1[i];
                 }
                 if (!AGG) {
-                    float2 r = f2(0.f, 0.f);
+                    // the lane's NS/RB readout blocks: sequential chains of RB
+                    // states, then summed as a balanced tree in state order
+                    float2 r[NS / RB];
 #pragma unroll
                     for (int i = 0; i < NS; ++i) {
                         const float2 cc = h2 ? f2(c4[i].z, c4[i].w) : f2(c4[i].x, c4[i].y);
-                        r = (i == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i])) : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r);
+                        r[i / RB] = (i % RB == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i]))
+                                                  : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r[i / RB]);
                     }
-                    acc[m] = r;
+                    acc[m] = tree2<NS / RB>(r);
                 }
             }
             if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
@@ -459,7 +463,7 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     // fused multiply-add chain C_0 h_0 -> fma(C_1, h_1, .) -> ...; the blocks
     // summed as a balanced binary tree in state order (its top level: one
     // half of the blocks + the other)
-    constexpr int BS = kN / kLPC, NB = kLPC, HB = NB / 2;
+    constexpr int BS = kReadBlock, NB = kN / kReadBlock, HB = NB / 2;
     float part[NB];
 #pragma unroll
     for (int blk = 0; blk < NB; ++blk) part[blk] = 0.f;

@@ -17,6 +17,13 @@ constexpr int kFwdThreads = 128;  // ssm_step_kernel
 #define SSM_FWD_LPC 2
 #endif
 constexpr int kFwdLPC = SSM_FWD_LPC;  // forward: lanes sharing one channel (16/kFwdLPC states each)
+#ifndef SSM_READ_BLOCK
+#define SSM_READ_BLOCK 8
+#endif
+// Readout order shared by the forward and ssm_step: sequential fused
+// multiply-add chains over blocks of kReadBlock consecutive states, the
+// blocks summed as a balanced binary tree in state order.
+constexpr int kReadBlock = SSM_READ_BLOCK;
 #ifndef SSM_FWD_WARPS
 #define SSM_FWD_WARPS 4
 #endif
