@@ -52,9 +52,11 @@ METRIC = "selective-scan fwd+bwd G(token·channel)/s on 1 GB300; % of HBM roofli
 UNIT = "G(token·channel)/s"
 DEFAULT_WORKLOAD = "mamba1.4b-bf16"
 FALLBACK_HBM_GBS = 6800.0
-# Special-function unit: ex2.approx issues 32 results per clock per SM on
-# GB300 (measured with a throughput probe); the SFU roofline is that rate at
-# the SM count and the maximum SM clock.
+# Special-function unit: ex2.approx / lg2.approx / rcp.approx run on the XU
+# pipe, whose peak ncu reports on GB300 as sm__inst_executed_pipe_xu
+# .avg.peak_sustained = 1 warp-instruction per cycle per SM, i.e. 32 results
+# per clock per SM; the SFU roofline is that rate at the SM count and the
+# maximum SM clock.
 SFU_EX2_PER_CLK_PER_SM = 32
 # A "pass" is one C-ABI call; its kernels (the main one plus, when the
 # sequence is split into L-groups, the aggregate pass and the carry scan)
@@ -578,7 +580,7 @@ def run_ours(args, w):
         ops = mufu_ops(w, name) / (ms * 1e-3)
         sfu[name] = {"bound": "sfu", "achieved": round(ops / 1e12, 3), "peak": round(sfu_peak / 1e12, 3),
                      "unit": "Tex2/s", "frac": round(ops / sfu_peak, 4),
-                     "peak_kind": "derived: 32 ex2/clk/SM x SMs x max SM clock"}
+                     "peak_kind": "derived: ncu XU peak (1 warp-instruction = 32 results /clk/SM) x SMs x max SM clock"}
     dom = "bwd" if ms_b >= ms_f else "fwd"
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
