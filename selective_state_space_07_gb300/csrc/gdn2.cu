@@ -22,21 +22,22 @@
 // Per chunk (the page's steps, with the products arranged so that M = 128):
 //  0. column pass (thread = one key channel, 32 tokens): G = cumsum of g,
 //     E+ = exp(G - G[m]) about the middle token m (fp32, in place of g).
-//     Row pass (thread = 8 channels of a token): [E+; E-] with E- = 1/E+,
-//     q*exp(G)*scale, b*k, b*k*exp(G), k*exp(G[last] - G), w*v;
-//  1. MMA [q; b*k] k^T and [E+; E-] E-^T (the first 64 lanes of the second
-//     are K * decay: the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K),
-//     and the output's inter-chunk term out^T = S^T (q*exp(G)*scale)^T;
-//  2. aqk = qk * decay * scale (j <= i); akk = (bk)k^T * decay (j < i), the
-//     decay passed between lane halves through shared memory;
+//     Row pass (thread = 8 channels of a token): [E+; E+], E- = 1/E+ (in
+//     place of v), q*exp(G)*scale, b*k, b*k*exp(G), k*exp(G[last] - G), w*v;
+//  1. MMA [q; b*k] k^T and [E+; E+] E-^T (K * decay in both lane halves:
+//     the key-mean of exp(G[i] - G[j]) = E+[i] . E-[j] / K); then, from
+//     the state before the chunk, out^T = S^T (q*exp(G)*scale)^T (the
+//     output's inter-chunk term) and Y^T = S^T (b*k*exp(G))^T;
+//  2. aqk = qk * decay * scale (j <= i), akk = (bk)k^T * decay (j < i);
+//     Z = w*v - Y (the page's u - W S before the triangular solve: with
+//     (I + akk) W = b*k*exp(G) and (I + akk) U = w*v, v_new = U - W S is
+//     (I + akk)^-1 Z);
 //  3. T = (I + akk)^-1 by 2 x 2 block inversion (16 x 16 diagonal blocks
 //     by forward substitution, the off-diagonal blocks as warp-level tf32
-//     products: T is rounded to bf16 for the products that use it);
-//     MMA W = T (b*k*exp G) in row layout and U^T = (w*v)^T T^T (the
-//     page's row-by-row WY substitution, as (I + akk) W = rhs);
-//  4. MMA (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T;
-//  5. MMA out^T += v_new^T aqk^T, and, after S^T is scaled column-wise by
-//     exp(G[last]), S^T += v_new^T (k*exp(G[last]-G)).
+//     products: T is rounded to bf16 for the product that uses it);
+//     MMA v_new^T = Z^T T^T;
+//  4. S^T scaled column-wise by exp(G[last]); MMA out^T += v_new^T aqk^T and
+//     S^T += v_new^T (k*exp(G[last]-G)).
 // The state's bf16 copy that the products read is refreshed from TMEM
 // after every chunk.
 //
@@ -60,28 +61,27 @@ constexpr int kGThreads = 256;
 // in disjoint phases of a chunk share space.
 constexpr int kA1 = 0;                  // [q; b*k]            128 rows x K=128 (q, b by TMA)
 constexpr int kB1 = kA1 + 32768;        // k                    64 rows x K=128 (TMA)
-constexpr int kA2 = kB1 + 16384;        // [E+; E-]            128 rows x K=128 (E- = rows 64.. as a B operand)
-constexpr int kA3 = kA2 + 32768;        // b*k*exp(G)          MN-major [64 tokens][128]  (then v_new^T)
+constexpr int kA2 = kB1 + 16384;        // [E+; E+]            128 rows x K=128
+constexpr int kA3 = kA2 + 32768;        // b*k*exp(G)          [64 tokens][128] (then Z^T, then v_new^T)
 constexpr int kA4 = kA3 + 16384;        // w (TMA), then w*v   MN-major [64 tokens][128]
 constexpr int kA5 = kA4 + 16384;        // S^T (bf16)          128 rows x K=128
 constexpr int kB7 = kA5 + 32768;        // q*exp(G)*scale       64 rows x K=128
 constexpr int kB8 = kB7 + 16384;        // k*exp(Glast-G)      MN-major [64 tokens][128]
-constexpr int kGS = kB8 + 16384;        // g staging fp32 [64][128] (TMA) -> E+; then the decay fp32 [64][64]
-constexpr int kVS = kGS + 32768;        // v staging, swz(token, channel, 64) image (TMA)
+constexpr int kGS = kB8 + 16384;        // g staging fp32 [64][128] (TMA) -> E+; then T fp32
+constexpr int kVS = kGS + 32768;        // v staging, swz(token, channel, 64) image (TMA); then E- 64 rows x K=128
 constexpr int kMisc = kVS + 16384;      // em, egl, elm [128] fp32; mbarriers; TMEM slot
 constexpr int kB6 = kA2;                // aqk                  64 rows x K=64
 constexpr int kB3 = kA2 + 8192;         // T                    64 rows x K=64 (as A: 128 rows, the rest unused)
 constexpr int kAKK = kA2 + 16384;       // akk fp32 [64][64], row-major, float4 chunks permuted per row
-constexpr int kB5 = kA2 + 16384;        // W                    64 rows x K=128
+constexpr int kAZ = kA3;                // Z^T = (w*v - b*k*exp(G) S)^T  128 rows x K=64
 constexpr int kA6 = kA3;                // v_new^T             128 rows x K=64
 constexpr int kGSmem = kMisc + 1536 + 64 + 1024;  // + slack for the 1024-byte alignment
 static_assert(kGSmem <= 227 * 1024, "shared memory");
 constexpr unsigned kQkbBytes = 3 * 2 * 64 * 128;  // q, b, k: two 64-column boxes each
 constexpr unsigned kGBytes = kGC * kGK * 4, kVBytes = kGC * kGV * 2;
 
-// TMEM columns: S^T, then per chunk qk|bkk and the decay, whose columns W
-// (row layout, 128 columns) reuses once they are read.
-constexpr unsigned kTS = 0, kTD1 = 128, kTD2 = 192, kTDW = 128, kTDU = 256, kTDWS = 320, kTDOUT = 384;
+// TMEM columns: S^T; per chunk qk|bkk, the decay, out^T, Y^T = (b*k*exp(G) S)^T and v_new^T.
+constexpr unsigned kTS = 0, kTD1 = 128, kTD2 = 192, kTDOUT = 256, kTDY = 320, kTDV = 384;
 
 // Byte offset of element (row, col) in a K-major, 128-byte-swizzled bf16
 // operand of `rows` rows.
@@ -242,8 +242,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
     float* s_em = reinterpret_cast<float*>(sm + kMisc);  // exp(G[m]) per key channel
     float* s_egl = s_em + kGK;                           // exp(G[last])
     float* s_elm = s_egl + kGK;                          // exp(G[last] - G[m])
-    uint64_t* bars = reinterpret_cast<uint64_t*>(s_elm + kGK);  // mma, qkb, g, v, w
-    unsigned* tslot = reinterpret_cast<unsigned*>(bars + 5);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(s_elm + kGK);  // mma, qkb, g, v, w, mma (second batch)
+    unsigned* tslot = reinterpret_cast<unsigned*>(bars + 6);
     float* s_gm = reinterpret_cast<float*>(sm + kA2);    // column-pass exchange (A2 is written after it)
     float* s_e = reinterpret_cast<float*>(sm + kGS);     // g, then E+ [64][128]; then the decay [64][64]
     float* s_akk = reinterpret_cast<float*>(sm + kAKK);
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int nchunks = (int)((T + kGC - 1) / kGC);
     const unsigned sbase = smem_u32(sm);
     const unsigned mbar = smem_u32(bars), bar_qkb = smem_u32(bars + 1), bar_g = smem_u32(bars + 2),
-                   bar_v = smem_u32(bars + 3), bar_w = smem_u32(bars + 4);
+                   bar_v = smem_u32(bars + 3), bar_w = smem_u32(bars + 4), mbar2 = smem_u32(bars + 5);
     constexpr float L2E = 1.4426950408889634f;
 
     if (warp == 0) {
@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(maps[m])) : "memory");
     }
     if (tid == 0) {
-        for (int b = 0; b < 5; ++b) mbar_init(smem_u32(bars + b), 1);
+        for (int b = 0; b < 6; ++b) mbar_init(smem_u32(bars + b), 1);
         mbar_fence_init();
     }
     __syncthreads();
@@ -335,7 +335,10 @@ __global__ void __launch_bounds__(kGThreads, 1)
     tc_before();
     __syncthreads();
 
-    unsigned phase = 0;
+    // Tensor-core completions: `mbar` for the rounds waited in order, `mbar2`
+    // for the second batch of round 1 (committed right after the first, so on
+    // one barrier the two could complete two phases before anyone polls).
+    unsigned phase = 0, phase2 = 0;
     // copies issued / waited for, per barrier (qkb, g, v, w); uniform over the CTA
     int issued[4] = {nchunks > 0, nchunks > 0, nchunks > 0, nchunks > 0}, waited[4] = {0, 0, 0, 0};
     const unsigned tbar[4] = {bar_qkb, bar_g, bar_v, bar_w};
@@ -349,6 +352,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (!ok) fail();
         return __syncthreads_and(ok) != 0;
     };
+    auto mma_wait2 = [&]() -> bool {  // the second batch of round 1
+        const bool ok = mbar_wait_try(mbar2, phase2 & 1u);
+        phase2++;
+        if (!ok) fail();
+        return __syncthreads_and(ok) != 0;
+    };
     auto copies_wait = [&](int b0, int b1) -> bool {  // copies b0..b1 of the current chunk, one CTA barrier
         bool ok = true;
         for (int b = b0; b <= b1; ++b) ok = ok && mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1));
@@ -358,10 +367,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
             for (int b = b0; b <= b1; ++b) waited[b]++;
         return all;
     };
-    auto commit = [&]() {
-        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar)
+    auto commit_to = [&](unsigned bar) {
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
                      : "memory");
     };
+    auto commit = [&]() { commit_to(mbar); };
     auto refill = [&](int b, int cj) {  // next chunk's copy into a buffer all threads are done reading
         if (cj >= nchunks) return;
         if (tid == kTmaThread) {
@@ -446,7 +456,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 wv[i] = live ? wv[i] * vv[i] : 0.f;
             }
             st8(sm + kA2, r, cc, 128, ep);
-            st8(sm + kA2, 64 + r, cc, 128, en);
+            st8(sm + kA2, 64 + r, cc, 128, ep);
+            st8(sm + kVS, r, cc, 64, en);  // in place of v (same thread, same chunk of the image)
             st8(sm + kB7, r, cc, 64, qg);
             st8(sm + kA1, 64 + r, cc, 128, bk);
             if (!live) st8(sm + kB1, r, cc, 64, kv);
@@ -458,61 +469,65 @@ __global__ void __launch_bounds__(kGThreads, 1)
         fence_async_smem();
         tc_before();
         __syncthreads();
-        refill(2, ci + 1);  // v has been read
 
-        // ---- 1. qk^T | (bk)k^T, and E+ E-^T (= K * decay in lanes 0-63)
+        // ---- 1. qk^T | (bk)k^T and [E+; E+] E-^T (K * decay in both lane halves); then the
+        // products that need only the state before the chunk: out^T = S^T (q exp(G) scale)^T
+        // and Y^T = S^T (b k exp(G))^T, committed separately
         if (tid == 0) {
             tc_after();
             mma_issue(tmem + kTD1, sbase + kA1, sbase + kB1, 64, 64, kGK, false);
-            mma_issue(tmem + kTD2, sbase + kA2, sbase + kA2 + 8192, 128, 64, kGK, false);
-            // the output's inter-chunk term S^T (q exp(G) scale)^T needs only the state before the chunk
-            mma_issue(tmem + kTDOUT, sbase + kA5, sbase + kB7, 64, 64, kGK, false);
+            mma_issue(tmem + kTD2, sbase + kA2, sbase + kVS, 64, 64, kGK, false);
             commit();
+            mma_issue(tmem + kTDOUT, sbase + kA5, sbase + kB7, 64, 64, kGK, false);
+            mma_issue(tmem + kTDY, sbase + kA5, sbase + kA3, 64, 64, kGK, false);
+            commit_to(mbar2);
         }
         if (!(ok = mma_wait())) break;
         tc_after();
         refill(0, ci + 1);  // q, k, b have been read
+        refill(2, ci + 1);  // E- (in v's buffer) has been read
 
-        // ---- 2. aqk (lanes 0-63) and akk (lanes 64-127; the decay through shared memory)
+        // ---- 2. aqk (lanes 0-63) and akk (lanes 64-127), the decay in both lane halves
         {
             const int jb = whalf * 32;
-            float d1[32];
+            float d1[32], d2[32];
             tmem_ld32(tmem + tlane + kTD1 + (unsigned)jb, d1);
-            // the decay [64][64] fp32, float4 chunks permuted per row as in akk
-            auto dec_at = [&](int i, int j) -> float* { return s_e + i * kGC + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3)); };
+            tmem_ld32(tmem + tlane + kTD2 + (unsigned)jb, d2);
             if (quarter < 2) {
                 const int i = vrow;
-                float d2[32];
-                tmem_ld32(tmem + tlane + kTD2 + (unsigned)jb, d2);
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const float dec = d2[jj] * (1.f / kGK);
-                    d2[jj] = dec;
-                    d1[jj] = (jb + jj <= i) ? d1[jj] * dec * p.scale : 0.f;
-                }
-#pragma unroll
-                for (int jj = 0; jj < 32; jj += 4)
-                    *reinterpret_cast<float4*>(dec_at(i, jb + jj)) = make_float4(d2[jj], d2[jj + 1], d2[jj + 2], d2[jj + 3]);
+                for (int jj = 0; jj < 32; ++jj) d1[jj] = (jb + jj <= i) ? d1[jj] * d2[jj] * (p.scale / kGK) : 0.f;
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 8) st8(sm + kB6, i, jb + jj, 64, d1 + jj);
-            }
-            __syncthreads();
-            if (quarter >= 2) {
+            } else {
                 const int i = vrow - 64;
 #pragma unroll
                 for (int jj = 0; jj < 32; jj += 4) {
-                    const float4 dec = *reinterpret_cast<const float4*>(dec_at(i, jb + jj));
-                    const float dv[4] = {dec.x, dec.y, dec.z, dec.w};
                     float a4[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) a4[e] = (jb + jj + e < i) ? d1[jj + e] * dv[e] : 0.f;
+                    for (int e = 0; e < 4; ++e) a4[e] = (jb + jj + e < i) ? d1[jj + e] * d2[jj + e] * (1.f / kGK) : 0.f;
                     *reinterpret_cast<float4*>(akk_at(i, jb + jj)) = make_float4(a4[0], a4[1], a4[2], a4[3]);
                 }
             }
         }
+        // Z^T = (w v)^T - Y^T (lane v, tokens j), the right-hand side of v_new = T Z
+        if (!(ok = mma_wait2())) break;
+        tc_after();
+        {
+            const int jb = whalf * 32;
+            float y[32];
+            tmem_ld32(tmem + tlane + kTDY + (unsigned)jb, y);
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+                y[jj] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + kA4 + swz(jb + jj, vrow, 64))) - y[jj];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj += 8) st8(sm + kAZ, vrow, jb + jj, 128, y + jj);
+        }
         tc_before();
         __syncthreads();
-        // ---- 3. T = (I + akk)^-1 by blocks; then W and U^T
+        refill(3, ci + 1);  // w*v has been read: the next w can land in its buffer
+
+        // ---- 3. T = (I + akk)^-1 by blocks; then v_new = T Z
         // The inverse of the unit lower-triangular I + akk by blocks: for
         // [[A, 0], [C, B]] the inverse is [[A^-1, 0], [-B^-1 C A^-1, B^-1]].
         // (a) the four diagonal 16 x 16 blocks by forward substitution (one
@@ -626,46 +641,18 @@ __global__ void __launch_bounds__(kGThreads, 1)
         fence_async_smem();
         tc_before();
         __syncthreads();
-        refill(1, ci + 1);  // g's buffer (E+, the decay, T) has been read
+        refill(1, ci + 1);  // g's buffer (E+, then T) has been read
         if (tid == 0) {
             tc_after();
-            // W = T (b*k*exp G): rows i in lanes 0-63, 128 columns; A = T as a 128-row operand
-            mma_issue(tmem + kTDW, sbase + kB3, sbase + kA3, 0, 128, kGC, false, false, true);
-            mma_issue(tmem + kTDU, sbase + kA4, sbase + kB3, 64, 64, kGC, false, true, false);  // U^T = (w*v)^T T^T
-            commit();
-        }
-        if (!(ok = mma_wait())) break;
-        tc_after();
-        refill(3, ci + 1);  // (w*v)^T has been read: the next w can land in A4
-        if (quarter < 2) {  // W (rows i, K = n) from lanes 0-63
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int n0 = whalf * 64 + cc * 32;
-                float wr[32];
-                tmem_ld32(tmem + tlane + kTDW + (unsigned)n0, wr);
-#pragma unroll
-                for (int nn = 0; nn < 32; nn += 8) st8(sm + kB5, vrow, n0 + nn, 64, wr + nn);
-            }
-        }
-        fence_async_smem();
-        tc_before();
-        __syncthreads();
-
-        // ---- 4. (W S)^T = S^T W^T; v_new^T = U^T - (W S)^T
-        if (tid == 0) {
-            tc_after();
-            mma_issue(tmem + kTDWS, sbase + kA5, sbase + kB5, 64, 64, kGK, false);
+            mma_issue(tmem + kTDV, sbase + kAZ, sbase + kB3, 64, 64, kGC, false);  // v_new^T = Z^T T^T
             commit();
         }
         if (!(ok = mma_wait())) break;
         tc_after();
         {
-            float u[32], ws[32];
+            float u[32];
             const int i0 = whalf * 32;
-            tmem_ld32(tmem + tlane + kTDU + (unsigned)i0, u);
-            tmem_ld32(tmem + tlane + kTDWS + (unsigned)i0, ws);
-#pragma unroll
-            for (int ii = 0; ii < 32; ++ii) u[ii] -= ws[ii];
+            tmem_ld32(tmem + tlane + kTDV + (unsigned)i0, u);
 #pragma unroll
             for (int ii = 0; ii < 32; ii += 8) st8(sm + kA6, vrow, i0 + ii, 128, u + ii);
             // S^T columns n scaled by exp(G[last][n]) before the update is added
