@@ -179,6 +179,13 @@ __device__ __forceinline__ void st8(char* base, int row, int col, int rows, cons
     *reinterpret_cast<uint4*>(base + swz(row, col, rows)) =
         make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
 }
+__device__ __forceinline__ void st1(char* base, int row, int col, int rows, float v) {
+    *reinterpret_cast<__nv_bfloat16*>(base + swz(row, col, rows)) = __float2bfloat16_rn(v);
+}
+// two consecutive bf16 (col even) of a K-major swizzled row
+__device__ __forceinline__ void st2(char* base, int row, int col, int rows, float a, float b) {
+    *reinterpret_cast<unsigned*>(base + swz(row, col, rows)) = pack_bf2(a, b);
+}
 __device__ __forceinline__ void unpack8(uint4 u, float* f) {
     const unsigned w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -478,6 +485,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             mma_issue(tmem + kTD1, sbase + kA1, sbase + kB1, 64, 64, kGK, false);
             mma_issue(tmem + kTD2, sbase + kA2, sbase + kVS, 64, 64, kGK, false);
             commit();
+        } else if (tid == 32) {  // a second issuing thread: its commit covers its own products
+            tc_after();
             mma_issue(tmem + kTDOUT, sbase + kA5, sbase + kB7, 64, 64, kGK, false);
             mma_issue(tmem + kTDY, sbase + kA5, sbase + kA3, 64, 64, kGK, false);
             commit_to(mbar2);
@@ -532,22 +541,37 @@ __global__ void __launch_bounds__(kGThreads, 1)
         // [[A, 0], [C, B]] the inverse is [[A^-1, 0], [-B^-1 C A^-1, B^-1]].
         // (a) the four diagonal 16 x 16 blocks by forward substitution (one
         // thread per column); (b) the two off-diagonal 16 x 16 blocks inside
-        // the 32 x 32 halves; (c) the lower 32 x 32 block. fp32 throughout.
+        // the 32 x 32 halves; (c) the lower 32 x 32 block. fp32 throughout; every
+        // block is also written as the bf16 K-major operand T (rows r, K = column).
         constexpr int TS = kGC + 4;   // row stride of T: rows 4 banks apart
         float* TT = s_e;              // T fp32 [64][TS], row-major (g's staging buffer is free)
         float* TY = s_e + kGC * TS;   // scratch products
-        if (tid < kGC) {
+        if (tid < kGC) {  // (a): thread = column cl of diagonal block base/16, rows in order
             const int base = (tid >> 4) * 16, cl = tid & 15;
             float x[16];
 #pragma unroll
-            for (int r = 0; r < 16; ++r) x[r] = r == cl ? 1.f : 0.f;
+            for (int r = 0; r < 16; ++r) {
+                float acc0 = r == cl ? 1.f : 0.f, acc1 = 0.f;
 #pragma unroll
-            for (int i = 0; i < 15; ++i) {
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    if (4 * q4 < r) {
+                        const float4 a = *reinterpret_cast<const float4*>(akk_at(base + r, base + 4 * q4));
+                        const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
-                for (int r = i + 1; r < 16; ++r) x[r] = __fmaf_rn(-*akk_at(base + r, base + i), x[i], x[r]);
+                        for (int e = 0; e < 4; ++e)
+                            if (4 * q4 + e < r) {
+                                if (e & 1) acc1 = __fmaf_rn(-av[e], x[4 * q4 + e], acc1);
+                                else acc0 = __fmaf_rn(-av[e], x[4 * q4 + e], acc0);
+                            }
+                    }
+                }
+                x[r] = acc0 + acc1;
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) TT[(base + r) * TS + base + cl] = x[r];
+            for (int r = 0; r < 16; ++r) {
+                TT[(base + r) * TS + base + cl] = x[r];
+                st1(sm + kB3, base + r, base + cl, 64, x[r]);
+            }
         } else {  // zeros above the diagonal blocks: blocks (0,1), (2,3) and the upper 32 x 32
             for (int e = tid - kGC; e < 1024 + 512; e += kGThreads - kGC) {
                 int r, cc;
@@ -560,6 +584,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
                     cc = 32 * blk + 16 + (f & 15);
                 }
                 TT[r * TS + cc] = 0.f;
+                st1(sm + kB3, r, cc, 64, 0.f);
             }
         }
         __syncthreads();
@@ -596,6 +621,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 }
                 float* o = TT + (R0 + g) * TS + C0 + 8 * nj + 2 * t;
                 o[0] = d[0]; o[1] = d[1]; o[8 * TS] = d[2]; o[8 * TS + 1] = d[3];
+                st2(sm + kB3, R0 + g, C0 + 8 * nj + 2 * t, 64, d[0], d[1]);
+                st2(sm + kB3, R0 + g + 8, C0 + 8 * nj + 2 * t, 64, d[2], d[3]);
             }
         }
         __syncthreads();
@@ -627,16 +654,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
             float* o = TT + (32 + r0 + g) * TS + cc + 2 * t;
             o[0] = d[0]; o[1] = d[1]; o[8 * TS] = d[2]; o[8 * TS + 1] = d[3];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int it = 0; it < 2; ++it) {  // T into the K-major operand (rows r, K = column)
-            const int e = tid + it * kGThreads;
-            const int r = e >> 3, cc = (e & 7) * 8;
-            float tv[8];
-            *reinterpret_cast<float4*>(tv) = *reinterpret_cast<const float4*>(TT + r * TS + cc);
-            *reinterpret_cast<float4*>(tv + 4) = *reinterpret_cast<const float4*>(TT + r * TS + cc + 4);
-            st8(sm + kB3, r, cc, 64, tv);
+            st2(sm + kB3, 32 + r0 + g, cc + 2 * t, 64, d[0], d[1]);
+            st2(sm + kB3, 32 + r0 + g + 8, cc + 2 * t, 64, d[2], d[3]);
         }
         fence_async_smem();
         tc_before();
