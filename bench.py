@@ -266,6 +266,14 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def with_cycles(clk, ms):
+    """The clock record plus the step's time in SM cycles at the median clock
+    sampled under load (ms x MHz), which stays comparable across clock drift."""
+    if clk and clk.get("sm_mhz"):
+        clk = dict(clk, sm_cycles_per_step=round(ms * clk["sm_mhz"] * 1e3))
+    return clk
+
+
 # ------------------------------------------------------------------ dist
 def dist_env():
     return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
@@ -607,7 +615,7 @@ def run_ours(args, w):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
-        "clocks": clk,
+        "clocks": with_cycles(clk, ms_step),
         "status": status,
         "wall_s_timed_loop": round(wall, 3),
     }
@@ -795,7 +803,8 @@ def run_conv(args, w):
                    "ms_fwd": round(ms_f, 5), "ms_bwd": round(ms_b, 5),
                    "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
         "roofline": rf[dom], "roofline_other": rf["fwd" if dom == "bwd" else "bwd"],
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk, "status": status,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": with_cycles(clk, ms_f + ms_b),
+        "status": status,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -986,7 +995,8 @@ def run_dtproj(args, w):
                    "ms_fwd": round(ms_f, 5), "ms_bwd": round(ms_b, 5),
                    "hbm_frac_fwd": rf["fwd"]["frac"], "hbm_frac_bwd": rf["bwd"]["frac"]},
         "roofline": rf[dom], "roofline_other": rf["fwd" if dom == "bwd" else "bwd"], "tensor_roofline": tens,
-        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clk, "status": status,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": with_cycles(clk, ms_f + ms_b),
+        "status": status,
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -1185,7 +1195,7 @@ def run_gdn2(args):
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (129 MB) and a 512 MiB write flushes L2 before every call"},
         "roofline": rf, "tensor_roofline": tens, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
-        "clocks": clk, "status": status,
+        "clocks": with_cycles(clk, ms), "status": status,
     }
     print(json.dumps(line), flush=True)
     if dist:
