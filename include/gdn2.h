@@ -75,6 +75,16 @@ typedef struct {
 
 int gdn2_chunk_fwd(const gdn2_fwd_args* args, void* stream);
 
+/* Test hook: arms a one-shot fault for this thread's next gdn2_chunk_fwd.
+ * The copies of q, k and b for chunk `chunk` (0-based, in every CTA) are not
+ * issued while the chunk's other copies are, and every bounded wait of that
+ * call gives up after wait_ns (0 keeps the 1 s default): the wait for the
+ * missing copies runs out, each CTA waits for the copies it did issue, frees
+ * its tensor memory and stops; ssm_poll_status then returns SSM_ERR_TIMEOUT
+ * and the outputs are not valid. chunk < 0 disarms. SSM_ERR_INVALID_ARG for
+ * wait_ns above 10 s. */
+int gdn2_debug_arm_wait_fault(int64_t chunk, uint64_t wait_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,7 +28,7 @@ __all__ = [
     "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
     "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
-    "gdn2_fwd", "GDN2_CHUNK",
+    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -119,6 +119,7 @@ EXPORTS = {
                         ctypes.c_int),
     "ssm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
     "gdn2_chunk_fwd": ([ctypes.POINTER(Gdn2Args), ctypes.c_void_p], ctypes.c_int),
+    "gdn2_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
 }
 
 
@@ -560,6 +561,12 @@ def gdn2_fwd(q, k, v, g, b, w, state=None, scale=None, *, out=None, state_out=No
                     state_out=_p(state_out), workspace=None if workspace is None else workspace.buf.data_ptr())
     _check(lib().gdn2_chunk_fwd(ctypes.byref(args), _stream(dev, stream)), "gdn2_chunk_fwd")
     return out, state_out
+
+
+def gdn2_arm_wait_fault(chunk: int, wait_ns: int) -> None:
+    """Test hook: the next gdn2_fwd of this thread does not issue chunk `chunk`'s q, k, b copies and bounds every
+    wait by wait_ns, so the call ends with SSM_ERR_TIMEOUT in the status word. chunk < 0 disarms."""
+    _check(lib().gdn2_debug_arm_wait_fault(int(chunk), int(wait_ns)), "gdn2_debug_arm_wait_fault")
 
 
 def poll_status(workspace, stream=None) -> int:

@@ -217,8 +217,8 @@ __device__ __forceinline__ void mma_tf32(float* d, const float* a, const float* 
 
 // Wait until phase `parity` of the barrier completes (mbarrier.try_wait,
 // which suspends the thread for a while in hardware between checks), at most
-// kWaitNs; returns whether it completed.
-__device__ __forceinline__ bool mbar_wait_try(unsigned bar, unsigned parity) {
+// limit_ns; returns whether it completed.
+__device__ __forceinline__ bool mbar_wait_try(unsigned bar, unsigned parity, unsigned long long limit_ns) {
     const unsigned long long t0 = global_ns();
     while (true) {
         unsigned done = 0;
@@ -228,7 +228,7 @@ __device__ __forceinline__ bool mbar_wait_try(unsigned bar, unsigned parity) {
             : "r"(bar), "r"(parity)
             : "memory");
         if (done) return true;
-        if (global_ns() - t0 > kWaitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -236,6 +236,8 @@ struct Gdn2Params {
     int64_t B, H, T;
     float scale;
     unsigned* status;
+    unsigned long long wait_ns;  // bound of every wait (kWaitNs unless a test armed a fault)
+    int64_t fault_chunk1;        // tests: chunk fault_chunk1 - 1's q, k, b copies are not issued (0: none)
 };
 struct Gdn2Maps {
     CUtensorMap q, k, b, g, v, w;  // rows = B*H*T tokens; q, k, b, v, w: 64-column swizzled boxes; g: whole rows
@@ -277,7 +279,11 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // tensor read as zero, rows of the next (batch, head) are zeroed or
     // ignored on the ragged last chunk
     auto row_of = [&](int cj) { return (int)(bh * T + (int64_t)cj * kGC); };
+    // a test-armed fault: this chunk's q, k, b copies are never issued, so the
+    // bounded wait for them runs out
+    auto qkb_skipped = [&](int cj) { return (int64_t)cj + 1 == p.fault_chunk1; };
     auto issue_qkb = [&](int cj) {
+        if (qkb_skipped(cj)) return;
         const int y = row_of(cj);
         mbar_expect_tx(bar_qkb, kQkbBytes);
 #pragma unroll
@@ -347,27 +353,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
     // one barrier the two could complete two phases before anyone polls).
     unsigned phase = 0, phase2 = 0;
     // copies issued / waited for, per barrier (qkb, g, v, w); uniform over the CTA
-    int issued[4] = {nchunks > 0, nchunks > 0, nchunks > 0, nchunks > 0}, waited[4] = {0, 0, 0, 0};
+    int issued[4] = {nchunks > 0 && !qkb_skipped(0), nchunks > 0, nchunks > 0, nchunks > 0}, waited[4] = {0, 0, 0, 0};
     const unsigned tbar[4] = {bar_qkb, bar_g, bar_v, bar_w};
     float nf = 0.f;
     auto fail = [&]() {
         if (tid == 0 && p.status) atomicOr(p.status, kStatusTimeout);
     };
     auto mma_wait = [&]() -> bool {  // every thread waits for the last commit; false if it never came
-        const bool ok = mbar_wait_try(mbar, phase & 1u);
+        const bool ok = mbar_wait_try(mbar, phase & 1u, p.wait_ns);
         phase++;
         if (!ok) fail();
         return __syncthreads_and(ok) != 0;
     };
     auto mma_wait2 = [&]() -> bool {  // the second batch of round 1
-        const bool ok = mbar_wait_try(mbar2, phase2 & 1u);
+        const bool ok = mbar_wait_try(mbar2, phase2 & 1u, p.wait_ns);
         phase2++;
         if (!ok) fail();
         return __syncthreads_and(ok) != 0;
     };
     auto copies_wait = [&](int b0, int b1) -> bool {  // copies b0..b1 of the current chunk, one CTA barrier
         bool ok = true;
-        for (int b = b0; b <= b1; ++b) ok = ok && mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1));
+        for (int b = b0; b <= b1; ++b) ok = ok && mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1), p.wait_ns);
         if (!ok) fail();
         const bool all = __syncthreads_and(ok) != 0;
         if (all)
@@ -388,7 +394,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
             else if (b == 2) issue_sw(bar_v, kVS, &mp.v, cj);
             else issue_sw(bar_w, kA4, &mp.w, cj);
         }
-        issued[b]++;
+        issued[b] += (b == 0 && qkb_skipped(cj)) ? 0 : 1;
     };
 
     bool ok = true;
@@ -727,7 +733,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         if (tid == kTmaThread)
             for (int b = 0; b < 4; ++b)
                 for (; waited[b] < issued[b]; ++waited[b])
-                    if (!mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1))) break;
+                    if (!mbar_wait_try(tbar[b], (unsigned)(waited[b] & 1), p.wait_ns)) break;
     } else if (state_out) {
         float* so = state_out + bh * kGK * kGV;
         for (int cc = 0; cc < 2; ++cc) {
@@ -752,8 +758,26 @@ bool misaligned16(const void* q) { return q && (reinterpret_cast<uintptr_t>(q) &
 }  // namespace
 }  // namespace ssm
 
+namespace {
+// One-shot wait fault for this thread's next gdn2_chunk_fwd (tests).
+thread_local int64_t g_gdn2_fault_chunk1 = 0;
+thread_local unsigned long long g_gdn2_fault_wait_ns = 0;
+}  // namespace
+
+extern "C" int gdn2_debug_arm_wait_fault(int64_t chunk, uint64_t wait_ns) {
+    if (wait_ns > 10000000000ull) return SSM_ERR_INVALID_ARG;
+    g_gdn2_fault_chunk1 = chunk < 0 ? 0 : chunk + 1;
+    g_gdn2_fault_wait_ns = chunk < 0 ? 0 : wait_ns;
+    return SSM_OK;
+}
+
 extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
     ssm::reset_launches();
+    // an armed fault applies to this call only
+    const int64_t fault_chunk1 = g_gdn2_fault_chunk1;
+    const unsigned long long fault_wait_ns = g_gdn2_fault_wait_ns;
+    g_gdn2_fault_chunk1 = 0;
+    g_gdn2_fault_wait_ns = 0;
     if (!a) return SSM_ERR_INVALID_ARG;
     if (a->B < 0 || a->H < 0 || a->T < 0) return SSM_ERR_INVALID_ARG;
     if (a->K != ssm::kGK || a->V != ssm::kGV || (a->chunk != 0 && a->chunk != ssm::kGC)) return SSM_ERR_UNSUPPORTED;
@@ -782,6 +806,8 @@ extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
     ssm::Gdn2Params p{};
     p.B = a->B; p.H = a->H; p.T = a->T; p.scale = a->scale;
     p.status = (unsigned*)a->workspace;
+    p.fault_chunk1 = fault_chunk1;
+    p.wait_ns = fault_chunk1 > 0 && fault_wait_ns > 0 ? fault_wait_ns : ssm::kWaitNs;
     const int64_t rows = BH * a->T;
     ssm::Gdn2Maps mp{};
     const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, f32 = CU_TENSOR_MAP_DATA_TYPE_FLOAT32;

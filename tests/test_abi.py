@@ -212,6 +212,11 @@ def test_gdn2_rejects_bad_arguments(ssm, over, code):
     assert ssm.lib().gdn2_chunk_fwd(ctypes.byref(args), None) == code
 
 
+def test_gdn2_fault_hook_arguments(ssm):
+    assert ssm.lib().gdn2_debug_arm_wait_fault(0, 20_000_000_000) == INVALID
+    assert ssm.lib().gdn2_debug_arm_wait_fault(-1, 0) == OK  # disarmed
+
+
 def test_null_args_struct(ssm):
     assert ssm.lib().gdn2_chunk_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
