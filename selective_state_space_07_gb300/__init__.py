@@ -13,6 +13,13 @@ The operation (rustytorch commit log, "MambaBlock" S6 forward commit):
 Layouts: x, z, dt, y [B, L, D]; Bm, Cm [B, L, 16]; A [D, 16]; Dskip,
 dt_bias [D]; states [B, D, 16]. x, z, Bm, Cm, y, dy, dx, dz are fp32 or bf16
 (one dtype per call); everything else is fp32.
+
+Also bound here: the conv1d + SiLU in front of the scan (``conv1d_fwd``,
+``conv1d_bwd``, ``conv1d_step``), the dt projection with its softplus on the
+tensor cores (``dtproj_fwd``, ``dtproj_bwd``), and the Gated DeltaNet-2
+chunkwise forward (``gdn2_fwd``; C ABI in ``include/gdn2.h``; docs.rs,
+burn-gdn2 0.1.4, src/forward.rs, chunk_wy_forward): q, k, b, g [B, H, T,
+128], v, w [B, H, T, 128], state [B, H, 128, 128], chunks of 64 tokens.
 """
 from __future__ import annotations
 

@@ -254,9 +254,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(s_elm + kGK);  // mma, qkb, g, v, w, mma (second batch)
     unsigned* tslot = reinterpret_cast<unsigned*>(bars + 6);
     float* s_gm = reinterpret_cast<float*>(sm + kA2);    // column-pass exchange (A2 is written after it)
-    float* s_e = reinterpret_cast<float*>(sm + kGS);     // g, then E+ [64][128]; then the decay [64][64]
+    float* s_e = reinterpret_cast<float*>(sm + kGS);     // g, then E+ [64][128]; then T (fp32) and scratch
     float* s_akk = reinterpret_cast<float*>(sm + kAKK);
-    // akk[i][j]: row i, its float4 chunks permuted by i % 16 (conflict-free row and column access)
+    // akk[i][j]: row i, its float4 chunks permuted by i % 16 (conflict-free row writes, one per lane)
     auto akk_at = [&](int i, int j) -> float* { return s_akk + i * kGC + ((((j >> 2) ^ (i & 15)) << 2) | (j & 3)); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
