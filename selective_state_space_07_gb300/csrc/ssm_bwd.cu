@@ -95,9 +95,13 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
     __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];      // a chunk's copies landed
     __shared__ int aborted;                                   // a copy did not arrive within the time bound
     __shared__ __align__(16) float AT[kN * CH];               // A^T of the CTA's channels
-    __shared__ __align__(16) float BT[kN * T];                // B^T, C^T of the chunk (fp32)
-    __shared__ __align__(16) float CT[kN * T];
-    __shared__ __align__(16) float OB[Ly::NW * 2 * T * kN];  // per-warp dB/dC [warp][dB|dC][token][state]
+    // double-buffered by chunk parity: a chunk's tables are written while the
+    // previous chunk's are still read, and its dB/dC rows while the previous
+    // chunk's are summed (one CTA barrier per chunk)
+    constexpr int OBSZ = Ly::NW * 2 * T * kN;
+    __shared__ __align__(16) float BT[2 * kN * T];            // B^T, C^T of the chunk (fp32)
+    __shared__ __align__(16) float CT[2 * kN * T];
+    __shared__ __align__(16) float OB[2 * OBSZ];              // per-warp dB/dC [warp][dB|dC][token][state]
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int hk = lane >> 4;                   // states 8*hk .. 8*hk+7
@@ -167,18 +171,37 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
     }
     __syncthreads();
 
+    // dB / dC of chunk s from its per-warp rows: sum the warps, one vector atomic per 4 outputs
+    auto flush_dbdc = [&](int s, const float* ob) {
+        if (tid >= 2 * T * (kN / 4)) return;
+        const int64_t t0 = tb0 + (int64_t)s * T;
+        const int rows = (int)min64(T, tb1 - t0);
+        const int type = tid / (T * kN / 4), rem = tid % (T * kN / 4);
+        const int tk = rem / (kN / 4), n0 = (rem % (kN / 4)) * 4;
+        if (tk < rows) {
+            float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < Ly::NW; ++w) {
+                const float4 v = *reinterpret_cast<const float4*>(ob + ((w * 2 + type) * T + tk) * kN + n0);
+                s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
+            }
+            red_add_v4((type == 0 ? p.dB : p.dC) + (b * L + t0 + tk) * kN + n0, s4);
+        }
+    };
+
     if (nsub > 0) issue(nsub - 1, 0);
     for (int it = 0; it < nsub; ++it) {
-        const int s_ = nsub - 1 - it;
-        char* st = smem + (it & 1) * Ly::STAGE;
-        if (s_ > 0) issue(s_ - 1, (it + 1) & 1);  // into the buffer chunk it-1 used
+        const int s_ = nsub - 1 - it, cb = it & 1;
+        char* st = smem + cb * Ly::STAGE;
+        float* BTc = BT + cb * kN * T;
+        float* CTc = CT + cb * kN * T;
+        float* OBc = OB + cb * OBSZ;
         // every thread waits for the chunk (bounded); after a timeout the block
         // stops waiting but keeps the barrier sequence (its results are flagged invalid)
-        if (!aborted && !mbar_wait_bounded(smem_u32(&fullb[it & 1]), (unsigned)((it >> 1) & 1))) {
+        if (!aborted && !mbar_wait_bounded(smem_u32(&fullb[cb]), (unsigned)((it >> 1) & 1))) {
             aborted = 1;
             if (p.status) atomicOr(p.status, kStatusTimeout);
         }
-        __syncthreads();
         const int64_t t0 = tb0 + (int64_t)s_ * T;
         const int rows = (int)min64(T, tb1 - t0);
         {
@@ -187,8 +210,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
             for (int i = tid; i < kN * T; i += NT) {
                 const int n = i / T, tok = i - n * T;
                 const bool live = tok < rows;  // rows past the end belong to other tokens: zero, not read
-                BT[i] = live ? IOT<IO>::to_f(Braw[tok * kN + n]) : 0.f;
-                CT[i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
+                BTc[i] = live ? IOT<IO>::to_f(Braw[tok * kN + n]) : 0.f;
+                CTc[i] = live ? IOT<IO>::to_f(Craw[tok * kN + n]) : 0.f;
             }
         }
 
@@ -236,7 +259,11 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
             Ul[1][m] = f2(__shfl_xor_sync(0xffffffffu, Ul[0][m].x, 16), __shfl_xor_sync(0xffffffffu, Ul[0][m].y, 16));
             Pl[1][m] = f2(__shfl_xor_sync(0xffffffffu, Pl[0][m].x, 16), __shfl_xor_sync(0xffffffffu, Pl[0][m].y, 16));
         }
-        __syncthreads();  // B^T / C^T ready
+        // the chunk's B^T / C^T are ready; every thread is done with the previous
+        // chunk (its staging buffer is free, its dB/dC rows are complete)
+        __syncthreads();
+        if (s_ > 0) issue(s_ - 1, cb ^ 1);  // into the buffer the previous chunk used
+        if (it > 0) flush_dbdc(s_ + 1, OB + (cb ^ 1) * OBSZ);
 
         // ---- S: per state, both channels; per-token state sums in registers
         float2 S1[2][T / 2], S2[2][T / 2], S3[2][T / 2];
@@ -251,8 +278,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         float2 aS[2][2][T / 2], hS[2][2][T / 2], bS[2][T / 2];  // [state parity][channel slot][token pair]
         float A2s[2][2], hps[2][2];
         auto load_state = [&](int n, int k) {
-            const float4 b4a = *reinterpret_cast<const float4*>(BT + n * T);
-            const float4 b4b = *reinterpret_cast<const float4*>(BT + n * T + 4);
+            const float4 b4a = *reinterpret_cast<const float4*>(BTc + n * T);
+            const float4 b4b = *reinterpret_cast<const float4*>(BTc + n * T + 4);
             bS[k][0] = f2(b4a.x, b4a.y); bS[k][1] = f2(b4a.z, b4a.w);
             bS[k][2] = f2(b4b.x, b4b.y); bS[k][3] = f2(b4b.z, b4b.w);
 #pragma unroll
@@ -282,8 +309,8 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         for (int s = 0; s < NS; ++s) {
             const int n = NS * hk + s, k = s & 1;
             const bool more = s + 1 < NS;
-            const float4 c4a = *reinterpret_cast<const float4*>(CT + n * T);
-            const float4 c4b = *reinterpret_cast<const float4*>(CT + n * T + 4);
+            const float4 c4a = *reinterpret_cast<const float4*>(CTc + n * T);
+            const float4 c4b = *reinterpret_cast<const float4*>(CTc + n * T + 4);
             const float2 cc[4] = {f2(c4a.x, c4a.y), f2(c4a.z, c4a.w), f2(c4b.x, c4b.y), f2(c4b.z, c4b.w)};
             float2 Ap[2];
 #pragma unroll
@@ -350,7 +377,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
                     acc = make_float4(lo.x, lo.y, hi.x, hi.y);
                 }
                 const int nn = NS * hk + s - (SPB - 1) + (o >> 2), type = (o >> 1) & 1, tk = (o & 1) * 4;
-                float* ob = OB + ((warp * 2 + type) * T + tk) * kN + nn;
+                float* ob = OBc + ((warp * 2 + type) * T + tk) * kN + nn;
                 ob[0] = acc.x;
                 ob[kN] = acc.y;
                 ob[2 * kN] = acc.z;
@@ -404,23 +431,9 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
                 }
             }
         }
-        __syncthreads();  // every warp's dB/dC rows are in OB
-        // dB / dC of the chunk: sum the warps, one vector atomic per 4 outputs
-        if (tid < 2 * T * (kN / 4)) {
-            const int type = tid / (T * kN / 4), rem = tid % (T * kN / 4);
-            const int tk = rem / (kN / 4), n0 = (rem % (kN / 4)) * 4;
-            if (tk < rows) {
-                float4 s4 = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int w = 0; w < Ly::NW; ++w) {
-                    const float4 v = *reinterpret_cast<const float4*>(OB + ((w * 2 + type) * T + tk) * kN + n0);
-                    s4.x += v.x; s4.y += v.y; s4.z += v.z; s4.w += v.w;
-                }
-                red_add_v4((type == 0 ? p.dB : p.dC) + (b * L + t0 + tk) * kN + n0, s4);
-            }
-        }
-        __syncthreads();
     }
+    __syncthreads();  // the last chunk's dB/dC rows are complete
+    if (nsub > 0) flush_dbdc(0, OB + ((nsub - 1) & 1) * OBSZ);
 
     // ---- reductions over the group
 #pragma unroll
