@@ -490,7 +490,9 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
     char* smem = smem_raw + ((128u - (smem_u32(smem_raw) & 127u)) & 127u);  // the TMA destinations
     __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];
     __shared__ int aborted;
-    __shared__ __align__(16) float CT[kN * T];
+    // C^T double-buffered by tile parity (one CTA barrier per tile); a
+    // channel's Delta / dp row is shared by its lane pair only (warp syncs)
+    __shared__ __align__(16) float CT2[2 * kN * T];
     __shared__ __align__(16) float DP[CH * Ly::ROW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -544,7 +546,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             aborted = 1;
             if (p.status) atomicOr(p.status, kStatusTimeout);
         }
-        __syncthreads();
+        float* CT = CT2 + (j & 1) * kN * T;
         const int64_t t0 = tb0 + (int64_t)(ntile - 1 - j) * T;
         const int rows = (int)min64(T, tb1 - t0);
         {
@@ -579,6 +581,8 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             *reinterpret_cast<float4*>(dp + T + NS * hk) = make_float4(pl[0].x, pl[0].y, pl[1].x, pl[1].y);
             *reinterpret_cast<float4*>(dp + T + NS * hk + 4) = make_float4(pl[2].x, pl[2].y, pl[3].x, pl[3].y);
         }
+        // the tile's C^T and Delta / dp rows are ready; every thread is done
+        // with the previous tile (so its staging slot may be refilled)
         __syncthreads();
         float2 Dl[T / 2], Pl[T / 2];
 #pragma unroll
@@ -632,7 +636,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
                 an[s + i] = nx[i];
             }
         }
-        __syncthreads();
+        __syncwarp();  // the lane pair is done with its Delta / dp row before the next tile rewrites it
     }
     ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, 16));
     if (dv) {
