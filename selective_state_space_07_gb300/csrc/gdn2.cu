@@ -275,8 +275,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
-    // the copies of chunk cj (thread 0); rows past the end of the whole
-    // tensor read as zero, rows of the next (batch, head) are zeroed or
+    // the copies of chunk cj (issued by kTmaThread); rows past the end of the
+    // whole tensor read as zero, rows of the next (batch, head) are zeroed or
     // ignored on the ragged last chunk
     auto row_of = [&](int cj) { return (int)(bh * T + (int64_t)cj * kGC); };
     // a test-armed fault: this chunk's q, k, b copies are never issued, so the
