@@ -320,6 +320,68 @@ def make_gdn2_inputs(B: int, H: int, T: int, K: int, V: int, *, seed: int = 0, i
     return Gdn2Inputs(B, H, T, K, V, q, k, v, g, b, w, state, float(1.0 / np.sqrt(K)))
 
 
+@dataclass
+class MlstmInputs:
+    """One problem for the mLSTM chunkwise forward (layout [batch, heads,
+    time, dim]): q, k [B,H,T,K]; v [B,H,T,V]; igate, fgate [B,H,T] (gate
+    pre-activations); the stabilized initial state C0 [B,H,K,V], n0 [B,H,K],
+    m0 [B,H]; the head-wise norm's weight [H,V]; scale."""
+    B: int
+    H: int
+    T: int
+    K: int
+    V: int
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    igate: np.ndarray
+    fgate: np.ndarray
+    C0: np.ndarray
+    n0: np.ndarray
+    m0: np.ndarray
+    norm_weight: np.ndarray
+    scale: float
+
+
+MLSTM_WORKLOADS = {
+    # name: (B, H, T, K, V, seed); chunks of 64 tokens
+    "mlstm-small": (1, 2, 200, 128, 128, 13),
+    "mlstm-8x16x2048": (8, 16, 2048, 128, 128, 14),
+}
+
+
+def make_mlstm_inputs(B: int, H: int, T: int, K: int, V: int, *, seed: int = 0, io: str = "bf16",
+                      with_state: bool = True, igate_mean: float = 0.0) -> MlstmInputs:
+    """Draw an mLSTM problem: q, k, v ~ N(0, 1); input-gate pre-activations
+    ~ N(igate_mean, 1) (i = exp(.) around 1); forget-gate pre-activations
+    uniform in [3, 6] (f = sigmoid(.) between 0.95 and 0.998: long memory);
+    with with_state, C0 ~ N(0, 0.1^2), n0 ~ N(0, 0.1^2) and m0 uniform in
+    [-2, 2] (else zeros); the norm weight ~ 1 + N(0, 0.1^2); scale =
+    1/sqrt(K). With io = "bf16", q, k, v are rounded to bfloat16 once; the
+    gates, the state and the weight stay float32. Per-tensor seeds from the
+    same SplitMix64 streams as make_inputs (x, z, Bm, Cm, dt, dy, h0,
+    dh_last slots in order)."""
+    s = tensor_seeds(seed)
+    nk, nv, nt = B * H * T * K, B * H * T * V, B * H * T
+    rnd = round_bf16 if io == "bf16" else (lambda a: np.asarray(a, np.float32))
+    q = rnd(normal_f32(s["x"], nk)).reshape(B, H, T, K)
+    k = rnd(normal_f32(s["z"], nk)).reshape(B, H, T, K)
+    v = rnd(normal_f32(s["Bm"], nv)).reshape(B, H, T, V)
+    igate = normal_f32(s["Cm"], nt, igate_mean, 1.0).reshape(B, H, T)
+    fgate = (3.0 + 3.0 * uniform53(s["dt"], nt)).astype(np.float32).reshape(B, H, T)
+    if with_state:
+        st = normal_f32(s["h0"], B * H * (K * V + K), 0.0, 0.1)
+        C0 = st[:B * H * K * V].reshape(B, H, K, V)
+        n0 = st[B * H * K * V:].reshape(B, H, K)
+        m0 = (-2.0 + 4.0 * uniform53(s["dh_last"], B * H)).astype(np.float32).reshape(B, H)
+    else:
+        C0 = np.zeros((B, H, K, V), np.float32)
+        n0 = np.zeros((B, H, K), np.float32)
+        m0 = np.zeros((B, H), np.float32)
+    wgt = (1.0 + normal_f32(s["dy"], H * V, 0.0, 0.1)).astype(np.float32).reshape(H, V)
+    return MlstmInputs(B, H, T, K, V, q, k, v, igate, fgate, C0, n0, m0, wgt, float(1.0 / np.sqrt(K)))
+
+
 def recipe_text() -> str:
     lines = []
     for w in WORKLOADS.values():
