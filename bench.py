@@ -26,7 +26,9 @@ an x_proj-shaped buffer) on the workload's B*L tokens and D channels.
 
 --op gdn2 times the Gated DeltaNet-2 chunkwise forward (gdn2_chunk_fwd) on
 a GDN2 workload (default gdn2-1.3b-like: 8 x 16 heads x 2048 tokens,
-K = V = 128, chunks of 64): one step = one forward call.
+K = V = 128, chunks of 64): one step = one forward call. --op mlstm times
+the mLSTM stabilized chunkwise forward (mlstm_chunk_fwd) the same way
+(default mlstm-8x16x2048: 8 x 16 heads x 2048 tokens, K = V = 128).
 """
 from __future__ import annotations
 
@@ -143,7 +145,8 @@ CALL_SOURCES = {
     "ssm_conv1d_bwd": ("ssm_conv.cu", "ssm_common.cuh", "ssm_internal.h"),
     "ssm_dtproj_fwd": ("ssm_dtproj.cu", "ssm_common.cuh", "ssm_internal.h"),
     "ssm_dtproj_bwd": ("ssm_dtproj.cu", "ssm_common.cuh", "ssm_internal.h"),
-    "gdn2_chunk_fwd": ("gdn2.cu", "ssm_common.cuh", "ssm_internal.h"),
+    "gdn2_chunk_fwd": ("gdn2.cu", "tc_common.cuh", "ssm_common.cuh", "ssm_internal.h"),
+    "mlstm_chunk_fwd": ("mlstm.cu", "tc_common.cuh", "ssm_common.cuh", "ssm_internal.h"),
 }
 
 
@@ -1004,10 +1007,11 @@ def run_dtproj(args, w):
     return 0
 
 
-# ------------------------------------------------------------------ gdn2
+# ------------------------------------------------------------------ gdn2, mlstm
 GDN2_METRIC = "gdn2 chunkwise forward M(token·head)/s on 1 GB300; % of HBM roofline"
-GDN2_UNIT = "M(token·head)/s"
-GDN2_CHUNK = 64
+MLSTM_METRIC = "mlstm chunkwise forward M(token·head)/s on 1 GB300; % of HBM roofline"
+CHUNK_UNIT = "M(token·head)/s"
+CHUNK = 64  # tokens per chunk of both chunked forwards
 
 
 def gdn2_algorithmic_bytes(B, H, T, K, V):
@@ -1018,7 +1022,7 @@ def gdn2_algorithmic_bytes(B, H, T, K, V):
     return B * H * T * (K * (3 * 2 + 4) + V * (2 * 2 + 2)) + 2 * B * H * K * V * 4
 
 
-def gdn2_flops(B, H, T, K, V, c=GDN2_CHUNK):
+def gdn2_flops(B, H, T, K, V, c=CHUNK):
     """The method's multiply-add work per full chunk, 2 flops each: q k^T and
     (b k) k^T (2 c^2 K), the key-mean decay as a product (c^2 K), the WY rows
     W and U from the inverse (c^2 K + c^2 V), W S (c K V), the output's two
@@ -1027,57 +1031,129 @@ def gdn2_flops(B, H, T, K, V, c=GDN2_CHUNK):
     return B * H * (T / c) * per_chunk
 
 
-def _gdn2_oracle_step(x, tmax):
-    from oracle import gdn2_oracle
-    sl = lambda a: a[:1, :1, :tmax]  # noqa: E731
-    t0 = time.perf_counter()
-    gdn2_oracle.chunk_wy_forward(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.b), sl(x.w), x.state[:1, :1], x.scale,
-                                 chunk=GDN2_CHUNK)
-    return time.perf_counter() - t0
+def mlstm_algorithmic_bytes(B, H, T, K, V):
+    """Bytes the forward moves at least once: q, k (bf16) per key channel, v
+    and h (bf16) per value channel and the two fp32 gate pre-activations, for
+    every (token, head); the fp32 state (C, n, m) read and written once per
+    (batch, head)."""
+    return B * H * T * (K * 2 * 2 + V * 2 * 2 + 2 * 4) + 2 * B * H * (K * V + K + 1) * 4
 
 
-def gdn2_cpu_sample(name, budget_s):
-    """The float64 GDN2 oracle (numpy) on head (0, 0) of the workload, the
-    first tokens (whole chunks), sized for about budget_s."""
-    B, H, T, K, V, seed = gen.GDN2_WORKLOADS[name]
-    x = gen.make_gdn2_inputs(1, 1, T, K, V, seed=seed)
-    t = _gdn2_oracle_step(x, GDN2_CHUNK)
-    tmax = int(min(T, max(GDN2_CHUNK, GDN2_CHUNK * budget_s / max(t, 1e-4))) // GDN2_CHUNK * GDN2_CHUNK)
-    return x, tmax
+def mlstm_flops(B, H, T, K, V, c=CHUNK):
+    """The method's multiply-add work per full chunk, 2 flops each: q k^T
+    (c^2 K), P v (c^2 V), the state's share of the output q C (c K V) and the
+    state update sum gamma k v^T (c K V)."""
+    return B * H * (T / c) * 2 * (c * c * K + c * c * V + 2 * c * K * V)
 
 
-def gdn2_name(args):
-    return args.workload if args.workload in gen.GDN2_WORKLOADS else "gdn2-1.3b-like"
+class ChunkOp:
+    """One of the chunked forwards as bench.py times it: its workloads, the
+    device tensors of a problem, the call, the oracle step and the roofline
+    figures."""
+
+    def __init__(self, op):
+        self.op = op
+        if op == "gdn2":
+            self.metric, self.workloads, self.default = GDN2_METRIC, gen.GDN2_WORKLOADS, "gdn2-1.3b-like"
+            self.call_name, self.kernel = "gdn2_chunk_fwd", "gdn2_chunk_fwd_kernel"
+            self.bytes, self.flops = gdn2_algorithmic_bytes, gdn2_flops
+        else:
+            self.metric, self.workloads, self.default = MLSTM_METRIC, gen.MLSTM_WORKLOADS, "mlstm-8x16x2048"
+            self.call_name, self.kernel = "mlstm_chunk_fwd", "mlstm_chunk_fwd_kernel"
+            self.bytes, self.flops = mlstm_algorithmic_bytes, mlstm_flops
+
+    def name(self, args):
+        return args.workload if args.workload in self.workloads else self.default
+
+    def inputs(self, B, H, T, K, V, seed):
+        if self.op == "gdn2":
+            return gen.make_gdn2_inputs(B, H, T, K, V, seed=seed)
+        return gen.make_mlstm_inputs(B, H, T, K, V, seed=seed)
+
+    def oracle_step(self, x, tmax):
+        """Seconds the float64 oracle takes on head (0, 0), the first tmax tokens."""
+        sl = lambda a: a[:1, :1, :tmax]  # noqa: E731
+        t0 = time.perf_counter()
+        if self.op == "gdn2":
+            from oracle import gdn2_oracle
+            gdn2_oracle.chunk_wy_forward(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.b), sl(x.w), x.state[:1, :1],
+                                         x.scale, chunk=CHUNK)
+        else:
+            from oracle import mlstm_oracle
+            mlstm_oracle.chunkwise(sl(x.q), sl(x.k), sl(x.v), sl(x.igate), sl(x.fgate), x.C0[:1, :1], x.n0[:1, :1],
+                                   x.m0[:1, :1], scale=x.scale, chunk=CHUNK)
+        return time.perf_counter() - t0
+
+    def cpu_sample(self, name, budget_s):
+        """Head (0, 0) of the workload, the first tokens (whole chunks), sized for
+        about budget_s of oracle time."""
+        B, H, T, K, V, seed = self.workloads[name]
+        x = self.inputs(1, 1, T, K, V, seed)
+        t = self.oracle_step(x, CHUNK)
+        tmax = int(min(T, max(CHUNK, CHUNK * budget_s / max(t, 1e-4))) // CHUNK * CHUNK)
+        return x, tmax
+
+    def device_setup(self, x, dev):
+        """Device inputs, outputs and the call (returning the launch count)."""
+        import torch
+        import selective_state_space_07_gb300 as ssm
+        bf, f32 = torch.bfloat16, torch.float32
+        B, H, T, K, V = x.B, x.H, x.T, x.K, x.V
+        scale = K ** -0.5
+        ws = ssm.Workspace(1, 1, 8, dev)
+        if self.op == "gdn2":
+            t = {n: torch.from_numpy(getattr(x, n)).to(dev, bf) for n in ("q", "k", "v", "b", "w")}
+            t["g"] = torch.from_numpy(x.g).to(dev, f32)
+            t["state"] = torch.from_numpy(x.state).to(dev, f32)
+            o = {"out": torch.empty(B, H, T, V, dtype=bf, device=dev),
+                 "state": torch.empty(B, H, K, V, dtype=f32, device=dev)}
+
+            def call():
+                ssm.gdn2_fwd(t["q"], t["k"], t["v"], t["g"], t["b"], t["w"], t["state"], scale, out=o["out"],
+                             state_out=o["state"], workspace=ws)
+                return ssm.last_launch_count()
+        else:
+            t = {n: torch.from_numpy(getattr(x, n)).to(dev, bf) for n in ("q", "k", "v")}
+            for n in ("igate", "fgate", "C0", "n0", "m0"):
+                t[n] = torch.from_numpy(np.ascontiguousarray(getattr(x, n))).to(dev, f32)
+            o = {"h": torch.empty(B, H, T, V, dtype=bf, device=dev), "C": torch.empty(B, H, K, V, dtype=f32, device=dev),
+                 "n": torch.empty(B, H, K, dtype=f32, device=dev), "m": torch.empty(B, H, dtype=f32, device=dev)}
+
+            def call():
+                ssm.mlstm_fwd(t["q"], t["k"], t["v"], t["igate"], t["fgate"], (t["C0"], t["n0"], t["m0"]), scale,
+                              h=o["h"], state_out=(o["C"], o["n"], o["m"]), workspace=ws)
+                return ssm.last_launch_count()
+        return t, o, call, ws
 
 
-def run_gdn2_reference(args):
+def run_chunk_reference(args, op):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    name = gdn2_name(args)
-    B, H, T, K, V, seed = gen.GDN2_WORKLOADS[name]
-    x, tmax = gdn2_cpu_sample(name, 150.0 / max(1, args.steps + args.warmup))
+    name = op.name(args)
+    B, H, T, K, V, seed = op.workloads[name]
+    x, tmax = op.cpu_sample(name, 150.0 / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        _gdn2_oracle_step(x, tmax)
-    ts = [_gdn2_oracle_step(x, tmax) for _ in range(args.steps)]
+        op.oracle_step(x, tmax)
+    ts = [op.oracle_step(x, tmax) for _ in range(args.steps)]
     total = sum(ts)
     val = tmax * len(ts) / total / 1e6
     sample = (f"per step: head (0, 0), the first {tmax} of {T} tokens, float64 numpy oracle of the chunked forward "
               f"(numpy's BLAS may thread its products over the host's cores)")
     line = {
-        "impl": "reference", "metric": GDN2_METRIC, "value": val, "unit": GDN2_UNIT, "n_gpus": world,
+        "impl": "reference", "metric": op.metric, "value": val, "unit": CHUNK_UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / len(ts), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": name, "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": GDN2_CHUNK},
-        "cpu_baseline": {"value": val, "unit": GDN2_UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
-        "e2e": {"value": val, "unit": GDN2_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "config": {"workload": name, "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": CHUNK},
+        "cpu_baseline": {"value": val, "unit": CHUNK_UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": val, "unit": CHUNK_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
 
 
-def run_gdn2(args):
-    """gdn2_chunk_fwd on a GDN2 workload: one step = one forward call timed with
+def run_chunk(args, op):
+    """A chunked forward on its workload: one step = one forward call timed with
     CUDA events after an L2 flush, inputs resident in HBM."""
     import torch
     import selective_state_space_07_gb300 as ssm
@@ -1087,25 +1163,13 @@ def run_gdn2(args):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     ssm.build()
-    name = gdn2_name(args)
-    B, H, T, K, V, seed = gen.GDN2_WORKLOADS[name]
-    x = gen.make_gdn2_inputs(B, H, T, K, V, seed=seed)
-    bf, f32 = torch.bfloat16, torch.float32
-    t = {n: torch.from_numpy(getattr(x, n)).to(dev, bf) for n in ("q", "k", "v", "b", "w")}
-    t["g"] = torch.from_numpy(x.g).to(dev, f32)
-    t["state"] = torch.from_numpy(x.state).to(dev, f32)
+    name = op.name(args)
+    B, H, T, K, V, seed = op.workloads[name]
+    x = op.inputs(B, H, T, K, V, seed)
+    t, outs, fwd, ws = op.device_setup(x, dev)
     del x
-    out = torch.empty(B, H, T, V, dtype=bf, device=dev)
-    st = torch.empty(B, H, K, V, dtype=f32, device=dev)
-    ws = ssm.Workspace(1, 1, 8, dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    scale = K ** -0.5
-
-    def fwd():
-        ssm.gdn2_fwd(t["q"], t["k"], t["v"], t["g"], t["b"], t["w"], t["state"], scale, out=out, state_out=st,
-                     workspace=ws)
-        return ssm.last_launch_count()
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -1138,15 +1202,14 @@ def run_gdn2(args):
     e2e = None
     if not args.no_e2e:  # inputs in from pinned host memory, the output and the final state back
         h_in = {n: v.cpu().pin_memory() for n, v in t.items()}
-        h_out = {"out": torch.empty_like(out, device="cpu").pin_memory(),
-                 "state": torch.empty_like(st, device="cpu").pin_memory()}
+        h_out = {n: torch.empty_like(v, device="cpu").pin_memory() for n, v in outs.items()}
 
         def e2e_step():
             for n, v in h_in.items():
                 t[n].copy_(v, non_blocking=True)
             fwd()
-            h_out["out"].copy_(out, non_blocking=True)
-            h_out["state"].copy_(st, non_blocking=True)
+            for n, v in h_out.items():
+                v.copy_(outs[n], non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -1159,39 +1222,39 @@ def run_gdn2(args):
         ee.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks([es.elapsed_time(ee) / n], dist, dev)[0]
-        e2e = {"value": round(world * units / (e2e_ms * 1e-3) / 1e6, 3), "unit": GDN2_UNIT,
+        e2e = {"value": round(world * units / (e2e_ms * 1e-3) / 1e6, 3), "unit": CHUNK_UNIT,
                "h2d_bytes_per_step": sum(v.numel() * v.element_size() for v in h_in.values()),
                "d2h_bytes_per_step": sum(v.numel() * v.element_size() for v in h_out.values()),
-               "ms_per_step": round(e2e_ms, 4), "api": "gdn2_fwd on one stream, pinned host copies"}
+               "ms_per_step": round(e2e_ms, 4), "api": f"{op.op}_fwd on one stream, pinned host copies"}
     if rank != 0:
         if dist:
             dist.destroy_process_group()
         return 0
     peak, peak_kind, peaks = measured_peaks()
-    ab = gdn2_algorithmic_bytes(B, H, T, K, V)
+    ab = op.bytes(B, H, T, K, V)
     ach = ab / (ms * 1e-3) / 1e9
     rf = {"bound": "hbm", "achieved": round(ach, 1), "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-          "peak_kind": peak_kind, "kernel": "gdn2_chunk_fwd_kernel", "algorithmic_bytes_per_launch": ab,
-          "ms_per_launch": round(ms, 5), "traffic": profiled_traffic("gdn2_chunk_fwd", name)}
-    fl = gdn2_flops(B, H, T, K, V)
+          "peak_kind": peak_kind, "kernel": op.kernel, "algorithmic_bytes_per_launch": ab,
+          "ms_per_launch": round(ms, 5), "traffic": profiled_traffic(op.call_name, name)}
+    fl = op.flops(B, H, T, K, V)
     tpk = float(peaks.get("bf16_tflops", 1900.0)) if peaks else 1900.0
     tf = fl / (ms * 1e-3) / 1e12
     tens = {"bound": "tensor", "achieved": round(tf, 2), "peak": tpk, "unit": "TFLOP/s", "frac": round(tf / tpk, 4),
             "peak_kind": "measured bf16 (burst)" if peaks else "fallback", "flops_per_launch": fl}
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        x1, tmax = gdn2_cpu_sample(name, 6.0)
+        x1, tmax = op.cpu_sample(name, 6.0)
         ts = []
         while sum(ts) < 12.0 and len(ts) < 50:
-            ts.append(_gdn2_oracle_step(x1, tmax))
-        cpu = {"value": tmax * len(ts) / sum(ts) / 1e6, "unit": GDN2_UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            ts.append(op.oracle_step(x1, tmax))
+        cpu = {"value": tmax * len(ts) / sum(ts) / 1e6, "unit": CHUNK_UNIT, "cores": os.cpu_count(), "kind": "oracle",
                "sample": f"head (0, 0), the first {tmax} of {T} tokens, float64 numpy oracle (its BLAS may thread "
                          f"over the host's cores), {len(ts)} repetitions, {sum(ts):.1f} s"}
     line = {
-        "metric": GDN2_METRIC, "value": round(value, 3), "unit": GDN2_UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": op.metric, "value": round(value, 3), "unit": CHUNK_UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": name, "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": GDN2_CHUNK, "seed": seed,
+        "config": {"workload": name, "B": B, "H": H, "T": T, "K": K, "V": V, "chunk": CHUNK, "seed": seed,
                    "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (129 MB) and a 512 MiB write flushes L2 before every call"},
         "roofline": rf, "tensor_roofline": tens, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
@@ -1209,22 +1272,27 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(gen.WORKLOAD_ORDER) + list(gen.GDN2_WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(gen.WORKLOAD_ORDER) + list(gen.GDN2_WORKLOADS) + list(gen.MLSTM_WORKLOADS))
     ap.add_argument("--nsplit", type=int, default=0, help="lanes per channel (0 = library's choice)")
     ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-extras", action="store_true", help="skip the inference-forward and decode timings")
-    ap.add_argument("--op", choices=("scan", "conv1d", "dtproj", "gdn2"), default="scan",
+    ap.add_argument("--op", choices=("scan", "conv1d", "dtproj", "gdn2", "mlstm"), default="scan",
                     help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it; "
-                         "dtproj: the dt projection with its softplus; gdn2: the Gated DeltaNet-2 chunkwise forward")
+                         "dtproj: the dt projection with its softplus; gdn2: the Gated DeltaNet-2 chunkwise forward; "
+                         "mlstm: the mLSTM stabilized chunkwise forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.op == "gdn2":
-        return run_gdn2_reference(args) if args.impl == "reference" else run_gdn2(args)
-    if args.workload in gen.GDN2_WORKLOADS:
-        ap.error("a GDN2 workload needs --op gdn2")
+    if args.op in ("gdn2", "mlstm"):
+        op = ChunkOp(args.op)
+        if args.workload != DEFAULT_WORKLOAD and args.workload not in op.workloads:
+            ap.error(f"--op {args.op} takes one of {sorted(op.workloads)}")
+        return run_chunk_reference(args, op) if args.impl == "reference" else run_chunk(args, op)
+    if args.workload in gen.GDN2_WORKLOADS or args.workload in gen.MLSTM_WORKLOADS:
+        ap.error("a GDN2 or mLSTM workload needs --op gdn2 or --op mlstm")
     w = gen.WORKLOADS[args.workload]
     if args.op == "dtproj":
         return run_dtproj_reference(args, w) if args.impl == "reference" else run_dtproj(args, w)

@@ -19,7 +19,12 @@ Also bound here: the conv1d + SiLU in front of the scan (``conv1d_fwd``,
 tensor cores (``dtproj_fwd``, ``dtproj_bwd``), and the Gated DeltaNet-2
 chunkwise forward (``gdn2_fwd``; C ABI in ``include/gdn2.h``; docs.rs,
 burn-gdn2 0.1.4, src/forward.rs, chunk_wy_forward): q, k, b, g [B, H, T,
-128], v, w [B, H, T, 128], state [B, H, 128, 128], chunks of 64 tokens.
+128], v, w [B, H, T, 128], state [B, H, 128, 128], chunks of 64 tokens; and
+the mLSTM stabilized chunkwise forward (``mlstm_fwd``; C ABI in
+``include/mlstm.h``; Evil-Inference-Code, README_FIX_RUST.md, "mLSTM
+Equivalence Fixes (Rust vs Python)"): q, k, v [B, H, T, 128] bf16, gate
+pre-activations [B, H, T] fp32, stabilized state C [B, H, 128, 128], n [B, H,
+128], m [B, H], an optional head-wise norm, chunks of 64 tokens.
 """
 from __future__ import annotations
 
@@ -35,7 +40,7 @@ __all__ = [
     "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
     "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
-    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault",
+    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -106,6 +111,17 @@ class Gdn2Args(ctypes.Structure):
 
 GDN2_CHUNK = 64
 
+
+class MlstmArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("V", ctypes.c_int64), ("chunk", ctypes.c_int32), ("scale", ctypes.c_float),
+                ("norm_eps", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("q", "k", "v", "igate", "fgate", "C_in", "n_in", "m_in", "norm_weight", "h",
+                                       "C_out", "n_out", "m_out", "workspace")]
+
+
+MLSTM_CHUNK = 64
+
 EXPORTS = {
     "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
@@ -127,6 +143,8 @@ EXPORTS = {
     "ssm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
     "gdn2_chunk_fwd": ([ctypes.POINTER(Gdn2Args), ctypes.c_void_p], ctypes.c_int),
     "gdn2_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
+    "mlstm_chunk_fwd": ([ctypes.POINTER(MlstmArgs), ctypes.c_void_p], ctypes.c_int),
+    "mlstm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
 }
 
 
@@ -574,6 +592,60 @@ def gdn2_arm_wait_fault(chunk: int, wait_ns: int) -> None:
     """Test hook: the next gdn2_fwd of this thread does not issue chunk `chunk`'s q, k, b copies and bounds every
     wait by wait_ns, so the call ends with SSM_ERR_TIMEOUT in the status word. chunk < 0 disarms."""
     _check(lib().gdn2_debug_arm_wait_fault(int(chunk), int(wait_ns)), "gdn2_debug_arm_wait_fault")
+
+
+def mlstm_fwd(q, k, v, igate, fgate, state=None, scale=None, *, norm_weight=None, norm_eps=1e-5, h=None,
+              state_out=None, want_state=True, workspace=None, stream=None):
+    """mLSTM stabilized chunkwise forward (C ABI in ``include/mlstm.h``; Evil-Inference-Code,
+    README_FIX_RUST.md, "mLSTM Equivalence Fixes (Rust vs Python)") on the tensor cores, chunks of 64 tokens.
+    q, k [B, H, T, 128] bf16; v [B, H, T, 128] bf16; igate, fgate [B, H, T] fp32 gate pre-activations;
+    state = (C [B, H, 128, 128], n [B, H, 128], m [B, H]) fp32 stabilized, or None (zeros, m = 0);
+    norm_weight [H, 128] fp32 applies the head-wise norm (no bias) to h; scale defaults to 1/sqrt(K).
+    Returns (h [B, H, T, V] bf16, final state (C, n, m) or None)."""
+    if q.dim() != 4:
+        raise ValueError("q must be [B, H, T, K]")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("the mLSTM forward runs on a CUDA device; q is on " + str(dev))
+    Bn, H, T, K = q.shape
+    V = v.shape[-1] if v.dim() == 4 else -1
+    bf, f32 = torch.bfloat16, torch.float32
+    _need(q, "q", (Bn, H, T, K), bf, dev)
+    _need(k, "k", (Bn, H, T, K), bf, dev)
+    _need(v, "v", (Bn, H, T, V), bf, dev)
+    _need(igate, "igate", (Bn, H, T), f32, dev)
+    _need(fgate, "fgate", (Bn, H, T), f32, dev)
+    shapes = ((Bn, H, K, V), (Bn, H, K), (Bn, H))
+    if state is not None:
+        if len(state) != 3:
+            raise ValueError("state must be (C, n, m)")
+        for t, n, shp in zip(state, ("C", "n", "m"), shapes):
+            _need(t, n, shp, f32, dev)
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", (H, V), f32, dev)
+    h = torch.empty((Bn, H, T, V), dtype=bf, device=dev) if h is None else h
+    _need(h, "h", (Bn, H, T, V), bf, dev)
+    if want_state and state_out is None:
+        state_out = tuple(torch.empty(shp, dtype=f32, device=dev) for shp in shapes)
+    if state_out is not None:
+        for t, n, shp in zip(state_out, ("C_out", "n_out", "m_out"), shapes):
+            _need(t, n, shp, f32, dev)
+    si = state if state is not None else (None, None, None)
+    so = state_out if state_out is not None else (None, None, None)
+    args = MlstmArgs(B=Bn, H=H, T=T, K=K, V=V, chunk=MLSTM_CHUNK,
+                     scale=float(K ** -0.5 if scale is None else scale), norm_eps=float(norm_eps),
+                     q=_p(q), k=_p(k), v=_p(v), igate=_p(igate), fgate=_p(fgate),
+                     C_in=_p(si[0]), n_in=_p(si[1]), m_in=_p(si[2]), norm_weight=_p(norm_weight), h=_p(h),
+                     C_out=_p(so[0]), n_out=_p(so[1]), m_out=_p(so[2]),
+                     workspace=None if workspace is None else workspace.buf.data_ptr())
+    _check(lib().mlstm_chunk_fwd(ctypes.byref(args), _stream(dev, stream)), "mlstm_chunk_fwd")
+    return h, state_out
+
+
+def mlstm_arm_wait_fault(chunk: int, wait_ns: int) -> None:
+    """Test hook: the next mlstm_fwd of this thread does not issue chunk `chunk`'s q copy and bounds every
+    wait by wait_ns, so the call ends with SSM_ERR_TIMEOUT in the status word. chunk < 0 disarms."""
+    _check(lib().mlstm_debug_arm_wait_fault(int(chunk), int(wait_ns)), "mlstm_debug_arm_wait_fault")
 
 
 def poll_status(workspace, stream=None) -> int:

@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build", "ssmscan")
 LIB = os.path.join(HERE, "libssmscan.so")
-SOURCES = ["ssm_fwd.cu", "ssm_bwd.cu", "ssm_api.cu", "ssm_noalloc.cu", "ssm_conv.cu", "ssm_dtproj.cu", "gdn2.cu"]
+SOURCES = ["ssm_fwd.cu", "ssm_bwd.cu", "ssm_api.cu", "ssm_noalloc.cu", "ssm_conv.cu", "ssm_dtproj.cu", "gdn2.cu",
+           "mlstm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I" + os.path.join(ROOT, "include")]

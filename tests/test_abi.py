@@ -26,7 +26,7 @@ def declared_functions():
         if fn.endswith(".h"):
             text = open(os.path.join(ROOT, "include", fn)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b((?:ssm|gdn2)_\w+)\s*\(", text, flags=re.M))
+            names |= set(re.findall(r"^[A-Za-z_][\w \*]*?\b((?:ssm|gdn2|mlstm)_\w+)\s*\(", text, flags=re.M))
     return names
 
 
@@ -34,7 +34,7 @@ def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("ssm_scan_fwd", "ssm_scan_bwd", "ssm_step", "ssm_scan_workspace_bytes", "ssm_scan_ckpt_elems",
               "ssm_poll_status", "ssm_status_string", "ssm_dA_log_grad", "ssm_conv1d_fwd", "ssm_conv1d_bwd",
-              "ssm_dtproj_fwd", "ssm_dtproj_bwd", "gdn2_chunk_fwd"):
+              "ssm_dtproj_fwd", "ssm_dtproj_bwd", "gdn2_chunk_fwd", "mlstm_chunk_fwd"):
         assert n in names
 
 
@@ -217,7 +217,37 @@ def test_gdn2_fault_hook_arguments(ssm):
     assert ssm.lib().gdn2_debug_arm_wait_fault(-1, 0) == OK  # disarmed
 
 
+def mlstm_args(ssm, **over):
+    a = dict(B=2, H=3, T=100, K=128, V=128, chunk=64, scale=0.088, norm_eps=1e-5, q=FAKE, k=FAKE + 4096,
+             v=FAKE + 8192, igate=FAKE + 12288, fgate=FAKE + 12292, C_in=None, n_in=None, m_in=None, norm_weight=None,
+             h=FAKE + 24576, C_out=None, n_out=None, m_out=None, workspace=None)
+    a.update(over)
+    return ssm.MlstmArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), UNSUPPORTED), (dict(V=256), UNSUPPORTED), (dict(chunk=32), UNSUPPORTED), (dict(B=-1), INVALID),
+    (dict(T=-5), INVALID), (dict(q=None), INVALID), (dict(igate=None), INVALID), (dict(fgate=None), INVALID),
+    (dict(h=None), INVALID), (dict(v=FAKE + 2), ALIGNMENT), (dict(igate=FAKE + 2), ALIGNMENT),
+    (dict(norm_weight=FAKE + 1), ALIGNMENT), (dict(norm_weight=FAKE + 4), ALIGNMENT),
+    (dict(C_in=FAKE + 8, n_in=FAKE, m_in=FAKE), ALIGNMENT), (dict(C_out=FAKE + 4, n_out=FAKE, m_out=FAKE), ALIGNMENT),
+    (dict(C_in=FAKE), INVALID), (dict(n_out=FAKE, m_out=FAKE), INVALID),  # a partial state
+    (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
+    (dict(norm_eps=-1.0), INVALID), (dict(norm_eps=float("nan")), INVALID),
+    (dict(B=1, H=1, T=1 << 31), UNSUPPORTED), (dict(B=4, H=8, T=1 << 26), UNSUPPORTED),
+])
+def test_mlstm_rejects_bad_arguments(ssm, over, code):
+    args = mlstm_args(ssm, **over)
+    assert ssm.lib().mlstm_chunk_fwd(ctypes.byref(args), None) == code
+
+
+def test_mlstm_fault_hook_arguments(ssm):
+    assert ssm.lib().mlstm_debug_arm_wait_fault(0, 20_000_000_000) == INVALID
+    assert ssm.lib().mlstm_debug_arm_wait_fault(-1, 0) == OK  # disarmed
+
+
 def test_null_args_struct(ssm):
+    assert ssm.lib().mlstm_chunk_fwd(None, None) == INVALID
     assert ssm.lib().gdn2_chunk_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_bwd(None, None) == INVALID
