@@ -56,7 +56,7 @@ constexpr int kMC = 64;    // tokens per chunk
 constexpr int kMK = 128;   // key channels
 constexpr int kMV = 128;   // value channels
 constexpr int kMThreads = 256;
-constexpr int kGateWarp = 3;  // runs the gate passes
+constexpr int kGateWarp = 1;  // runs the gate passes (during round 2, where it has no other work)
 constexpr int kCqWarp = 7;    // a thread of it issues the state term C^T q'^T
 
 // Shared-memory regions (bytes from a 1024-byte aligned base).
@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         }
     };
     // m after the last chunk whose gate pass has run (warp kGateWarp); the first chunk's pass runs here,
-    // every later one while the previous chunk's state term is issued
+    // every later one during the previous chunk's round 2
     float m_run = p.m_in ? p.m_in[bh] : 0.f;
     if (warp == kGateWarp && nchunks > 0) {
         load_gates(0);
@@ -337,10 +337,13 @@ __global__ void __launch_bounds__(kMThreads, 1)
         issued[b] += (b == 0 && q_skipped(cj)) ? 0 : 1;
     };
 
-    // the head-wise norm's weights for this lane's channels 4*lane..4*lane+3
+    // the head-wise norm's weights for this lane's output channels 4 (lane % 8) + 32 u, u = 0..3
     const bool has_norm = p.norm_weight != nullptr;
-    const float4 w4 = has_norm ? *reinterpret_cast<const float4*>(p.norm_weight + (bh % p.H) * kMV + 4 * lane)
-                               : make_float4(1.f, 1.f, 1.f, 1.f);
+    float4 w4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+        w4[u] = has_norm ? *reinterpret_cast<const float4*>(p.norm_weight + (bh % p.H) * kMV + 4 * (lane & 7) + 32 * u)
+                         : make_float4(1.f, 1.f, 1.f, 1.f);
 
     bool ok = true;
     for (int ci = 0; ci < nchunks && ok; ++ci) {
@@ -406,20 +409,18 @@ __global__ void __launch_bounds__(kMThreads, 1)
         __syncthreads();
 
         // ---- 2. out^T = C^T (alpha*scale*q)^T, the state's share of the output (issued by a thread of warp
-        // kCqWarp: issuing blocks the issuing thread while the tensor pipe works); meanwhile warp kGateWarp
-        // runs the next chunk's gate pass; then the wait for S
+        // kCqWarp: issuing blocks the issuing thread while the tensor pipe works); every other thread waits
+        // for S by itself (no CTA barrier: the outcome is agreed at the end of phase 3) and goes on
         if (tid == kCqWarp * 32) {
             tc_after();
             mma_issue(tmem + kTO, sbase + kCT, sbase + kQP, 64, 64, kMK, false);
             commit(mbar_c);
         }
-        if (warp == kGateWarp && ci + 1 < nchunks) {
-            m_run = gate_pass(ci + 1, gb ^ 1, m_run, ig_nx, fg_nx);
-            if (ci + 2 < nchunks) load_gates(ci + 2);
-        }
-        if (!(ok = mma_wait(mbar_s, phase_s))) break;
+        const bool ok_s = mbar_wait_try(mbar_s, phase_s & 1u, p.wait_ns);
+        phase_s++;
+        if (!ok_s) fail();
         tc_after();
-        refill(0, ci + 1);  // q has been read (S and the row pass)
+        if (ok_s) refill(0, ci + 1);  // q has been read (the row pass before the barrier, S now)
 
         // ---- 3. P as two bf16 parts and its row sums, every warp a quarter of the columns of 32 rows
         // (rows 0-31 on lanes 0-31 and 64-95, rows 32-63 on lanes 32-63 and 96-127); q.n; then C^T *= beta
@@ -466,13 +467,19 @@ __global__ void __launch_bounds__(kMThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
         fence_async_smem();
         tc_before();
-        // the state term must be complete before round 2 accumulates into out^T (one barrier either way)
-        if (!(ok = mma_wait(mbar_c, phase_c))) break;
+        // the state term must be complete before round 2 accumulates into out^T; one barrier agrees on
+        // both waits
+        {
+            const bool ok_c = mbar_wait_try(mbar_c, phase_c & 1u, p.wait_ns);
+            phase_c++;
+            if (!ok_c) fail();
+            if (!(ok = __syncthreads_and(ok_s && ok_c) != 0)) break;
+        }
         refill(1, ci + 1);  // k has been read
 
-        // ---- 4. out^T += V^T P_hi^T + V^T P_lo^T;  C^T += V^T (gamma*k); meanwhile the
-        // per-token reciprocal of the stabilized denominator and n (the first product, which read
-        // n's rows of the k operand, is complete)
+        // ---- 4. out^T += V^T P_hi^T + V^T P_lo^T;  C^T += V^T (gamma*k); meanwhile the next chunk's
+        // gate pass, the per-token reciprocal of the stabilized denominator and n (the first product,
+        // which read n's rows of the k operand, is complete)
         if (tid == 0) {
             tc_after();
             mma_issue(tmem + kTO, sbase + kVB, sbase + kP, 64, 64, kMC, true, true, false);
@@ -480,7 +487,10 @@ __global__ void __launch_bounds__(kMThreads, 1)
             mma_issue(tmem + kTC, sbase + kVB, sbase + kKP, 0, kMK, kMC, true, true, true);
             commit(mbar);
         }
-        if (tid >= 64 && tid < 64 + kMC) {
+        if (warp == kGateWarp && ci + 1 < nchunks) {  // the next chunk's gate tables
+            m_run = gate_pass(ci + 1, gb ^ 1, m_run, ig_nx, fg_nx);
+            if (ci + 2 < nchunks) load_gates(ci + 2);
+        } else if (tid >= 64 && tid < 64 + kMC) {
             const int t = tid - 64;
             const float rs = (s_rs[t] + s_rs[kMC + t]) + (s_rs[2 * kMC + t] + s_rs[3 * kMC + t]);
             const float den = __fmaf_rn(g_al[t], s_qn[t], rs);
@@ -517,46 +527,45 @@ __global__ void __launch_bounds__(kMThreads, 1)
             for (int i = 0; i < 64; i += 8) st8(sm + kCT, vrow, k0 + i, 128, cv + i);
         }
         __syncthreads();
-        // rows: warp w takes tokens w, w + 8, ..., all eight at once; lane l the channels 4l..4l+3
+        // rows: warp w takes tokens w, w + 8, ..., w + 56, four at a time on lane groups of 8 (group g the
+        // token w + 8 (4 it + g); lane j of it channels 4j + 32u, u = 0..3), so the norm's two sums take
+        // three shuffle rounds per four tokens
         {
-            float4 x[8];
+            const int g = lane >> 3, j = lane & 7;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = warp + 8 * i;
-                x[i] = t < c ? *reinterpret_cast<const float4*>(s_os + t * kOSR + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            if (has_norm) {
-                float sum[8], sq[8];
+            for (int it = 0; it < 2; ++it) {
+                const int t = warp + 8 * (4 * it + g);
+                float4 x[4];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) sum[i] = (x[i].x + x[i].y) + (x[i].z + x[i].w);
+                for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float4*>(s_os + t * kOSR + 4 * j + 32 * u);
+                if (has_norm) {
+                    float sum = 0.f;
 #pragma unroll
-                for (int off = 16; off >= 1; off >>= 1)
+                    for (int u = 0; u < 4; ++u) sum += (x[u].x + x[u].y) + (x[u].z + x[u].w);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) sum[i] += __shfl_xor_sync(0xffffffffu, sum[i], off);
+                    for (int off = 4; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                    const float mean = sum * (1.f / kMV);
+                    float sq = 0.f;
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float mean = sum[i] * (1.f / kMV);
-                    x[i] = make_float4(x[i].x - mean, x[i].y - mean, x[i].z - mean, x[i].w - mean);
-                    sq[i] = (x[i].x * x[i].x + x[i].y * x[i].y) + (x[i].z * x[i].z + x[i].w * x[i].w);
+                    for (int u = 0; u < 4; ++u) {
+                        x[u] = make_float4(x[u].x - mean, x[u].y - mean, x[u].z - mean, x[u].w - mean);
+                        sq += (x[u].x * x[u].x + x[u].y * x[u].y) + (x[u].z * x[u].z + x[u].w * x[u].w);
+                    }
+#pragma unroll
+                    for (int off = 4; off >= 1; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+                    const float rstd = rsqrtf(sq * (1.f / kMV) + p.norm_eps);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        x[u] = make_float4(x[u].x * rstd * w4[u].x, x[u].y * rstd * w4[u].y, x[u].z * rstd * w4[u].z,
+                                           x[u].w * rstd * w4[u].w);
                 }
-#pragma unroll
-                for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) sq[i] += __shfl_xor_sync(0xffffffffu, sq[i], off);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float rstd = rsqrtf(sq[i] * (1.f / kMV) + p.norm_eps);
-                    x[i] = make_float4(x[i].x * rstd * w4.x, x[i].y * rstd * w4.y, x[i].z * rstd * w4.z,
-                                       x[i].w * rstd * w4.w);
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int t = warp + 8 * i;
                 if (t < c) {
-                    nf = __fmaf_rn((x[i].x + x[i].y) + (x[i].z + x[i].w), 0.f, nf);
-                    *reinterpret_cast<uint2*>(p.h + (row0 + t) * kMV + 4 * lane) =
-                        make_uint2(pack_bf2(x[i].x, x[i].y), pack_bf2(x[i].z, x[i].w));
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        nf = __fmaf_rn((x[u].x + x[u].y) + (x[u].z + x[u].w), 0.f, nf);
+                        *reinterpret_cast<uint2*>(p.h + (row0 + t) * kMV + 4 * j + 32 * u) =
+                            make_uint2(pack_bf2(x[u].x, x[u].y), pack_bf2(x[u].z, x[u].w));
+                    }
                 }
             }
         }
