@@ -200,6 +200,19 @@ def test_forward_is_deterministic(ssm):
     assert np.array_equal(h1, h2) and all(np.array_equal(a, b) for a, b in zip(s1, s2))
 
 
+def test_without_final_state(ssm):
+    # want_state=False passes no state buffers (the NULL branch of the C ABI); h is unchanged
+    x = gen.make_mlstm_inputs(1, 2, 90, 128, 128, seed=41)
+    bf = torch.bfloat16
+    st = (dev(x.C0), dev(x.n0), dev(x.m0))
+    h1, s1 = ssm.mlstm_fwd(dev(x.q, bf), dev(x.k, bf), dev(x.v, bf), dev(x.igate), dev(x.fgate), st, x.scale)
+    h2, s2 = ssm.mlstm_fwd(dev(x.q, bf), dev(x.k, bf), dev(x.v, bf), dev(x.igate), dev(x.fgate), st, x.scale,
+                           want_state=False)
+    torch.cuda.synchronize()
+    assert s2 is None and s1 is not None
+    assert torch.equal(h1, h2)
+
+
 def test_binding_rejects_bad_tensors(ssm):
     x = gen.make_mlstm_inputs(1, 1, 16, 128, 128, seed=43)
     bf = torch.bfloat16
