@@ -8,6 +8,10 @@ batch of the workload, inputs resident in HBM. Metric: G(token*channel)/s =
 B*L*D / (t_fwd + t_bwd) / 1e9, summed over ranks. Each pass is timed with
 CUDA events on the launching stream; L2 (129 MB) is flushed before every
 pass, outside the timed segments, and the inputs are larger than L2 anyway.
+After the timed region (unless --no-extras) the line also carries the
+forward without checkpoints, decode throughput through ssm_step, and
+`other_ops`: the path's other calls (conv1d, dt projection, GDN2, mLSTM)
+timed briefly the way their own --op runs time them.
 
 Multi-GPU: one process per GPU (torchrun). Every rank runs the same workload
 as an independent replica (the scan needs no exchange between replicas);
@@ -442,6 +446,45 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ ours
+def emit(args, line, dist):
+    """End a run: print its JSON line (the command-line path), or hand the
+    line back when bench.py collects it as an extra of the scan's run."""
+    if dist:
+        dist.destroy_process_group()
+    if getattr(args, "collect", False):
+        return line
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def other_ops(args, w):
+    """The path's other calls, each timed briefly after the scan's timed
+    region (50 calls, the same L2 flush and CUDA events as its own --op run,
+    no CPU baseline or e2e): conv1d + SiLU fwd+bwd and the dt projection
+    fwd+bwd on the scan workload's shapes, the GDN2 and mLSTM chunkwise
+    forwards on their default workloads."""
+    sub = argparse.Namespace(**vars(args))
+    sub.steps, sub.warmup, sub.no_cpu_baseline, sub.no_e2e, sub.collect = 50, 3, True, True, True
+    runs = (("conv1d", lambda: run_conv(sub, w)), ("dtproj", lambda: run_dtproj(sub, w)),
+            ("gdn2", lambda: run_chunk(sub, ChunkOp("gdn2"))), ("mlstm", lambda: run_chunk(sub, ChunkOp("mlstm"))))
+    out = {}
+    for name, fn in runs:
+        try:
+            line = fn()
+        except Exception as ex:  # an extra must not sink the scan's line
+            log(f"extra {name} failed: {ex}")
+            continue
+        rf = line["roofline"]
+        out[name] = {"workload": line["config"]["workload"], "metric": line["metric"], "value": line["value"],
+                     "unit": line["unit"], "ms_per_call": line["ms_per_step"], "steps": line["steps"],
+                     "roofline": {k: rf.get(k) for k in ("bound", "kernel", "achieved", "peak", "unit", "frac",
+                                                          "traffic")},
+                     "gpu_launches": line["gpu_launches"], "status": line["status"],
+                     "sm_mhz": (line.get("clocks") or {}).get("sm_mhz"),
+                     "reasons": (line.get("clocks") or {}).get("reasons")}
+    return out
+
+
 def run_ours(args, w):
     import torch
     import selective_state_space_07_gb300 as ssm
@@ -543,6 +586,7 @@ def run_ours(args, w):
                 ts.append(a_.elapsed_time(b_))
         ms_inf = max_over_ranks([sum(ts) / len(ts)], dist, dev)[0]
     decode = decode_throughput(ssm, dv, w, dev, stream) if not args.no_extras else None
+    others = other_ops(args, w) if not args.no_extras and world == 1 else None
 
     # ---- end to end through the public API with host buffers
     e2e = None
@@ -614,6 +658,7 @@ def run_ours(args, w):
             "ms": round(ms_inf, 5), "what": "ssm_scan_fwd with ckpt = NULL (y and h_last only)",
             "hbm_frac": round(algorithmic_bytes(w, "fwd") / (ms_inf * 1e-3) / 1e9 / peak, 4)},
         "decode": decode,
+        "other_ops": others,
         "sfu_roofline": sfu,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -809,10 +854,7 @@ def run_conv(args, w):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": with_cycles(clk, ms_f + ms_b),
         "status": status,
     }
-    print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
-    return 0
+    return emit(args, line, dist)
 
 
 def _dtproj_oracle_step(a, wt, bias, dd):
@@ -1001,10 +1043,7 @@ def run_dtproj(args, w):
         "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": with_cycles(clk, ms_f + ms_b),
         "status": status,
     }
-    print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
-    return 0
+    return emit(args, line, dist)
 
 
 # ------------------------------------------------------------------ gdn2, mlstm
@@ -1260,10 +1299,7 @@ def run_chunk(args, op):
         "roofline": rf, "tensor_roofline": tens, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": with_cycles(clk, ms), "status": status,
     }
-    print(json.dumps(line), flush=True)
-    if dist:
-        dist.destroy_process_group()
-    return 0
+    return emit(args, line, dist)
 
 
 def main():
@@ -1278,7 +1314,8 @@ def main():
     ap.add_argument("--groups", type=int, default=0, help="L-groups (0 = library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the inference-forward and decode timings")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the inference-forward, decode and other-op timings after the scan's")
     ap.add_argument("--op", choices=("scan", "conv1d", "dtproj", "gdn2", "mlstm"), default="scan",
                     help="scan: the S6 scan fwd+bwd (default); conv1d: the conv1d + SiLU in front of it; "
                          "dtproj: the dt projection with its softplus; gdn2: the Gated DeltaNet-2 chunkwise forward; "
