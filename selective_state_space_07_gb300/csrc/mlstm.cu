@@ -15,25 +15,31 @@
 // Per chunk, with F the chunk's inclusive cumulative log forget gates,
 // g_s = log i_s - F_s, mx_t = max(m_prev, max_{s<=t} g_s) and m_t = F_t +
 // mx_t (the recurrent stabilizer unrolled):
-//  0. gate pass (warp 0): F by a warp scan, the running maximum of g, and
+//  0. gate pass (one warp, for the next chunk, during this chunk's round 2;
+//     two table sets): F by a warp scan, the running maximum of g, and
 //     alpha_t = exp(m_prev - mx_t), gamma_s = exp(g_s - mx_last), the
-//     state's decay beta = alpha_last and m_new = m_last -- for the next
-//     chunk, while this chunk's first products run (two table sets);
-//  1. row pass: q' = alpha * scale * q and gamma * k (MN-major);
-//  2. MMA [S | q.n] = q [k; n_hi; n_lo]^T (n rides as two bf16 rows of the
-//     k operand, so q.n needs no reduction) and out^T = C^T q'^T (the
-//     state's share of the output);
+//     state's decay beta = alpha_last and m_new = m_last;
+//  1. as soon as q and k land, [S | q.n] = q [k; n_hi; n_lo]^T (n rides as
+//     two bf16 rows of the k operand, so q.n needs no reduction); under it
+//     the row pass: gamma * k (MN-major) and the per-warp partial sums of
+//     gamma * k (n's increment);
+//  2. C^T q^T (the state's share of the output, scaled by alpha_t * scale
+//     in step 5), issued by a thread of another warp (issuing blocks the
+//     issuing thread while the tensor pipe works); every other thread waits
+//     for S by itself;
 //  3. P = S * scale * exp(g_s - mx_t) on and below the diagonal, held as two
 //     bf16 parts P = P_hi + P_lo (the normaliser divides by a sum of signed
 //     terms that can nearly cancel, so P's one bf16 rounding would reach the
-//     output at up to 4e-2; the two parts carry 16 bits), with the row sums
-//     of P_hi + P_lo (TMEM lanes 0-63, four warps); n <- beta n + sum
-//     gamma_s k_s (the other four warps); C^T <- beta C^T in TMEM (all);
-//  4. MMA out^T += V^T P_hi^T + V^T P_lo^T and C^T += V^T (gamma k), while
-//     64 threads form 1 / max(|alpha_t q.n + rowsum_t|, exp(-m_t));
-//  5. h_t = out_t times that reciprocal, staged as rows and (with weights)
-//     normalised per token over V, eight tokens per warp at once; the bf16
-//     copy of C^T that the next chunk's product reads is refreshed from TMEM.
+//     output at up to 4e-2; the two parts carry 16 bits), and its row sums:
+//     every warp a quarter of the columns of 32 rows (S is in TMEM twice);
+//     C^T <- beta C^T in TMEM;
+//  4. MMA out^T = V^T P_hi^T + V^T P_lo^T and C^T += V^T (gamma k), while
+//     the gate pass runs, 64 threads form 1 / max(|alpha_t q.n + rowsum_t|,
+//     exp(-m_t)) and 128 threads n <- beta n + sum gamma_s k_s;
+//  5. h_t = (alpha_t scale (C^T q^T)_t + (P v)_t) times that reciprocal,
+//     staged as rows and (with weights) normalised per token over V, eight
+//     tokens per warp at once; the bf16 copy of C^T that the next chunk's
+//     product reads is refreshed from TMEM.
 // Every exponent is <= 0 (mx is a running maximum), so no gate overflows.
 //
 // Every wait (copies, tensor-core completions) is bounded (1 s); a wait that
@@ -57,7 +63,7 @@ constexpr int kMK = 128;   // key channels
 constexpr int kMV = 128;   // value channels
 constexpr int kMThreads = 256;
 constexpr int kGateWarp = 1;  // runs the gate passes (during round 2, where it has no other work)
-constexpr int kCqWarp = 7;    // a thread of it issues the state term C^T q'^T
+constexpr int kCqWarp = 7;    // a thread of it issues the state term C^T q^T
 
 // Shared-memory regions (bytes from a 1024-byte aligned base).
 constexpr int kKR = 80;                 // rows of the k operand: k (64), n_hi, n_lo, zeros (N = 80)
@@ -65,8 +71,7 @@ constexpr int kQ = 0;                   // [q; q]             128 rows x K=128 (
 constexpr int kKB = kQ + 32768;         // [k; n_hi; n_lo; 0]  80 rows x K=128 (k by TMA into rows 0-63)
 constexpr int kVB = kKB + 2 * kKR * 128;  // v                 MN-major [64 tokens][128] (TMA)
 constexpr int kCT = kVB + 16384;        // C^T (bf16)         128 rows x K=128
-constexpr int kQP = kCT + 32768;        // alpha*scale*q       64 rows x K=128
-constexpr int kKP = kQP + 16384;        // gamma*k             MN-major [64 tokens][128]
+constexpr int kKP = kCT + 32768;        // gamma*k             MN-major [64 tokens][128]
 constexpr int kP = kKP + 16384;         // P_hi                64 rows x K=64
 constexpr int kP2 = kP + 8192;          // P_lo = P - P_hi     64 rows x K=64
 constexpr int kOS = kP2 + 8192;         // output rows fp32 [64][kOSR]
@@ -81,13 +86,14 @@ constexpr int kBarOff = kMisc + kMiscFloats * 4;
 constexpr int kMSmem = kBarOff + 64 + 1024;  // + slack for the 1024-byte alignment
 static_assert(kMSmem <= 227 * 1024, "shared memory");
 static_assert(kBarOff % 8 == 0, "mbarriers 8-byte aligned");
-static_assert(kKB % 1024 == 0 && kVB % 1024 == 0 && kCT % 1024 == 0 && kQP % 1024 == 0 && kKP % 1024 == 0 &&
+static_assert(kKB % 1024 == 0 && kVB % 1024 == 0 && kCT % 1024 == 0 && kKP % 1024 == 0 &&
                   kP % 1024 == 0 && kP2 % 1024 == 0 && (kKR * 128) % 1024 == 0,
               "swizzled operands and copy destinations on 1024-byte boundaries");
 constexpr unsigned kQBytes = 4 * 64 * 64 * 2, kKBytes = 2 * 64 * 64 * 2, kVBytes = 2 * 64 * 64 * 2;
 
-// TMEM columns: C^T; per chunk S (twice: lanes 0-63 and 64-127) with q.n_hi, q.n_lo in columns 64, 65, and out^T.
-constexpr unsigned kTC = 0, kTS = 128, kTO = 256, kTCols = 512;
+// TMEM columns: C^T; per chunk S (twice: lanes 0-63 and 64-127) with q.n_hi, q.n_lo in columns 64, 65, the
+// chunk's own share of out^T (P v) and the state's share (C^T q^T, scaled per token in the epilogue).
+constexpr unsigned kTC = 0, kTS = 128, kTO = 256, kTQ = 320, kTCols = 512;
 
 struct MlstmParams {
     int64_t B, H, T;
@@ -369,9 +375,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
             commit(mbar_s);
         }
 
-        // ---- 1b. row pass (thread = token r, channels cc..cc+7): alpha*scale*q and gamma*k
-        // (MN-major), the per-warp partial sums of gamma*k over tokens (n's increment); v rows
-        // past the chunk's end zeroed
+        // ---- 1b. row pass (thread = token r, channels cc..cc+7): gamma*k (MN-major) and the per-warp
+        // partial sums of gamma*k over tokens (n's increment); v rows past the chunk's end zeroed
         {
             const int cc = (tid & 15) * 8;
             float np[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -379,17 +384,14 @@ __global__ void __launch_bounds__(kMThreads, 1)
             for (int it = 0; it < 4; ++it) {
                 const int r = (tid >> 4) + it * (kMThreads >> 4);
                 const bool live = r < c;
-                float qv[8], kv[8];
-                ld8(sm + kQ, r, cc, 128, qv);
+                float kv[8];
                 ld8(sm + kKB, r, cc, kKR, kv);
-                const float a = g_al[r] * p.scale, gm = g_gam[r];
+                const float gm = g_gam[r];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                    qv[i] *= a;
                     kv[i] = live ? kv[i] * gm : 0.f;
                     np[i] += kv[i];
                 }
-                st8(sm + kQP, r, cc, 64, qv);
                 st8(sm + kKP, r, cc, 64, kv);
                 if (!live) {
                     const float z[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -408,19 +410,19 @@ __global__ void __launch_bounds__(kMThreads, 1)
         tc_before();
         __syncthreads();
 
-        // ---- 2. out^T = C^T (alpha*scale*q)^T, the state's share of the output (issued by a thread of warp
-        // kCqWarp: issuing blocks the issuing thread while the tensor pipe works); every other thread waits
-        // for S by itself (no CTA barrier: the outcome is agreed at the end of phase 3) and goes on
+        // ---- 2. the state's share of the output, C^T q^T (the rows of q are its N operand; alpha_t * scale is
+        // applied per token in phase 5), issued by a thread of warp kCqWarp once S has had the tensor pipe to
+        // itself (issuing blocks the issuing thread while the pipe works); every other thread waits for S by
+        // itself (no CTA barrier: the outcome is agreed at the end of phase 3) and goes on
         if (tid == kCqWarp * 32) {
             tc_after();
-            mma_issue(tmem + kTO, sbase + kCT, sbase + kQP, 64, 64, kMK, false);
+            mma_issue(tmem + kTQ, sbase + kCT, sbase + kQ, 128, 64, kMK, false);
             commit(mbar_c);
         }
         const bool ok_s = mbar_wait_try(mbar_s, phase_s & 1u, p.wait_ns);
         phase_s++;
         if (!ok_s) fail();
         tc_after();
-        if (ok_s) refill(0, ci + 1);  // q has been read (the row pass before the barrier, S now)
 
         // ---- 3. P as two bf16 parts and its row sums, every warp a quarter of the columns of 32 rows
         // (rows 0-31 on lanes 0-31 and 64-95, rows 32-63 on lanes 32-63 and 96-127); q.n; then C^T *= beta
@@ -467,14 +469,15 @@ __global__ void __launch_bounds__(kMThreads, 1)
         asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
         fence_async_smem();
         tc_before();
-        // the state term must be complete before round 2 accumulates into out^T; one barrier agrees on
-        // both waits
+        // one barrier agrees on the waits for S and for the state's share (which must have read q and the
+        // bf16 copy of C^T before q's buffer is refilled and phase 5 rewrites the copy)
         {
             const bool ok_c = mbar_wait_try(mbar_c, phase_c & 1u, p.wait_ns);
             phase_c++;
             if (!ok_c) fail();
             if (!(ok = __syncthreads_and(ok_s && ok_c) != 0)) break;
         }
+        refill(0, ci + 1);  // q has been read (by the two products only)
         refill(1, ci + 1);  // k has been read
 
         // ---- 4. out^T += V^T P_hi^T + V^T P_lo^T;  C^T += V^T (gamma*k); meanwhile the next chunk's
@@ -482,7 +485,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
         // which read n's rows of the k operand, is complete)
         if (tid == 0) {
             tc_after();
-            mma_issue(tmem + kTO, sbase + kVB, sbase + kP, 64, 64, kMC, true, true, false);
+            mma_issue(tmem + kTO, sbase + kVB, sbase + kP, 64, 64, kMC, false, true, false);
             mma_issue(tmem + kTO, sbase + kVB, sbase + kP2, 64, 64, kMC, true, true, false);
             mma_issue(tmem + kTC, sbase + kVB, sbase + kKP, 0, kMK, kMC, true, true, true);
             commit(mbar);
@@ -508,18 +511,25 @@ __global__ void __launch_bounds__(kMThreads, 1)
         tc_after();
         refill(2, ci + 1);  // v has been read
 
-        // ---- 5. h = out / max(|den|, exp(-m)) into the staging rows; the bf16 copy of C^T
+        // ---- 5. h = (alpha * scale * C^T q^T + P v) / max(|den|, exp(-m)) into the staging rows; the bf16
+        // copy of C^T
         {
             const int tb = whalf * 32, k0 = whalf * 64;
-            unsigned orr[32], cr[64];
+            unsigned orr[32], oqr[32], cr[64];
             tmem_ld32_nw(tmem + tlane + kTO + (unsigned)tb, orr);
+            tmem_ld32_nw(tmem + tlane + kTQ + (unsigned)tb, oqr);
             tmem_ld32_nw(tmem + tlane + kTC + (unsigned)k0, cr);
             tmem_ld32_nw(tmem + tlane + kTC + (unsigned)(k0 + 32), cr + 32);
             tmem_wait_ld();
             tmem_regs_ready<32>(orr);
+            tmem_regs_ready<32>(oqr);
             tmem_regs_ready<64>(cr);
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) s_os[(tb + jj) * kOSR + vrow] = __uint_as_float(orr[jj]) * s_rd[tb + jj];
+            for (int jj = 0; jj < 32; ++jj) {
+                const int t = tb + jj;
+                const float o = __fmaf_rn(g_al[t] * p.scale, __uint_as_float(oqr[jj]), __uint_as_float(orr[jj]));
+                s_os[t * kOSR + vrow] = o * s_rd[t];
+            }
             float cv[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) cv[i] = __uint_as_float(cr[i]);
