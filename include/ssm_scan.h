@@ -197,6 +197,13 @@ int ssm_scan_fwd_noalloc(const ssm_fwd_args* args, void* stream);
  * i < n, fp32 device arrays; dA_log may alias dA. Asynchronous on stream. */
 int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, void* stream);
 
+/* The library's FMA-pipe 2^x (the Cody-Waite split and degree-6 polynomial
+ * that a kernel can use instead of the MUFU ex2 where the XU pipe binds):
+ * y[i] = 2^x[i] for i < n, fp32 device arrays, relative error below 2^-23
+ * for -125.5 <= x <= 127 and 0 below -125.5. For tests and error-bound
+ * checks; asynchronous on stream. */
+int ssm_exp2_fma(const float* x, float* y, int64_t n, void* stream);
+
 /* Causal depthwise conv1d + SiLU, the step in front of the scan
  * (rustytorch commit log, "MambaBlock" S6 forward commit: "in_proj -> causal
  * depthwise conv1d -> SiLU -> x_proj -> ..."; the MambaRecurrence commit

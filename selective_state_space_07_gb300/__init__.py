@@ -40,7 +40,7 @@ __all__ = [
     "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
     "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
-    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault",
+    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault", "exp2_fma",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -141,6 +141,7 @@ EXPORTS = {
     "ssm_dA_log_grad": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p],
                         ctypes.c_int),
     "ssm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
+    "ssm_exp2_fma": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p], ctypes.c_int),
     "gdn2_chunk_fwd": ([ctypes.POINTER(Gdn2Args), ctypes.c_void_p], ctypes.c_int),
     "gdn2_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
     "mlstm_chunk_fwd": ([ctypes.POINTER(MlstmArgs), ctypes.c_void_p], ctypes.c_int),
@@ -646,6 +647,17 @@ def mlstm_arm_wait_fault(chunk: int, wait_ns: int) -> None:
     """Test hook: the next mlstm_fwd of this thread does not issue chunk `chunk`'s q copy and bounds every
     wait by wait_ns, so the call ends with SSM_ERR_TIMEOUT in the status word. chunk < 0 disarms."""
     _check(lib().mlstm_debug_arm_wait_fault(int(chunk), int(wait_ns)), "mlstm_debug_arm_wait_fault")
+
+
+def exp2_fma(x, *, out=None, stream=None):
+    """The library's FMA-pipe 2^x (Cody-Waite split + degree-6 polynomial; C ABI ssm_exp2_fma) on an fp32
+    device tensor: for tests and error-bound checks of the exponential a kernel can use instead of the MUFU."""
+    if not isinstance(x, torch.Tensor) or x.dtype != torch.float32 or x.device.type != "cuda" or not x.is_contiguous():
+        raise TypeError("x must be a contiguous fp32 CUDA tensor")
+    out = torch.empty_like(x) if out is None else out
+    _need(out, "out", tuple(x.shape), torch.float32, x.device)
+    _check(lib().ssm_exp2_fma(_p(x), _p(out), x.numel(), _stream(x.device, stream)), "ssm_exp2_fma")
+    return out
 
 
 def poll_status(workspace, stream=None) -> int:

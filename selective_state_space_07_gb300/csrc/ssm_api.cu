@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include "../../include/ssm_scan.h"
+#include "ssm_common.cuh"
 #include "ssm_internal.h"
 
 namespace ssm {
@@ -126,6 +127,12 @@ int check_fwd(const ssm_fwd_args* a, bool need_y) {
 __global__ void dA_log_kernel(const float* dA, const float* __restrict__ A, float* dA_log, int64_t n) {
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
         dA_log[i] = dA[i] * A[i];
+}
+
+// The FMA-pipe 2^x applied to n values (tests and error-bound checks).
+__global__ void exp2_fma_kernel(const float* __restrict__ x, float* __restrict__ y, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+        y[i] = ssm::ex2_fma(x[i]);
 }
 
 int tally(int r) {
@@ -319,6 +326,16 @@ int ssm_dA_log_grad(const float* dA, const float* A, float* dA_log, int64_t n, v
     if (!dA || !A || !dA_log) return SSM_ERR_INVALID_ARG;
     const int64_t blocks = std::min<int64_t>(ceil_div(n, 256), 4096);
     dA_log_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(dA, A, dA_log, n);
+    return tally(cudaGetLastError() == cudaSuccess ? 1 : -1);
+}
+
+int ssm_exp2_fma(const float* x, float* y, int64_t n, void* stream) {
+    g_launches = 0;
+    if (n < 0) return SSM_ERR_INVALID_ARG;
+    if (n == 0) return SSM_OK;
+    if (!x || !y) return SSM_ERR_INVALID_ARG;
+    const int64_t blocks = std::min<int64_t>(ceil_div(n, 256), 4096);
+    exp2_fma_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(x, y, n);
     return tally(cudaGetLastError() == cudaSuccess ? 1 : -1);
 }
 

@@ -599,6 +599,12 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
 #define SSM_AGG_SA 4
 #endif
         constexpr int SA = SSM_AGG_SA;
+        // the first SSM_AGG_FMA_STATES of a lane's states take the FMA-pipe 2^x instead of the MUFU
+        // (0 = none: the XU pipe does not bind here; measured with 1 and 2, kept for such measurements)
+#ifndef SSM_AGG_FMA_STATES
+#define SSM_AGG_FMA_STATES 0
+#endif
+        constexpr int kAggFma = SSM_AGG_FMA_STATES;
 #pragma unroll
         for (int s = 0; s < NS; s += SA) {
             const int n = NS * hk + s;
@@ -623,7 +629,9 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
                         const float2 cc = h2 ? make_float2(c4[i].z, c4[i].w) : make_float2(c4[i].x, c4[i].y);
                         const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
                         const float2 r = __fmul2_rn(Pl[m], cc);
-                        const float a1 = ex2(arg.y), a0 = ex2(arg.x);
+                        const bool on_fma = s + i < kAggFma;
+                        const float a1 = on_fma ? ex2_fma(arg.y) : ex2(arg.y);
+                        const float a0 = on_fma ? ex2_fma(arg.x) : ex2(arg.x);
                         Ev[i] = __fmaf_rn(nx[i], Ev[i], r.y);
                         Ev[i] = __fmaf_rn(a1, Ev[i], r.x);
                         nx[i] = a0;

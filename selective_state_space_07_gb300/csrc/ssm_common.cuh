@@ -27,6 +27,30 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// 2^x without the MUFU (XU) pipe, for a kernel whose XU pipe binds: a
+// Cody-Waite split x = n + f, n = x rounded to the nearest integer by adding
+// and subtracting 1.5 * 2^23 (exact for |x| < 2^22; f = x - n in [-0.5, 0.5]
+// is exact too), 2^f by the degree-6 polynomial that interpolates it at the
+// Chebyshev nodes of [-0.5, 0.5] (coefficients from csrc/exp2_poly.py;
+// largest relative error 1.1e-7 in float32), and n added to the exponent
+// field: the shifted sum's bits hold 0x4B400000 + n, whose low nine bits
+// shifted up by 23 are n << 23 (mod 2^32). 13 instructions on the FMA and ALU
+// pipes. Arguments below -125.5 give 0 (the result would not be a normal
+// number: flushed as ex2.approx.ftz flushes); arguments must be <= 127.
+__device__ __forceinline__ float ex2_fma(float x) {
+    const float xc = fmaxf(x, -127.f);
+    const float sh = __fadd_rn(xc, 12582912.f);
+    const float f = __fsub_rn(xc, __fsub_rn(sh, 12582912.f));
+    float p = 1.5461444854736328e-4f;
+    p = __fmaf_rn(p, f, 1.3400427997112274e-3f);
+    p = __fmaf_rn(p, f, 9.618056938052177e-3f);
+    p = __fmaf_rn(p, f, 5.550327152013779e-2f);
+    p = __fmaf_rn(p, f, 2.4022650718688965e-1f);
+    p = __fmaf_rn(p, f, 6.931471824645996e-1f);
+    p = __fmaf_rn(p, f, 1.0f);
+    const float r = __int_as_float((int)((unsigned)__float_as_int(sh) * (1u << 23) + (unsigned)__float_as_int(p)));
+    return xc < -125.5f ? 0.f : r;
+}
 __device__ __forceinline__ float lg2(float x) {
     float y;
     asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
