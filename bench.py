@@ -446,6 +446,58 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ ours
+def mlstm_decode_throughput(ssm, t, dev, n_tok=64):
+    """mlstm_step at the workload's B and H (one token of every head per call) over the first n_tok tokens
+    of the resident inputs, from the workload's initial state: eager, and replayed from one CUDA graph that
+    holds the same n_tok calls."""
+    import torch
+    B, H, T, K = t["q"].shape
+    V = t["v"].shape[-1]
+    st = (t["C0"].clone(), t["n0"].clone(), t["m0"].clone())
+    cols = [{n: t[n][:, :, i].contiguous() for n in ("q", "k", "v", "igate", "fgate")} for i in range(n_tok)]
+    hs = [torch.empty(B, H, V, dtype=torch.bfloat16, device=dev) for _ in range(n_tok)]
+
+    def run():
+        for i in range(n_tok):
+            c = cols[i]
+            ssm.mlstm_step(c["q"], c["k"], c["v"], c["igate"], c["fgate"], st, K ** -0.5, h=hs[i])
+
+    def timed(fn, reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        cur = torch.cuda.current_stream(dev)
+        a.record(cur)
+        for _ in range(reps):
+            fn()
+        b.record(cur)
+        b.synchronize()
+        return a.elapsed_time(b) / reps / n_tok
+
+    run()
+    eager_ms = timed(run, 5)
+    graph_ms = None
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            run()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        g.replay()
+        graph_ms = timed(g.replay, 20)
+    except Exception as ex:  # a torch without graph capture: report the eager number only
+        log("mlstm decode graph capture failed:", ex)
+    per_call = B * H * (K * 2 * 2 + V * 2 * 2 + 2 * 4 + 2 * (K * V + K + 1) * 4)
+    best = graph_ms if graph_ms is not None else eager_ms
+    return {"what": f"mlstm_step, one token for all {B}x{H} heads per call (state read and written in place)",
+            "us_per_call_eager": round(eager_ms * 1e3, 3),
+            "us_per_call_graph": None if graph_ms is None else round(graph_ms * 1e3, 3),
+            "tokens_per_s": round(B / (best * 1e-3), 1),
+            "algorithmic_bytes_per_call": per_call,
+            "hbm_frac": round(per_call / (best * 1e-3) / 1e9 / measured_peaks()[0], 4)}
+
+
 def emit(args, line, dist):
     """End a run: print its JSON line (the command-line path), or hand the
     line back when bench.py collects it as an extra of the scan's run."""
@@ -1237,6 +1289,7 @@ def run_chunk(args, op):
     status = ssm.poll_status(ws)
     units = B * H * T
     value = world * units / (ms * 1e-3) / 1e6
+    decode = mlstm_decode_throughput(ssm, t, dev) if op.op == "mlstm" and not getattr(args, "no_extras", False) else None
 
     e2e = None
     if not args.no_e2e:  # inputs in from pinned host memory, the output and the final state back
@@ -1299,6 +1352,8 @@ def run_chunk(args, op):
         "roofline": rf, "tensor_roofline": tens, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
         "clocks": with_cycles(clk, ms), "status": status,
     }
+    if decode is not None:
+        line["decode"] = decode
     return emit(args, line, dist)
 
 

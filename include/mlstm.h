@@ -88,6 +88,41 @@ typedef struct {
 
 int mlstm_chunk_fwd(const mlstm_fwd_args* args, void* stream);
 
+/* One token of the cell (the recurrent step; decoding): with the state (C, n,
+ * m) read and updated in place,
+ *   m' = max(log sigmoid(fgate) + m, igate)
+ *   C' = exp(log sigmoid(fgate) + m - m') C + exp(igate - m') k v^T,  n' likewise
+ *   h  = (q^T C') / max(|q . n'|, exp(-m'))  (q scaled by `scale`), then the
+ *        head-wise norm when norm_weight is non-null.
+ * Layout: q, k [B, H, K] bf16; v [B, H, V] bf16; igate, fgate [B, H] fp32;
+ * C [B, H, K, V], n [B, H, K], m [B, H] fp32 (stabilized, in place);
+ * norm_weight [H, V] fp32 or NULL; h [B, H, V] bf16. Everything in fp32
+ * (no tensor cores: one token is a matrix-vector step). K = V = 128 (else
+ * SSM_ERR_UNSUPPORTED); q, k, v, C, norm_weight and h 16-byte aligned, the
+ * gates, n and m 4-byte aligned (else SSM_ERR_ALIGNMENT); q, k, v, the
+ * gates, C, n, m and h non-null when B*H > 0, B*H below 2^31, scale finite,
+ * norm_eps finite and non-negative (else SSM_ERR_INVALID_ARG). A zero state
+ * is C = n = 0 and m = 0. Asynchronous on `stream`; workspace (nullable)
+ * receives the status word (non-finite outputs). */
+typedef struct {
+    int64_t B, H, K, V;
+    float scale;
+    float norm_eps;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* igate;
+    const float* fgate;
+    float* C;
+    float* n;
+    float* m;
+    const float* norm_weight;
+    void* h;
+    void* workspace;
+} mlstm_step_args;
+
+int mlstm_step(const mlstm_step_args* args, void* stream);
+
 /* Test hook: arms a one-shot fault for this thread's next mlstm_chunk_fwd.
  * The copy of q for chunk `chunk` (0-based, in every CTA) is not issued
  * while the chunk's other copies are, and every bounded wait of that call

@@ -40,7 +40,7 @@ __all__ = [
     "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
     "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
-    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault", "exp2_fma",
+    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault", "mlstm_step", "exp2_fma",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -122,6 +122,12 @@ class MlstmArgs(ctypes.Structure):
 
 MLSTM_CHUNK = 64
 
+
+class MlstmStepArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("scale", ctypes.c_float), ("norm_eps", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("q", "k", "v", "igate", "fgate", "C", "n", "m", "norm_weight", "h", "workspace")]
+
 EXPORTS = {
     "ssm_scan_fwd": ([ctypes.POINTER(FwdArgs), ctypes.c_void_p], ctypes.c_int),
     "ssm_scan_bwd": ([ctypes.POINTER(BwdArgs), ctypes.c_void_p], ctypes.c_int),
@@ -146,6 +152,7 @@ EXPORTS = {
     "gdn2_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
     "mlstm_chunk_fwd": ([ctypes.POINTER(MlstmArgs), ctypes.c_void_p], ctypes.c_int),
     "mlstm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
+    "mlstm_step": ([ctypes.POINTER(MlstmStepArgs), ctypes.c_void_p], ctypes.c_int),
 }
 
 
@@ -641,6 +648,41 @@ def mlstm_fwd(q, k, v, igate, fgate, state=None, scale=None, *, norm_weight=None
                      workspace=None if workspace is None else workspace.buf.data_ptr())
     _check(lib().mlstm_chunk_fwd(ctypes.byref(args), _stream(dev, stream)), "mlstm_chunk_fwd")
     return h, state_out
+
+
+def mlstm_step(q, k, v, igate, fgate, state, scale=None, *, norm_weight=None, norm_eps=1e-5, h=None, workspace=None,
+               stream=None):
+    """One token of the mLSTM cell, the recurrent step (C ABI in ``include/mlstm.h``): q, k [B, H, 128] and v
+    [B, H, 128] bf16; igate, fgate [B, H] fp32 gate pre-activations; state = (C [B, H, 128, 128], n [B, H, 128],
+    m [B, H]) fp32 stabilized, updated in place (zeros and m = 0 for a fresh sequence); norm_weight [H, 128] fp32
+    applies the head-wise norm; scale defaults to 1/sqrt(K). Returns h [B, H, V] bf16."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, K]")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("the mLSTM step runs on a CUDA device; q is on " + str(dev))
+    Bn, H, K = q.shape
+    V = v.shape[-1] if v.dim() == 3 else -1
+    bf, f32 = torch.bfloat16, torch.float32
+    _need(q, "q", (Bn, H, K), bf, dev)
+    _need(k, "k", (Bn, H, K), bf, dev)
+    _need(v, "v", (Bn, H, V), bf, dev)
+    _need(igate, "igate", (Bn, H), f32, dev)
+    _need(fgate, "fgate", (Bn, H), f32, dev)
+    if state is None or len(state) != 3:
+        raise ValueError("state must be (C, n, m)")
+    for t, n, shp in zip(state, ("C", "n", "m"), ((Bn, H, K, V), (Bn, H, K), (Bn, H))):
+        _need(t, n, shp, f32, dev)
+    if norm_weight is not None:
+        _need(norm_weight, "norm_weight", (H, V), f32, dev)
+    h = torch.empty((Bn, H, V), dtype=bf, device=dev) if h is None else h
+    _need(h, "h", (Bn, H, V), bf, dev)
+    args = MlstmStepArgs(B=Bn, H=H, K=K, V=V, scale=float(K ** -0.5 if scale is None else scale),
+                         norm_eps=float(norm_eps), q=_p(q), k=_p(k), v=_p(v), igate=_p(igate), fgate=_p(fgate),
+                         C=_p(state[0]), n=_p(state[1]), m=_p(state[2]), norm_weight=_p(norm_weight), h=_p(h),
+                         workspace=None if workspace is None else workspace.buf.data_ptr())
+    _check(lib().mlstm_step(ctypes.byref(args), _stream(dev, stream)), "mlstm_step")
+    return h
 
 
 def mlstm_arm_wait_fault(chunk: int, wait_ns: int) -> None:

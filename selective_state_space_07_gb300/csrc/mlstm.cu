@@ -610,6 +610,93 @@ __global__ void __launch_bounds__(kMThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- one token: the recurrent step
+struct MlstmStepParams {
+    int64_t H;
+    float scale, norm_eps;
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* igate;
+    const float* fgate;
+    float* C;
+    float* n;
+    float* m;
+    const float* norm_weight;
+    __nv_bfloat16* h;
+    unsigned* status;
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+    return x;
+}
+
+// One CTA of 256 threads per (batch, head); everything in fp32. Thread (v = tid % 128, kh = tid / 128)
+// updates C[k][v] for the 64 key channels kh*64.. (rows of C are read and written coalesced) and keeps its
+// share of q . C'[:, v]; the two shares, q . n' and the norm's mean and variance meet in shared memory.
+__global__ void __launch_bounds__(kMThreads) mlstm_step_kernel(const MlstmStepParams p) {
+    __shared__ float s_q[kMK], s_k[kMK];
+    __shared__ float s_part[2][kMV];
+    __shared__ float s_red[8];
+    __shared__ float s_rd;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t bh = blockIdx.x;
+    if (tid < kMK) {
+        s_q[tid] = __bfloat162float(p.q[bh * kMK + tid]) * p.scale;
+        s_k[tid] = __bfloat162float(p.k[bh * kMK + tid]);
+    }
+    // the stabilizer and the two decays (the same scalars in every thread)
+    const float lf = log_sigmoid(p.fgate[bh]), li = p.igate[bh], m0 = p.m[bh];
+    const float m1 = fmaxf(lf + m0, li);
+    const float fs = expf(lf + m0 - m1), is = expf(li - m1);
+    __syncthreads();
+    // n' = f' n + i' k and the partial sums of q . n'
+    float qn = 0.f, nv = 0.f;
+    if (tid < kMK) {
+        nv = __fmaf_rn(fs, p.n[bh * kMK + tid], is * s_k[tid]);
+        qn = s_q[tid] * nv;
+    }
+    // C' = f' C + i' k v^T and this thread's share of q . C'[:, v]
+    const int v = tid & (kMV - 1), kh = tid >> 7;
+    const float iv = is * __bfloat162float(p.v[bh * kMV + v]);
+    float* Cb = p.C + bh * kMK * kMV;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int kk = 0; kk < kMK / 2; ++kk) {
+        const int k = kh * (kMK / 2) + kk;
+        const float c = __fmaf_rn(fs, Cb[(int64_t)k * kMV + v], iv * s_k[k]);
+        Cb[(int64_t)k * kMV + v] = c;
+        acc = __fmaf_rn(s_q[k], c, acc);
+    }
+    s_part[kh][v] = acc;
+    qn = warp_sum(qn);
+    if (lane == 0 && warp < 4) s_red[warp] = qn;
+    __syncthreads();
+    if (tid == 0) {
+        s_rd = 1.f / fmaxf(fabsf((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])), expf(-m1));
+        p.m[bh] = m1;
+    }
+    if (tid < kMK) p.n[bh * kMK + tid] = nv;
+    __syncthreads();
+    float hv = tid < kMV ? (s_part[0][tid] + s_part[1][tid]) * s_rd : 0.f;
+    if (p.norm_weight) {  // the head-wise norm over the V values held by threads 0-127
+        const float sum = warp_sum(hv);
+        if (lane == 0 && warp < 4) s_red[4 + warp] = sum;
+        __syncthreads();
+        const float mean = ((s_red[4] + s_red[5]) + (s_red[6] + s_red[7])) * (1.f / kMV);
+        const float d = tid < kMV ? hv - mean : 0.f;
+        const float sq = warp_sum(d * d);
+        if (lane == 0 && warp < 4) s_red[warp] = sq;
+        __syncthreads();
+        const float var = ((s_red[0] + s_red[1]) + (s_red[2] + s_red[3])) * (1.f / kMV);
+        hv = tid < kMV ? d * rsqrtf(var + p.norm_eps) * p.norm_weight[(bh % p.H) * kMV + tid] : 0.f;
+    }
+    if (tid < kMV) p.h[bh * kMV + tid] = __float2bfloat16_rn(hv);
+    flag_nonfinite(p.status, __fmaf_rn(hv, 0.f, 0.f));
+}
+
 bool misaligned(const void* q, uintptr_t a) { return q && (reinterpret_cast<uintptr_t>(q) & (a - 1)) != 0; }
 
 }  // namespace
@@ -696,5 +783,31 @@ extern "C" int mlstm_chunk_fwd(const mlstm_fwd_args* a, void* stream) {
         ssm::encode_2d(&mp.v, bf, a->v, ssm::kMV, rows, ssm::kMV * 2, 64, ssm::kMC, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!enc) return SSM_ERR_CUDA;
     ssm::mlstm_chunk_fwd_kernel<<<(unsigned)BH, ssm::kMThreads, ssm::kMSmem, s>>>(p, mp);
+    return ssm::count_launches(cudaGetLastError() == cudaSuccess ? 1 : -1);
+}
+
+extern "C" int mlstm_step(const mlstm_step_args* a, void* stream) {
+    ssm::reset_launches();
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->B < 0 || a->H < 0) return SSM_ERR_INVALID_ARG;
+    if (a->K != ssm::kMK || a->V != ssm::kMV) return SSM_ERR_UNSUPPORTED;
+    if (!(fabsf(a->scale) <= 3.0e38f)) return SSM_ERR_INVALID_ARG;
+    if (!(a->norm_eps >= 0.f && a->norm_eps <= 3.0e38f)) return SSM_ERR_INVALID_ARG;
+    if (a->B * a->H > 0x7fffffff) return SSM_ERR_INVALID_ARG;
+    const int64_t BH = a->B * a->H;
+    if (BH == 0) return SSM_OK;
+    if (!a->q || !a->k || !a->v || !a->igate || !a->fgate || !a->C || !a->n || !a->m || !a->h) return SSM_ERR_INVALID_ARG;
+    const void* p16[] = {a->q, a->k, a->v, a->C, a->norm_weight, a->h, a->workspace};
+    for (const void* q : p16)
+        if (ssm::misaligned(q, 16)) return SSM_ERR_ALIGNMENT;
+    const void* p4[] = {a->igate, a->fgate, a->n, a->m};
+    for (const void* q : p4)
+        if (ssm::misaligned(q, 4)) return SSM_ERR_ALIGNMENT;
+    ssm::MlstmStepParams p{};
+    p.H = a->H; p.scale = a->scale; p.norm_eps = a->norm_eps;
+    p.q = (const __nv_bfloat16*)a->q; p.k = (const __nv_bfloat16*)a->k; p.v = (const __nv_bfloat16*)a->v;
+    p.igate = a->igate; p.fgate = a->fgate; p.C = a->C; p.n = a->n; p.m = a->m;
+    p.norm_weight = a->norm_weight; p.h = (__nv_bfloat16*)a->h; p.status = (unsigned*)a->workspace;
+    ssm::mlstm_step_kernel<<<(unsigned)BH, ssm::kMThreads, 0, (cudaStream_t)stream>>>(p);
     return ssm::count_launches(cudaGetLastError() == cudaSuccess ? 1 : -1);
 }

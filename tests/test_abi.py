@@ -241,6 +241,25 @@ def test_mlstm_rejects_bad_arguments(ssm, over, code):
     assert ssm.lib().mlstm_chunk_fwd(ctypes.byref(args), None) == code
 
 
+def mlstm_step_args(ssm, **over):
+    a = dict(B=2, H=3, K=128, V=128, scale=0.088, norm_eps=1e-5, q=FAKE, k=FAKE + 4096, v=FAKE + 8192,
+             igate=FAKE + 12288, fgate=FAKE + 12292, C=FAKE + 16384, n=FAKE + 20480, m=FAKE + 20484,
+             norm_weight=None, h=FAKE + 24576, workspace=None)
+    a.update(over)
+    return ssm.MlstmStepArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), UNSUPPORTED), (dict(V=256), UNSUPPORTED), (dict(B=-1), INVALID), (dict(q=None), INVALID),
+    (dict(C=None), INVALID), (dict(m=None), INVALID), (dict(h=None), INVALID), (dict(C=FAKE + 8), ALIGNMENT),
+    (dict(norm_weight=FAKE + 4), ALIGNMENT), (dict(n=FAKE + 2), ALIGNMENT), (dict(scale=float("nan")), INVALID),
+    (dict(norm_eps=-1.0), INVALID), (dict(B=0), OK), (dict(B=0, q=None, C=None), OK),
+])
+def test_mlstm_step_rejects_bad_arguments(ssm, over, code):
+    args = mlstm_step_args(ssm, **over)
+    assert ssm.lib().mlstm_step(ctypes.byref(args), None) == code
+
+
 def test_mlstm_fault_hook_arguments(ssm):
     assert ssm.lib().mlstm_debug_arm_wait_fault(0, 20_000_000_000) == INVALID
     assert ssm.lib().mlstm_debug_arm_wait_fault(-1, 0) == OK  # disarmed
@@ -248,6 +267,7 @@ def test_mlstm_fault_hook_arguments(ssm):
 
 def test_null_args_struct(ssm):
     assert ssm.lib().mlstm_chunk_fwd(None, None) == INVALID
+    assert ssm.lib().mlstm_step(None, None) == INVALID
     assert ssm.lib().gdn2_chunk_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_bwd(None, None) == INVALID

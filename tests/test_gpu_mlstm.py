@@ -228,3 +228,67 @@ def test_binding_rejects_bad_tensors(ssm):
     small = [a[..., :64].contiguous() for a in (q, k, v)]
     with pytest.raises(ssm.SsmError):
         ssm.mlstm_fwd(*small, ig, fg)                               # K = V = 64: unsupported by the kernel
+
+
+# ---------------------------------------------------------------- the recurrent step (one token)
+# fp32 throughout (no bf16 operands): h carries only its own bf16 rounding, so 1e-2; the state 1e-4.
+TOL_STEP_H, TOL_STEP_S = 1e-2, 1e-4
+
+
+def step_run(ssm, x, norm=False):
+    """Steps through x's tokens one at a time from x's initial state; returns h [B,H,T,V] and the state."""
+    bf = torch.bfloat16
+    st = (dev(x.C0), dev(x.n0), dev(x.m0))
+    q, k, v, ig, fg = dev(x.q, bf), dev(x.k, bf), dev(x.v, bf), dev(x.igate), dev(x.fgate)
+    w = dev(x.norm_weight) if norm else None
+    hs = [ssm.mlstm_step(q[:, :, t].contiguous(), k[:, :, t].contiguous(), v[:, :, t].contiguous(),
+                         ig[:, :, t].contiguous(), fg[:, :, t].contiguous(), st, x.scale, norm_weight=w)
+          for t in range(x.T)]
+    torch.cuda.synchronize()
+    return torch.stack(hs, dim=2).float().cpu().numpy(), tuple(t.cpu().numpy() for t in st)
+
+
+@pytest.mark.parametrize("norm,igate_mean", [(False, 0.0), (True, 0.0), (False, 60.0)])
+def test_step_matches_the_recurrent_oracle(ssm, norm, igate_mean):
+    x = gen.make_mlstm_inputs(2, 3, 20, 128, 128, seed=51, igate_mean=igate_mean)
+    h, (C, n, m) = step_run(ssm, x, norm)
+    rh, rC, rn, rm = M.recurrent(x.q, x.k, x.v, x.igate, x.fgate, x.C0, x.n0, x.m0, scale=x.scale)
+    if norm:
+        rh = M.head_layer_norm(rh, x.norm_weight, 1e-5)
+    eh, eC, en = rel_err(h, rh), rel_err(C, rC), rel_err(n, rn)
+    print(f"mlstm step norm={norm} igate~N({igate_mean},1): h {eh:.2e} C {eC:.2e} n {en:.2e}")
+    assert eh < TOL_STEP_H and eC < TOL_STEP_S and en < TOL_STEP_S
+    assert float(np.max(np.abs(m - rm))) < TOL_STEP_S
+
+
+def test_step_continues_the_chunkwise_forward(ssm):
+    # decoding after a prompt: the chunkwise kernel's final state, then one step, equals the oracle over T + 1
+    x = gen.make_mlstm_inputs(2, 2, 131, 128, 128, seed=53)
+    bf = torch.bfloat16
+    T = 130
+    q, k, v, ig, fg = dev(x.q, bf), dev(x.k, bf), dev(x.v, bf), dev(x.igate), dev(x.fgate)
+    _, st = ssm.mlstm_fwd(q[:, :, :T].contiguous(), k[:, :, :T].contiguous(), v[:, :, :T].contiguous(),
+                          ig[:, :, :T].contiguous(), fg[:, :, :T].contiguous(), (dev(x.C0), dev(x.n0), dev(x.m0)),
+                          x.scale)
+    h = ssm.mlstm_step(q[:, :, T].contiguous(), k[:, :, T].contiguous(), v[:, :, T].contiguous(),
+                       ig[:, :, T].contiguous(), fg[:, :, T].contiguous(), st, x.scale)
+    torch.cuda.synchronize()
+    rh, rC, rn, rm = M.recurrent(x.q, x.k, x.v, x.igate, x.fgate, x.C0, x.n0, x.m0, scale=x.scale)
+    assert rel_err(h.float().cpu().numpy(), rh[:, :, T]) < TOL
+    assert rel_err(st[0].cpu().numpy(), rC) < TOL and rel_err(st[1].cpu().numpy(), rn) < TOL_N
+    assert float(np.max(np.abs(st[2].cpu().numpy() - rm))) < TOL_M
+
+
+def test_step_from_a_zero_state_and_non_finite_gates(ssm):
+    x = gen.make_mlstm_inputs(1, 2, 3, 128, 128, seed=55, with_state=False)
+    h, (C, n, m) = step_run(ssm, x)
+    rh, rC, _, _ = M.recurrent(x.q, x.k, x.v, x.igate, x.fgate, scale=x.scale)
+    assert rel_err(h, rh) < TOL_STEP_H and rel_err(C, rC) < TOL_STEP_S
+    bf = torch.bfloat16
+    ws = ssm.Workspace(1, 1, 8, "cuda")
+    st = (dev(x.C0), dev(x.n0), dev(x.m0))
+    ig = dev(x.igate[:, :, 0]).contiguous()
+    ig[0, 1] = float("nan")
+    ssm.mlstm_step(dev(x.q[:, :, 0], bf), dev(x.k[:, :, 0], bf), dev(x.v[:, :, 0], bf), ig,
+                   dev(x.fgate[:, :, 0]).contiguous(), st, x.scale, workspace=ws)
+    assert ssm.poll_status(ws) == -7
