@@ -446,21 +446,33 @@ def run_reference(args, w):
 
 
 # ------------------------------------------------------------------ ours
-def mlstm_decode_throughput(ssm, t, dev, n_tok=64):
-    """mlstm_step at the workload's B and H (one token of every head per call) over the first n_tok tokens
-    of the resident inputs, from the workload's initial state: eager, and replayed from one CUDA graph that
-    holds the same n_tok calls."""
+def chunk_decode_throughput(op, ssm, t, dev, n_tok=64):
+    """The op's one-token step (mlstm_step or gdn2_step) at the workload's B and H, one token of every head
+    per call, over the first n_tok tokens of the resident inputs from the workload's initial state: eager,
+    and replayed from one CUDA graph that holds the same n_tok calls."""
     import torch
     B, H, T, K = t["q"].shape
     V = t["v"].shape[-1]
-    st = (t["C0"].clone(), t["n0"].clone(), t["m0"].clone())
-    cols = [{n: t[n][:, :, i].contiguous() for n in ("q", "k", "v", "igate", "fgate")} for i in range(n_tok)]
+    if op == "mlstm":
+        names = ("q", "k", "v", "igate", "fgate")
+        st = (t["C0"].clone(), t["n0"].clone(), t["m0"].clone())
+        per_call = B * H * (K * 2 * 2 + V * 2 * 2 + 2 * 4 + 2 * (K * V + K + 1) * 4)
+
+        def call(c, h):
+            ssm.mlstm_step(c["q"], c["k"], c["v"], c["igate"], c["fgate"], st, K ** -0.5, h=h)
+    else:
+        names = ("q", "k", "v", "g", "b", "w")
+        st = t["state"].clone()
+        per_call = B * H * (K * (3 * 2 + 4) + V * (2 * 2 + 2) + 2 * K * V * 4)
+
+        def call(c, h):
+            ssm.gdn2_step(c["q"], c["k"], c["v"], c["g"], c["b"], c["w"], st, K ** -0.5, out=h)
+    cols = [{n: t[n][:, :, i].contiguous() for n in names} for i in range(n_tok)]
     hs = [torch.empty(B, H, V, dtype=torch.bfloat16, device=dev) for _ in range(n_tok)]
 
     def run():
         for i in range(n_tok):
-            c = cols[i]
-            ssm.mlstm_step(c["q"], c["k"], c["v"], c["igate"], c["fgate"], st, K ** -0.5, h=hs[i])
+            call(cols[i], hs[i])
 
     def timed(fn, reps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -487,10 +499,9 @@ def mlstm_decode_throughput(ssm, t, dev, n_tok=64):
         g.replay()
         graph_ms = timed(g.replay, 20)
     except Exception as ex:  # a torch without graph capture: report the eager number only
-        log("mlstm decode graph capture failed:", ex)
-    per_call = B * H * (K * 2 * 2 + V * 2 * 2 + 2 * 4 + 2 * (K * V + K + 1) * 4)
+        log(f"{op} decode graph capture failed:", ex)
     best = graph_ms if graph_ms is not None else eager_ms
-    return {"what": f"mlstm_step, one token for all {B}x{H} heads per call (state read and written in place)",
+    return {"what": f"{op}_step, one token for all {B}x{H} heads per call (state read and written in place)",
             "us_per_call_eager": round(eager_ms * 1e3, 3),
             "us_per_call_graph": None if graph_ms is None else round(graph_ms * 1e3, 3),
             "tokens_per_s": round(B / (best * 1e-3), 1),
@@ -1289,7 +1300,7 @@ def run_chunk(args, op):
     status = ssm.poll_status(ws)
     units = B * H * T
     value = world * units / (ms * 1e-3) / 1e6
-    decode = mlstm_decode_throughput(ssm, t, dev) if op.op == "mlstm" and not getattr(args, "no_extras", False) else None
+    decode = chunk_decode_throughput(op.op, ssm, t, dev) if not getattr(args, "no_extras", False) else None
 
     e2e = None
     if not args.no_e2e:  # inputs in from pinned host memory, the output and the final state back

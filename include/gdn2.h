@@ -75,6 +75,38 @@ typedef struct {
 
 int gdn2_chunk_fwd(const gdn2_fwd_args* args, void* stream);
 
+/* One token of the mixer, the per-token form the chunked steps reduce to
+ * with chunks of one token (the fused recurrent forward the page checks the
+ * chunked one against; decoding): with S the state, updated in place,
+ *   S     = S * exp(g) (per key row)
+ *   v_new = w * v - (b * k)^T S
+ *   S     = S + k v_new^T
+ *   out   = scale * q^T S
+ * Layout: q, k, b [B, H, K] bf16; g [B, H, K] fp32; v, w [B, H, V] bf16;
+ * state [B, H, K, V] fp32 (in place); out [B, H, V] bf16. Everything in
+ * fp32 (one token is a matrix-vector step: no tensor cores). With gates that
+ * differ across key channels the chunked forward's key-mean decay makes it a
+ * different evaluation from this one; with one gate per token they agree.
+ * K = V = 128 (else SSM_ERR_UNSUPPORTED); q, k, b, g, v, w, state and out
+ * 16-byte aligned (else SSM_ERR_ALIGNMENT) and non-null when B*H > 0, B*H
+ * below 2^31, scale finite (else SSM_ERR_INVALID_ARG). Asynchronous on
+ * `stream`; workspace (nullable) receives the status word. */
+typedef struct {
+    int64_t B, H, K, V;
+    float scale;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* g;
+    const void* b;
+    const void* w;
+    float* state;
+    void* out;
+    void* workspace;
+} gdn2_step_args;
+
+int gdn2_step(const gdn2_step_args* args, void* stream);
+
 /* Test hook: arms a one-shot fault for this thread's next gdn2_chunk_fwd.
  * The copies of q, k and b for chunk `chunk` (0-based, in every CTA) are not
  * issued while the chunk's other copies are, and every bounded wait of that

@@ -40,7 +40,7 @@ __all__ = [
     "clear_status", "workspace_bytes", "ckpt_elems", "ckpt_states", "CKPT_INTERVAL", "Workspace",
     "scan_fwd_bwd_host", "arm_wait_fault",
     "last_launch_count", "HostPipeline", "conv1d_fwd", "conv1d_bwd", "conv1d_step", "dtproj_fwd", "dtproj_bwd",
-    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault", "mlstm_step", "exp2_fma",
+    "gdn2_fwd", "GDN2_CHUNK", "gdn2_arm_wait_fault", "gdn2_step", "mlstm_fwd", "MLSTM_CHUNK", "mlstm_arm_wait_fault", "mlstm_step", "exp2_fma",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -112,6 +112,12 @@ class Gdn2Args(ctypes.Structure):
 GDN2_CHUNK = 64
 
 
+class Gdn2StepArgs(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("K", ctypes.c_int64), ("V", ctypes.c_int64),
+                ("scale", ctypes.c_float)] + [
+        (n, ctypes.c_void_p) for n in ("q", "k", "v", "g", "b", "w", "state", "out", "workspace")]
+
+
 class MlstmArgs(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("T", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("V", ctypes.c_int64), ("chunk", ctypes.c_int32), ("scale", ctypes.c_float),
@@ -150,6 +156,7 @@ EXPORTS = {
     "ssm_exp2_fma": ([ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p], ctypes.c_int),
     "gdn2_chunk_fwd": ([ctypes.POINTER(Gdn2Args), ctypes.c_void_p], ctypes.c_int),
     "gdn2_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
+    "gdn2_step": ([ctypes.POINTER(Gdn2StepArgs), ctypes.c_void_p], ctypes.c_int),
     "mlstm_chunk_fwd": ([ctypes.POINTER(MlstmArgs), ctypes.c_void_p], ctypes.c_int),
     "mlstm_debug_arm_wait_fault": ([ctypes.c_int64, ctypes.c_uint64], ctypes.c_int),
     "mlstm_step": ([ctypes.POINTER(MlstmStepArgs), ctypes.c_void_p], ctypes.c_int),
@@ -594,6 +601,33 @@ def gdn2_fwd(q, k, v, g, b, w, state=None, scale=None, *, out=None, state_out=No
                     state_out=_p(state_out), workspace=None if workspace is None else workspace.buf.data_ptr())
     _check(lib().gdn2_chunk_fwd(ctypes.byref(args), _stream(dev, stream)), "gdn2_chunk_fwd")
     return out, state_out
+
+
+def gdn2_step(q, k, v, g, b, w, state, scale=None, *, out=None, workspace=None, stream=None):
+    """One token of the Gated DeltaNet-2 mixer, the per-token form (C ABI in ``include/gdn2.h``): q, k, b [B, H, 128]
+    bf16; g [B, H, 128] fp32 log-gates; v, w [B, H, 128] bf16; state [B, H, 128, 128] fp32, updated in place;
+    scale defaults to 1/sqrt(K). Returns out [B, H, V] bf16."""
+    if q.dim() != 3:
+        raise ValueError("q must be [B, H, K]")
+    dev = q.device
+    if dev.type != "cuda":
+        raise ValueError("the GDN2 step runs on a CUDA device; q is on " + str(dev))
+    Bn, H, K = q.shape
+    V = v.shape[-1] if v.dim() == 3 else -1
+    bf, f32 = torch.bfloat16, torch.float32
+    for t, n in ((q, "q"), (k, "k"), (b, "b")):
+        _need(t, n, (Bn, H, K), bf, dev)
+    _need(g, "g", (Bn, H, K), f32, dev)
+    for t, n in ((v, "v"), (w, "w")):
+        _need(t, n, (Bn, H, V), bf, dev)
+    _need(state, "state", (Bn, H, K, V), f32, dev)
+    out = torch.empty((Bn, H, V), dtype=bf, device=dev) if out is None else out
+    _need(out, "out", (Bn, H, V), bf, dev)
+    args = Gdn2StepArgs(B=Bn, H=H, K=K, V=V, scale=float(K ** -0.5 if scale is None else scale), q=_p(q), k=_p(k),
+                        v=_p(v), g=_p(g), b=_p(b), w=_p(w), state=_p(state), out=_p(out),
+                        workspace=None if workspace is None else workspace.buf.data_ptr())
+    _check(lib().gdn2_step(ctypes.byref(args), _stream(dev, stream)), "gdn2_step")
+    return out
 
 
 def gdn2_arm_wait_fault(chunk: int, wait_ns: int) -> None:

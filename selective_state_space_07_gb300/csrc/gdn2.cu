@@ -623,6 +623,73 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------- one token: the per-token form
+struct Gdn2StepParams {
+    float scale;
+    const __nv_bfloat16* q;
+    const __nv_bfloat16* k;
+    const __nv_bfloat16* v;
+    const float* g;
+    const __nv_bfloat16* b;
+    const __nv_bfloat16* w;
+    float* S;
+    __nv_bfloat16* out;
+    unsigned* status;
+};
+
+// One CTA of 256 threads per (batch, head), fp32. Thread (v = tid % 128, kh = tid / 128) holds the 64 entries
+// S[k][v] of its key half in registers: one pass decays them and sums (b k)^T S for v_new, a second adds
+// k v_new^T, writes them back and sums q^T S; the key halves meet in shared memory.
+__global__ void __launch_bounds__(kGThreads) gdn2_step_kernel(const Gdn2StepParams p) {
+    __shared__ float s_eg[kGK], s_bk[kGK], s_k[kGK], s_q[kGK];
+    __shared__ float s_part[2][kGV];
+    __shared__ float s_vn[kGV];
+    const int tid = threadIdx.x;
+    const int64_t bh = blockIdx.x;
+    if (tid < kGK) {
+        const int64_t i = bh * kGK + tid;
+        const float kk = __bfloat162float(p.k[i]);
+        s_eg[tid] = expf(p.g[i]);
+        s_k[tid] = kk;
+        s_bk[tid] = __bfloat162float(p.b[i]) * kk;
+        s_q[tid] = __bfloat162float(p.q[i]) * p.scale;
+    }
+    __syncthreads();
+    const int v = tid & (kGV - 1), kh = tid >> 7, k0 = kh * (kGK / 2);
+    float* Sb = p.S + bh * kGK * kGV;
+    float sv[kGK / 2];
+    float acc = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kGK / 2; ++kk) {
+        sv[kk] = Sb[(int64_t)(k0 + kk) * kGV + v] * s_eg[k0 + kk];
+        acc = __fmaf_rn(s_bk[k0 + kk], sv[kk], acc);
+    }
+    s_part[kh][v] = acc;
+    __syncthreads();
+    if (tid < kGV) {
+        const int64_t i = bh * kGV + tid;
+        s_vn[tid] = __bfloat162float(p.w[i]) * __bfloat162float(p.v[i]) - (s_part[0][tid] + s_part[1][tid]);
+    }
+    __syncthreads();
+    const float vn = s_vn[v];
+    acc = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < kGK / 2; ++kk) {
+        const float x = __fmaf_rn(s_k[k0 + kk], vn, sv[kk]);
+        Sb[(int64_t)(k0 + kk) * kGV + v] = x;
+        acc = __fmaf_rn(s_q[k0 + kk], x, acc);
+    }
+    __syncthreads();  // every thread has read s_part before it is reused
+    s_part[kh][v] = acc;
+    __syncthreads();
+    float o = 0.f;
+    if (tid < kGV) {
+        o = s_part[0][tid] + s_part[1][tid];
+        p.out[bh * kGV + tid] = __float2bfloat16_rn(o);
+    }
+    flag_nonfinite(p.status, __fmaf_rn(o, 0.f, 0.f));
+}
+
 bool misaligned16(const void* q) { return q && (reinterpret_cast<uintptr_t>(q) & 15u) != 0; }
 
 }  // namespace
@@ -691,5 +758,27 @@ extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
     if (!enc) return SSM_ERR_CUDA;
     ssm::gdn2_chunk_fwd_kernel<<<(unsigned)BH, ssm::kGThreads, ssm::kGSmem, s>>>(
         p, a->state_in, (__nv_bfloat16*)a->out, a->state_out, mp);
+    return ssm::count_launches(cudaGetLastError() == cudaSuccess ? 1 : -1);
+}
+
+extern "C" int gdn2_step(const gdn2_step_args* a, void* stream) {
+    ssm::reset_launches();
+    if (!a) return SSM_ERR_INVALID_ARG;
+    if (a->B < 0 || a->H < 0) return SSM_ERR_INVALID_ARG;
+    if (a->K != ssm::kGK || a->V != ssm::kGV) return SSM_ERR_UNSUPPORTED;
+    if (!(fabsf(a->scale) <= 3.0e38f)) return SSM_ERR_INVALID_ARG;
+    if (a->B * a->H > 0x7fffffff) return SSM_ERR_INVALID_ARG;
+    const int64_t BH = a->B * a->H;
+    if (BH == 0) return SSM_OK;
+    if (!a->q || !a->k || !a->v || !a->g || !a->b || !a->w || !a->state || !a->out) return SSM_ERR_INVALID_ARG;
+    const void* ptrs[] = {a->q, a->k, a->v, a->g, a->b, a->w, a->state, a->out, a->workspace};
+    for (const void* q : ptrs)
+        if (ssm::misaligned16(q)) return SSM_ERR_ALIGNMENT;
+    ssm::Gdn2StepParams p{};
+    p.scale = a->scale;
+    p.q = (const __nv_bfloat16*)a->q; p.k = (const __nv_bfloat16*)a->k; p.v = (const __nv_bfloat16*)a->v;
+    p.g = a->g; p.b = (const __nv_bfloat16*)a->b; p.w = (const __nv_bfloat16*)a->w;
+    p.S = a->state; p.out = (__nv_bfloat16*)a->out; p.status = (unsigned*)a->workspace;
+    ssm::gdn2_step_kernel<<<(unsigned)BH, ssm::kGThreads, 0, (cudaStream_t)stream>>>(p);
     return ssm::count_launches(cudaGetLastError() == cudaSuccess ? 1 : -1);
 }

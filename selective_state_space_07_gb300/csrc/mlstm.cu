@@ -662,13 +662,16 @@ __global__ void __launch_bounds__(kMThreads) mlstm_step_kernel(const MlstmStepPa
     const int v = tid & (kMV - 1), kh = tid >> 7;
     const float iv = is * __bfloat162float(p.v[bh * kMV + v]);
     float* Cb = p.C + bh * kMK * kMV;
+    const int k0 = kh * (kMK / 2);
+    float cv[kMK / 2];  // every load in flight before the first use
+#pragma unroll
+    for (int kk = 0; kk < kMK / 2; ++kk) cv[kk] = Cb[(int64_t)(k0 + kk) * kMV + v];
     float acc = 0.f;
-#pragma unroll 8
+#pragma unroll
     for (int kk = 0; kk < kMK / 2; ++kk) {
-        const int k = kh * (kMK / 2) + kk;
-        const float c = __fmaf_rn(fs, Cb[(int64_t)k * kMV + v], iv * s_k[k]);
-        Cb[(int64_t)k * kMV + v] = c;
-        acc = __fmaf_rn(s_q[k], c, acc);
+        const float c = __fmaf_rn(fs, cv[kk], iv * s_k[k0 + kk]);
+        Cb[(int64_t)(k0 + kk) * kMV + v] = c;
+        acc = __fmaf_rn(s_q[k0 + kk], c, acc);
     }
     s_part[kh][v] = acc;
     qn = warp_sum(qn);

@@ -212,6 +212,23 @@ def test_gdn2_rejects_bad_arguments(ssm, over, code):
     assert ssm.lib().gdn2_chunk_fwd(ctypes.byref(args), None) == code
 
 
+def gdn2_step_args(ssm, **over):
+    a = dict(B=2, H=3, K=128, V=128, scale=0.088, q=FAKE, k=FAKE + 4096, v=FAKE + 8192, g=FAKE + 12288,
+             b=FAKE + 16384, w=FAKE + 20480, state=FAKE + 24576, out=FAKE + 28672, workspace=None)
+    a.update(over)
+    return ssm.Gdn2StepArgs(**a)
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(K=64), UNSUPPORTED), (dict(V=256), UNSUPPORTED), (dict(H=-1), INVALID), (dict(g=None), INVALID),
+    (dict(state=None), INVALID), (dict(out=None), INVALID), (dict(state=FAKE + 8), ALIGNMENT),
+    (dict(b=FAKE + 2), ALIGNMENT), (dict(scale=float("inf")), INVALID), (dict(B=0), OK),
+])
+def test_gdn2_step_rejects_bad_arguments(ssm, over, code):
+    args = gdn2_step_args(ssm, **over)
+    assert ssm.lib().gdn2_step(ctypes.byref(args), None) == code
+
+
 def test_gdn2_fault_hook_arguments(ssm):
     assert ssm.lib().gdn2_debug_arm_wait_fault(0, 20_000_000_000) == INVALID
     assert ssm.lib().gdn2_debug_arm_wait_fault(-1, 0) == OK  # disarmed
@@ -268,6 +285,7 @@ def test_mlstm_fault_hook_arguments(ssm):
 def test_null_args_struct(ssm):
     assert ssm.lib().mlstm_chunk_fwd(None, None) == INVALID
     assert ssm.lib().mlstm_step(None, None) == INVALID
+    assert ssm.lib().gdn2_step(None, None) == INVALID
     assert ssm.lib().gdn2_chunk_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_fwd(None, None) == INVALID
     assert ssm.lib().ssm_scan_bwd(None, None) == INVALID

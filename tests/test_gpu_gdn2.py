@@ -210,3 +210,56 @@ def test_binding_rejects_bad_tensors(ssm):
     small = [a[..., :64].contiguous() for a in args()]
     with pytest.raises(ssm.SsmError):
         ssm.gdn2_fwd(*small)                                 # K = V = 64: unsupported by the kernel
+
+
+# ---------------------------------------------------------------- the per-token form (one token per call)
+# fp32 throughout: the output carries its own bf16 rounding (1e-2), the state 1e-4.
+TOL_STEP_O, TOL_STEP_S = 1e-2, 1e-4
+
+
+def step_run(ssm, x, state=None):
+    bf, f32 = torch.bfloat16, torch.float32
+    st = dev(x.state, f32) if state is None else state
+    t = {n: dev(getattr(x, n), bf) for n in ("q", "k", "v", "b", "w")}
+    g = dev(x.g, f32)
+    col = lambda a, i: a[:, :, i].contiguous()  # noqa: E731
+    outs = [ssm.gdn2_step(col(t["q"], i), col(t["k"], i), col(t["v"], i), col(g, i), col(t["b"], i), col(t["w"], i),
+                          st, x.scale) for i in range(x.T)]
+    torch.cuda.synchronize()
+    return torch.stack(outs, dim=2).float().cpu().numpy(), st.cpu().numpy()
+
+
+def test_step_matches_the_per_token_oracle(ssm):
+    x = gen.make_gdn2_inputs(2, 3, 24, 128, 128, seed=61)
+    o, s = step_run(ssm, x)
+    ro, rs = G.recurrent(x.q, x.k, x.v, x.g, x.b, x.w, x.state, x.scale)
+    eo, es = rel_err(o, ro), rel_err(s, rs)
+    print(f"gdn2 step: out {eo:.2e} state {es:.2e}")
+    assert eo < TOL_STEP_O and es < TOL_STEP_S
+
+
+def test_chunked_forward_against_the_per_token_form_on_the_gpu(ssm):
+    # the page's check of the chunked forward against the fused recurrent one, both evaluated here: with
+    # one gate per token the two agree (to the chunked products' bf16 rounding); then decoding one more
+    # token from the chunked call's final state continues the same sequence
+    x = gen.make_gdn2_inputs(1, 2, 151, 128, 128, seed=63, key_uniform_gates=True)
+    T = 150
+    bf, f32 = torch.bfloat16, torch.float32
+    t = {n: dev(getattr(x, n), bf) for n in ("q", "k", "v", "b", "w")}
+    g = dev(x.g, f32)
+    cut = lambda a: a[:, :, :T].contiguous()  # noqa: E731
+    oc, sc = ssm.gdn2_fwd(*(cut(t[n]) for n in ("q", "k", "v")), cut(g), cut(t["b"]), cut(t["w"]), dev(x.state, f32),
+                          x.scale)
+    xs = gen.make_gdn2_inputs(1, 2, 151, 128, 128, seed=63, key_uniform_gates=True)
+    for n in ("q", "k", "v", "g", "b", "w"):
+        setattr(xs, n, getattr(xs, n)[:, :, :T])
+    xs.T = T
+    os_, ss = step_run(ssm, xs)
+    oc = oc.float().cpu().numpy()
+    print(f"gdn2 chunked vs per-token (GPU): out {rel_err(oc, os_):.2e} state {rel_err(sc.cpu().numpy(), ss):.2e}")
+    assert rel_err(oc, os_) < TOL and rel_err(sc.cpu().numpy(), ss) < TOL
+    col = lambda a: a[:, :, T].contiguous()  # noqa: E731
+    o1 = ssm.gdn2_step(*(col(t[n]) for n in ("q", "k", "v")), col(g), col(t["b"]), col(t["w"]), sc, x.scale)
+    torch.cuda.synchronize()
+    ro, rs = G.recurrent(x.q, x.k, x.v, x.g, x.b, x.w, x.state, x.scale)
+    assert rel_err(o1.float().cpu().numpy(), ro[:, :, T]) < TOL and rel_err(sc.cpu().numpy(), rs) < TOL
