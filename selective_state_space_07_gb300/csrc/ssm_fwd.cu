@@ -459,6 +459,18 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
     const float delta = token_delta<FAST>(dtv, bias, p.sp != 0);
     const float u = __fmul_rn(delta, xv);
     float* st = p.state + (b * D + (dv ? d : 0)) * kN;
+    // the lane's states and row of A, every load issued before anything is
+    // stored (16-byte vectors; the state is updated in place)
+    constexpr int NL = kN / NSPLIT;          // states of this lane
+    const int nb0 = NSPLIT == 2 ? k * NL : 0;
+    float hs[NL], As[NL];
+#pragma unroll
+    for (int q = 0; q < NL; q += 4) {
+        const float4 h4 = dv ? *reinterpret_cast<const float4*>(st + nb0 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 a4 = dv ? *reinterpret_cast<const float4*>(p.A + d * kN + nb0 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        hs[q] = h4.x; hs[q + 1] = h4.y; hs[q + 2] = h4.z; hs[q + 3] = h4.w;
+        As[q] = a4.x; As[q + 1] = a4.y; As[q + 2] = a4.z; As[q + 3] = a4.w;
+    }
     // the forward's readout order: blocks of BS states, each a sequential
     // fused multiply-add chain C_0 h_0 -> fma(C_1, h_1, .) -> ...; the blocks
     // summed as a balanced binary tree in state order (its top level: one
@@ -473,15 +485,22 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
         float acc = 0.f;
 #pragma unroll
         for (int s = 0; s < BS; ++s) {
-            const int n = BS * blk + s;
-            const float A2 = dv ? __fmul_rn(p.A[d * kN + n], kLog2e) : 0.f;
+            // j: the state's slot in this lane's registers (the lane holds states nb0 .. nb0 + NL - 1, nb0 a
+            // multiple of NL, so j = n mod NL: known at compile time)
+            const int n = BS * blk + s, j = n & (NL - 1);
+            const float A2 = __fmul_rn(As[j], kLog2e);
             const float a = ex2(__fmul_rn(delta, A2));
             const float ub = __fmul_rn(u, Bs[n]);
-            const float hv = __fmaf_rn(a, dv ? st[n] : 0.f, ub);
-            if (dv) st[n] = hv;
+            const float hv = __fmaf_rn(a, hs[j], ub);
+            hs[j] = hv;
             acc = s == 0 ? __fmul_rn(Cs[n], hv) : __fmaf_rn(Cs[n], hv, acc);
         }
         part[blk] = acc;
+    }
+    if (dv) {
+#pragma unroll
+        for (int q = 0; q < NL; q += 4)
+            *reinterpret_cast<float4*>(st + nb0 + q) = make_float4(hs[q], hs[q + 1], hs[q + 2], hs[q + 3]);
     }
 #pragma unroll
     for (int w = 1; w < HB; w <<= 1)
