@@ -721,7 +721,7 @@ extern "C" int gdn2_chunk_fwd(const gdn2_fwd_args* a, void* stream) {
     if (!(fabsf(a->scale) <= 3.0e38f)) return SSM_ERR_INVALID_ARG;  // NaN or infinite scale
     if (a->B * a->H > 0x7fffffff) return SSM_ERR_INVALID_ARG;
     // token rows are addressed by 32-bit copy coordinates
-    if (a->B * a->H * a->T > 0x7fffffff - 2 * ssm::kGC) return SSM_ERR_UNSUPPORTED;
+    if (a->T > 0x7fffffff || a->B * a->H * a->T > 0x7fffffff - 2 * ssm::kGC) return SSM_ERR_UNSUPPORTED;
     const bool work = a->B > 0 && a->H > 0 && a->T > 0;
     if (work && (!a->q || !a->k || !a->v || !a->g || !a->b || !a->w || !a->out)) return SSM_ERR_INVALID_ARG;
     const void* ptrs[] = {a->q, a->k, a->v, a->g, a->b, a->w, a->state_in, a->out, a->state_out, a->workspace};

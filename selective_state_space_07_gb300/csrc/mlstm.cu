@@ -732,7 +732,7 @@ extern "C" int mlstm_chunk_fwd(const mlstm_fwd_args* a, void* stream) {
     if (!(a->norm_eps >= 0.f && a->norm_eps <= 3.0e38f)) return SSM_ERR_INVALID_ARG;  // NaN, negative or infinite
     if (a->B * a->H > 0x7fffffff) return SSM_ERR_INVALID_ARG;
     // token rows are addressed by 32-bit copy coordinates
-    if (a->B * a->H * a->T > 0x7fffffff - 2 * ssm::kMC) return SSM_ERR_UNSUPPORTED;
+    if (a->T > 0x7fffffff || a->B * a->H * a->T > 0x7fffffff - 2 * ssm::kMC) return SSM_ERR_UNSUPPORTED;
     const bool in_all = a->C_in && a->n_in && a->m_in, in_none = !a->C_in && !a->n_in && !a->m_in;
     const bool out_all = a->C_out && a->n_out && a->m_out, out_none = !a->C_out && !a->n_out && !a->m_out;
     if (!(in_all || in_none) || !(out_all || out_none)) return SSM_ERR_INVALID_ARG;

@@ -106,7 +106,8 @@ int check_fwd(const ssm_fwd_args* a, bool need_y) {
     if (a->nsplit != 0 && a->nsplit != 1 && a->nsplit != 2 && a->nsplit != 4) return SSM_ERR_INVALID_ARG;
     if (a->groups < 0) return SSM_ERR_INVALID_ARG;
     if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
-    if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 40))
+    // (L below 2^30, which B * L <= 2^30 below implies anyway, keeps that product inside int64)
+    if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 30))
         return SSM_ERR_INVALID_ARG;
     const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
     if (bc != SSM_OK) return bc;

@@ -206,6 +206,7 @@ def gdn2_args(ssm, **over):
     (dict(w=FAKE + 2), ALIGNMENT), (dict(state_in=FAKE + 8), ALIGNMENT), (dict(state_out=FAKE + 4), ALIGNMENT),
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(B=1, H=1, T=1 << 31), UNSUPPORTED), (dict(B=4, H=8, T=1 << 26), UNSUPPORTED),
+    (dict(B=1 << 20, H=1 << 10, T=1 << 40), UNSUPPORTED),  # B*H*T beyond int64 if multiplied unchecked
 ])
 def test_gdn2_rejects_bad_arguments(ssm, over, code):
     args = gdn2_args(ssm, **over)
@@ -252,6 +253,7 @@ def mlstm_args(ssm, **over):
     (dict(scale=float("nan")), INVALID), (dict(scale=float("inf")), INVALID),
     (dict(norm_eps=-1.0), INVALID), (dict(norm_eps=float("nan")), INVALID),
     (dict(B=1, H=1, T=1 << 31), UNSUPPORTED), (dict(B=4, H=8, T=1 << 26), UNSUPPORTED),
+    (dict(B=1 << 20, H=1 << 10, T=1 << 40), UNSUPPORTED),  # B*H*T beyond int64 if multiplied unchecked
 ])
 def test_mlstm_rejects_bad_arguments(ssm, over, code):
     args = mlstm_args(ssm, **over)
