@@ -106,14 +106,14 @@ int check_fwd(const ssm_fwd_args* a, bool need_y) {
     if (a->nsplit != 0 && a->nsplit != 1 && a->nsplit != 2 && a->nsplit != 4) return SSM_ERR_INVALID_ARG;
     if (a->groups < 0) return SSM_ERR_INVALID_ARG;
     if (a->D % 8 != 0) return SSM_ERR_ALIGNMENT;
-    // (L below 2^30, which B * L <= 2^30 below implies anyway, keeps that product inside int64)
-    if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 30))
+    if (a->B > (int64_t(1) << 31) || a->D > (int64_t(1) << 31) || a->L > (int64_t(1) << 40))
         return SSM_ERR_INVALID_ARG;
     const int bc = ssm::check_bc_stride(a->bc_stride, a->N, a->io_dtype);
     if (bc != SSM_OK) return bc;
     // the tiles are addressed by 32-bit rows of the flattened [B*L] tensors and of the
     // checkpoints (2 rows per token: 16 states every 8 tokens)
-    if (a->B * a->L > (int64_t(1) << 30)) return SSM_ERR_UNSUPPORTED;
+    // (L is bounded first so that B * L stays inside int64)
+    if (a->L > (int64_t(1) << 30) || a->B * a->L > (int64_t(1) << 30)) return SSM_ERR_UNSUPPORTED;
     const bool work = a->B > 0 && a->L > 0 && a->D > 0;
     if (work && (!a->x || !a->dt || !a->Bm || !a->Cm || !a->A || (need_y && !a->y))) return SSM_ERR_INVALID_ARG;
     const void* ptrs[] = {a->x, a->z, a->Bm, a->Cm, a->dt, a->dt_bias, a->A, a->Dskip, a->h0, a->y, a->h_last,

@@ -89,6 +89,7 @@ def fwd_args(ssm, **over):
     (dict(bc_stride=8), INVALID), (dict(bc_stride=20), ALIGNMENT), (dict(bc_stride=-16), INVALID),
     (dict(B=2, L=1 << 30), UNSUPPORTED),  # 2^31 token rows: past the 32-bit row coordinates of the copies
     (dict(B=1, L=(1 << 30) + 1), UNSUPPORTED),
+    (dict(B=1 << 30, L=1 << 34), UNSUPPORTED),  # B*L would wrap past int64 (to 0) if multiplied unchecked
 ])
 def test_fwd_rejects_bad_arguments(ssm, over, code):
     args = fwd_args(ssm, **over)
