@@ -454,13 +454,17 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
 }
 
 // Chunk aggregate of the reverse recurrence for groups 1..G-1: with the
-// adjoint carry set to zero at the group's end, run E_t = a_{t+1} E_{t+1} +
-// dp_t C_t back to the group's start and publish Q = a_{t0} E_{t0} (the carry
-// the group passes to its left neighbour) and the group's sum of Delta. The
-// carry entering group g-1 from the right is then exp(A*sum Delta_g) *
-// carry_g + Q_g. Layout as in the forward: a lane pair per channel, each lane
-// 8 states and 8 of a tile's 16 tokens for the per-token work; C staged
-// state-major (broadcast loads); two states advance together.
+// adjoint carry set to zero at the group's end, the carry the group passes to
+// its left neighbour is Q = a_{t0} E_{t0}, and unrolling E_t = a_{t+1} E_{t+1}
+// + dp_t C_t gives it in closed form,
+//   Q_n = sum_t exp(A_n Lambda_t) dp_t C_t,n,  Lambda_t = Delta_{t0} + ... + Delta_t,
+// every term independent of the others (the product of the decays up to t is
+// the exponential of A times the prefix sum of Delta). The kernel walks the
+// group from its start, keeps the running Lambda per channel and publishes
+// Q and the group's sum of Delta. The carry entering group g-1 from the right
+// is then exp(A*sum Delta_g) * carry_g + Q_g. Layout as in the forward: a lane
+// pair per channel, each lane 8 states and 8 of a tile's 16 tokens for the
+// per-token work; C staged state-major (broadcast loads).
 template <typename IO> struct BwdAggLayout {
     static constexpr int NT = kBwdThreads;
     static constexpr int CH = NT / 2;
@@ -470,7 +474,7 @@ template <typename IO> struct BwdAggLayout {
     static constexpr int STAGE = OFF_C + kCK * BCROW;
     static constexpr int NSTAGE = 3;
     static constexpr int SMEM = NSTAGE * STAGE + 128;  // + slack for 128-byte alignment
-    static constexpr int ROW = 2 * kCK + 4;  // per-channel row [Delta 0..15 | dp 0..15], padded
+    static constexpr int ROW = 2 * kCK + 4;  // per-channel row [Lambda 0..15 | dp 0..15], padded
     static_assert(OFF_DY % 128 == 0 && OFF_DT % 128 == 0 && OFF_C % 128 == 0 && STAGE % 128 == 0,
                   "TMA destinations on 128-byte boundaries");
 };
@@ -491,7 +495,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
     __shared__ __align__(8) uint64_t fullb[Ly::NSTAGE];
     __shared__ int aborted;
     // C^T double-buffered by tile parity (one CTA barrier per tile); a
-    // channel's Delta / dp row is shared by its lane pair only (warp syncs)
+    // channel's Lambda / dp row is shared by its lane pair only (warp syncs)
     __shared__ __align__(16) float CT2[2 * kN * T];
     __shared__ __align__(16) float DP[CH * Ly::ROW];
 
@@ -507,20 +511,20 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
     const int ntile = (int)((tb1 - tb0 + T - 1) / T);
     const bool has_z = p.has_z != 0, sp = p.sp != 0;
 
-    float A2[NS], E[NS], an[NS];
+    float2 A2p[NS], acc[NS];  // A log2(e) twice; per state the even- and odd-token partial sums of Q
 #pragma unroll
     for (int s = 0; s < NS; ++s) {
-        A2[s] = dv ? __fmul_rn(p.A[d * kN + NS * hk + s], kLog2e) : 0.f;
-        E[s] = 0.f;
-        an[s] = 1.f;
+        const float a2 = dv ? __fmul_rn(p.A[d * kN + NS * hk + s], kLog2e) : 0.f;
+        A2p[s] = make_float2(a2, a2);
+        acc[s] = make_float2(0.f, 0.f);
     }
     const float bias = (dv && p.dt_bias) ? p.dt_bias[d] : 0.f;
     const unsigned tile_bytes = (unsigned)(T * (Ly::XROW * (has_z ? 2 : 1) + Ly::DTROW + Ly::BCROW));
-    auto issue = [&](int j) {  // tile j counted from the group's end
+    auto issue = [&](int j) {  // tile j counted from the group's start
         if (tid != 0) return;
         const int slot = j % Ly::NSTAGE;
         char* st = smem + slot * Ly::STAGE;
-        const int y = (int)(b * L + tb0 + (int64_t)(ntile - 1 - j) * T);
+        const int y = (int)(b * L + tb0 + (int64_t)j * T);
         const unsigned bar = smem_u32(&fullb[slot]);
         mbar_expect_tx(bar, tile_bytes);
         if (has_z) tma_load_2d(st + Ly::OFF_Z, &mp.z, (int)d0, y, bar);
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
     }
     __syncthreads();
     float* dp = DP + c * Ly::ROW;
-    float ssum = 0.f;
+    float lam = 0.f;  // Lambda at the end of the previous tile (the same in both lanes of a pair)
 #pragma unroll
     for (int q = 0; q < Ly::NSTAGE - 1; ++q)
         if (q < ntile) issue(q);
@@ -547,7 +551,7 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             if (p.status) atomicOr(p.status, kStatusTimeout);
         }
         float* CT = CT2 + (j & 1) * kN * T;
-        const int64_t t0 = tb0 + (int64_t)(ntile - 1 - j) * T;
+        const int64_t t0 = tb0 + (int64_t)j * T;
         const int rows = (int)min64(T, tb1 - t0);
         {
             const IO* Craw = reinterpret_cast<const IO*>(st + Ly::OFF_C);
@@ -557,9 +561,10 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
             }
         }
         {
-            // Delta and dp of this lane's 8 tokens, a token pair at a time
+            // Delta and dp of this lane's 8 tokens, a token pair at a time;
+            // tokens past the end add nothing to Lambda and have dp = 0
             const float2 bias2 = make_float2(bias, bias);
-            float2 dl[NS / 2], pl[NS / 2];
+            float dl[NS], pl[NS];
 #pragma unroll
             for (int i = 0; i < NS / 2; ++i) {
                 const int t = NS * hk + 2 * i;
@@ -571,87 +576,71 @@ __global__ void __launch_bounds__(kBwdThreads) ssm_bwd_agg_kernel(const BwdParam
                     const float2 zv = ld_pair<IO>(st + Ly::OFF_Z + t * Ly::XROW, Ly::XROW, c);
                     dpv = __fmul2_rn(dyv, __fmul2_rn(zv, sigmoid2<FAST>(zv)));
                 }
-                const bool l0 = t < rows, l1 = t + 1 < rows;  // tokens past the end: a = 1, no adjoint input
-                dl[i] = make_float2(l0 ? delta.x : 0.f, l1 ? delta.y : 0.f);
-                pl[i] = make_float2(l0 ? dpv.x : 0.f, l1 ? dpv.y : 0.f);
-                ssum = __fadd_rn(__fadd_rn(ssum, dl[i].x), dl[i].y);
+                const bool l0 = t < rows, l1 = t + 1 < rows;
+                dl[2 * i] = l0 ? delta.x : 0.f;
+                dl[2 * i + 1] = l1 ? delta.y : 0.f;
+                pl[2 * i] = l0 ? dpv.x : 0.f;
+                pl[2 * i + 1] = l1 ? dpv.y : 0.f;
             }
-            *reinterpret_cast<float4*>(dp + NS * hk) = make_float4(dl[0].x, dl[0].y, dl[1].x, dl[1].y);
-            *reinterpret_cast<float4*>(dp + NS * hk + 4) = make_float4(dl[2].x, dl[2].y, dl[3].x, dl[3].y);
-            *reinterpret_cast<float4*>(dp + T + NS * hk) = make_float4(pl[0].x, pl[0].y, pl[1].x, pl[1].y);
-            *reinterpret_cast<float4*>(dp + T + NS * hk + 4) = make_float4(pl[2].x, pl[2].y, pl[3].x, pl[3].y);
+            // the lane's inclusive prefix over its 8 tokens; the second lane
+            // of the pair starts after the first lane's 8
+#pragma unroll
+            for (int i = 1; i < NS; ++i) dl[i] = __fadd_rn(dl[i - 1], dl[i]);
+            const float own = dl[NS - 1], other = __shfl_xor_sync(0xffffffffu, own, 16);
+            const float base = hk ? __fadd_rn(lam, other) : lam;
+#pragma unroll
+            for (int i = 0; i < NS; ++i) dl[i] = __fadd_rn(base, dl[i]);
+            lam = __fadd_rn(lam, __fadd_rn(own, other));  // the same in both lanes: s0 + s1 = s1 + s0
+            *reinterpret_cast<float4*>(dp + NS * hk) = make_float4(dl[0], dl[1], dl[2], dl[3]);
+            *reinterpret_cast<float4*>(dp + NS * hk + 4) = make_float4(dl[4], dl[5], dl[6], dl[7]);
+            *reinterpret_cast<float4*>(dp + T + NS * hk) = make_float4(pl[0], pl[1], pl[2], pl[3]);
+            *reinterpret_cast<float4*>(dp + T + NS * hk + 4) = make_float4(pl[4], pl[5], pl[6], pl[7]);
         }
-        // the tile's C^T and Delta / dp rows are ready; every thread is done
+        // the tile's C^T and Lambda / dp rows are ready; every thread is done
         // with the previous tile (so its staging slot may be refilled)
         __syncthreads();
-        float2 Dl[T / 2], Pl[T / 2];
+        float2 Lm[T / 2], Pl[T / 2];
 #pragma unroll
         for (int q = 0; q < T / 4; ++q) {
-            const float4 dq = *reinterpret_cast<const float4*>(dp + 4 * q);
+            const float4 lq = *reinterpret_cast<const float4*>(dp + 4 * q);
             const float4 pq = *reinterpret_cast<const float4*>(dp + T + 4 * q);
-            Dl[2 * q] = make_float2(dq.x, dq.y);
-            Dl[2 * q + 1] = make_float2(dq.z, dq.w);
+            Lm[2 * q] = make_float2(lq.x, lq.y);
+            Lm[2 * q + 1] = make_float2(lq.z, lq.w);
             Pl[2 * q] = make_float2(pq.x, pq.y);
             Pl[2 * q + 1] = make_float2(pq.z, pq.w);
         }
-        // SA states at a time: independent adjoint chains for the scheduler
-#ifndef SSM_AGG_SA
-#define SSM_AGG_SA 4
-#endif
-        constexpr int SA = SSM_AGG_SA;
-        // the first SSM_AGG_FMA_STATES of a lane's states take the FMA-pipe 2^x instead of the MUFU
-        // (0 = none: the XU pipe does not bind here; measured with 1 and 2, kept for such measurements)
+        // Q_n += exp2(A_n log2(e) Lambda_t) * dp_t C_t,n: no term waits for another.
+        // The first SSM_AGG_FMA_STATES of a lane's states take the FMA-pipe 2^x
+        // instead of the MUFU (0 = none).
 #ifndef SSM_AGG_FMA_STATES
 #define SSM_AGG_FMA_STATES 0
 #endif
         constexpr int kAggFma = SSM_AGG_FMA_STATES;
 #pragma unroll
-        for (int s = 0; s < NS; s += SA) {
+        for (int s = 0; s < NS; ++s) {
             const int n = NS * hk + s;
-            float2 A2p[SA];
-            float Ev[SA], nx[SA];
 #pragma unroll
-            for (int i = 0; i < SA; ++i) {
-                A2p[i] = make_float2(A2[s + i], A2[s + i]);
-                Ev[i] = E[s + i];
-                nx[i] = an[s + i];
-            }
+            for (int q = 0; q < T / 4; ++q) {
+                const float4 c4 = *reinterpret_cast<const float4*>(CT + n * T + 4 * q);
 #pragma unroll
-            for (int q = T / 4 - 1; q >= 0; --q) {
-                float4 c4[SA];
-#pragma unroll
-                for (int i = 0; i < SA; ++i) c4[i] = *reinterpret_cast<const float4*>(CT + (n + i) * T + 4 * q);
-#pragma unroll
-                for (int h2 = 1; h2 >= 0; --h2) {
+                for (int h2 = 0; h2 < 2; ++h2) {
                     const int m = 2 * q + h2;
-#pragma unroll
-                    for (int i = 0; i < SA; ++i) {
-                        const float2 cc = h2 ? make_float2(c4[i].z, c4[i].w) : make_float2(c4[i].x, c4[i].y);
-                        const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
-                        const float2 r = __fmul2_rn(Pl[m], cc);
-                        const bool on_fma = s + i < kAggFma;
-                        const float a1 = on_fma ? ex2_fma(arg.y) : ex2(arg.y);
-                        const float a0 = on_fma ? ex2_fma(arg.x) : ex2(arg.x);
-                        Ev[i] = __fmaf_rn(nx[i], Ev[i], r.y);
-                        Ev[i] = __fmaf_rn(a1, Ev[i], r.x);
-                        nx[i] = a0;
-                    }
+                    const float2 cc = h2 ? make_float2(c4.z, c4.w) : make_float2(c4.x, c4.y);
+                    const float2 arg = __fmul2_rn(Lm[m], A2p[s]);
+                    const float2 r = __fmul2_rn(Pl[m], cc);
+                    const float2 e = s < kAggFma ? make_float2(ex2_fma(arg.x), ex2_fma(arg.y))
+                                                 : make_float2(ex2(arg.x), ex2(arg.y));
+                    acc[s] = __ffma2_rn(e, r, acc[s]);
                 }
             }
-#pragma unroll
-            for (int i = 0; i < SA; ++i) {
-                E[s + i] = Ev[i];
-                an[s + i] = nx[i];
-            }
         }
-        __syncwarp();  // the lane pair is done with its Delta / dp row before the next tile rewrites it
+        __syncwarp();  // the lane pair is done with its Lambda / dp row before the next tile rewrites it
     }
-    ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, 16));
     if (dv) {
         float* Q = p.aggQ + ((b * p.G + g) * D + d) * kN + NS * hk;
 #pragma unroll
-        for (int s = 0; s < NS; ++s) Q[s] = __fmul_rn(an[s], E[s]);
-        if (hk == 0) p.aggS[(b * p.G + g) * D + d] = ssum;
+        for (int s = 0; s < NS; ++s) Q[s] = __fadd_rn(acc[s].x, acc[s].y);
+        if (hk == 0) p.aggS[(b * p.G + g) * D + d] = lam;
     }
 }
 

@@ -38,10 +38,14 @@
 // multiplied by z * sigmoid(z).
 //
 // Parallelism along L: the sequence splits into G groups. A first pass
-// (AGG) runs every group but the last from a zero state and publishes its
-// end state and sum of Delta; a warp-shuffle associative scan of the affine
+// (AGG) computes, for every group but the last, its end state from a zero
+// state and its sum of Delta; a warp-shuffle associative scan of the affine
 // maps h -> exp(A*sum Delta)*h + H_end across groups produces each group's
-// carry-in; the main pass then reruns every group from its carry.
+// carry-in; the main pass then reruns every group from its carry. The
+// aggregate needs no per-token state: per tile, h <- exp(A sum Delta) h +
+// sum_t exp(A S_t) u_t B_t with S_t the sum of Delta over the tile's later
+// tokens (the product of the decays after t), so its terms are independent
+// of one another instead of one multiply-add chain per state.
 #include "ssm_common.cuh"
 #include "ssm_internal.h"
 
@@ -55,7 +59,8 @@ namespace {
 constexpr int kLPC = kFwdLPC;
 constexpr int kCPW = 32 / kLPC;  // channels per warp
 
-template <typename IO> struct FwdLayout {
+// AGG stages neither z nor C: its stages are smaller (more CTAs per SM).
+template <typename IO, bool AGG = false> struct FwdLayout {
     static constexpr int NT = kFwdCtaThreads;
     static constexpr int CH = NT / kLPC;          // channels per CTA
     static constexpr int ES = sizeof(IO);
@@ -64,10 +69,10 @@ template <typename IO> struct FwdLayout {
     static constexpr int BCROW = kN * ES;         // one token of B or C
     static constexpr int OFF_X = 0;
     static constexpr int OFF_Z = OFF_X + kCK * XROW;
-    static constexpr int OFF_DT = OFF_Z + kCK * XROW;
+    static constexpr int OFF_DT = OFF_Z + (AGG ? 0 : kCK * XROW);
     static constexpr int OFF_B = OFF_DT + kCK * DTROW;
     static constexpr int OFF_C = OFF_B + kCK * BCROW;
-    static constexpr int STAGE = OFF_C + kCK * BCROW;
+    static constexpr int STAGE = OFF_C + (AGG ? 0 : kCK * BCROW);
     static constexpr int NSTAGE = 4;              // tiles in flight
     static constexpr int SMEM = NSTAGE * STAGE + 128;  // dynamic shared memory (+ slack for 128-byte alignment)
     static_assert(OFF_Z % 128 == 0 && OFF_DT % 128 == 0 && OFF_B % 128 == 0 && OFF_C % 128 == 0 &&
@@ -99,7 +104,7 @@ struct FwdMaps {
 template <typename IO, bool AGG, int MINB>
 __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
     ssm_fwd_kernel(const FwdParams p, const __grid_constant__ FwdMaps mp) {
-    using Ly = FwdLayout<IO>;
+    using Ly = FwdLayout<IO, AGG>;
     constexpr int NT = Ly::NT, CH = Ly::CH, T = kCK, NS = kN / kLPC, TPL = kCK / kLPC, RB = kReadBlock;
     static_assert(NS % RB == 0, "whole readout blocks per lane");
     constexpr bool FAST = IOT<IO>::kFast;
@@ -168,8 +173,9 @@ __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
     }
     __syncthreads();
 
-    float nf = 0.f;     // Inf/NaN detector
-    float ssum = 0.f;   // AGG: this lane's part of the sum of Delta over the group
+    float nf = 0.f;        // Inf/NaN detector
+    float ssum = 0.f;      // AGG: the sum of Delta over the group (the same in every lane of a channel)
+    float tile_sum = 0.f;  // AGG: the sum of Delta over the current tile
 
     // prologue: tiles 0 .. NSTAGE-2 in flight
     if (tid == 0)
@@ -219,13 +225,34 @@ __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
                 const float2 u = __fmul2_rn(delta, xv);
                 ul[i] = f2(l0 ? u.x : 0.f, l1 ? u.y : 0.f);
                 xo[i] = xv;
-                if (AGG) ssum = __fadd_rn(__fadd_rn(ssum, dl[i].x), dl[i].y);
                 if (has_z) {
                     const char* zr = st + Ly::OFF_Z + t * Ly::XROW;
                     const float2 zv = f2(IOT<IO>::to_f(reinterpret_cast<const IO*>(zr)[c]),
                                          IOT<IO>::to_f(reinterpret_cast<const IO*>(zr + Ly::XROW)[c]));
                     gz[i] = __fmul2_rn(zv, sigmoid2<FAST>(zv));
                 }
+            }
+            if constexpr (AGG) {
+                // the Delta row becomes, per token, the sum of Delta over the
+                // tile's later tokens (exclusive suffix): the lane's own tokens,
+                // then the totals of the channel's later lane blocks
+                float sf[TPL];
+                sf[TPL - 1] = 0.f;
+#pragma unroll
+                for (int k = TPL - 2; k >= 0; --k)
+                    sf[k] = __fadd_rn(sf[k + 1], (k + 1) & 1 ? dl[(k + 1) / 2].y : dl[(k + 1) / 2].x);
+                const float own = __fadd_rn(sf[0], dl[0].x);
+                float after = 0.f, tot = 0.f;
+#pragma unroll
+                for (int r = 0; r < kLPC; ++r) {
+                    const float tr = __shfl_sync(0xffffffffu, own, (lane % kCPW) + kCPW * r);
+                    tot = __fadd_rn(tot, tr);  // the same order in every lane of the channel
+                    if (r > hk) after = __fadd_rn(after, tr);
+                }
+#pragma unroll
+                for (int i = 0; i < TPL / 2; ++i) dl[i] = f2(__fadd_rn(sf[2 * i], after), __fadd_rn(sf[2 * i + 1], after));
+                tile_sum = tot;
+                ssum = __fadd_rn(ssum, tot);
             }
 #pragma unroll
             for (int i = 0; i < TPL / 4; ++i) {
@@ -269,6 +296,32 @@ __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
         if (ck) {  // states before token t0
 #pragma unroll
             for (int i = 0; i < NS; i += 2) *reinterpret_cast<float2*>(ckp + (int64_t)(i / 2) * D * 2) = f2(hp[i], hp[i + 1]);
+        }
+        if constexpr (AGG) {
+            // the group's end state from a zero start, tile by tile: h <- exp(A
+            // sum Delta) h + sum_t exp(A S_t) u_t B_t, S_t the sum of Delta over
+            // the tile's tokens after t -- no term of the sum waits for another
+            float2 ha[NS];
+#pragma unroll
+            for (int i = 0; i < NS; ++i) ha[i] = f2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < T / 4; ++q) {
+#pragma unroll
+                for (int i = 0; i < NS; ++i) {
+                    const float4 b4 = *reinterpret_cast<const float4*>(BTb + (n0 + i) * T + 4 * q);
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int m = 2 * q + h2;
+                        const float2 bb = h2 ? f2(b4.z, b4.w) : f2(b4.x, b4.y);
+                        const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
+                        const float2 ub = __fmul2_rn(Ul[m], bb);
+                        ha[i] = __ffma2_rn(f2(ex2(arg.x), ex2(arg.y)), ub, ha[i]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < NS; ++i) h[i] = __fmaf_rn(ex2(__fmul_rn(A2[i], tile_sum)), h[i], __fadd_rn(ha[i].x, ha[i].y));
+            continue;
         }
 #pragma unroll
         for (int q = 0; q < T / 4; ++q) {
@@ -363,8 +416,6 @@ __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
         return;
     }
     if (AGG) {
-#pragma unroll
-        for (int off = kCPW; off < 32; off <<= 1) ssum = __fadd_rn(ssum, __shfl_xor_sync(0xffffffffu, ssum, off));
         if (dv) {
             float* H = p.aggH + ((b * p.G + g) * D + d) * kN + NS * hk;
 #pragma unroll
@@ -522,7 +573,7 @@ __global__ void __launch_bounds__(kFwdThreads) ssm_step_kernel(const StepParams 
 
 template <typename IO, bool AGG, int MINB>
 int launch_fwd_v(const FwdParams& p, const FwdMaps& mp, dim3 grid, cudaStream_t s) {
-    using Ly = FwdLayout<IO>;
+    using Ly = FwdLayout<IO, AGG>;
     static unsigned long long mask = 0;
     auto kern = ssm_fwd_kernel<IO, AGG, MINB>;
     if (!ensure_smem(kern, Ly::SMEM, mask)) return -1;
@@ -556,9 +607,14 @@ template <typename IO, bool AGG> int launch_fwd_t(const FwdParams& p, cudaStream
     const int64_t ctas = (int64_t)grid.x * grid.y * grid.z;
     // the register budget: uncut when one L-group's grid fits in two CTAs
     // per SM (the scheduler gets registers for the interleaved state
-    // chains), else cut to three CTAs per SM
-    if (!AGG && p.G == 1 && ctas <= 2 * (int64_t)sm_count()) return launch_fwd_v<IO, AGG, 1>(p, mp, grid, s);
-    return launch_fwd_v<IO, AGG, 3>(p, mp, grid, s);
+    // chains), else cut to three CTAs per SM; the aggregate pass (no readout)
+    // fits four
+    if constexpr (AGG) {
+        return launch_fwd_v<IO, AGG, 4>(p, mp, grid, s);
+    } else {
+        if (p.G == 1 && ctas <= 2 * (int64_t)sm_count()) return launch_fwd_v<IO, AGG, 1>(p, mp, grid, s);
+        return launch_fwd_v<IO, AGG, 3>(p, mp, grid, s);
+    }
 }
 
 template <typename IO, int NSPLIT> int launch_step_t(const StepParams& p, cudaStream_t s) {
