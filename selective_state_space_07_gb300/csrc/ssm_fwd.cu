@@ -321,83 +321,83 @@ __global__ void __launch_bounds__(kFwdCtaThreads, MINB)
             }
 #pragma unroll
             for (int i = 0; i < NS; ++i) h[i] = __fmaf_rn(ex2(__fmul_rn(A2[i], tile_sum)), h[i], __fadd_rn(ha[i].x, ha[i].y));
-            continue;
-        }
+        } else {
 #pragma unroll
-        for (int q = 0; q < T / 4; ++q) {
-            float4 b4[NS], c4[NS];
-#pragma unroll
-            for (int i = 0; i < NS; ++i) {
-                b4[i] = *reinterpret_cast<const float4*>(BTb + (n0 + i) * T + 4 * q);
-                if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CTb + (n0 + i) * T + 4 * q);
-            }
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int m = 2 * q + h2;
-                float hv0[NS], hv1[NS];
+            for (int q = 0; q < T / 4; ++q) {
+                float4 b4[NS], c4[NS];
 #pragma unroll
                 for (int i = 0; i < NS; ++i) {
-                    const float2 bb = h2 ? f2(b4[i].z, b4[i].w) : f2(b4[i].x, b4[i].y);
-                    const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
-                    const float a0 = ex2(arg.x), a1 = ex2(arg.y);
-                    const float2 ub = __fmul2_rn(Ul[m], bb);
-                    hv0[i] = __fmaf_rn(a0, hp[i], ub.x);
-                    hv1[i] = __fmaf_rn(a1, hv0[i], ub.y);
-                    hp[i] = hv1[i];
+                    b4[i] = *reinterpret_cast<const float4*>(BTb + (n0 + i) * T + 4 * q);
+                    if (!AGG) c4[i] = *reinterpret_cast<const float4*>(CTb + (n0 + i) * T + 4 * q);
                 }
-                if (!AGG) {
-                    // the lane's NS/RB readout blocks: sequential chains of RB
-                    // states, then summed as a balanced tree in state order
-                    float2 r[NS / RB];
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const int m = 2 * q + h2;
+                    float hv0[NS], hv1[NS];
 #pragma unroll
                     for (int i = 0; i < NS; ++i) {
-                        const float2 cc = h2 ? f2(c4[i].z, c4[i].w) : f2(c4[i].x, c4[i].y);
-                        r[i / RB] = (i % RB == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i]))
-                                                  : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r[i / RB]);
+                        const float2 bb = h2 ? f2(b4[i].z, b4[i].w) : f2(b4[i].x, b4[i].y);
+                        const float2 arg = __fmul2_rn(Dl[m], A2p[i]);
+                        const float a0 = ex2(arg.x), a1 = ex2(arg.y);
+                        const float2 ub = __fmul2_rn(Ul[m], bb);
+                        hv0[i] = __fmaf_rn(a0, hp[i], ub.x);
+                        hv1[i] = __fmaf_rn(a1, hv0[i], ub.y);
+                        hp[i] = hv1[i];
                     }
-                    acc[m] = tree2<NS / RB>(r);
+                    if (!AGG) {
+                        // the lane's NS/RB readout blocks: sequential chains of RB
+                        // states, then summed as a balanced tree in state order
+                        float2 r[NS / RB];
+#pragma unroll
+                        for (int i = 0; i < NS; ++i) {
+                            const float2 cc = h2 ? f2(c4[i].z, c4[i].w) : f2(c4[i].x, c4[i].y);
+                            r[i / RB] = (i % RB == 0) ? __fmul2_rn(cc, f2(hv0[i], hv1[i]))
+                                                      : __ffma2_rn(cc, f2(hv0[i], hv1[i]), r[i / RB]);
+                        }
+                        acc[m] = tree2<NS / RB>(r);
+                    }
+                }
+                if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
+#pragma unroll
+                    for (int i = 0; i < NS; i += 2)
+                        *reinterpret_cast<float2*>(ckp + (int64_t)(i / 2) * D * 2 + (int64_t)kN * D) = f2(hp[i], hp[i + 1]);
                 }
             }
-            if (q == 1 && ck && rows > kCkpt) {  // states before token t0+8
 #pragma unroll
-                for (int i = 0; i < NS; i += 2)
-                    *reinterpret_cast<float2*>(ckp + (int64_t)(i / 2) * D * 2 + (int64_t)kN * D) = f2(hp[i], hp[i + 1]);
-            }
-        }
+            for (int i = 0; i < NS; ++i) h[i] = hp[i];
+            if (!AGG) {
+                // ---- E: the kLPC partial readouts of this lane's TPL tokens
+                float* pb = PB + c * Ly::PROW;
+                __syncwarp();  // the previous tile's reads of PB are done
 #pragma unroll
-        for (int i = 0; i < NS; ++i) h[i] = hp[i];
-        if (!AGG) {
-            // ---- E: the kLPC partial readouts of this lane's TPL tokens
-            float* pb = PB + c * Ly::PROW;
-            __syncwarp();  // the previous tile's reads of PB are done
+                for (int q = 0; q < T / 4; ++q)
+                    *reinterpret_cast<float4*>(pb + T * hk + 4 * q) =
+                        make_float4(acc[2 * q].x, acc[2 * q].y, acc[2 * q + 1].x, acc[2 * q + 1].y);
+                __syncwarp();
+                IO* yrow = reinterpret_cast<IO*>(p.y) + (b * L + t0) * D + d;
 #pragma unroll
-            for (int q = 0; q < T / 4; ++q)
-                *reinterpret_cast<float4*>(pb + T * hk + 4 * q) =
-                    make_float4(acc[2 * q].x, acc[2 * q].y, acc[2 * q + 1].x, acc[2 * q + 1].y);
-            __syncwarp();
-            IO* yrow = reinterpret_cast<IO*>(p.y) + (b * L + t0) * D + d;
+                for (int i = 0; i < TPL / 4; ++i) {
+                    float2 qa[kLPC], qb[kLPC];  // tokens TPL*hk + 4i + (0, 1) and (2, 3), one per lane block
 #pragma unroll
-            for (int i = 0; i < TPL / 4; ++i) {
-                float2 qa[kLPC], qb[kLPC];  // tokens TPL*hk + 4i + (0, 1) and (2, 3), one per lane block
-#pragma unroll
-                for (int r = 0; r < kLPC; ++r) {
-                    const float4 v = *reinterpret_cast<const float4*>(pb + T * r + TPL * hk + 4 * i);
-                    qa[r] = f2(v.x, v.y);
-                    qb[r] = f2(v.z, v.w);
-                }
-                const float2 pr[2] = {tree2<kLPC>(qa), tree2<kLPC>(qb)};
-#pragma unroll
-                for (int k2 = 0; k2 < 2; ++k2) {
-                    const int t = TPL * hk + 4 * i + 2 * k2;
-                    const float2 pp = __ffma2_rn(D2, xo[2 * i + k2], pr[k2]);
-                    const float2 yv = has_z ? __fmul2_rn(pp, gz[2 * i + k2]) : pp;
-                    if (dv && t < rows) {
-                        nf = __fmaf_rn(yv.x, 0.0f, nf);
-                        yrow[(int64_t)t * D] = IOT<IO>::from_f(yv.x);
+                    for (int r = 0; r < kLPC; ++r) {
+                        const float4 v = *reinterpret_cast<const float4*>(pb + T * r + TPL * hk + 4 * i);
+                        qa[r] = f2(v.x, v.y);
+                        qb[r] = f2(v.z, v.w);
                     }
-                    if (dv && t + 1 < rows) {
-                        nf = __fmaf_rn(yv.y, 0.0f, nf);
-                        yrow[(int64_t)(t + 1) * D] = IOT<IO>::from_f(yv.y);
+                    const float2 pr[2] = {tree2<kLPC>(qa), tree2<kLPC>(qb)};
+#pragma unroll
+                    for (int k2 = 0; k2 < 2; ++k2) {
+                        const int t = TPL * hk + 4 * i + 2 * k2;
+                        const float2 pp = __ffma2_rn(D2, xo[2 * i + k2], pr[k2]);
+                        const float2 yv = has_z ? __fmul2_rn(pp, gz[2 * i + k2]) : pp;
+                        if (dv && t < rows) {
+                            nf = __fmaf_rn(yv.x, 0.0f, nf);
+                            yrow[(int64_t)t * D] = IOT<IO>::from_f(yv.x);
+                        }
+                        if (dv && t + 1 < rows) {
+                            nf = __fmaf_rn(yv.y, 0.0f, nf);
+                            yrow[(int64_t)(t + 1) * D] = IOT<IO>::from_f(yv.y);
+                        }
                     }
                 }
             }
