@@ -407,9 +407,19 @@ def cpu_baseline(w, budget_s=12.0):
     while sum(ts) < budget_s and len(ts) < 50:
         ts.append(_oracle_step(s, cores))
     tc = w.L * ds * len(ts)
+    # the same loop on one thread, on as many channels as take about a
+    # tenth of a quarter of the budget, repeated for that quarter
+    t1p = _oracle_step(_sample(row, min(w.D, 8)), 1)
+    s1 = _sample(row, int(min(w.D, max(8, 8 * budget_s / 40 / max(t1p, 1e-4))) // 8 * 8))
+    t1 = []
+    while sum(t1) < budget_s / 4 and len(t1) < 50:
+        t1.append(_oracle_step(s1, 1))
     return {"value": tc / sum(ts) / 1e9, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"batch row 0, first {ds} of {w.D} channels, all {w.L} tokens, fp32 oracle fwd+bwd, "
-                      f"{len(ts)} repetitions, {sum(ts):.1f} s"}
+                      f"{len(ts)} repetitions, {sum(ts):.1f} s",
+            "one_core": {"value": w.L * s1.D * len(t1) / sum(t1) / 1e9, "unit": UNIT, "cores": 1,
+                         "sample": f"batch row 0, first {s1.D} channels, all {w.L} tokens, {len(t1)} repetitions, "
+                                   f"{sum(t1):.1f} s"}}
 
 
 def run_reference(args, w):
