@@ -83,8 +83,8 @@ WsLayout ws_layout(int64_t B, int64_t L, int64_t D) {
 
 bool misaligned(const void* p) { return p && (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-// Price of the backward's aggregate pass (only the adjoint chain) relative to
-// the backward main pass.
+// Price of the backward's aggregate pass (one exponential per element, no
+// outputs) relative to the backward main pass.
 constexpr double kBwdAggCost = 0.15;
 
 int auto_groups_fwd(int io, int64_t B, int64_t D, int64_t gmax) {

@@ -143,9 +143,10 @@ inline int choose_groups(int64_t ctas_per_group, int64_t capacity, double alpha,
 
 // Forward L-groups: one group when the grid already gives every SM more
 // than one CTA (>= 1.5 per SM); otherwise as many groups as fill the resident
-// CTA slots once. (The forward's aggregate pass costs most of a pass, and an
-// SM that holds fewer CTAs finishes them sooner, so a partly filled single
-// wave beats paying for aggregates; a grid far below one CTA per SM does not.)
+// CTA slots once. (The forward's aggregate pass costs about 0.6 of a main
+// pass per token, and an SM that holds fewer CTAs finishes them sooner, so a
+// partly filled single wave beats paying for aggregates; a grid far below
+// one CTA per SM does not.)
 inline int choose_groups_fwd(int64_t ctas_per_group, int64_t sms, int64_t blocks_per_sm, int64_t gmax) {
     if (ctas_per_group < 1) ctas_per_group = 1;
     if (2 * ctas_per_group >= 3 * sms) return 1;
