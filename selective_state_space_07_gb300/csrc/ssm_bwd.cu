@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
         // input, no adjoint input, nothing accumulated)
         const bool full = rows == T;
         float2 Dl[2][T / 2], Ul[2][T / 2], Pl[2][T / 2];
-        float2 sgp[T / 2], ddp[T / 2];
+        float2 sgp[T / 2], ddp[T / 2], Xl[T / 2];  // x stays in registers for phase E
 #pragma unroll
         for (int m = 0; m < T / 2; ++m) {
             const int t = 2 * m;
@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
                 dyds = __fmul2_rn(dyv, __fmul2_rn(sz, __ffma2_rn(zv, __fadd2_rn(one, f2(-sz.x, -sz.y)), one)));
             }
             float2 ul = __fmul2_rn(dl, xv);
+            Xl[m] = xv;
             if (!full) {
                 const bool l0 = t < rows, l1 = t + 1 < rows;
                 dl = f2(l0 ? dl.x : 0.f, l1 ? dl.y : 0.f);
@@ -401,7 +402,7 @@ __global__ void __launch_bounds__(kBwdThreads, 2)
 #pragma unroll
             for (int m = 0; m < T / 2; ++m) {
                 const int t = 2 * m;
-                float2 xv = ld_pair<IO>(st + Ly::OFF_X + t * Ly::XROW, Ly::XROW, cO);
+                float2 xv = Xl[m];
                 if (!full) xv = f2(t < rows ? xv.x : 0.f, t + 1 < rows ? xv.y : 0.f);
                 const float2 s1 = S1[0][m], s2 = S2[0][m];
                 const float2 dxv = __ffma2_rn(Pl[0][m], D2, __fmul2_rn(Dl[0][m], s1));
