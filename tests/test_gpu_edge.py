@@ -44,18 +44,19 @@ def test_ragged_lengths(ssm, L, io):
 
 @pytest.mark.parametrize("regime", ["no decay", "fast decay", "slow decay"])
 @pytest.mark.parametrize("groups", [3, 5])
-def test_carries_across_decay_regimes(ssm, regime, groups):
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_carries_across_decay_regimes(ssm, regime, groups, io):
     # the L-group aggregates take the product of a group's decays as exp(A
     # times a running sum of Delta): states that never decay (A = 0, the
     # carries are plain sums over the group), decays that underflow within a
     # few tokens (Delta ~ 5) and decays that barely act (Delta ~ 1e-4), each
     # against the oracle's sequential recurrence, with ragged groups
     target = {"no decay": 0.05, "fast decay": 5.0, "slow decay": 1e-4}[regime]
-    inp = gen.make_inputs(2, 300, 40, 16, io="f32", seed=groups, dt_std=0.5, delta_target=target,
+    inp = gen.make_inputs(2, 300, 40, 16, io=io, seed=groups, dt_std=0.5, delta_target=target,
                           with_h0=True, with_dh_last=True)
     if regime == "no decay":
         inp.A[:, :5] = 0.0
-    compare(ssm, inp, "f32", dict(groups=groups), dict(groups=groups))
+    compare(ssm, inp, io, dict(groups=groups), dict(groups=groups))
 
 
 @pytest.mark.parametrize("D", [8, 40, 136, 264])
